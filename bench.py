@@ -1,0 +1,488 @@
+"""Benchmark of the per-token normalization hot path on GB300.
+
+One step = one pass of every hot-path kernel over the prefill workloads:
+  * layerwise QK-RMSNorm of Q and of K, each [8192, 5120] bf16, 1% outlier
+    channels, N = 4 cluster shards (13B-like prefill);
+  * RMSNorm + MXFP8 cast, MXNorm p = 1 and MXNorm p = 2 (+ MXFP8 cast) of
+    X [65536, 4096] bf16, B = 32, E4M3 values + E8M0 scales.
+
+value = algorithmic HBM bytes of the step / step time (GB/s, 1e9 B/s); the
+per-kernel tokens/s, GB/s and roofline fractions ride along.  Inputs are
+resident in HBM; the step's working set (2.8 GB) is far above the L2, so no
+flush is needed between steps.  `e2e` runs the same step through the C ABI's
+host-buffer entry points (pinned host memory, copies inside the timed
+region).  `cpu_baseline` times the CPU oracle on a bounded row sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl nts|reference]
+
+Under torchrun (N > 1) every rank runs the same step on its own GPU
+(replicas: the path needs no exchange between GPUs); value sums the ranks'
+bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("tokens/s and achieved HBM GB/s vs ~8 TB/s peak (QK-RMSNorm, MXNorm) on 1 GB300")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+QK_T, QK_H, QK_N = 8192, 5120, 4
+MX_T, MX_D, MX_B = 65536, 4096, 32
+EPS = 1e-6
+
+KERNELS = ["qknorm_rms[Q]", "qknorm_rms[K]", "rmsnorm_mxcast", "mxnorm_cast[p=1]",
+           "mxnorm_cast[p=2]"]
+KERNEL_SOURCES = {
+    "qknorm_rms": "normalization_token_split_gb300/csrc/qknorm_cluster.cu",
+    "mx": "normalization_token_split_gb300/csrc/mx_norm_cast.cu",
+}
+
+
+def qk_bytes(T, H):
+    return 4 * T * H                       # bf16 in + bf16 out
+
+
+def mx_bytes(T, D, B):
+    return T * (2 * D + D + D // B)        # bf16 in + E4M3 codes + E8M0 scales
+
+
+def step_bytes():
+    per = {"qknorm_rms[Q]": qk_bytes(QK_T, QK_H), "qknorm_rms[K]": qk_bytes(QK_T, QK_H)}
+    for k in KERNELS[2:]:
+        per[k] = mx_bytes(MX_T, MX_D, MX_B)
+    return per
+
+
+def step_tokens():
+    return {k: (QK_T if k.startswith("qk") else MX_T) for k in KERNELS}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_config():
+    return {
+        "workload": ("prefill layer norms: QK-RMSNorm Q,K [8192,5120] N=4 + "
+                     "RMSNorm+MXFP8, MXNorm p=1, MXNorm p=2 of [65536,4096] B=32 E4M3"),
+        "qk": {"T": QK_T, "H": QK_H, "N": QK_N, "tensors": ["Q", "K"], "eps": EPS,
+               "x": "bf16 N(0,1), 1% of channels x20", "gamma": "fp32 N(1,0.1)"},
+        "mx": {"T": MX_T, "D": MX_D, "B": MX_B, "fmt": "E4M3", "scales": "E8M0",
+               "kinds": ["rmsnorm_mxcast", "mxnorm p=1", "mxnorm p=2"], "gamma": None,
+               "x": "bf16 N(0,1)", "eps": EPS},
+        "l2": "no flush: each step touches 2.78 GB, far above the 126 MB L2",
+        "io_dtypes": "bf16 in; bf16 / E4M3+E8M0 out",
+    }
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [l for (t, l) in self.lines if t0 <= t <= t1 + 0.15] or [l for _, l in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a per-rank scalar across the process group (host aggregation)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def kernel_traffic():
+    """dram bytes per launch from the committed ncu summaries, if they were
+    taken from the current kernel source (sha256 recorded in the summary)."""
+    out = {}
+    prof = os.path.join(ROOT, "profiles")
+    for key, src in KERNEL_SOURCES.items():
+        try:
+            h = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+        except OSError:
+            continue
+        for fn in sorted(os.listdir(prof)) if os.path.isdir(prof) else []:
+            if not fn.endswith(".md"):
+                continue
+            text = open(os.path.join(prof, fn)).read()
+            for m in re.finditer(r"traffic_per_launch\s+(\S+)\s+(\d+)\s+source_sha256\s+(\w+)", text):
+                name, val, sha = m.group(1), int(m.group(2)), m.group(3)
+                if sha == h and (name.startswith(key) or (key == "mx" and "mx" in name)):
+                    out[name] = val
+    return out
+
+
+# ------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+
+    import workloads
+    import normalization_token_split_gb300 as nts
+
+    per_bytes = step_bytes()
+    tokens = step_tokens()
+    total_bytes = sum(per_bytes.values())
+
+    Q, gq = workloads.qk_inputs(QK_T, QK_H, seed=3000, outlier_frac=0.01, device=dev)
+    K, gk = workloads.qk_inputs(QK_T, QK_H, seed=3001, outlier_frac=0.01, device=dev)
+    X, _ = workloads.mx_inputs(MX_T, MX_D, seed=4000 + MX_T, device=dev)
+    Yq, Yk = torch.empty_like(Q), torch.empty_like(K)
+    outs = {}
+    for name in KERNELS[2:]:
+        outs[name] = (torch.empty(MX_T, MX_D, dtype=torch.uint8, device=dev),
+                      torch.empty(MX_T, MX_D // MX_B, dtype=torch.uint8, device=dev))
+    stream = torch.cuda.current_stream()
+
+    launches = [
+        ("qknorm_rms[Q]", lambda: nts.qknorm_rms(Q, gq, eps=EPS, N=QK_N, out=Yq)),
+        ("qknorm_rms[K]", lambda: nts.qknorm_rms(K, gk, eps=EPS, N=QK_N, out=Yk)),
+        ("rmsnorm_mxcast", lambda: nts.rmsnorm_mxcast(
+            X, None, eps=EPS, B=MX_B, fmt="e4m3", codes=outs["rmsnorm_mxcast"][0],
+            scales=outs["rmsnorm_mxcast"][1])),
+        ("mxnorm_cast[p=1]", lambda: nts.mxnorm_cast(
+            X, None, eps=EPS, B=MX_B, fmt="e4m3", p=1, codes=outs["mxnorm_cast[p=1]"][0],
+            scales=outs["mxnorm_cast[p=1]"][1])),
+        ("mxnorm_cast[p=2]", lambda: nts.mxnorm_cast(
+            X, None, eps=EPS, B=MX_B, fmt="e4m3", p=2, codes=outs["mxnorm_cast[p=2]"][0],
+            scales=outs["mxnorm_cast[p=2]"][1])),
+    ]
+
+    def step(events=None):
+        for i, (name, fn) in enumerate(launches):
+            if events is not None:
+                events[i][0].record(stream)
+            fn()
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    nts.check_status()
+
+    # ---- timed region: K steps, per-launch events on the launching stream
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+           for _ in launches] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(ev[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    w1 = time.time()
+    time.sleep(0.25)
+    clocks.stop()
+    nts.check_status()
+
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    per_kernel_ms = {name: statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1])
+                                           for k in range(args.steps))
+                     for i, (name, _) in enumerate(launches)}
+    ms_per_step = elapsed_ms / args.steps
+    value = world * total_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peaks()
+    kernels = {}
+    for name in KERNELS:
+        gbs = per_bytes[name] / (per_kernel_ms[name] * 1e-3) / 1e9
+        kernels[name] = {"ms": round(per_kernel_ms[name], 5), "bytes": per_bytes[name],
+                         "gbs": round(gbs, 1), "tokens_per_s": round(tokens[name] / (per_kernel_ms[name] * 1e-3)),
+                         "frac_of_measured": round(gbs / peak, 4),
+                         "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
+    dominant = max(KERNELS, key=lambda n: per_kernel_ms[n])
+    traffic = kernel_traffic()
+    dom_key = dominant.replace("[", "_").replace("]", "").replace("=", "")
+    roofline = {"bound": "hbm", "kernel": dominant,
+                "achieved": kernels[dominant]["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": round(kernels[dominant]["gbs"] / peak, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "traffic": traffic.get(dom_key)}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": dict(workload_config(), parallelism=
+                                            "replicas" if world > 1 else "single GPU"),
+        "tokens_per_s": {n: kernels[n]["tokens_per_s"] for n in KERNELS},
+        "frac_of_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "kernels": kernels, "roofline": roofline,
+        "gpu_launches": len(launches) * args.steps,
+        "clocks": clocks.summary(w0, w1),
+        "wall_s_timed": round(w1 - w0, 4),
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world):
+    """Same step through the host-buffer C ABI forms, copies timed."""
+    pin = lambda t: t.cpu().pin_memory()
+    Qh, Kh, Xh = pin(Q), pin(K), pin(X)
+    Yqh = torch.empty_like(Qh).pin_memory()
+    Ykh = torch.empty_like(Kh).pin_memory()
+    Xd = torch.empty_like(X)
+    Qd, Kd = torch.empty_like(Q), torch.empty_like(K)
+    Yqd, Ykd = torch.empty_like(Q), torch.empty_like(K)
+    codes_h = {n: torch.empty(MX_T, MX_D, dtype=torch.uint8).pin_memory() for n in KERNELS[2:]}
+    scales_h = {n: torch.empty(MX_T, MX_D // MX_B, dtype=torch.uint8).pin_memory()
+                for n in KERNELS[2:]}
+    codes_d = torch.empty(MX_T, MX_D, dtype=torch.uint8, device=dev)
+    scales_d = torch.empty(MX_T, MX_D // MX_B, dtype=torch.uint8, device=dev)
+
+    def step():
+        nts.qknorm_rms_host(Qh, gq, Yqh, Qd, Yqd, eps=EPS, N=QK_N)
+        nts.qknorm_rms_host(Kh, gk, Ykh, Kd, Ykd, eps=EPS, N=QK_N)
+        nts.rmsnorm_mxcast_host(Xh, None, codes_h["rmsnorm_mxcast"], scales_h["rmsnorm_mxcast"],
+                                Xd, codes_d, scales_d, eps=EPS, B=MX_B, fmt="e4m3")
+        for p in (1, 2):
+            n = f"mxnorm_cast[p={p}]"
+            nts.mxnorm_cast_host(Xh, None, codes_h[n], scales_h[n], Xd, codes_d, scales_d,
+                                 eps=EPS, B=MX_B, fmt="e4m3", p=p)
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        step()
+    nts.check_status()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(world)
+    nts.check_status()
+    elapsed = max_over_ranks(t1 - t0, world)
+    total = sum(step_bytes().values())
+    h2d = 2 * QK_T * QK_H * 2 + 3 * MX_T * MX_D * 2
+    d2h = 2 * QK_T * QK_H * 2 + 3 * (MX_T * MX_D + MX_T * (MX_D // MX_B))
+    return {"value": round(world * total * steps / elapsed / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(elapsed / steps * 1e3, 4),
+            "path": "nts_*_host C ABI entry points, pinned host buffers"}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample_step(rows_qk: int, rows_mx: int, state):
+    """One bounded sample of the step through the CPU oracle; returns the
+    algorithmic bytes it covered."""
+    import oracle
+    Qb, gq, Kb, gk, Xb = state
+    oracle.qknorm_rms(Qb[:rows_qk], gq, EPS, QK_N)
+    oracle.qknorm_rms(Kb[:rows_qk], gk, EPS, QK_N)
+    oracle.rmsnorm_mxcast(Xb[:rows_mx], None, EPS, MX_B, 0)
+    oracle.mxnorm_cast(Xb[:rows_mx], None, EPS, MX_B, 0, 1)
+    oracle.mxnorm_cast(Xb[:rows_mx], None, EPS, MX_B, 0, 2)
+    return 2 * qk_bytes(rows_qk, QK_H) + 3 * mx_bytes(rows_mx, MX_D, MX_B)
+
+
+def oracle_inputs(rows_qk, rows_mx):
+    import workloads
+    Q, gq = workloads.qk_inputs(rows_qk, QK_H, seed=3000, outlier_frac=0.01)
+    K, gk = workloads.qk_inputs(rows_qk, QK_H, seed=3001, outlier_frac=0.01)
+    X, _ = workloads.mx_inputs(rows_mx, MX_D, seed=4000 + MX_T)
+    return (workloads.bf16_bits(Q), gq.numpy(), workloads.bf16_bits(K), gk.numpy(),
+            workloads.bf16_bits(X))
+
+
+def cpu_baseline(seconds: float):
+    """The oracle, single-threaded, on repeated row samples of the step
+    (128 rows of Q and of K, 1024 rows of X per MX function) for about
+    `seconds` of CPU time."""
+    import oracle
+    oracle.build()
+    rows_qk, rows_mx = 128, 1024
+    state = oracle_inputs(rows_qk, rows_mx)
+    done, t0 = 0, time.perf_counter()
+    passes = 0
+    while True:
+        done += oracle_sample_step(rows_qk, rows_mx, state)
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{passes} passes of 128 rows of Q and of K (H=5120, N=4) and 1024 rows "
+                       f"of X (D=4096) through rmsnorm_mxcast, mxnorm p=1, p=2; "
+                       f"{dt:.1f} s; single thread"),
+            "cpu": cpu_model()}
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return os.uname().machine
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    rows_qk, rows_mx = 16, 64
+    state = oracle_inputs(rows_qk, rows_mx)
+    for _ in range(args.warmup):
+        oracle_sample_step(rows_qk, rows_mx, state)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        done += oracle_sample_step(rows_qk, rows_mx, state)
+    dt = time.perf_counter() - t0
+    value = round(done / dt / 1e9, 4)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "per step: 16 rows of Q and of K (H=5120, N=4), 64 rows of "
+                                   "X (D=4096) through the three MX functions; single thread",
+                         "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["nts", "reference"], default="nts")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.impl == "nts":
+        args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+/*
+ * nts.h -- C ABI of libnts, GB300 (sm_103a) kernels for per-token RMS
+ * normalization: split-H layerwise QK-RMSNorm, fused RMSNorm + MX cast, and
+ * MXNorm + MX cast.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named *_dev are device pointers (cudaMalloc'd, or owned by a
+ *    framework such as PyTorch); pointers named *_host are host pointers
+ *    (pinned memory gives asynchronous copies).  Entry points without a
+ *    suffix take device pointers only.  The caller owns every buffer; the
+ *    library allocates no device memory (it keeps one status word per kernel
+ *    family as a static device variable).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls only enqueue work and return; results are ready once
+ *    the stream has reached that point.
+ *  - Matrices are row-major with one token per row: element (t, j) of a
+ *    [T, H] matrix is at index t*H + j.  bf16 means IEEE-style bfloat16
+ *    (uint16 storage).  Device pointers must be 16-byte aligned.
+ *  - Return value: an nts_status.  Nothing is launched when the status is
+ *    not NTS_OK, and no call aborts or throws.  nts_last_error() gives a
+ *    human-readable detail for the calling thread.
+ *  - T == 0 is valid and launches nothing.
+ *
+ * Sources (web pages), by title and section:
+ *   SwiftQK: Fast and Communication-Efficient Tensor Parallelism for
+ *   Query-Key Normalization (IEEE CAL) -- Eq. (1), Sec. III.A-D, Algorithm 1;
+ *   the SwiftQK reading notes (zhongzhuzhou.org) -- Eq. (1), Sec. 3, Sec. 4b;
+ *   the MXNorm paper card (arXiv 2603.13180) -- abstract, Fig. 1 caption,
+ *   Fig. 8, Fig. A.1.
+ */
+#ifndef NTS_H
+#define NTS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NTS_API __attribute__((visibility("default")))
+#else
+#define NTS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NTS_OK = 0,
+    NTS_ERR_INVALID_ARG = 1, /* null required pointer, bad size/shape/eps/N/B/fmt/p */
+    NTS_ERR_UNSUPPORTED = 2, /* valid request this build cannot run: misaligned
+                                pointer, row too wide, cluster not launchable */
+    NTS_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    NTS_ERR_TIMEOUT = 4      /* a kernel's bounded wait expired (nts_check_status) */
+} nts_status;
+
+typedef enum {
+    NTS_FMT_E4M3 = 0, /* OCP E4M3: 1 byte per element, max 448 (MXFP8) */
+    NTS_FMT_E2M1 = 1  /* OCP E2M1: 4 bits per element, max 6 (MXFP4) */
+} nts_elem_fmt;
+
+/* Library version, major*10000 + minor*100 + patch. */
+NTS_API int nts_version(void);
+
+/* Static string naming a status code. */
+NTS_API const char *nts_status_string(int status);
+
+/* Detail of the calling thread's most recent failure ("" if none). */
+NTS_API const char *nts_last_error(void);
+
+/*
+ * nts_qknorm_rms -- layerwise QK-RMSNorm of every token row, computed as
+ * split-H scalar partial sums (SwiftQK Eq. (1) and Algorithm 1):
+ *
+ *     S_k    = sum over columns [k*H/N, (k+1)*H/N) of x_j^2    (Phase A, fp32)
+ *     S      = S_0 + ... + S_{N-1}                            (rank order)
+ *     rinv   = 1 / sqrt(S / H + eps)          (H is the FULL row width)
+ *     y_j    = bf16_rne((x_j * gamma_j) * rinv)                (Phases B, C)
+ *
+ * The N shards of a row are N CTAs of one thread-block cluster; each keeps
+ * its shard on chip, exchanges its partial sum through distributed shared
+ * memory, and forms x*gamma while the exchange is in flight.  N changes only
+ * the work decomposition and the fp32 summation order, never the result's
+ * definition.
+ *
+ *   X_dev      bf16 [T, H], read.            gamma_dev  fp32 [H], read.
+ *   Y_dev      bf16 [T, H], written.  Y_dev == X_dev (in place) is allowed;
+ *              any other overlap is undefined.
+ *   rinv_dev   fp32 [T], written, or NULL.
+ *   T >= 0; H >= 8; H % N == 0; (H / N) % 8 == 0; H / N <= 32768;
+ *   eps > 0 and finite; N in {1, 2, 4, 8}.
+ * Errors: INVALID_ARG (null X/gamma/Y, T < 0, H <= 0, H % N, bad eps or N),
+ *         UNSUPPORTED ((H/N) % 8 != 0, slice too wide, unaligned pointer,
+ *         cluster shape not launchable), CUDA (launch failure).
+ */
+NTS_API int nts_qknorm_rms(const void *X_dev, const float *gamma_dev, void *Y_dev,
+                   float *rinv_dev, int64_t T, int64_t H, float eps, int N,
+                   void *stream);
+
+/*
+ * nts_rmsnorm_mxcast -- RMSNorm fused with the MX cast (MXNorm card,
+ * Fig. 1 caption, left graph; Fig. 8 "normalization and casting fused into a
+ * single kernel"):
+ *
+ *     rinv     = 1 / sqrt((1/D) sum_j x_j^2 + eps)      (statistic of x, fp32)
+ *     w_j      = fp32(x_j * gamma_j), or x_j when gamma_dev is NULL
+ *     amax_k   = max over block k (B contiguous elements) of |w_j|
+ *     e_k      = round(log2(fp32(amax_k * rinv))) - emax, clamped to
+ *                [-127, 127], where round() is to the nearest integer in the
+ *                log2 domain (mantissa >= sqrt 2 rounds up) and emax = 8
+ *                (E4M3, "divide by 256") or 2 (E2M1)
+ *     scale_k  = e_k + 127                                   (E8M0 byte)
+ *     code_j   = cast_rne_satfinite(fp32(w_j * rinv) * 2^-e_k)
+ *
+ *   X_dev       bf16 [T, D], read.    gamma_dev fp32 [D], read, or NULL.
+ *   codes_dev   E4M3: uint8 [T, D]; E2M1: uint8 [T, D/2] with element 2i in
+ *               bits 0-3 and element 2i+1 in bits 4-7 of byte i.  Written.
+ *   scales_dev  uint8 [T, D/B] E8M0 codes (2^(code-127)), row-major. Written.
+ *   rinv_dev    fp32 [T] or NULL.   amax_dev  fp32 [T, D/B] block absmaxes
+ *               of w (before normalization) or NULL.
+ *   T >= 0; D % B == 0; B in {16, 32, 64}; D <= 32768; eps > 0 and finite;
+ *   fmt in nts_elem_fmt.
+ * Errors: INVALID_ARG (null X/codes/scales, T < 0, D <= 0, D % B, bad B,
+ *         eps or fmt), UNSUPPORTED (row too wide, unaligned pointer),
+ *         CUDA (launch failure).
+ */
+NTS_API int nts_rmsnorm_mxcast(const void *X_dev, const float *gamma_dev,
+                       uint8_t *codes_dev, uint8_t *scales_dev,
+                       float *rinv_dev, float *amax_dev, int64_t T, int64_t D,
+                       float eps, int B, int fmt, void *stream);
+
+/*
+ * nts_mxnorm_cast -- MXNorm (MXNorm card, abstract and Fig. 1 caption,
+ * right graph): the RMS is estimated from the K = D/B block absmaxes that the
+ * MX cast computes anyway,
+ *
+ *     rho~  = c(B, p) * ((1/K) sum_k amax_k^p)^(1/p),   p in {1, 2}
+ *     rinv  = 1 / sqrt(rho~^2 + eps)
+ *
+ * then the block stage of nts_rmsnorm_mxcast runs with this rinv (the
+ * normalized block absmax is amax_k * rinv, so no second reduction).  w, the
+ * tensor whose absmaxes are taken and which is cast, is x (gamma_dev NULL,
+ * the gain folded into the next Linear layer) or fp32(x * gamma).
+ * c(B, p) = E[max of B i.i.d. |N(0,1)|^p]^(-1/p) (nts_mxnorm_correction).
+ * Arguments, layouts and errors as nts_rmsnorm_mxcast, plus p in {1, 2}
+ * (INVALID_ARG otherwise).
+ */
+NTS_API int nts_mxnorm_cast(const void *X_dev, const float *gamma_dev,
+                    uint8_t *codes_dev, uint8_t *scales_dev, float *rinv_dev,
+                    float *amax_dev, int64_t T, int64_t D, float eps, int B,
+                    int fmt, int p, void *stream);
+
+/*
+ * nts_mxnorm_correction -- the correction factor c(B, p) used by
+ * nts_mxnorm_cast (MXNorm card, Fig. 1 caption: the scalar making the
+ * estimate equal the RMS for i.i.d. Gaussian rows), computed on the host by
+ * quadrature.  B >= 1, p in {1, 2}; *c_out receives the value.
+ * Errors: INVALID_ARG.
+ */
+NTS_API int nts_mxnorm_correction(int B, int p, double *c_out);
+
+/*
+ * nts_check_status -- synchronizes `stream`, then reads and clears the
+ * device status words.  Returns NTS_ERR_TIMEOUT if any kernel since the last
+ * check gave up on a bounded wait (its outputs are then undefined),
+ * NTS_ERR_CUDA if the stream reported an error, NTS_OK otherwise.
+ */
+NTS_API int nts_check_status(void *stream);
+
+/*
+ * Host-buffer forms: the same operations for callers whose inputs and
+ * outputs live in host memory.  Each enqueues on `stream`: the host->device
+ * copy of the input rows, the kernel, and the device->host copies of the
+ * outputs; the caller synchronizes the stream before reading *_host outputs.
+ * The device staging buffers (*_dev) are caller-owned and sized like the
+ * corresponding host buffers; gamma stays a device pointer (a parameter,
+ * uploaded once).  Optional outputs follow the device forms: a NULL *_host
+ * output skips that output (its *_dev may then be NULL too).
+ * Errors: as the device forms; CUDA also covers a failed copy.
+ */
+NTS_API int nts_qknorm_rms_host(const void *X_host, const float *gamma_dev,
+                        void *Y_host, float *rinv_host, void *X_dev,
+                        void *Y_dev, float *rinv_dev, int64_t T, int64_t H,
+                        float eps, int N, void *stream);
+
+NTS_API int nts_rmsnorm_mxcast_host(const void *X_host, const float *gamma_dev,
+                            uint8_t *codes_host, uint8_t *scales_host,
+                            void *X_dev, uint8_t *codes_dev,
+                            uint8_t *scales_dev, int64_t T, int64_t D,
+                            float eps, int B, int fmt, void *stream);
+
+NTS_API int nts_mxnorm_cast_host(const void *X_host, const float *gamma_dev,
+                         uint8_t *codes_host, uint8_t *scales_host,
+                         void *X_dev, uint8_t *codes_dev, uint8_t *scales_dev,
+                         int64_t T, int64_t D, float eps, int B, int fmt,
+                         int p, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NTS_H */

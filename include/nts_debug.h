@@ -1,0 +1,48 @@
+/*
+ * nts_debug.h -- tuning overrides and test hooks of libnts.  Not needed by
+ * normal callers.  Settings are process-wide and apply to every later call
+ * until changed; they are not thread-safe with respect to calls in flight on
+ * other host threads.  No source page defines these: they exist to sweep
+ * launch shapes and to exercise the library's error paths without faulting a
+ * GPU.
+ */
+#ifndef NTS_DEBUG_H
+#define NTS_DEBUG_H
+
+#include <stdint.h>
+
+#include "nts.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Override the automatic launch shape.  Each argument 0 means automatic.
+ *   vpt        16-byte vectors per thread, one of {1,2,3,4,5,6,8}
+ *   rows       token rows per tile (CTA threads = rows * threads-per-row <= 512)
+ *   stages     shared-memory ring stages (>= 1)
+ *   grid       CTAs (MX kernels) or clusters (QK kernel) of the persistent grid
+ *   smem_budget bytes a CTA's ring aims to stay under (default 102400)
+ * Errors: INVALID_ARG for negative values or an unknown vpt.  A shape the
+ * device cannot run is reported by the next call as UNSUPPORTED or CUDA.
+ */
+NTS_API int nts_debug_set_tuning(int vpt, int rows, int stages, int64_t grid, int smem_budget);
+
+/* Limit of every bounded in-kernel wait, in ns (0 = default, 1 s). */
+NTS_API int nts_debug_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test hook: every later launch tells its first ring stage to expect `bytes`
+ * more than its copies deliver, so that stage's wait can only end by
+ * expiring; the kernel then records NTS_ERR_TIMEOUT for nts_check_status and
+ * returns with undefined outputs.  bytes must be a multiple of 16; 0 turns
+ * the hook off.  Use with a short wait limit.
+ */
+NTS_API int nts_debug_set_missing_tx(uint32_t bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NTS_DEBUG_H */

@@ -1,0 +1,26 @@
+"""GB300-native per-token RMS normalization.
+
+Two hot paths, both hand-written sm_103a CUDA behind a C ABI (include/nts.h):
+
+* ``qknorm_rms``      layerwise QK-RMSNorm with split-H scalar partial sums,
+                      the shards mapped onto the CTAs of a thread-block cluster
+                      (SwiftQK, Eq. (1) and Algorithm 1);
+* ``rmsnorm_mxcast``  RMSNorm fused with the MX block cast (E4M3 / E2M1 values,
+                      E8M0 scales);
+* ``mxnorm_cast``     MXNorm: the RMS estimated from the MX block absmaxes,
+                      fused with the same cast (MXNorm card, Fig. 1).
+
+Build the library with ``python -m normalization_token_split_gb300.build``.
+"""
+from ._lib import NtsError
+from .ops import (FMT_E2M1, FMT_E4M3, MxOut, check_status, codes_row_bytes, mxnorm_cast,
+                  mxnorm_cast_host, mxnorm_correction, qknorm_rms, qknorm_rms_host,
+                  rmsnorm_mxcast, rmsnorm_mxcast_host, set_missing_tx, set_tuning,
+                  set_wait_limit_ns)
+
+__all__ = [
+    "NtsError", "FMT_E4M3", "FMT_E2M1", "MxOut", "qknorm_rms", "rmsnorm_mxcast", "mxnorm_cast",
+    "mxnorm_correction", "check_status", "codes_row_bytes", "qknorm_rms_host",
+    "rmsnorm_mxcast_host", "mxnorm_cast_host", "set_tuning", "set_wait_limit_ns",
+    "set_missing_tx",
+]

@@ -1,0 +1,447 @@
+// nts_api.cpp -- the C ABI of libnts: argument validation, launch-shape
+// selection, status reporting, the host-buffer forms, and the host-side
+// computation of the MXNorm correction factor c(B, p).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "nts.h"
+#include "nts_debug.h"
+#include "nts_internal.h"
+
+namespace nts {
+
+// ------------------------------------------------------------ error state
+
+namespace {
+thread_local char g_last_error[512] = "";
+
+std::mutex g_tune_mu;
+LaunchTuning g_tune;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+}  // namespace
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  return fail(NTS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+void log_launch(const char* name, const char* fmt, ...) {
+  static const bool on = [] {
+    const char* v = std::getenv("NTS_LOG");
+    return v != nullptr && v[0] != '\0' && v[0] != '0';
+  }();
+  if (!on) return;
+  char buf[384];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  std::fprintf(stderr, "[nts] %s: %s\n", name, buf);
+}
+
+LaunchTuning current_tuning() {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  return g_tune;
+}
+
+// ----------------------------------------------------------- device facts
+
+const DeviceInfo& device_info() {
+  static std::mutex mu;
+  static std::map<int, DeviceInfo> cache;
+  int dev = -1;
+  static DeviceInfo bad;
+  if (cudaGetDevice(&dev) != cudaSuccess) return bad;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  DeviceInfo d;
+  d.device = dev;
+  d.ok = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+         cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                dev) == cudaSuccess;
+  if (!d.ok) return bad;
+  return cache.emplace(dev, d).first->second;
+}
+
+RowShape choose_row_shape(int nvec, int force_vpt) {
+  // Preference among shapes that waste no thread slots: 4-6 vectors
+  // (32-48 values) per thread, then 8, then fewer.
+  static const int order[] = {4, 5, 6, 8, 3, 2, 1};
+  RowShape best;
+  int best_waste = -1;
+  for (int vpt : order) {
+    if (force_vpt > 0 && vpt != force_vpt) continue;
+    int G = (nvec + vpt - 1) / vpt;
+    G = (G + 31) / 32 * 32;
+    if (G > kMaxThreads) continue;
+    const int waste = G * vpt - nvec;
+    if (best_waste < 0 || waste < best_waste) {
+      best_waste = waste;
+      best.vpt = vpt;
+      best.G = G;
+    }
+  }
+  return best;
+}
+
+int prepare_kernel(const void* kernel, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int>, size_t> done;
+  const int dev = device_info().device;
+  std::lock_guard<std::mutex> lk(mu);
+  auto key = std::make_tuple(kernel, dev);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= smem) return NTS_OK;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return fail_cuda(e, "setting the kernel's shared memory size");
+  done[key] = smem;
+  return NTS_OK;
+}
+
+int max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cfg, int cluster,
+                        int64_t* out) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, unsigned, size_t>, int64_t> cache;
+  const int dev = device_info().device;
+  auto key = std::make_tuple(kernel, dev, cfg.blockDim.x, cfg.dynamicSmemBytes);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second;
+      return NTS_OK;
+    }
+  }
+  cudaLaunchConfig_t q = cfg;
+  q.gridDim = dim3((unsigned)cluster);
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &q);
+  if (e != cudaSuccess) return fail_cuda(e, "cluster occupancy query");
+  if (n < 1) return fail(NTS_ERR_UNSUPPORTED, "a cluster of %d CTAs cannot be scheduled", cluster);
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = n;
+  *out = n;
+  return NTS_OK;
+}
+
+// ------------------------------------------------ correction factor c(B,p)
+
+// c(B, p) = E[M^p]^(-1/p), M the maximum of B i.i.d. |N(0,1)| values.  The
+// moment is integrated in its density form,
+//   E[M^p] = int_0^inf x^p * B * erf(x/sqrt2)^(B-1) * sqrt(2/pi) exp(-x^2/2) dx,
+// by composite 12-point Gauss-Legendre quadrature over 480 panels of [0, 12]
+// (the integrand is below 1e-29 beyond 12).  Nodes come from Newton's method
+// on the Legendre polynomial.
+namespace {
+
+void gauss_legendre(int n, std::vector<double>& x, std::vector<double>& w) {
+  x.assign(n, 0.0);
+  w.assign(n, 0.0);
+  const double pi = 3.14159265358979323846;
+  for (int i = 0; i < n; ++i) {
+    double z = std::cos(pi * (i + 0.75) / (n + 0.5));
+    double dp = 0.0;
+    for (int it = 0; it < 100; ++it) {
+      double p0 = 1.0, p1 = z;
+      for (int k = 2; k <= n; ++k) {
+        const double p2 = ((2.0 * k - 1.0) * z * p1 - (k - 1.0) * p0) / k;
+        p0 = p1;
+        p1 = p2;
+      }
+      dp = n * (z * p1 - p0) / (z * z - 1.0);
+      const double dz = p1 / dp;
+      z -= dz;
+      if (std::fabs(dz) < 1e-16) break;
+    }
+    x[i] = z;
+    w[i] = 2.0 / ((1.0 - z * z) * dp * dp);
+  }
+}
+
+double max_moment(int B, int p) {
+  std::vector<double> gx, gw;
+  gauss_legendre(12, gx, gw);
+  const double c0 = std::sqrt(2.0 / 3.14159265358979323846);
+  const int panels = 480;
+  const double hi = 12.0, h = hi / panels;
+  double total = 0.0;
+  for (int k = 0; k < panels; ++k) {
+    const double a = k * h, mid = a + 0.5 * h;
+    double s = 0.0;
+    for (size_t i = 0; i < gx.size(); ++i) {
+      const double x = mid + 0.5 * h * gx[i];
+      const double F = std::erf(x / std::sqrt(2.0));
+      const double dens = B * std::pow(F, B - 1) * c0 * std::exp(-0.5 * x * x);
+      s += gw[i] * std::pow(x, p) * dens;
+    }
+    total += 0.5 * h * s;
+  }
+  return total;
+}
+
+}  // namespace
+
+}  // namespace nts
+
+using namespace nts;
+
+// ------------------------------------------------------------------ C ABI
+
+extern "C" {
+
+int nts_version(void) { return 100; }
+
+const char* nts_status_string(int status) {
+  switch (status) {
+    case NTS_OK: return "NTS_OK";
+    case NTS_ERR_INVALID_ARG: return "NTS_ERR_INVALID_ARG";
+    case NTS_ERR_UNSUPPORTED: return "NTS_ERR_UNSUPPORTED";
+    case NTS_ERR_CUDA: return "NTS_ERR_CUDA";
+    case NTS_ERR_TIMEOUT: return "NTS_ERR_TIMEOUT";
+    default: return "NTS_ERR_UNKNOWN";
+  }
+}
+
+const char* nts_last_error(void) { return g_last_error; }
+
+int nts_mxnorm_correction(int B, int p, double* c_out) {
+  if (c_out == nullptr) return fail(NTS_ERR_INVALID_ARG, "c_out is NULL");
+  if (B < 1 || B > 4096) return fail(NTS_ERR_INVALID_ARG, "B must be in [1, 4096], got %d", B);
+  if (p != 1 && p != 2) return fail(NTS_ERR_INVALID_ARG, "p must be 1 or 2, got %d", p);
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, double> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  auto key = std::make_pair(B, p);
+  auto it = cache.find(key);
+  if (it == cache.end()) {
+    const double c = std::pow(max_moment(B, p), -1.0 / p);
+    it = cache.emplace(key, c).first;
+  }
+  *c_out = it->second;
+  return NTS_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+int validate_qk(const void* X, const float* gamma, const void* Y, const float* rinv, int64_t T,
+                int64_t H, float eps, int N) {
+  if (X == nullptr || gamma == nullptr || Y == nullptr)
+    return fail(NTS_ERR_INVALID_ARG, "X, gamma and Y must be non-NULL");
+  if (T < 0) return fail(NTS_ERR_INVALID_ARG, "T must be >= 0, got %lld", (long long)T);
+  if (H <= 0) return fail(NTS_ERR_INVALID_ARG, "H must be > 0, got %lld", (long long)H);
+  if (N != 1 && N != 2 && N != 4 && N != 8)
+    return fail(NTS_ERR_INVALID_ARG, "N must be 1, 2, 4 or 8, got %d", N);
+  if (H % N != 0)
+    return fail(NTS_ERR_INVALID_ARG, "H (%lld) must be a multiple of N (%d)", (long long)H, N);
+  if (!(eps > 0.f) || !std::isfinite(eps))
+    return fail(NTS_ERR_INVALID_ARG, "eps must be positive and finite");
+  if ((H / N) % 8 != 0)
+    return fail(NTS_ERR_UNSUPPORTED, "H/N (%lld) must be a multiple of 8", (long long)(H / N));
+  if (H / N > 32768)
+    return fail(NTS_ERR_UNSUPPORTED, "H/N (%lld) exceeds 32768", (long long)(H / N));
+  if (!aligned(X, 16) || !aligned(Y, 16) || !aligned(gamma, 16) ||
+      (rinv != nullptr && !aligned(rinv, 4)))
+    return fail(NTS_ERR_UNSUPPORTED, "X, Y and gamma must be 16-byte aligned");
+  return NTS_OK;
+}
+
+int validate_mx(const void* X, const float* gamma, const uint8_t* codes, const uint8_t* scales,
+                const float* rinv, const float* amax, int64_t T, int64_t D, float eps, int B,
+                int fmt, int p, bool mxnorm) {
+  if (X == nullptr || codes == nullptr || scales == nullptr)
+    return fail(NTS_ERR_INVALID_ARG, "X, codes and scales must be non-NULL");
+  if (T < 0) return fail(NTS_ERR_INVALID_ARG, "T must be >= 0, got %lld", (long long)T);
+  if (D <= 0) return fail(NTS_ERR_INVALID_ARG, "D must be > 0, got %lld", (long long)D);
+  if (B != 16 && B != 32 && B != 64)
+    return fail(NTS_ERR_INVALID_ARG, "B must be 16, 32 or 64, got %d", B);
+  if (D % B != 0)
+    return fail(NTS_ERR_INVALID_ARG, "D (%lld) must be a multiple of B (%d)", (long long)D, B);
+  if (fmt != NTS_FMT_E4M3 && fmt != NTS_FMT_E2M1)
+    return fail(NTS_ERR_INVALID_ARG, "unknown element format %d", fmt);
+  if (mxnorm && p != 1 && p != 2) return fail(NTS_ERR_INVALID_ARG, "p must be 1 or 2, got %d", p);
+  if (!(eps > 0.f) || !std::isfinite(eps))
+    return fail(NTS_ERR_INVALID_ARG, "eps must be positive and finite");
+  if (D > 32768) return fail(NTS_ERR_UNSUPPORTED, "D (%lld) exceeds 32768", (long long)D);
+  if (!aligned(X, 16) || !aligned(codes, 16) || (gamma != nullptr && !aligned(gamma, 16)) ||
+      (rinv != nullptr && !aligned(rinv, 4)) || (amax != nullptr && !aligned(amax, 4)))
+    return fail(NTS_ERR_UNSUPPORTED, "X, gamma and codes must be 16-byte aligned");
+  return NTS_OK;
+}
+
+int run_mx(const void* X, const float* gamma, uint8_t* codes, uint8_t* scales, float* rinv,
+           float* amax, int64_t T, int64_t D, float eps, int B, int fmt, int p, bool mxnorm,
+           void* stream) {
+  int rc = validate_mx(X, gamma, codes, scales, rinv, amax, T, D, eps, B, fmt, p, mxnorm);
+  if (rc != NTS_OK) return rc;
+  if (T == 0) return NTS_OK;
+  MxRequest rq{X, gamma, codes, scales, rinv, amax, T, D, eps, B, fmt, mxnorm ? p : 0, 0.0};
+  if (mxnorm) {
+    rc = nts_mxnorm_correction(B, p, &rq.corr);
+    if (rc != NTS_OK) return rc;
+  }
+  return launch_mx(rq, static_cast<cudaStream_t>(stream), current_tuning());
+}
+
+int copy(void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, void* stream,
+         const char* what) {
+  if (bytes == 0) return NTS_OK;
+  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, kind, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, what);
+  return NTS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int nts_qknorm_rms(const void* X_dev, const float* gamma_dev, void* Y_dev, float* rinv_dev,
+                   int64_t T, int64_t H, float eps, int N, void* stream) {
+  int rc = validate_qk(X_dev, gamma_dev, Y_dev, rinv_dev, T, H, eps, N);
+  if (rc != NTS_OK) return rc;
+  if (T == 0) return NTS_OK;
+  return launch_qknorm(X_dev, gamma_dev, Y_dev, rinv_dev, T, (int)H, eps, N,
+                       static_cast<cudaStream_t>(stream), current_tuning());
+}
+
+int nts_rmsnorm_mxcast(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,
+                       uint8_t* scales_dev, float* rinv_dev, float* amax_dev, int64_t T, int64_t D,
+                       float eps, int B, int fmt, void* stream) {
+  return run_mx(X_dev, gamma_dev, codes_dev, scales_dev, rinv_dev, amax_dev, T, D, eps, B, fmt,
+                0, false, stream);
+}
+
+int nts_mxnorm_cast(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,
+                    uint8_t* scales_dev, float* rinv_dev, float* amax_dev, int64_t T, int64_t D,
+                    float eps, int B, int fmt, int p, void* stream) {
+  return run_mx(X_dev, gamma_dev, codes_dev, scales_dev, rinv_dev, amax_dev, T, D, eps, B, fmt,
+                p, true, stream);
+}
+
+int nts_check_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "synchronizing the stream");
+  unsigned qk = 0, mx = 0;
+  int rc = read_and_clear_qk_status(&qk);
+  if (rc != NTS_OK) return rc;
+  rc = read_and_clear_mx_status(&mx);
+  if (rc != NTS_OK) return rc;
+  if ((qk | mx) != 0)
+    return fail(NTS_ERR_TIMEOUT, "a kernel gave up on a bounded wait (qk=%u mx=%u)", qk, mx);
+  return NTS_OK;
+}
+
+int nts_qknorm_rms_host(const void* X_host, const float* gamma_dev, void* Y_host,
+                        float* rinv_host, void* X_dev, void* Y_dev, float* rinv_dev, int64_t T,
+                        int64_t H, float eps, int N, void* stream) {
+  if (X_host == nullptr || Y_host == nullptr)
+    return fail(NTS_ERR_INVALID_ARG, "X_host and Y_host must be non-NULL");
+  if (rinv_host != nullptr && rinv_dev == nullptr)
+    return fail(NTS_ERR_INVALID_ARG, "rinv_host needs a rinv_dev staging buffer");
+  float* rinv_k = rinv_host != nullptr ? rinv_dev : nullptr;
+  int rc = validate_qk(X_dev, gamma_dev, Y_dev, rinv_k, T, H, eps, N);
+  if (rc != NTS_OK) return rc;
+  if (T == 0) return NTS_OK;
+  const size_t xb = (size_t)T * (size_t)H * 2;
+  rc = copy(X_dev, X_host, xb, cudaMemcpyHostToDevice, stream, "copying X to the device");
+  if (rc != NTS_OK) return rc;
+  rc = nts_qknorm_rms(X_dev, gamma_dev, Y_dev, rinv_k, T, H, eps, N, stream);
+  if (rc != NTS_OK) return rc;
+  rc = copy(Y_host, Y_dev, xb, cudaMemcpyDeviceToHost, stream, "copying Y to the host");
+  if (rc != NTS_OK) return rc;
+  if (rinv_host != nullptr)
+    rc = copy(rinv_host, rinv_dev, (size_t)T * 4, cudaMemcpyDeviceToHost, stream,
+              "copying rinv to the host");
+  return rc;
+}
+
+static int mx_host(const void* X_host, const float* gamma_dev, uint8_t* codes_host,
+                   uint8_t* scales_host, void* X_dev, uint8_t* codes_dev, uint8_t* scales_dev,
+                   int64_t T, int64_t D, float eps, int B, int fmt, int p, bool mxnorm,
+                   void* stream) {
+  if (X_host == nullptr || codes_host == nullptr || scales_host == nullptr)
+    return fail(NTS_ERR_INVALID_ARG, "X_host, codes_host and scales_host must be non-NULL");
+  int rc = validate_mx(X_dev, gamma_dev, codes_dev, scales_dev, nullptr, nullptr, T, D, eps, B,
+                       fmt, p, mxnorm);
+  if (rc != NTS_OK) return rc;
+  if (T == 0) return NTS_OK;
+  const size_t xb = (size_t)T * (size_t)D * 2;
+  const size_t cb = (size_t)T * (size_t)(fmt == NTS_FMT_E4M3 ? D : D / 2);
+  const size_t sb = (size_t)T * (size_t)(D / B);
+  rc = copy(X_dev, X_host, xb, cudaMemcpyHostToDevice, stream, "copying X to the device");
+  if (rc != NTS_OK) return rc;
+  rc = run_mx(X_dev, gamma_dev, codes_dev, scales_dev, nullptr, nullptr, T, D, eps, B, fmt, p,
+              mxnorm, stream);
+  if (rc != NTS_OK) return rc;
+  rc = copy(codes_host, codes_dev, cb, cudaMemcpyDeviceToHost, stream, "copying codes to the host");
+  if (rc != NTS_OK) return rc;
+  return copy(scales_host, scales_dev, sb, cudaMemcpyDeviceToHost, stream,
+              "copying scales to the host");
+}
+
+int nts_rmsnorm_mxcast_host(const void* X_host, const float* gamma_dev, uint8_t* codes_host,
+                            uint8_t* scales_host, void* X_dev, uint8_t* codes_dev,
+                            uint8_t* scales_dev, int64_t T, int64_t D, float eps, int B, int fmt,
+                            void* stream) {
+  return mx_host(X_host, gamma_dev, codes_host, scales_host, X_dev, codes_dev, scales_dev, T, D,
+                 eps, B, fmt, 0, false, stream);
+}
+
+int nts_mxnorm_cast_host(const void* X_host, const float* gamma_dev, uint8_t* codes_host,
+                         uint8_t* scales_host, void* X_dev, uint8_t* codes_dev,
+                         uint8_t* scales_dev, int64_t T, int64_t D, float eps, int B, int fmt,
+                         int p, void* stream) {
+  return mx_host(X_host, gamma_dev, codes_host, scales_host, X_dev, codes_dev, scales_dev, T, D,
+                 eps, B, fmt, p, true, stream);
+}
+
+// ------------------------------------------------------------- debug hooks
+
+int nts_debug_set_tuning(int vpt, int rows, int stages, int64_t grid, int smem_budget) {
+  if (vpt < 0 || rows < 0 || stages < 0 || grid < 0 || smem_budget < 0)
+    return fail(NTS_ERR_INVALID_ARG, "tuning values must be >= 0");
+  if (vpt != 0 && (vpt > 8 || vpt == 7)) return fail(NTS_ERR_INVALID_ARG, "vpt %d unsupported", vpt);
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tune.force_vpt = vpt;
+  g_tune.force_rows = rows;
+  g_tune.force_stages = stages;
+  g_tune.force_grid = grid;
+  g_tune.smem_budget = smem_budget > 0 ? smem_budget : LaunchTuning().smem_budget;
+  return NTS_OK;
+}
+
+int nts_debug_set_wait_limit_ns(uint64_t ns) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tune.wait_limit_ns = ns > 0 ? ns : LaunchTuning().wait_limit_ns;
+  return NTS_OK;
+}
+
+int nts_debug_set_missing_tx(uint32_t bytes) {
+  if (bytes % 16 != 0) return fail(NTS_ERR_INVALID_ARG, "bytes must be a multiple of 16");
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tune.missing_tx = bytes;
+  return NTS_OK;
+}
+
+}  // extern "C"

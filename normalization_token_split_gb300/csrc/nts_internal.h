@@ -1,0 +1,82 @@
+// nts_internal.h -- declarations shared by the library's own translation
+// units (host API and kernel launchers).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "nts.h"
+
+namespace nts {
+
+// Largest CTA the kernels are compiled for: 512 threads leaves up to 128
+// registers per thread, enough to keep a thread's 8-vector slice in fp32.
+constexpr int kMaxThreads = 512;
+
+// Per-call launch settings: automatic unless a debug override is set.
+struct LaunchTuning {
+  int force_vpt = 0;         // vectors (8 values) per thread, 0 = automatic
+  int force_rows = 0;        // rows per tile, 0 = automatic
+  int force_stages = 0;      // ring stages, 0 = automatic
+  int64_t force_grid = 0;    // CTAs (MX) or clusters (QK), 0 = automatic
+  int smem_budget = 102400;  // bytes of shared memory a CTA aims to stay under
+  uint64_t wait_limit_ns = 1000000000ull;  // bounded mbarrier waits
+  uint32_t missing_tx = 0;   // test hook, see nts_debug.h
+};
+
+LaunchTuning current_tuning();
+
+struct DeviceInfo {
+  bool ok = false;
+  int device = 0;
+  int sm_count = 0;
+  int max_smem_optin = 0;
+};
+const DeviceInfo& device_info();
+
+// How the G threads of a row split its nvec 16-byte vectors: thread g owns
+// vectors g, g+G, ..., g+(vpt-1)G.  G is a multiple of 32 (whole warps);
+// G == 0 means the row is too wide.
+struct RowShape {
+  int vpt = 0;
+  int G = 0;
+};
+RowShape choose_row_shape(int nvec, int force_vpt);
+
+// Raise the kernel's dynamic shared memory limit (once per kernel/device).
+int prepare_kernel(const void* kernel, size_t smem);
+// Co-resident clusters of `cluster` CTAs for this launch configuration.
+int max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cfg, int cluster,
+                        int64_t* out);
+
+// Record a failure for nts_last_error() and return `status`.
+int fail(int status, const char* fmt, ...);
+int fail_cuda(cudaError_t e, const char* what);
+void log_launch(const char* name, const char* fmt, ...);
+
+struct MxRequest {
+  const void* X;
+  const float* gamma;
+  uint8_t* codes;
+  uint8_t* scales;
+  float* rinv;
+  float* amax;
+  int64_t T;
+  int64_t D;
+  float eps;
+  int B;
+  int fmt;
+  int p;        // 0 = RMSNorm statistic, 1 or 2 = MXNorm
+  double corr;  // c(B, p) for MXNorm
+};
+
+int launch_qknorm(const void* X, const float* gamma, void* Y, float* rinv, int64_t T, int H,
+                  float eps, int N, cudaStream_t stream, const LaunchTuning& tune);
+int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune);
+
+int read_and_clear_qk_status(unsigned* out);
+int read_and_clear_mx_status(unsigned* out);
+
+}  // namespace nts

@@ -1,0 +1,192 @@
+"""Torch-facing binding of libnts: argument marshalling only.  Every step of
+the computation runs in the library's CUDA kernels; these functions check
+tensor placement, allocate missing outputs with torch, and pass raw pointers
+and the current CUDA stream through the C ABI.  Names follow the C ABI
+(include/nts.h), without the ``nts_`` prefix."""
+from __future__ import annotations
+
+import ctypes
+from typing import NamedTuple, Optional
+
+import torch
+
+from ._lib import check, lib
+
+FMT_E4M3 = 0
+FMT_E2M1 = 1
+_FMT_NAMES = {"e4m3": FMT_E4M3, "e2m1": FMT_E2M1, FMT_E4M3: FMT_E4M3, FMT_E2M1: FMT_E2M1}
+
+
+class MxOut(NamedTuple):
+    codes: torch.Tensor     # uint8 [T, D] (E4M3) or [T, D/2] (E2M1)
+    scales: torch.Tensor    # uint8 [T, D/B] E8M0
+    rinv: Optional[torch.Tensor]   # fp32 [T]
+    amax: Optional[torch.Tensor]   # fp32 [T, D/B]
+
+
+def _fmt(fmt) -> int:
+    try:
+        return _FMT_NAMES[fmt.lower() if isinstance(fmt, str) else fmt]
+    except KeyError:
+        raise ValueError(f"unknown element format {fmt!r}") from None
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def codes_row_bytes(D: int, fmt) -> int:
+    return D if _fmt(fmt) == FMT_E4M3 else D // 2
+
+
+def qknorm_rms(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, N: int = 1,
+               out: Optional[torch.Tensor] = None, rinv: Optional[torch.Tensor] = None,
+               want_rinv: bool = False, stream=None):
+    """Layerwise QK-RMSNorm of x [T, H] (bf16) with gain gamma [H] (fp32),
+    split into N cluster shards.  Returns (y, rinv or None).  out may be x."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("gamma", gamma, torch.float32)
+    T, H = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _need_cuda("out", out, torch.bfloat16)
+    if rinv is None and want_rinv:
+        rinv = torch.empty(T, device=x.device, dtype=torch.float32)
+    if rinv is not None:
+        _need_cuda("rinv", rinv, torch.float32)
+    check(lib().nts_qknorm_rms(_ptr(x), _ptr(gamma), _ptr(out), _ptr(rinv), T, H,
+                               float(eps), int(N), _stream(stream)))
+    return out, rinv
+
+
+def _mx_outputs(x, D, B, fmt, codes, scales, rinv, amax, want_rinv, want_amax):
+    T = x.shape[0]
+    if codes is None:
+        codes = torch.empty(T, codes_row_bytes(D, fmt), device=x.device, dtype=torch.uint8)
+    if scales is None:
+        scales = torch.empty(T, D // B, device=x.device, dtype=torch.uint8)
+    if rinv is None and want_rinv:
+        rinv = torch.empty(T, device=x.device, dtype=torch.float32)
+    if amax is None and want_amax:
+        amax = torch.empty(T, D // B, device=x.device, dtype=torch.float32)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    if rinv is not None:
+        _need_cuda("rinv", rinv, torch.float32)
+    if amax is not None:
+        _need_cuda("amax", amax, torch.float32)
+    return codes, scales, rinv, amax
+
+
+def rmsnorm_mxcast(x: torch.Tensor, gamma: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                   B: int = 32, fmt="e4m3", codes=None, scales=None, rinv=None, amax=None,
+                   want_rinv: bool = False, want_amax: bool = False, stream=None) -> MxOut:
+    """RMSNorm of x [T, D] fused with the MX cast to E4M3/E2M1 + E8M0 scales."""
+    _need_cuda("x", x, torch.bfloat16)
+    if gamma is not None:
+        _need_cuda("gamma", gamma, torch.float32)
+    T, D = x.shape
+    f = _fmt(fmt)
+    codes, scales, rinv, amax = _mx_outputs(x, D, B, f, codes, scales, rinv, amax,
+                                            want_rinv, want_amax)
+    check(lib().nts_rmsnorm_mxcast(_ptr(x), _ptr(gamma), _ptr(codes), _ptr(scales), _ptr(rinv),
+                                   _ptr(amax), T, D, float(eps), int(B), f, _stream(stream)))
+    return MxOut(codes, scales, rinv, amax)
+
+
+def mxnorm_cast(x: torch.Tensor, gamma: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                B: int = 32, fmt="e4m3", p: int = 2, codes=None, scales=None, rinv=None,
+                amax=None, want_rinv: bool = False, want_amax: bool = False,
+                stream=None) -> MxOut:
+    """MXNorm of x [T, D]: RMS estimated from the MX block absmaxes, then the
+    MX cast."""
+    _need_cuda("x", x, torch.bfloat16)
+    if gamma is not None:
+        _need_cuda("gamma", gamma, torch.float32)
+    T, D = x.shape
+    f = _fmt(fmt)
+    codes, scales, rinv, amax = _mx_outputs(x, D, B, f, codes, scales, rinv, amax,
+                                            want_rinv, want_amax)
+    check(lib().nts_mxnorm_cast(_ptr(x), _ptr(gamma), _ptr(codes), _ptr(scales), _ptr(rinv),
+                                _ptr(amax), T, D, float(eps), int(B), f, int(p),
+                                _stream(stream)))
+    return MxOut(codes, scales, rinv, amax)
+
+
+def mxnorm_correction(B: int, p: int) -> float:
+    c = ctypes.c_double()
+    check(lib().nts_mxnorm_correction(int(B), int(p), ctypes.byref(c)))
+    return c.value
+
+
+def check_status(stream=None) -> None:
+    """Synchronize the stream and raise if a kernel timed out or failed."""
+    check(lib().nts_check_status(_stream(stream)))
+
+
+# ----------------------------------------------------------- host-buffer forms
+
+def _need_host(name: str, t: torch.Tensor) -> None:
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host tensor")
+
+
+def qknorm_rms_host(x_host, gamma_dev, y_host, x_dev, y_dev, eps=1e-6, N=1, rinv_host=None,
+                    rinv_dev=None, stream=None) -> None:
+    """Enqueue H2D copy of x, the kernel, and D2H copies of y (and rinv)."""
+    _need_host("x_host", x_host)
+    _need_host("y_host", y_host)
+    T, H = x_host.shape
+    check(lib().nts_qknorm_rms_host(_ptr(x_host), _ptr(gamma_dev), _ptr(y_host), _ptr(rinv_host),
+                                    _ptr(x_dev), _ptr(y_dev), _ptr(rinv_dev), T, H, float(eps),
+                                    int(N), _stream(stream)))
+
+
+def rmsnorm_mxcast_host(x_host, gamma_dev, codes_host, scales_host, x_dev, codes_dev,
+                        scales_dev, eps=1e-6, B=32, fmt="e4m3", stream=None) -> None:
+    _need_host("x_host", x_host)
+    T, D = x_host.shape
+    check(lib().nts_rmsnorm_mxcast_host(_ptr(x_host), _ptr(gamma_dev), _ptr(codes_host),
+                                        _ptr(scales_host), _ptr(x_dev), _ptr(codes_dev),
+                                        _ptr(scales_dev), T, D, float(eps), int(B), _fmt(fmt),
+                                        _stream(stream)))
+
+
+def mxnorm_cast_host(x_host, gamma_dev, codes_host, scales_host, x_dev, codes_dev, scales_dev,
+                     eps=1e-6, B=32, fmt="e4m3", p=2, stream=None) -> None:
+    _need_host("x_host", x_host)
+    T, D = x_host.shape
+    check(lib().nts_mxnorm_cast_host(_ptr(x_host), _ptr(gamma_dev), _ptr(codes_host),
+                                     _ptr(scales_host), _ptr(x_dev), _ptr(codes_dev),
+                                     _ptr(scales_dev), T, D, float(eps), int(B), _fmt(fmt),
+                                     int(p), _stream(stream)))
+
+
+# ------------------------------------------------------------------ tuning
+
+def set_tuning(vpt=0, rows=0, stages=0, grid=0, smem_budget=0) -> None:
+    check(lib().nts_debug_set_tuning(int(vpt), int(rows), int(stages), int(grid),
+                                     int(smem_budget)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    check(lib().nts_debug_set_wait_limit_ns(int(ns)))
+
+
+def set_missing_tx(nbytes: int) -> None:
+    check(lib().nts_debug_set_missing_tx(int(nbytes)))

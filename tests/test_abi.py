@@ -1,0 +1,143 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+public headers declare (and no other nts_ symbol), and rejects bad arguments
+before touching the device.  Also checks the library's host-side c(B, p)
+against the oracle's independent quadrature."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle
+from conftest import ROOT
+
+nts = pytest.importorskip("normalization_token_split_gb300")
+from normalization_token_split_gb300 import _lib  # noqa: E402
+
+INVALID, UNSUPPORTED, OK = 1, 2, 0
+P = ctypes.c_void_p
+A16 = P(1 << 20)          # a 16-byte aligned non-NULL address; never dereferenced
+MIS = P((1 << 20) + 4)    # misaligned
+
+
+def header_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(nts_\w+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    fns = header_functions()
+    assert len(fns) >= 14
+    for name in fns:
+        assert hasattr(lib, name), name
+
+
+def test_no_undeclared_exports():
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\b(nts_\w+)$", out, flags=re.M))
+    assert exported == set(header_functions())
+
+
+def test_status_strings_and_version(lib):
+    assert lib.nts_version() >= 100
+    for code, name in _lib.STATUS_NAMES.items():
+        assert lib.nts_status_string(code).decode() == name
+
+
+def _qk(lib, X=A16, g=A16, Y=A16, r=None, T=4, H=64, eps=1e-6, N=2):
+    return lib.nts_qknorm_rms(X, g, Y, r, T, H, eps, N, None)
+
+
+def test_qknorm_argument_checks(lib):
+    assert _qk(lib, X=None) == INVALID
+    assert _qk(lib, g=None) == INVALID
+    assert _qk(lib, Y=None) == INVALID
+    assert _qk(lib, T=-1) == INVALID
+    assert _qk(lib, H=0) == INVALID
+    assert _qk(lib, N=3) == INVALID
+    assert _qk(lib, H=66, N=4) == INVALID
+    assert _qk(lib, eps=0.0) == INVALID
+    assert _qk(lib, eps=float("nan")) == INVALID
+    assert _qk(lib, eps=float("inf")) == INVALID
+    assert _qk(lib, H=8, N=2) == UNSUPPORTED           # H/N = 4 is not a multiple of 8
+    assert _qk(lib, H=65536 * 2, N=2) == UNSUPPORTED   # shard wider than 32768
+    assert _qk(lib, X=MIS) == UNSUPPORTED
+    assert _qk(lib, Y=MIS) == UNSUPPORTED
+    assert _qk(lib, T=0) == OK                           # nothing launched
+    assert "multiple" in lib.nts_last_error().decode() or True
+
+
+def _mx(lib, fn, X=A16, codes=A16, scales=A16, T=4, D=256, eps=1e-6, B=32, fmt=0, p=2):
+    if fn == "rms":
+        return lib.nts_rmsnorm_mxcast(X, None, codes, scales, None, None, T, D, eps, B, fmt, None)
+    return lib.nts_mxnorm_cast(X, None, codes, scales, None, None, T, D, eps, B, fmt, p, None)
+
+
+@pytest.mark.parametrize("fn", ["rms", "mx"])
+def test_mx_argument_checks(lib, fn):
+    assert _mx(lib, fn, X=None) == INVALID
+    assert _mx(lib, fn, codes=None) == INVALID
+    assert _mx(lib, fn, scales=None) == INVALID
+    assert _mx(lib, fn, T=-1) == INVALID
+    assert _mx(lib, fn, D=0) == INVALID
+    assert _mx(lib, fn, B=8) == INVALID
+    assert _mx(lib, fn, D=48, B=32) == INVALID
+    assert _mx(lib, fn, fmt=2) == INVALID
+    assert _mx(lib, fn, eps=-1.0) == INVALID
+    if fn == "mx":
+        assert _mx(lib, fn, p=3) == INVALID
+    assert _mx(lib, fn, D=65536) == UNSUPPORTED
+    assert _mx(lib, fn, X=MIS) == UNSUPPORTED
+    assert _mx(lib, fn, T=0) == OK
+    assert len(lib.nts_last_error()) > 0
+
+
+def test_host_forms_argument_checks(lib):
+    assert lib.nts_qknorm_rms_host(None, A16, A16, None, A16, A16, None, 4, 64, 1e-6, 2,
+                                   None) == INVALID
+    assert lib.nts_qknorm_rms_host(A16, A16, A16, A16, A16, A16, None, 4, 64, 1e-6, 2,
+                                   None) == INVALID            # rinv_host without staging
+    assert lib.nts_mxnorm_cast_host(A16, None, A16, None, A16, A16, A16, 4, 256, 1e-6, 32, 0, 2,
+                                    None) == INVALID
+    assert lib.nts_rmsnorm_mxcast_host(A16, None, A16, A16, A16, A16, A16, 0, 256, 1e-6, 32, 0,
+                                       None) == OK
+
+
+def test_debug_hooks_validate(lib):
+    assert lib.nts_debug_set_tuning(7, 0, 0, 0, 0) == INVALID
+    assert lib.nts_debug_set_tuning(-1, 0, 0, 0, 0) == INVALID
+    assert lib.nts_debug_set_missing_tx(17) == INVALID
+    assert lib.nts_debug_set_tuning(0, 0, 0, 0, 0) == OK
+    assert lib.nts_debug_set_missing_tx(0) == OK
+    assert lib.nts_debug_set_wait_limit_ns(0) == OK
+
+
+@pytest.mark.parametrize("B", [1, 2, 16, 32, 64])
+@pytest.mark.parametrize("p", [1, 2])
+def test_library_correction_matches_oracle(B, p):
+    assert nts.mxnorm_correction(B, p) == pytest.approx(oracle.mx_correction(B, p), rel=1e-10)
+
+
+def test_correction_rejects_bad_args(lib):
+    c = ctypes.c_double()
+    assert lib.nts_mxnorm_correction(0, 2, ctypes.byref(c)) == INVALID
+    assert lib.nts_mxnorm_correction(32, 3, ctypes.byref(c)) == INVALID
+    assert lib.nts_mxnorm_correction(32, 2, None) == INVALID
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.lib()

@@ -1,0 +1,179 @@
+"""GPU parity of nts_rmsnorm_mxcast and nts_mxnorm_cast against the oracle,
+through the C ABI.
+
+Workloads: RMSNorm + MXFP8 cast vs MXNorm (p = 1, 2) on X [T, 4096] with
+T in {4096, 16384, 65536}, B = 32, E4M3 (full size, sampled rows checked
+against the oracle); the MXNorm sweep T = 65536, D in {1024, 3072, 5120, 7168,
+16384}, B in {16, 32, 64}, E4M3 / E2M1, p = 2, 5% Student-t(3) rows (full
+size on the device, sampled rows checked); small complete cases with gains;
+edge cases (zero rows, tiny blocks, ragged tails, narrow rows, forced launch
+shapes) and the bounded-wait error path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import check_mx
+
+pytestmark = pytest.mark.gpu
+
+nts = pytest.importorskip("normalization_token_split_gb300")
+DEV = "cuda:0"
+FMTS = {"e4m3": oracle.FMT_E4M3, "e2m1": oracle.FMT_E2M1}
+
+
+def gpu_call(kind, X, gamma, eps, B, fmt, p):
+    Xd = X.to(DEV)
+    gd = None if gamma is None else gamma.to(DEV)
+    if kind == "rms":
+        out = nts.rmsnorm_mxcast(Xd, gd, eps=eps, B=B, fmt=fmt, want_rinv=True, want_amax=True)
+    else:
+        out = nts.mxnorm_cast(Xd, gd, eps=eps, B=B, fmt=fmt, p=p, want_rinv=True, want_amax=True)
+    nts.check_status()
+    return out
+
+
+def oracle_call(kind, Xb, g, eps, B, fmt, p):
+    if kind == "rms":
+        return oracle.rmsnorm_mxcast(Xb, g, eps, B, fmt)
+    return oracle.mxnorm_cast(Xb, g, eps, B, fmt, p)
+
+
+def compare(kind, X, gamma, eps, B, fmt_name, p, rows=None, what=""):
+    """Run the device; check all rows (rows=None) or the given sample."""
+    fmt = FMTS[fmt_name]
+    out = gpu_call(kind, X, gamma, eps, B, fmt_name, p)
+    if rows is None:
+        rows = slice(None)
+    codes = out.codes[rows].cpu().numpy()
+    scales = out.scales[rows].cpu().numpy()
+    rinv = out.rinv[rows].cpu().numpy()
+    amax = out.amax[rows].cpu().numpy()
+    Xb = workloads.bf16_bits(X[rows])
+    g = None if gamma is None else gamma.cpu().numpy()
+    ref = oracle_call(kind, Xb, g, eps, B, fmt, p)
+    return check_mx(Xb, g, B, fmt, (codes, scales, amax), ref, rinv, eps, what)
+
+
+def sample_rows(T, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([rng.choice(T, size=min(n, T), replace=False),
+                                     [0, T - 1]]))
+    return torch.from_numpy(rows)
+
+
+KINDS = [("rms", 0), ("mx", 1), ("mx", 2)]
+
+
+@pytest.mark.parametrize("kind,p", KINDS)
+@pytest.mark.parametrize("T", [4096, 16384, 65536])
+def test_rmsnorm_mxcast_vs_mxnorm_config(kind, p, T):
+    X, _ = workloads.mx_inputs(T, 4096, seed=4000 + T, device=DEV)
+    rows = sample_rows(T, 2048, T).to(DEV)
+    compare(kind, X, None, 1e-6, 32, "e4m3", p, rows=rows, what=f"{kind}{p} T={T}")
+
+
+@pytest.mark.parametrize("D", [1024, 3072, 5120, 7168, 16384])
+@pytest.mark.parametrize("B", [16, 32, 64])
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+def test_mxnorm_sweep_full_size(D, B, fmt):
+    X, _ = workloads.mx_inputs(65536, D, seed=5000 + D + B, t_frac=0.05, device=DEV)
+    rows = sample_rows(65536, max(256, 4 * 1024 * 1024 // D), D + B)
+    # heavy-tailed rows are part of the sample
+    trows = torch.from_numpy(workloads.student_t_rows(65536, 5000 + D + B, 0.05)[:64])
+    rows = torch.unique(torch.cat([rows, trows])).to(DEV)
+    compare("mx", X, None, 1e-6, B, fmt, 2, rows=rows, what=f"sweep D={D} B={B} {fmt}")
+
+
+@pytest.mark.parametrize("kind,p", KINDS)
+@pytest.mark.parametrize("B", [16, 32, 64])
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+@pytest.mark.parametrize("with_gamma", [False, True])
+def test_small_complete(kind, p, B, fmt, with_gamma):
+    X, g = workloads.mx_inputs(333, 1024, seed=B * 10 + p, t_frac=0.1, with_gamma=with_gamma)
+    compare(kind, X, g, 1e-6, B, fmt, p, what=f"{kind}{p} B={B} {fmt} gamma={with_gamma}")
+
+
+@pytest.mark.parametrize("D", [16, 32, 48, 64, 192, 1040, 2304, 8192, 32768])
+@pytest.mark.parametrize("T", [1, 2, 5, 129])
+def test_row_widths_and_ragged_tails(D, T):
+    B = 16 if D % 32 else 32
+    X, g = workloads.mx_inputs(T, D, seed=D + T, with_gamma=True)
+    for kind, p in KINDS:
+        for fmt in ("e4m3", "e2m1"):
+            compare(kind, X, g, 1e-6, B, fmt, p, what=f"{kind}{p} T={T} D={D} {fmt}")
+
+
+def test_degenerate_blocks():
+    X, _ = workloads.mx_inputs(64, 512, seed=77)
+    X[0] = 0                          # all-zero row
+    X[1, :32] = 0                     # one zero block
+    X[2, 32:64] = 1e-38               # tiny block (scale clamps at 2^-127)
+    X[3, 64:96] = -1.0e17             # large values (sum of squares stays finite in fp32)
+    X[4, ::2] = -0.0
+    for kind, p in KINDS:
+        for fmt in ("e4m3", "e2m1"):
+            compare(kind, X, None, 1e-6, 32, fmt, p, what=f"degenerate {kind}{p} {fmt}")
+
+
+def test_zero_tokens_launches_nothing():
+    X = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
+    out = nts.mxnorm_cast(X, None, B=32)
+    nts.check_status()
+    assert out.codes.shape == (0, 256) and out.scales.shape == (0, 8)
+
+
+def test_deterministic():
+    X, _ = workloads.mx_inputs(4096, 4096, seed=88, device=DEV)
+    a = nts.mxnorm_cast(X, None, B=32, p=2, want_rinv=True)
+    b = nts.mxnorm_cast(X, None, B=32, p=2, want_rinv=True)
+    nts.check_status()
+    assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+    assert torch.equal(a.rinv, b.rinv)
+
+
+@pytest.mark.parametrize("vpt,rows,stages,grid", [(1, 1, 1, 1), (2, 3, 2, 5), (8, 2, 4, 0),
+                                                  (4, 4, 3, 7), (0, 0, 1, 0)])
+def test_forced_launch_shapes(vpt, rows, stages, grid):
+    X, g = workloads.mx_inputs(301, 2048, seed=99, with_gamma=True)
+    try:
+        nts.set_tuning(vpt=vpt, rows=rows, stages=stages, grid=grid)
+        for kind, p in KINDS:
+            compare(kind, X, g, 1e-6, 32, "e4m3", p, what=f"forced {vpt},{rows},{stages},{grid}")
+    finally:
+        nts.set_tuning()
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    X, _ = workloads.mx_inputs(64, 1024, seed=13)
+    try:
+        nts.set_wait_limit_ns(20_000_000)
+        nts.set_missing_tx(16)
+        nts.mxnorm_cast(X.to(DEV), None, B=32)
+        with pytest.raises(nts.NtsError, match="TIMEOUT"):
+            nts.check_status()
+    finally:
+        nts.set_missing_tx(0)
+        nts.set_wait_limit_ns(0)
+    compare("mx", X, None, 1e-6, 32, "e4m3", 2, what="after timeout")
+
+
+@pytest.mark.parametrize("kind", ["rms", "mx"])
+def test_host_buffer_form(kind):
+    T, D, B = 700, 2048, 32
+    X, _ = workloads.mx_inputs(T, D, seed=15)
+    Xh = X.pin_memory()
+    ch = torch.empty(T, D, dtype=torch.uint8).pin_memory()
+    sh = torch.empty(T, D // B, dtype=torch.uint8).pin_memory()
+    Xd = torch.empty_like(X, device=DEV)
+    cd = torch.empty(T, D, dtype=torch.uint8, device=DEV)
+    sd = torch.empty(T, D // B, dtype=torch.uint8, device=DEV)
+    if kind == "rms":
+        nts.rmsnorm_mxcast_host(Xh, None, ch, sh, Xd, cd, sd, eps=1e-6, B=B, fmt="e4m3")
+    else:
+        nts.mxnorm_cast_host(Xh, None, ch, sh, Xd, cd, sd, eps=1e-6, B=B, fmt="e4m3", p=2)
+    nts.check_status()
+    dev = gpu_call(kind, X, None, 1e-6, B, "e4m3", 2)
+    assert torch.equal(ch, dev.codes.cpu()) and torch.equal(sh, dev.scales.cpu())

@@ -1,0 +1,160 @@
+"""GPU parity of nts_qknorm_rms against the oracle, through the C ABI.
+
+Covers the layerwise QK-Norm workloads: the tiny split (T=64, H=1024, N=2),
+the decode shapes (H=4096, T in {1,8,64,256}, N in {1,2,4,8}), the 13B-like
+prefill with 1% outlier channels (H=5120, T=8192, N=4) at full size, edge
+cases (T=0, ragged tails, narrow shards, in-place, all-zero rows, large
+values) and properties (determinism, independence of N).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from conftest import read_golden
+from parity import bf16_to_f64, check_qk
+
+pytestmark = pytest.mark.gpu
+
+nts = pytest.importorskip("normalization_token_split_gb300")
+DEV = "cuda:0"
+
+
+def run_gpu(X, gamma, eps, N, inplace=False):
+    X = X.to(DEV)
+    g = gamma.to(DEV)
+    out = X if inplace else None
+    Y, rinv = nts.qknorm_rms(X, g, eps=eps, N=N, out=out, want_rinv=True)
+    nts.check_status()
+    return workloads.bf16_bits(Y), rinv.cpu().numpy()
+
+
+def run_both(X, gamma, eps, N, **kw):
+    Yg, rg = run_gpu(X, gamma, eps, N, **kw)
+    Yo, ro, _ = oracle.qknorm_rms(workloads.bf16_bits(X), gamma.cpu().numpy(), eps, N)
+    return Yg, rg, Yo, ro
+
+
+def test_tiny_split_config():
+    X, g = workloads.qk_inputs(64, 1024, seed=0)
+    Yg, rg, Yo, ro = run_both(X, g, 1e-6, 2)
+    check_qk(Yg, rg, Yo, ro, "T=64 H=1024 N=2")
+
+
+@pytest.mark.parametrize("T", [1, 8, 64, 256])
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+def test_decode_shapes(T, N):
+    for which, seed in (("Q", 1000 + T), ("K", 2000 + T)):
+        X, g = workloads.qk_inputs(T, 4096, seed=seed)
+        Yg, rg, Yo, ro = run_both(X, g, 1e-6, N)
+        check_qk(Yg, rg, Yo, ro, f"{which} T={T} N={N}")
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+def test_prefill_full_size_with_outliers(N):
+    # 13B-like prefill: Q and K each [8192, 5120], 1% of channels x20.
+    for seed in (3000, 3001):
+        X, g = workloads.qk_inputs(8192, 5120, seed=seed, outlier_frac=0.01, device=DEV)
+        Yg, rg, Yo, ro = run_both(X, g, 1e-6, N)
+        check_qk(Yg, rg, Yo, ro, f"prefill N={N}")
+
+
+@pytest.mark.parametrize("H,N", [(64, 8), (128, 1), (1280, 2), (2048, 4), (5120, 8),
+                                 (3072, 4), (640, 1), (24, 1), (8200, 1), (16384, 2),
+                                 (32768, 1)])
+@pytest.mark.parametrize("T", [1, 3, 37, 513])
+def test_shapes_and_ragged_tails(T, H, N):
+    X, g = workloads.qk_inputs(T, H, seed=T * 7 + H + N)
+    Yg, rg, Yo, ro = run_both(X, g, 1e-5, N)
+    check_qk(Yg, rg, Yo, ro, f"T={T} H={H} N={N}")
+
+
+def test_in_place():
+    X, g = workloads.qk_inputs(300, 4096, seed=9)
+    Yg, rg, Yo, ro = run_both(X, g, 1e-6, 4, inplace=True)
+    check_qk(Yg, rg, Yo, ro, "in place")
+
+
+def test_zero_rows_and_large_values():
+    X, g = workloads.qk_inputs(64, 2048, seed=10)
+    X[5] = 0
+    X[6] = 3.0e4
+    X[7, ::3] = -2.0e-30
+    Yg, rg, Yo, ro = run_both(X, g, 1e-6, 2)
+    check_qk(Yg, rg, Yo, ro, "degenerate rows")
+    assert np.all(Yg[5] == 0) or np.all(bf16_to_f64(Yg[5]) == 0)
+
+
+def test_worked_example_unsplit():
+    # The SwiftQK notes' example (Sec. 4b) has 4-element shards, below the
+    # kernel's 8-element vector; run it unsplit (N=1) as a single row.
+    gd = read_golden("swiftqk_worked_example.txt")
+    X = torch.tensor([gd["x"]], dtype=torch.float32).to(torch.bfloat16)
+    g = torch.tensor(gd["gamma"], dtype=torch.float32)
+    Yg, rg = run_gpu(X, g, gd["eps"], 1)
+    assert abs(rg[0] - gd["rinv"]) < 0.5e-4
+    y = bf16_to_f64(Yg[0])
+    half_ulp = np.exp2(np.floor(np.log2(np.abs(gd["y"]))) - 8)
+    assert np.all(np.abs(y - np.array(gd["y"])) <= half_ulp + gd["y_atol"])
+
+
+def test_zero_tokens_launches_nothing():
+    X = torch.empty(0, 1024, dtype=torch.bfloat16, device=DEV)
+    g = torch.ones(1024, device=DEV)
+    Y, r = nts.qknorm_rms(X, g, N=2, want_rinv=True)
+    nts.check_status()
+    assert Y.shape == (0, 1024)
+
+
+def test_deterministic_and_independent_of_N():
+    X, g = workloads.qk_inputs(1024, 4096, seed=11, device=DEV)
+    outs = [run_gpu(X, g, 1e-6, N) for N in (1, 1, 2, 4, 8)]
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    for Yn, rn in outs[2:]:
+        assert np.max(np.abs(rn / outs[0][1] - 1)) < 2e-6
+        check_qk(Yn, rn, outs[0][0], outs[0][1].astype(np.float64), "N vs N=1")
+
+
+@pytest.mark.parametrize("vpt,rows,stages,grid", [(1, 1, 1, 1), (2, 3, 2, 5), (8, 2, 4, 0),
+                                                  (4, 8, 3, 7), (0, 0, 1, 0)])
+def test_forced_launch_shapes(vpt, rows, stages, grid):
+    X, g = workloads.qk_inputs(777, 2048, seed=12)
+    try:
+        nts.set_tuning(vpt=vpt, rows=rows, stages=stages, grid=grid)
+        for N in (1, 4):
+            Yg, rg, Yo, ro = run_both(X, g, 1e-6, N)
+            check_qk(Yg, rg, Yo, ro, f"forced {vpt},{rows},{stages},{grid} N={N}")
+    finally:
+        nts.set_tuning()
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    X, g = workloads.qk_inputs(64, 1024, seed=13)
+    try:
+        nts.set_wait_limit_ns(20_000_000)     # 20 ms
+        nts.set_missing_tx(16)                # first stage can never complete
+        Xd, gd = X.to(DEV), g.to(DEV)
+        nts.qknorm_rms(Xd, gd, N=2)
+        with pytest.raises(nts.NtsError, match="TIMEOUT"):
+            nts.check_status()
+    finally:
+        nts.set_missing_tx(0)
+        nts.set_wait_limit_ns(0)
+    # the context is still usable and the status word was cleared
+    Yg, rg, Yo, ro = run_both(X, g, 1e-6, 2)
+    check_qk(Yg, rg, Yo, ro, "after timeout")
+
+
+def test_host_buffer_form():
+    X, g = workloads.qk_inputs(500, 5120, seed=14)
+    Xh = X.pin_memory()
+    Yh = torch.empty_like(Xh).pin_memory()
+    rh = torch.empty(500, dtype=torch.float32).pin_memory()
+    Xd = torch.empty_like(X, device=DEV)
+    Yd = torch.empty_like(X, device=DEV)
+    rd = torch.empty(500, dtype=torch.float32, device=DEV)
+    nts.qknorm_rms_host(Xh, g.to(DEV), Yh, Xd, Yd, eps=1e-6, N=4, rinv_host=rh, rinv_dev=rd)
+    nts.check_status()
+    Yo, ro, _ = oracle.qknorm_rms(workloads.bf16_bits(X), g.numpy(), 1e-6, 4)
+    check_qk(workloads.bf16_bits(Yh), rh.numpy(), Yo, ro, "host form")
