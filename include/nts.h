@@ -20,7 +20,8 @@
  *  - Return value: an nts_status.  Nothing is launched when the status is
  *    not NTS_OK, and no call aborts or throws.  nts_last_error() gives a
  *    human-readable detail for the calling thread.
- *  - T == 0 is valid and launches nothing.
+ *  - T == 0 is valid and launches nothing; the data pointers may then be
+ *    NULL (an empty tensor's storage), the other arguments are still checked.
  *
  * Sources (web pages), by title and section:
  *   SwiftQK: Fast and Communication-Efficient Tensor Parallelism for
@@ -87,7 +88,7 @@ NTS_API const char *nts_last_error(void);
  *   Y_dev      bf16 [T, H], written.  Y_dev == X_dev (in place) is allowed;
  *              any other overlap is undefined.
  *   rinv_dev   fp32 [T], written, or NULL.
- *   T >= 0; H >= 8; H % N == 0; (H / N) % 8 == 0; H / N <= 32768;
+ *   T >= 0; H >= 8; H % N == 0; (H / N) % 8 == 0; H / N <= 30720;
  *   eps > 0 and finite; N in {1, 2, 4, 8}.
  * Errors: INVALID_ARG (null X/gamma/Y, T < 0, H <= 0, H % N, bad eps or N),
  *         UNSUPPORTED ((H/N) % 8 != 0, slice too wide, unaligned pointer,

@@ -19,8 +19,9 @@ extern "C" {
 
 /*
  * Override the automatic launch shape.  Each argument 0 means automatic.
- *   vpt        16-byte vectors per thread, one of {1,2,3,4,5,6,8}
- *   rows       token rows per tile (CTA threads = rows * threads-per-row <= 512)
+ *   vpt        QK kernel: 16-byte vectors per thread, one of {1,2,3,4,5,6,8};
+ *              MX kernels: MX blocks per thread, one of {1,2,4,8}
+ *   rows       token rows per tile (rows * threads-per-row <= 480)
  *   stages     shared-memory ring stages (>= 1)
  *   grid       CTAs (MX kernels) or clusters (QK kernel) of the persistent grid
  *   smem_budget bytes a CTA's ring aims to stay under (default 102400)

@@ -1,0 +1,12 @@
+// mx_e4m3.cu -- instantiates the fused normalization + MX cast kernels
+// (mx_kernel.cuh) for E4M3 elements; a unit of its own so that the
+// two element formats compile in parallel.
+#include "mx_kernel.cuh"
+
+namespace nts {
+
+MxKernel pick_mx_e4m3(int stat, int B, int bpt) { return pick_mx_format<NTS_FMT_E4M3>(stat, B, bpt); }
+
+int read_and_clear_mx_e4m3_status(unsigned* out) { return read_and_clear_local_mx_status(out); }
+
+}  // namespace nts

@@ -1,0 +1,372 @@
+// mx_kernel.cuh -- fused per-token normalization + MX block cast on one
+// GB300: RMSNorm + MXCast, and MXNorm + MXCast (p = 1 or 2).
+//
+// Method (MXNorm paper card, abstract, Fig. 1 caption and Fig. A.1):
+//   a row of D values is cut into K = D/B blocks of B contiguous values; each
+//   block is stored as B element codes (E4M3 or E2M1) sharing one E8M0 scale
+//   2^round(log2(normalized absmax / 2^emax)).  RMSNorm + MXCast takes the
+//   RMS from sum x^2 over the row; MXNorm estimates it from the block
+//   absmaxes the cast computes anyway, rho~ = c(B,p) * M_p(absmax), a
+//   reduction B times smaller.  Both are fused into one kernel (Fig. 8).
+//
+// GB300 mapping:
+//  * a persistent grid of CTAs walks tiles of R whole rows.  A producer warp
+//    keeps a ring of S shared-memory stages filled with one 1-D bulk TMA copy
+//    per tile (the rows are contiguous); consumer warps hand a stage back
+//    through an "empty" mbarrier;
+//  * every consumer thread owns whole MX blocks, so a block's absmax, its
+//    E8M0 exponent and its scale byte are thread-local: no shuffles, one
+//    exponent per block.  Without a gain the absmax runs on packed bf16
+//    pairs (max.xorsign.abs.bf16x2); the products x*rinv*2^-e run on the
+//    packed f32x2 pipes, and the element cast is the hardware
+//    cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32;
+//  * a thread's block is B/8 16-byte vectors 2B bytes apart from its
+//    neighbours'; thread L reads them starting at vector (L*B/64) mod (B/8)
+//    so the eight lanes of each shared-memory phase hit eight distinct bank
+//    groups;
+//  * the row is read from shared memory twice (statistic, then cast), so no
+//    thread holds more than its block absmaxes between the passes; the stage
+//    is released after the second pass;
+//  * the row statistic is a warp shuffle reduction; a row wider than one
+//    warp adds one exchange through shared memory guarded by an mbarrier.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "nts_device.cuh"
+#include "nts_internal.h"
+
+namespace nts {
+
+// kStatusTimeout bits of the MX kernels of the including translation unit;
+// every unit has its own word (no relocatable device code) and exports a
+// reader built on read_and_clear_local_mx_status().
+static __device__ unsigned int g_mx_status;
+
+struct MxParams {
+  const __nv_bfloat16* X;
+  const float* gamma;   // nullable
+  uint8_t* codes;
+  uint8_t* scales;
+  float* rinv_out;      // nullable
+  float* amax_out;      // nullable
+  int64_t T;
+  int64_t ntiles;
+  int D;
+  int K;                // D / B blocks per row
+  int G;                // consumer threads per row (multiple of 32)
+  int R;                // rows per tile
+  int S;                // ring stages
+  float eps;
+  float corr;           // MXNorm: c(B,1) for p = 1, c(B,2)^2 for p = 2
+  uint64_t wait_limit_ns;
+  uint32_t missing_tx;  // test hook: bytes expected on the first stage but never sent
+};
+
+enum { kStatRms = 0, kStatMxP1 = 1, kStatMxP2 = 2 };
+
+// Shared memory layout (bytes, in order):
+//   ring [S][R][D] bf16 | full[S] | empty[S] | rbar[2][R] | red[2][R][WPR] f32
+struct MxLayout {
+  uint32_t ring, full, empty, rbar, red, total;
+};
+
+__host__ __device__ inline MxLayout mx_layout(int S, int R, int D, int G) {
+  MxLayout L;
+  L.ring = 0;
+  L.full = L.ring + (uint32_t)S * R * D * 2;
+  L.empty = L.full + (uint32_t)S * 8;
+  L.rbar = L.empty + (uint32_t)S * 8;
+  L.red = L.rbar + (uint32_t)2 * R * 8;
+  L.total = L.red + (uint32_t)2 * R * (G / 32) * 4;
+  return L;
+}
+
+// E8M0 exponent of a block whose normalized absmax is `ay` (>= 0):
+// round(log2 ay) - emax, where the log2 rounding goes up exactly when the
+// fp32 significand is >= the first fp32 value above sqrt(2) (0x3504F4 in the
+// mantissa field); zero and subnormal absmaxes give the smallest scale.
+__device__ __forceinline__ int e8m0_exponent(float ay, int emax) {
+  const uint32_t b = __float_as_uint(ay);
+  const int field = (int)(b >> 23);
+  if (field == 0) return -127;
+  const int e = field - 127 + ((b & 0x7FFFFFu) >= 0x3504F4u ? 1 : 0) - emax;
+  return max(-127, min(127, e));
+}
+
+// 8 bf16 values (one vector) times an fp32 gain vector at `gp`, as four
+// f32x2 pairs.
+__device__ __forceinline__ void weigh_vector(const uint4& v, const float* gp, uint64_t (&w)[4]) {
+  const float4 g0 = __ldg(reinterpret_cast<const float4*>(gp));
+  const float4 g1 = __ldg(reinterpret_cast<const float4*>(gp) + 1);
+  w[0] = f2_mul(bf16x2_to_f2(v.x), f2(g0.x, g0.y));
+  w[1] = f2_mul(bf16x2_to_f2(v.y), f2(g0.z, g0.w));
+  w[2] = f2_mul(bf16x2_to_f2(v.z), f2(g1.x, g1.y));
+  w[3] = f2_mul(bf16x2_to_f2(v.w), f2(g1.z, g1.w));
+}
+
+template <int VB, int BPT, int FMT, int STAT>
+__global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxParams p) {
+  constexpr int kB = VB * 8;                                 // block size
+  constexpr int kEmax = (FMT == NTS_FMT_E4M3) ? 8 : 2;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int nconsumer = p.R * p.G;
+  const int wpr = p.G >> 5;
+  const MxLayout L = mx_layout(p.S, p.R, p.D, p.G);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t stage_bytes = (uint32_t)p.R * p.D * 2;
+  const int64_t cta = blockIdx.x, ncta = gridDim.x;
+  const int64_t my_tiles = cta < p.ntiles ? (p.ntiles - 1 - cta) / ncta + 1 : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < p.S; ++s) {
+      mbar_init(sbase + L.full + 8 * s, 1);
+      mbar_init(sbase + L.empty + 8 * s, nconsumer / 32);
+    }
+    for (int b = 0; b < 2 * p.R; ++b) mbar_init(sbase + L.rbar + 8 * b, wpr);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (tid >= nconsumer) {
+    // ------------------------------------------------------ producer warp
+    if (lane == 0) {
+      bool aborted = false;
+      const uint64_t policy = l2_policy_evict_first();
+      for (int64_t j = 0; j < my_tiles; ++j) {
+        const int s = (int)(j % p.S);
+        if (j >= p.S &&
+            !mbar_wait_bounded(sbase + L.empty + 8 * s, (uint32_t)((j / p.S - 1) & 1),
+                               p.wait_limit_ns)) {
+          atomicOr(&g_mx_status, kStatusTimeout);
+          aborted = true;
+          break;
+        }
+        const int64_t t0 = (cta + j * ncta) * p.R;
+        const uint32_t bytes = (uint32_t)min64(p.R, p.T - t0) * p.D * 2;
+        const uint32_t bar = sbase + L.full + 8 * s;
+        mbar_arrive_expect_tx(bar, bytes + (j == 0 ? p.missing_tx : 0u));
+        bulk_g2s(sbase + L.ring + (uint32_t)s * stage_bytes, p.X + (size_t)t0 * p.D, bytes, bar,
+                 policy);
+      }
+      for (int64_t j = max64(0, my_tiles - p.S); j < my_tiles && !aborted; ++j)
+        (void)mbar_wait_bounded(sbase + L.full + 8 * (int)(j % p.S), (uint32_t)((j / p.S) & 1),
+                                p.wait_limit_ns);
+    }
+    __syncwarp();
+    return;
+  }
+
+  // --------------------------------------------------------- consumer warps
+  const int row = tid / p.G;
+  const int g = tid - row * p.G;
+  const int wir = g >> 5;
+  const int sig = ((lane * VB) >> 3) & (VB - 1);   // bank-conflict-free start vector
+  const size_t cbytes = (FMT == NTS_FMT_E4M3) ? (size_t)p.D : (size_t)p.D / 2;
+  bool aborted = false;
+
+  for (int64_t j = 0; j < my_tiles; ++j) {
+    const int s = (int)(j % p.S);
+    const int64_t t = (cta + j * ncta) * p.R + row;
+    const bool valid = t < p.T;
+    if (!mbar_wait_bounded(sbase + L.full + 8 * s, (uint32_t)((j / p.S) & 1),
+                           aborted ? 0 : p.wait_limit_ns)) {
+      if (!aborted) atomicOr(&g_mx_status, kStatusTimeout);
+      aborted = true;
+    }
+    const uint32_t srow = sbase + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * p.D * 2;
+
+    // ---- pass 1: block absmaxes (of w = x or x*gamma) and the statistic
+    float am[BPT];
+    float stat = 0.f;
+    uint64_t acc = 0;  // RMSNorm: packed sum of x^2
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      const int b = i * p.G + g;
+      am[i] = 0.f;
+      if (valid && b < p.K) {
+        const uint32_t base = srow + (uint32_t)b * kB * 2;
+        if (p.gamma == nullptr) {
+          uint32_t m = 0;
+#pragma unroll
+          for (int k = 0; k < VB; ++k) {
+            const int u = (k + sig) & (VB - 1);
+            const uint4 v = ld_shared_v4(base + u * 16);
+            m = bf16x2_absmax(m, v.x);
+            m = bf16x2_absmax(m, v.y);
+            m = bf16x2_absmax(m, v.z);
+            m = bf16x2_absmax(m, v.w);
+            if (STAT == kStatRms) {
+              const uint64_t a = bf16x2_to_f2(v.x), c = bf16x2_to_f2(v.y);
+              const uint64_t d = bf16x2_to_f2(v.z), e = bf16x2_to_f2(v.w);
+              acc = f2_fma(a, a, acc);
+              acc = f2_fma(c, c, acc);
+              acc = f2_fma(d, d, acc);
+              acc = f2_fma(e, e, acc);
+            }
+          }
+          am[i] = bf16x2_hmax_abs(m);
+        } else {
+          float mf = 0.f;
+#pragma unroll
+          for (int k = 0; k < VB; ++k) {
+            const int u = (k + sig) & (VB - 1);
+            const uint4 v = ld_shared_v4(base + u * 16);
+            if (STAT == kStatRms) {
+              const uint64_t a = bf16x2_to_f2(v.x), c = bf16x2_to_f2(v.y);
+              const uint64_t d = bf16x2_to_f2(v.z), e = bf16x2_to_f2(v.w);
+              acc = f2_fma(a, a, acc);
+              acc = f2_fma(c, c, acc);
+              acc = f2_fma(d, d, acc);
+              acc = f2_fma(e, e, acc);
+            }
+            uint64_t w[4];
+            weigh_vector(v, p.gamma + (size_t)b * kB + u * 8, w);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              mf = fmaxf(mf, fmaxf(fabsf(f2_lo(w[q])), fabsf(f2_hi(w[q]))));
+          }
+          am[i] = mf;
+        }
+        if (STAT == kStatMxP1) stat += am[i];
+        if (STAT == kStatMxP2) stat = fmaf(am[i], am[i], stat);
+      }
+    }
+    if (STAT == kStatRms) stat = f2_lo(acc) + f2_hi(acc);
+    stat = warp_sum(stat);
+    if (wpr > 1) {
+      // a row spans several warps: add their partials in warp order
+      const int bsel = (int)(j & 1);
+      float* red = reinterpret_cast<float*>(smem + L.red) + (size_t)(bsel * p.R + row) * wpr;
+      const uint32_t rbar = sbase + L.rbar + 8 * (bsel * p.R + row);
+      if (lane == 0) {
+        red[wir] = stat;
+        mbar_arrive(rbar);
+      }
+      if (!mbar_wait_bounded(rbar, (uint32_t)((j >> 1) & 1), aborted ? 0 : p.wait_limit_ns)) {
+        if (!aborted) atomicOr(&g_mx_status, kStatusTimeout);
+        aborted = true;
+      }
+      stat = 0.f;
+      for (int k = 0; k < wpr; ++k) stat += red[k];
+    }
+
+    // ---- the row's normalization factor
+    float ms;
+    if (STAT == kStatRms) {
+      ms = stat / (float)p.D;
+    } else if (STAT == kStatMxP1) {
+      const float rho = p.corr * (stat / (float)p.K);
+      ms = rho * rho;
+    } else {
+      ms = p.corr * (stat / (float)p.K);
+    }
+    const float rinv = 1.0f / sqrtf(ms + p.eps);
+    if (valid && p.rinv_out != nullptr && g == 0) p.rinv_out[t] = rinv;
+
+    // ---- pass 2: scales and element codes
+    if (valid) {
+      const uint64_t rr = f2(rinv, rinv);
+      uint8_t* crow = p.codes + (size_t)t * cbytes;
+#pragma unroll
+      for (int i = 0; i < BPT; ++i) {
+        const int b = i * p.G + g;
+        if (b < p.K) {
+          const int e = e8m0_exponent(am[i] * rinv, kEmax);
+          const float is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+          const uint64_t ss = f2(is, is);
+          p.scales[(size_t)t * p.K + b] = (uint8_t)(e + 127);
+          if (p.amax_out != nullptr) p.amax_out[(size_t)t * p.K + b] = am[i];
+          const uint32_t base = srow + (uint32_t)b * kB * 2;
+#pragma unroll
+          for (int k = 0; k < VB; ++k) {
+            const int u = (k + sig) & (VB - 1);
+            const uint4 v = ld_shared_v4(base + u * 16);
+            uint64_t w[4];
+            if (p.gamma == nullptr) {
+              w[0] = bf16x2_to_f2(v.x);
+              w[1] = bf16x2_to_f2(v.y);
+              w[2] = bf16x2_to_f2(v.z);
+              w[3] = bf16x2_to_f2(v.w);
+            } else {
+              weigh_vector(v, p.gamma + (size_t)b * kB + u * 8, w);
+            }
+            uint64_t q[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) q[h] = f2_mul(f2_mul(w[h], rr), ss);
+            if (FMT == NTS_FMT_E4M3) {
+              const uint32_t lo = cvt_e4m3x2(f2_lo(q[0]), f2_hi(q[0])) |
+                                  (cvt_e4m3x2(f2_lo(q[1]), f2_hi(q[1])) << 16);
+              const uint32_t hi = cvt_e4m3x2(f2_lo(q[2]), f2_hi(q[2])) |
+                                  (cvt_e4m3x2(f2_lo(q[3]), f2_hi(q[3])) << 16);
+              st_global_v2(crow + (size_t)b * kB + u * 8, lo, hi);
+            } else {
+              const uint32_t c = cvt_e2m1x2(f2_lo(q[0]), f2_hi(q[0])) |
+                                 (cvt_e2m1x2(f2_lo(q[1]), f2_hi(q[1])) << 8) |
+                                 (cvt_e2m1x2(f2_lo(q[2]), f2_hi(q[2])) << 16) |
+                                 (cvt_e2m1x2(f2_lo(q[3]), f2_hi(q[3])) << 24);
+              st_global_u32(crow + (size_t)b * (kB / 2) + u * 4, c);
+            }
+          }
+        }
+      }
+    }
+    // every read of stage s by this warp is done
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
+  }
+}
+
+using MxKernel = void (*)(MxParams);
+
+template <int FMT, int STAT, int VB>
+MxKernel pick_mx_bpt(int bpt) {
+  switch (bpt) {
+    case 1: return mx_norm_cast_kernel<VB, 1, FMT, STAT>;
+    case 2: return mx_norm_cast_kernel<VB, 2, FMT, STAT>;
+    case 4: return mx_norm_cast_kernel<VB, 4, FMT, STAT>;
+    case 8: return mx_norm_cast_kernel<VB, 8, FMT, STAT>;
+    default: return nullptr;
+  }
+}
+
+template <int FMT, int STAT>
+MxKernel pick_mx_block(int B, int bpt) {
+  switch (B) {
+    case 16: return pick_mx_bpt<FMT, STAT, 2>(bpt);
+    case 32: return pick_mx_bpt<FMT, STAT, 4>(bpt);
+    case 64: return pick_mx_bpt<FMT, STAT, 8>(bpt);
+    default: return nullptr;
+  }
+}
+
+// Instantiates every kernel of element format FMT in the calling unit.
+template <int FMT>
+MxKernel pick_mx_format(int stat, int B, int bpt) {
+  switch (stat) {
+    case kStatRms: return pick_mx_block<FMT, kStatRms>(B, bpt);
+    case kStatMxP1: return pick_mx_block<FMT, kStatMxP1>(B, bpt);
+    case kStatMxP2: return pick_mx_block<FMT, kStatMxP2>(B, bpt);
+    default: return nullptr;
+  }
+}
+
+static inline int read_and_clear_local_mx_status(unsigned* out) {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_mx_status, sizeof(v));
+  if (e != cudaSuccess) return fail_cuda(e, "reading an MX status word");
+  e = cudaMemcpyToSymbol(g_mx_status, &zero, sizeof(zero));
+  if (e != cudaSuccess) return fail_cuda(e, "clearing an MX status word");
+  *out = v;
+  return NTS_OK;
+}
+
+// Defined by mx_e4m3.cu and mx_e2m1.cu.
+MxKernel pick_mx_e4m3(int stat, int B, int bpt);
+MxKernel pick_mx_e2m1(int stat, int B, int bpt);
+int read_and_clear_mx_e4m3_status(unsigned* out);
+int read_and_clear_mx_e2m1_status(unsigned* out);
+
+}  // namespace nts

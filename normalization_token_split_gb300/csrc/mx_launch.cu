@@ -1,0 +1,121 @@
+// mx_launch.cu -- launch-shape selection and launch of the fused
+// normalization + MX cast kernels (mx_kernel.cuh).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "mx_kernel.cuh"
+
+namespace nts {
+
+namespace {
+
+struct MxShape {
+  int bpt = 0;  // blocks per consumer thread
+  int G = 0;    // consumer threads per row
+};
+
+// One warp per row while a thread holds at most 8 blocks; wider rows take
+// more warps.  bpt is the smallest of {1, 2, 4, 8} that covers the row.
+MxShape choose_mx_shape(int K, int force_bpt) {
+  static const int opts[] = {1, 2, 4, 8};
+  MxShape best;
+  for (int bpt : opts) {
+    if (force_bpt > 0 && bpt != force_bpt) continue;
+    int G = (K + bpt - 1) / bpt;
+    G = (G + 31) / 32 * 32;
+    if (G > kMaxConsumers) continue;
+    if (best.G == 0 || G < best.G || (G == best.G && bpt < best.bpt)) {
+      best.bpt = bpt;
+      best.G = G;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune) {
+  const int D = (int)rq.D;
+  const int K = D / rq.B;
+  const DeviceInfo& dev = device_info();
+  if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
+
+  // tune.force_vpt selects the blocks per thread for this kernel family
+  const MxShape sh = choose_mx_shape(K, tune.force_vpt);
+  if (sh.G == 0) return fail(NTS_ERR_UNSUPPORTED, "row too wide: D = %d", D);
+
+  // Rows per tile: about four consumer warps, and a ring of at least three
+  // stages inside the shared-memory budget; fewer rows when T is small.
+  int R = std::max(1, 128 / sh.G);
+  while (R > 1 && mx_layout(3, R, D, sh.G).total > (uint32_t)tune.smem_budget) R /= 2;
+  while (R > 1 && (rq.T + R - 1) / R < (int64_t)2 * dev.sm_count) R /= 2;
+  if (tune.force_rows > 0) R = tune.force_rows;
+  if (R * sh.G > kMaxConsumers) return fail(NTS_ERR_UNSUPPORTED, "tile of %d rows too large", R);
+
+  int S = 6;
+  while (S > 2 && mx_layout(S, R, D, sh.G).total > (uint32_t)tune.smem_budget) --S;
+  while (S > 1 && mx_layout(S, R, D, sh.G).total > (uint32_t)dev.max_smem_optin) --S;
+  if (tune.force_stages > 0) S = tune.force_stages;
+  const size_t smem = mx_layout(S, R, D, sh.G).total;
+  if (smem > (size_t)dev.max_smem_optin)
+    return fail(NTS_ERR_UNSUPPORTED, "row too wide for shared memory: D = %d", D);
+
+  const int stat = rq.p == 0 ? kStatRms : (rq.p == 1 ? kStatMxP1 : kStatMxP2);
+  MxKernel kern = rq.fmt == NTS_FMT_E4M3 ? pick_mx_e4m3(stat, rq.B, sh.bpt)
+                                         : pick_mx_e2m1(stat, rq.B, sh.bpt);
+  if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for B=%d bpt=%d", rq.B, sh.bpt);
+
+  MxParams prm;
+  prm.X = static_cast<const __nv_bfloat16*>(rq.X);
+  prm.gamma = rq.gamma;
+  prm.codes = rq.codes;
+  prm.scales = rq.scales;
+  prm.rinv_out = rq.rinv;
+  prm.amax_out = rq.amax;
+  prm.T = rq.T;
+  prm.ntiles = (rq.T + R - 1) / R;
+  prm.D = D;
+  prm.K = K;
+  prm.G = sh.G;
+  prm.R = R;
+  prm.S = S;
+  prm.eps = rq.eps;
+  prm.corr = 0.f;
+  if (rq.p == 1) prm.corr = (float)rq.corr;
+  if (rq.p == 2) prm.corr = (float)(rq.corr * rq.corr);
+  prm.wait_limit_ns = tune.wait_limit_ns;
+  prm.missing_tx = tune.missing_tx;
+
+  int rc = prepare_kernel((const void*)kern, smem);
+  if (rc != NTS_OK) return rc;
+
+  const int nthreads = R * sh.G + 32;  // consumers + producer warp
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nthreads, smem);
+  if (e != cudaSuccess) return fail_cuda(e, "occupancy query for the MX kernel");
+  if (per_sm < 1) return fail(NTS_ERR_UNSUPPORTED, "MX kernel does not fit on an SM");
+  int64_t grid = std::min<int64_t>(prm.ntiles, (int64_t)per_sm * dev.sm_count);
+  if (tune.force_grid > 0) grid = std::min<int64_t>(prm.ntiles, tune.force_grid);
+
+  log_launch(rq.p == 0 ? "rmsnorm_mxcast" : "mxnorm_cast",
+             "T=%lld D=%d B=%d fmt=%d p=%d bpt=%d G=%d R=%d S=%d smem=%zu grid=%lld (%d/SM)",
+             (long long)rq.T, D, rq.B, rq.fmt, rq.p, sh.bpt, sh.G, R, S, smem, (long long)grid,
+             per_sm);
+  kern<<<(unsigned)grid, nthreads, smem, stream>>>(prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "launching the MX kernel");
+  return NTS_OK;
+}
+
+int read_and_clear_mx_status(unsigned* out) {
+  unsigned a = 0, b = 0;
+  int rc = read_and_clear_mx_e4m3_status(&a);
+  if (rc != NTS_OK) return rc;
+  rc = read_and_clear_mx_e2m1_status(&b);
+  if (rc != NTS_OK) return rc;
+  *out = a | b;
+  return NTS_OK;
+}
+
+}  // namespace nts

@@ -92,7 +92,7 @@ RowShape choose_row_shape(int nvec, int force_vpt) {
     if (force_vpt > 0 && vpt != force_vpt) continue;
     int G = (nvec + vpt - 1) / vpt;
     G = (G + 31) / 32 * 32;
-    if (G > kMaxThreads) continue;
+    if (G > kMaxConsumers) continue;
     const int waste = G * vpt - nvec;
     if (best_waste < 0 || waste < best_waste) {
       best_waste = waste;
@@ -247,9 +247,9 @@ namespace {
 
 int validate_qk(const void* X, const float* gamma, const void* Y, const float* rinv, int64_t T,
                 int64_t H, float eps, int N) {
-  if (X == nullptr || gamma == nullptr || Y == nullptr)
-    return fail(NTS_ERR_INVALID_ARG, "X, gamma and Y must be non-NULL");
   if (T < 0) return fail(NTS_ERR_INVALID_ARG, "T must be >= 0, got %lld", (long long)T);
+  if (T > 0 && (X == nullptr || gamma == nullptr || Y == nullptr))
+    return fail(NTS_ERR_INVALID_ARG, "X, gamma and Y must be non-NULL");
   if (H <= 0) return fail(NTS_ERR_INVALID_ARG, "H must be > 0, got %lld", (long long)H);
   if (N != 1 && N != 2 && N != 4 && N != 8)
     return fail(NTS_ERR_INVALID_ARG, "N must be 1, 2, 4 or 8, got %d", N);
@@ -259,8 +259,8 @@ int validate_qk(const void* X, const float* gamma, const void* Y, const float* r
     return fail(NTS_ERR_INVALID_ARG, "eps must be positive and finite");
   if ((H / N) % 8 != 0)
     return fail(NTS_ERR_UNSUPPORTED, "H/N (%lld) must be a multiple of 8", (long long)(H / N));
-  if (H / N > 32768)
-    return fail(NTS_ERR_UNSUPPORTED, "H/N (%lld) exceeds 32768", (long long)(H / N));
+  if (H / N > 30720)
+    return fail(NTS_ERR_UNSUPPORTED, "H/N (%lld) exceeds 30720", (long long)(H / N));
   if (!aligned(X, 16) || !aligned(Y, 16) || !aligned(gamma, 16) ||
       (rinv != nullptr && !aligned(rinv, 4)))
     return fail(NTS_ERR_UNSUPPORTED, "X, Y and gamma must be 16-byte aligned");
@@ -270,9 +270,9 @@ int validate_qk(const void* X, const float* gamma, const void* Y, const float* r
 int validate_mx(const void* X, const float* gamma, const uint8_t* codes, const uint8_t* scales,
                 const float* rinv, const float* amax, int64_t T, int64_t D, float eps, int B,
                 int fmt, int p, bool mxnorm) {
-  if (X == nullptr || codes == nullptr || scales == nullptr)
-    return fail(NTS_ERR_INVALID_ARG, "X, codes and scales must be non-NULL");
   if (T < 0) return fail(NTS_ERR_INVALID_ARG, "T must be >= 0, got %lld", (long long)T);
+  if (T > 0 && (X == nullptr || codes == nullptr || scales == nullptr))
+    return fail(NTS_ERR_INVALID_ARG, "X, codes and scales must be non-NULL");
   if (D <= 0) return fail(NTS_ERR_INVALID_ARG, "D must be > 0, got %lld", (long long)D);
   if (B != 16 && B != 32 && B != 64)
     return fail(NTS_ERR_INVALID_ARG, "B must be 16, 32 or 64, got %d", B);
@@ -355,7 +355,7 @@ int nts_check_status(void* stream) {
 int nts_qknorm_rms_host(const void* X_host, const float* gamma_dev, void* Y_host,
                         float* rinv_host, void* X_dev, void* Y_dev, float* rinv_dev, int64_t T,
                         int64_t H, float eps, int N, void* stream) {
-  if (X_host == nullptr || Y_host == nullptr)
+  if (T > 0 && (X_host == nullptr || Y_host == nullptr))
     return fail(NTS_ERR_INVALID_ARG, "X_host and Y_host must be non-NULL");
   if (rinv_host != nullptr && rinv_dev == nullptr)
     return fail(NTS_ERR_INVALID_ARG, "rinv_host needs a rinv_dev staging buffer");
@@ -380,7 +380,7 @@ static int mx_host(const void* X_host, const float* gamma_dev, uint8_t* codes_ho
                    uint8_t* scales_host, void* X_dev, uint8_t* codes_dev, uint8_t* scales_dev,
                    int64_t T, int64_t D, float eps, int B, int fmt, int p, bool mxnorm,
                    void* stream) {
-  if (X_host == nullptr || codes_host == nullptr || scales_host == nullptr)
+  if (T > 0 && (X_host == nullptr || codes_host == nullptr || scales_host == nullptr))
     return fail(NTS_ERR_INVALID_ARG, "X_host, codes_host and scales_host must be non-NULL");
   int rc = validate_mx(X_dev, gamma_dev, codes_dev, scales_dev, nullptr, nullptr, T, D, eps, B,
                        fmt, p, mxnorm);

@@ -187,6 +187,96 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
   return r;
 }
 
+// ------------------------------------------------- more mbarrier / proxies
+
+// Arrive once (release at CTA scope) without a transaction count.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Store a 32-bit value into the shared memory of a CTA of this cluster and
+// signal 4 transaction bytes on that CTA's mbarrier (both addresses mapped
+// with map_to_rank).  No fence, no barrier: the receiver's wait on its
+// mbarrier makes the value visible.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+          remote_addr),
+      "r"(__float_as_uint(v)), "r"(remote_bar)
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared without an L2 hint (for re-read data).
+__device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ------------------------------------------------------- packed fp32 math
+// Two fp32 lanes in one 64-bit register pair (Blackwell f32x2 pipes).
+
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// bf16 pair (low half = element 0) -> the two fp32 values, exactly.
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t v) {
+  return f2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// max(|a|, |b|) lane-wise on bf16 pairs; the sign bits of the result are the
+// XOR of the inputs' (callers mask them off).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Larger magnitude of the two bf16 halves, as an exact fp32 value.
+__device__ __forceinline__ float bf16x2_hmax_abs(uint32_t m) {
+  m &= 0x7FFF7FFFu;
+  return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ void st_global_v2(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void st_global_u32(void* p, uint32_t a) {
+  asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

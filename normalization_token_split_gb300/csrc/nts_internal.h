@@ -11,13 +11,15 @@
 
 namespace nts {
 
-// Largest CTA the kernels are compiled for: 512 threads leaves up to 128
-// registers per thread, enough to keep a thread's 8-vector slice in fp32.
-constexpr int kMaxThreads = 512;
+// A CTA has up to 480 consumer threads (the threads that own data) plus one
+// producer warp that only issues the TMA copies.  512 threads leave up to
+// 128 registers per thread.
+constexpr int kMaxConsumers = 480;
+constexpr int kMaxThreads = kMaxConsumers + 32;
 
 // Per-call launch settings: automatic unless a debug override is set.
 struct LaunchTuning {
-  int force_vpt = 0;         // vectors (8 values) per thread, 0 = automatic
+  int force_vpt = 0;         // QK: 16-byte vectors per thread; MX: blocks per thread; 0 = auto
   int force_rows = 0;        // rows per tile, 0 = automatic
   int force_stages = 0;      // ring stages, 0 = automatic
   int64_t force_grid = 0;    // CTAs (MX) or clusters (QK), 0 = automatic

@@ -1,7 +1,7 @@
 // qknorm_cluster.cu -- layerwise QK-RMSNorm with split-H scalar partial sums
 // on one GB300: the N shards of a row are the N CTAs of a thread-block
-// cluster, and the per-shard sums of squares are exchanged through
-// distributed shared memory.
+// cluster, and the per-shard sums of squares travel through distributed
+// shared memory.
 //
 // Method (SwiftQK, Eq. (1) and Algorithm 1, Sec. III.A-D):
 //   Phase A  each shard forms its local sum of squares in fp32;
@@ -10,23 +10,28 @@
 //   Phase C  y = (x*gamma) * 1/sqrt(S/H_total + eps), written once.
 //
 // GB300 mapping (what differs from the pages' multi-GPU kernel):
-//  * shard k of every row is handled by CTA k of a cluster of N CTAs, so the
-//    "remote write + spin on a peer flag" of Algorithm 1 becomes N stores to
-//    the peers' shared memory (st.shared::cluster) followed by a split
-//    hardware cluster barrier (arrive.release ... wait.acquire);
-//  * the overlap of Phase B is between the two halves of that split barrier:
-//    every warp issues x*gamma after arriving and only then waits;
+//  * shard k of every row is handled by CTA k of a cluster of N CTAs.  The
+//    "remote write + spin on a peer flag" of Algorithm 1 becomes, per warp,
+//    N st.async stores of its fp32 partial into the peers' shared memory,
+//    each completing 4 transaction bytes on the receiving row's mbarrier.
+//    A receiver waits on its own mbarrier only: no cluster barrier and no
+//    memory fence sits in the token loop, so nothing waits for the previous
+//    tile's global stores;
+//  * Phase B is the window between those sends and the wait: every warp
+//    multiplies its registers by gamma (staged once in shared memory) with
+//    packed f32x2 instructions, then waits;
 //  * the block-level token pipeline of Sec. III.D is a persistent loop over
-//    tiles of R rows, fed by a ring of S shared-memory stages that one thread
-//    fills with bulk TMA copies (cp.async.bulk) S-1 tiles ahead;
-//  * deadlock safety (Sec. III.D) needs no bounded grid here: the hardware
+//    tiles of R rows.  A producer warp keeps a ring of S shared-memory stages
+//    filled with bulk TMA copies; consumer warps release a stage (an
+//    "empty" mbarrier) as soon as its data is in registers;
+//  * deadlock safety (Sec. III.D) needs no bounded grid: the hardware
 //    co-schedules a cluster's CTAs and no CTA waits on another cluster.  The
 //    grid is still sized from the cluster occupancy query, for throughput.
+//    Every wait in the kernel is bounded in time (an expired wait sets the
+//    status word and the kernel finishes with undefined outputs).
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <mutex>
-#include <vector>
 
 #include "nts_device.cuh"
 #include "nts_internal.h"
@@ -45,7 +50,7 @@ struct QkParams {
   int H;        // full row width H_total
   int W;        // H / N, the columns of one shard
   int nvec;     // W / 8 16-byte vectors per shard row
-  int G;        // threads per row (multiple of 32)
+  int G;        // consumer threads per row (multiple of 32)
   int R;        // rows per tile
   int S;        // ring stages
   float eps;
@@ -53,161 +58,211 @@ struct QkParams {
   uint32_t missing_tx;  // test hook: bytes expected on the first stage but never sent
 };
 
-// Shared memory: ring[S][R][W] bf16 | full[S] mbarriers | part[2][R][N][WPR] f32.
-template <int N>
-__host__ __device__ inline size_t qk_smem_bytes(int S, int R, int W, int G) {
-  size_t ring = (size_t)S * R * W * 2;
-  size_t bars = (size_t)S * 8;
-  size_t part = (size_t)2 * R * N * (G / 32) * 4;
-  return ring + bars + part;
+// Shared memory layout (bytes, in order):
+//   ring  [S][R][W] bf16          the staged shard rows
+//   gam   [2][nvec] float4        gamma of this shard, halves of each vector
+//   full  [S], empty [S]          ring mbarriers
+//   xbar  [2][R]                  exchange mbarriers (double-buffered by tile)
+//   part  [2][R][N][WPR] f32      partial sums received from every warp of
+//                                 every shard of a row
+struct QkLayout {
+  uint32_t ring, gam, full, empty, xbar, part, total;
+};
+
+__host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int W, int G) {
+  QkLayout L;
+  L.ring = 0;
+  L.gam = L.ring + (uint32_t)S * R * W * 2;
+  L.full = L.gam + (uint32_t)W * 4;
+  L.empty = L.full + (uint32_t)S * 8;
+  L.xbar = L.empty + (uint32_t)S * 8;
+  L.part = L.xbar + (uint32_t)2 * R * 8;
+  L.total = L.part + (uint32_t)2 * R * N * (G / 32) * 4;
+  return L;
 }
 
 template <int N, int VPT>
 __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const QkParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t rank = (N > 1) ? cluster_ctarank() : 0u;
   const int64_t cid = cluster_id_x();
   const int64_t ncl = num_clusters_x();
   const int tid = threadIdx.x;
-  const int row = tid / p.G;
-  const int g = tid - row * p.G;
-  const int wpr = p.G >> 5;
-  const int wir = g >> 5;
+  const int nconsumer = p.R * p.G;
   const int lane = tid & 31;
-
+  const int wpr = p.G >> 5;
+  const QkLayout L = qk_layout(N, p.S, p.R, p.W, p.G);
+  const uint32_t sbase = smem_addr(smem);
   const uint32_t stage_bytes = (uint32_t)p.R * p.W * 2;
-  const uint32_t ring = smem_addr(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.S * stage_bytes);
-  float* part = reinterpret_cast<float*>(full + p.S);
-
   const int64_t my_tiles = cid < p.ntiles ? (p.ntiles - 1 - cid) / ncl + 1 : 0;
-  const __nv_bfloat16* Xs = p.X + (size_t)rank * p.W;  // this shard's column origin
 
+  // gamma of this shard, split into the low and high halves of each
+  // 8-value vector so that consecutive lanes read consecutive 16 bytes
+  {
+    const float4* gsrc = reinterpret_cast<const float4*>(p.gamma + (size_t)rank * p.W);
+    float4* gam = reinterpret_cast<float4*>(smem + L.gam);
+    for (int q = tid; q < p.nvec; q += blockDim.x) {
+      gam[q] = __ldg(gsrc + 2 * q);
+      gam[p.nvec + q] = __ldg(gsrc + 2 * q + 1);
+    }
+  }
   if (tid == 0) {
-    for (int s = 0; s < p.S; ++s) mbar_init(smem_addr(&full[s]), 1);
+    for (int s = 0; s < p.S; ++s) {
+      mbar_init(sbase + L.full + 8 * s, 1);
+      mbar_init(sbase + L.empty + 8 * s, nconsumer / 32);
+    }
+    for (int b = 0; b < 2 * p.R; ++b) mbar_init(sbase + L.xbar + 8 * b, 1);
     fence_mbar_init();
   }
   __syncthreads();
-  // Peers must be running before anyone stores into their shared memory:
-  // this arrive is matched by a wait just before the first exchange.
-  if (N > 1) cluster_arrive_relaxed();
-
-  const uint64_t policy = l2_policy_evict_first();
-  auto issue = [&](int64_t j) {
-    const int64_t t0 = (cid + j * ncl) * p.R;
-    const int nrows = (int)min64(p.R, p.T - t0);
-    const int s = (int)(j % p.S);
-    const uint32_t bar = smem_addr(&full[s]);
-    const uint32_t row_bytes = (uint32_t)p.W * 2;
-    mbar_arrive_expect_tx(bar, nrows * row_bytes + (j == 0 ? p.missing_tx : 0u));
-    const uint32_t dst = ring + (uint32_t)s * stage_bytes;
-    for (int r = 0; r < nrows; ++r)
-      bulk_g2s(dst + r * row_bytes, Xs + (size_t)(t0 + r) * p.H, row_bytes, bar, policy);
-  };
-
-  if (tid == 0) {
-    const int64_t pre = min64(p.S, my_tiles);
-    for (int64_t j = 0; j < pre; ++j) issue(j);
+  // Every CTA of the cluster is running and has initialised its barriers
+  // before anyone stores into a peer's shared memory.
+  if (N > 1) {
+    cluster_arrive_release();
+    cluster_wait_acquire();
   }
 
   bool aborted = false;
-  bool first = true;
-  for (int64_t j = 0; j < my_tiles; ++j) {
-    const int s = (int)(j % p.S);
-    const uint32_t parity = (uint32_t)((j / p.S) & 1);
-    const int64_t t = (cid + j * ncl) * p.R + row;
-    const bool valid = t < p.T;
-
-    if (!mbar_wait_bounded(smem_addr(&full[s]), parity, aborted ? 0 : p.wait_limit_ns)) {
-      if (!aborted) atomicOr(&g_qk_status, kStatusTimeout);
-      aborted = true;
-    }
-
-    // ---- Phase A: local sum of squares of this shard (fp32).
-    uint4 xr[VPT];
-    float ss = 0.f;
-    const uint32_t srow = ring + (uint32_t)s * stage_bytes + (uint32_t)row * p.W * 2;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = i * p.G + g;
-      if (valid && v < p.nvec) {
-        xr[i] = ld_shared_v4(srow + v * 16);
-        float f[8];
-        bf16x8_to_f32(xr[i], f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-      } else {
-        xr[i] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    ss = warp_sum(ss);
-
-    // ---- Exchange: every warp publishes its partial into slot
-    // part[j&1][row][rank][wir] of every CTA of the cluster.
-    if (N > 1 && first) cluster_wait_acquire();
-    first = false;
+  if (tid >= nconsumer) {
+    // ------------------------------------------------------ producer warp
     if (lane == 0) {
-      float* slot = part + ((((size_t)(j & 1) * p.R + row) * N + rank) * wpr + wir);
-      const uint32_t local = smem_addr(slot);
-#pragma unroll
-      for (int k = 0; k < N; ++k) st_cluster_f32(map_to_rank(local, k), ss);
-    }
-    cluster_arrive_release();
-
-    // ---- Phase B (overlapped with the exchange): w = x * gamma.
-    float w[VPT][8];
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = i * p.G + g;
-      float f[8];
-      bf16x8_to_f32(xr[i], f);
-      if (valid && v < p.nvec) {
-        const float4* gp = reinterpret_cast<const float4*>(p.gamma + (size_t)rank * p.W + v * 8);
-        const float4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
-        w[i][0] = f[0] * g0.x; w[i][1] = f[1] * g0.y; w[i][2] = f[2] * g0.z; w[i][3] = f[3] * g0.w;
-        w[i][4] = f[4] * g1.x; w[i][5] = f[5] * g1.y; w[i][6] = f[6] * g1.z; w[i][7] = f[7] * g1.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[i][e] = 0.f;
+      const uint64_t policy = l2_policy_evict_first();
+      const __nv_bfloat16* Xs = p.X + (size_t)rank * p.W;
+      const uint32_t row_bytes = (uint32_t)p.W * 2;
+      for (int64_t j = 0; j < my_tiles; ++j) {
+        const int s = (int)(j % p.S);
+        if (j >= p.S &&
+            !mbar_wait_bounded(sbase + L.empty + 8 * s, (uint32_t)((j / p.S - 1) & 1),
+                               p.wait_limit_ns)) {
+          atomicOr(&g_qk_status, kStatusTimeout);
+          aborted = true;
+          break;
+        }
+        const int64_t t0 = (cid + j * ncl) * p.R;
+        const int nrows = (int)min64(p.R, p.T - t0);
+        const uint32_t bar = sbase + L.full + 8 * s;
+        const uint32_t dst = sbase + L.ring + (uint32_t)s * stage_bytes;
+        mbar_arrive_expect_tx(bar, nrows * row_bytes + (j == 0 ? p.missing_tx : 0u));
+        if (N == 1) {
+          bulk_g2s(dst, Xs + (size_t)t0 * p.H, nrows * row_bytes, bar, policy);
+        } else {
+          for (int r = 0; r < nrows; ++r)
+            bulk_g2s(dst + r * row_bytes, Xs + (size_t)(t0 + r) * p.H, row_bytes, bar, policy);
+        }
       }
+      // let the last copies land before this CTA can retire
+      for (int64_t j = max64(0, my_tiles - p.S); j < my_tiles && !aborted; ++j)
+        (void)mbar_wait_bounded(sbase + L.full + 8 * (int)(j % p.S), (uint32_t)((j / p.S) & 1),
+                                p.wait_limit_ns);
     }
-    cluster_wait_acquire();
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- consumer warps
+    const int row = tid / p.G;
+    const int g = tid - row * p.G;
+    const int wir = g >> 5;
+    const bool exchange = (N > 1) || (wpr > 1);
+    const uint32_t gam_lo = sbase + L.gam;
+    const uint32_t gam_hi = gam_lo + (uint32_t)p.nvec * 16;
+    for (int64_t j = 0; j < my_tiles; ++j) {
+      const int s = (int)(j % p.S);
+      const int64_t t = (cid + j * ncl) * p.R + row;
+      const bool valid = t < p.T;
 
-    // Every thread of this CTA has finished Phase A of tile j: stage s is
-    // free for tile j + S.
-    if (tid == 0 && !aborted && j + p.S < my_tiles) issue(j + p.S);
+      if (!mbar_wait_bounded(sbase + L.full + 8 * s, (uint32_t)((j / p.S) & 1),
+                             aborted ? 0 : p.wait_limit_ns)) {
+        if (!aborted) atomicOr(&g_qk_status, kStatusTimeout);
+        aborted = true;
+      }
 
-    // ---- Phase C: combine in rank order, scale, store the shard.
-    if (valid) {
-      const float* sl = part + (((size_t)(j & 1) * p.R + row) * N) * wpr;
-      float S = 0.f;
-      for (int k = 0; k < N * wpr; ++k) S += sl[k];
-      const float rinv = 1.0f / sqrtf(S / (float)p.H + p.eps);
-      __nv_bfloat16* yrow = p.Y + (size_t)t * p.H + (size_t)rank * p.W;
+      // ---- Phase A: this shard's sum of squares (fp32, packed pairs)
+      uint4 xr[VPT];
+      uint64_t acc = 0;  // {0.f, 0.f}
+      const uint32_t srow = sbase + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * p.W * 2;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = i * p.G + g;
-        if (v < p.nvec) {
-          uint4 o;
-          o.x = pack_bf16x2_rn(w[i][0] * rinv, w[i][1] * rinv);
-          o.y = pack_bf16x2_rn(w[i][2] * rinv, w[i][3] * rinv);
-          o.z = pack_bf16x2_rn(w[i][4] * rinv, w[i][5] * rinv);
-          o.w = pack_bf16x2_rn(w[i][6] * rinv, w[i][7] * rinv);
-          st_global_v4_stream(yrow + v * 8, o);
+        xr[i] = make_uint4(0, 0, 0, 0);
+        if (valid && v < p.nvec) xr[i] = ld_shared_v4(srow + v * 16);
+        const uint64_t a = bf16x2_to_f2(xr[i].x), b = bf16x2_to_f2(xr[i].y);
+        const uint64_t c = bf16x2_to_f2(xr[i].z), d = bf16x2_to_f2(xr[i].w);
+        acc = f2_fma(a, a, acc);
+        acc = f2_fma(b, b, acc);
+        acc = f2_fma(c, c, acc);
+        acc = f2_fma(d, d, acc);
+      }
+      // the stage's data is in registers: hand it back to the producer
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
+      const float ss = warp_sum(f2_lo(acc) + f2_hi(acc));
+
+      // ---- exchange: send this warp's partial to every shard of the row
+      const int b = (int)(j & 1);
+      const uint32_t xbar = sbase + L.xbar + 8 * (b * p.R + row);
+      const uint32_t slot0 = sbase + L.part + 4 * (uint32_t)((b * p.R + row) * N * wpr);
+      if (exchange) {
+        if (g == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(N * wpr * 4));
+        if (lane == 0) {
+          const uint32_t slot = slot0 + 4 * (rank * wpr + wir);
+#pragma unroll
+          for (int k = 0; k < N; ++k)
+            st_async_f32(map_to_rank(slot, k), ss, map_to_rank(xbar, k));
         }
       }
-      if (p.rinv_out != nullptr && rank == 0 && g == 0) p.rinv_out[t] = rinv;
+
+      // ---- Phase B (overlapping the exchange): w = x * gamma
+      uint64_t w[VPT][4];
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = min(i * p.G + g, p.nvec - 1);
+        const uint4 glo = ld_shared_v4(gam_lo + v * 16);
+        const uint4 ghi = ld_shared_v4(gam_hi + v * 16);
+        w[i][0] = f2_mul(bf16x2_to_f2(xr[i].x), f2(__uint_as_float(glo.x), __uint_as_float(glo.y)));
+        w[i][1] = f2_mul(bf16x2_to_f2(xr[i].y), f2(__uint_as_float(glo.z), __uint_as_float(glo.w)));
+        w[i][2] = f2_mul(bf16x2_to_f2(xr[i].z), f2(__uint_as_float(ghi.x), __uint_as_float(ghi.y)));
+        w[i][3] = f2_mul(bf16x2_to_f2(xr[i].w), f2(__uint_as_float(ghi.z), __uint_as_float(ghi.w)));
+      }
+
+      // ---- combine in rank order (then warp order within a shard)
+      float S = ss;
+      if (exchange) {
+        if (!mbar_wait_bounded(xbar, (uint32_t)((j >> 1) & 1), aborted ? 0 : p.wait_limit_ns)) {
+          if (!aborted) atomicOr(&g_qk_status, kStatusTimeout);
+          aborted = true;
+        }
+        const float* sl = reinterpret_cast<const float*>(smem + (slot0 - sbase));
+        S = 0.f;
+        for (int k = 0; k < N * wpr; ++k) S += sl[k];
+      }
+
+      // ---- Phase C: scale and store the shard
+      if (valid) {
+        const float rinv = 1.0f / sqrtf(S / (float)p.H + p.eps);
+        const uint64_t rr = f2(rinv, rinv);
+        __nv_bfloat16* yrow = p.Y + (size_t)t * p.H + (size_t)rank * p.W;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = i * p.G + g;
+          if (v < p.nvec) {
+            uint4 o;
+            const uint64_t y0 = f2_mul(w[i][0], rr), y1 = f2_mul(w[i][1], rr);
+            const uint64_t y2 = f2_mul(w[i][2], rr), y3 = f2_mul(w[i][3], rr);
+            o.x = pack_bf16x2_rn(f2_lo(y0), f2_hi(y0));
+            o.y = pack_bf16x2_rn(f2_lo(y1), f2_hi(y1));
+            o.z = pack_bf16x2_rn(f2_lo(y2), f2_hi(y2));
+            o.w = pack_bf16x2_rn(f2_lo(y3), f2_hi(y3));
+            st_global_v4_stream(yrow + v * 8, o);
+          }
+        }
+        if (p.rinv_out != nullptr && rank == 0 && g == 0) p.rinv_out[t] = rinv;
+      }
     }
   }
-  // A CTA with no tiles still matches its start-up arrive.
-  if (N > 1 && first) cluster_wait_acquire();
 
-  // After a timeout, let copies still in flight land before the CTA's shared
-  // memory is released (bounded again).
-  if (aborted && tid == 0) {
-    for (int64_t j = max64(0, my_tiles - p.S); j < my_tiles; ++j)
-      (void)mbar_wait_bounded(smem_addr(&full[j % p.S]), (uint32_t)((j / p.S) & 1),
-                              p.wait_limit_ns);
+  // No CTA leaves while a peer may still store into its shared memory.
+  if (N > 1) {
+    cluster_arrive_release();
+    cluster_wait_acquire();
   }
 }
 
@@ -241,15 +296,6 @@ QkKernel pick_qk(int N, int vpt) {
   }
 }
 
-size_t qk_smem(int N, int S, int R, int W, int G) {
-  switch (N) {
-    case 1: return qk_smem_bytes<1>(S, R, W, G);
-    case 2: return qk_smem_bytes<2>(S, R, W, G);
-    case 4: return qk_smem_bytes<4>(S, R, W, G);
-    default: return qk_smem_bytes<8>(S, R, W, G);
-  }
-}
-
 }  // namespace
 
 int launch_qknorm(const void* X, const float* gamma, void* Y, float* rinv, int64_t T, int H,
@@ -259,25 +305,25 @@ int launch_qknorm(const void* X, const float* gamma, void* Y, float* rinv, int64
   const DeviceInfo& dev = device_info();
   if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
 
-  RowShape rs = choose_row_shape(nvec, tune.force_vpt);
+  const RowShape rs = choose_row_shape(nvec, tune.force_vpt);
   if (rs.G == 0) return fail(NTS_ERR_UNSUPPORTED, "shard row too wide: H/N = %d", W);
 
-  // Rows per tile: about 256 threads per CTA, fewer when T is small so that
-  // the tiles spread over the GPU.
+  // Rows per tile: about 256 consumer threads, fewer when T is small so
+  // that the tiles spread over the GPU.
   int R = std::max(1, 256 / rs.G);
   R = std::min(R, 16);
   while (R > 1 && (T + R - 1) / R < (int64_t)2 * dev.sm_count / N) R /= 2;
   if (tune.force_rows > 0) R = tune.force_rows;
-  if (R * rs.G > kMaxThreads) return fail(NTS_ERR_UNSUPPORTED, "tile of %d rows too large", R);
+  if (R * rs.G > kMaxConsumers) return fail(NTS_ERR_UNSUPPORTED, "tile of %d rows too large", R);
 
-  // Ring depth: as many stages (up to 4) as fit in ~100 KB, at least 2 when
-  // one row-tile allows it.
-  const size_t stage = (size_t)R * W * 2;
-  int S = 4;
-  while (S > 1 && qk_smem(N, S, R, W, rs.G) > (size_t)tune.smem_budget) --S;
+  // Ring depth: up to 6 stages within the shared-memory budget; the widest
+  // shards (whose staged gamma alone is up to 120 KB) fall back to fewer.
+  int S = 6;
+  while (S > 2 && qk_layout(N, S, R, W, rs.G).total > (uint32_t)tune.smem_budget) --S;
+  while (S > 1 && qk_layout(N, S, R, W, rs.G).total > (uint32_t)dev.max_smem_optin) --S;
   if (tune.force_stages > 0) S = tune.force_stages;
-  const size_t smem = qk_smem(N, S, R, W, rs.G);
-  if (smem > (size_t)dev.max_smem_optin || stage == 0)
+  const size_t smem = qk_layout(N, S, R, W, rs.G).total;
+  if (smem > (size_t)dev.max_smem_optin)
     return fail(NTS_ERR_UNSUPPORTED, "shard row too wide for shared memory: H/N = %d", W);
 
   QkKernel kern = pick_qk(N, rs.vpt);
@@ -300,7 +346,7 @@ int launch_qknorm(const void* X, const float* gamma, void* Y, float* rinv, int64
   prm.wait_limit_ns = tune.wait_limit_ns;
   prm.missing_tx = tune.missing_tx;
 
-  const int nthreads = R * rs.G;
+  const int nthreads = R * rs.G + 32;  // consumers + producer warp
   int rc = prepare_kernel((const void*)kern, smem);
   if (rc != NTS_OK) return rc;
 

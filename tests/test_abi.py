@@ -71,11 +71,12 @@ def test_qknorm_argument_checks(lib):
     assert _qk(lib, eps=float("nan")) == INVALID
     assert _qk(lib, eps=float("inf")) == INVALID
     assert _qk(lib, H=8, N=2) == UNSUPPORTED           # H/N = 4 is not a multiple of 8
-    assert _qk(lib, H=65536 * 2, N=2) == UNSUPPORTED   # shard wider than 32768
+    assert _qk(lib, H=30728 * 2, N=2) == UNSUPPORTED   # shard wider than 30720
     assert _qk(lib, X=MIS) == UNSUPPORTED
     assert _qk(lib, Y=MIS) == UNSUPPORTED
     assert _qk(lib, T=0) == OK                           # nothing launched
-    assert "multiple" in lib.nts_last_error().decode() or True
+    assert _qk(lib, T=0, X=None, g=None, Y=None) == OK  # empty tensors
+    assert _qk(lib, T=0, N=3) == INVALID
 
 
 def _mx(lib, fn, X=A16, codes=A16, scales=A16, T=4, D=256, eps=1e-6, B=32, fmt=0, p=2):
@@ -100,6 +101,8 @@ def test_mx_argument_checks(lib, fn):
     assert _mx(lib, fn, D=65536) == UNSUPPORTED
     assert _mx(lib, fn, X=MIS) == UNSUPPORTED
     assert _mx(lib, fn, T=0) == OK
+    assert _mx(lib, fn, T=0, X=None, codes=None, scales=None) == OK
+    assert _mx(lib, fn, T=0, B=8) == INVALID
     assert len(lib.nts_last_error()) > 0
 
 
