@@ -2,7 +2,8 @@
 
 One step = one pass of every hot-path kernel over the prefill workloads:
   * layerwise QK-RMSNorm of Q and of K, each [8192, 5120] bf16, 1% outlier
-    channels, N = 4 cluster shards (13B-like prefill);
+    channels, N = 4 cluster shards (13B-like prefill), both tensors in one
+    launch;
   * RMSNorm + MXFP8 cast, MXNorm p = 1 and MXNorm p = 2 (+ MXFP8 cast) of
     X [65536, 4096] bf16, B = 32, E4M3 values + E8M0 scales.
 
@@ -43,8 +44,7 @@ QK_T, QK_H, QK_N = 8192, 5120, 4
 MX_T, MX_D, MX_B = 65536, 4096, 32
 EPS = 1e-6
 
-KERNELS = ["qknorm_rms[Q]", "qknorm_rms[K]", "rmsnorm_mxcast", "mxnorm_cast[p=1]",
-           "mxnorm_cast[p=2]"]
+KERNELS = ["qknorm_rms_qk[Q+K]", "rmsnorm_mxcast", "mxnorm_cast[p=1]", "mxnorm_cast[p=2]"]
 KERNEL_SOURCES = {
     "qknorm_rms": "normalization_token_split_gb300/csrc/qknorm_cluster.cu",
     "mx": "normalization_token_split_gb300/csrc/mx_norm_cast.cu",
@@ -60,8 +60,8 @@ def mx_bytes(T, D, B):
 
 
 def step_bytes():
-    per = {"qknorm_rms[Q]": qk_bytes(QK_T, QK_H), "qknorm_rms[K]": qk_bytes(QK_T, QK_H)}
-    for k in KERNELS[2:]:
+    per = {"qknorm_rms_qk[Q+K]": 2 * qk_bytes(QK_T, QK_H)}
+    for k in KERNELS[1:]:
         per[k] = mx_bytes(MX_T, MX_D, MX_B)
     return per
 
@@ -82,7 +82,7 @@ def measured_peaks():
 
 def workload_config():
     return {
-        "workload": ("prefill layer norms: QK-RMSNorm Q,K [8192,5120] N=4 + "
+        "workload": ("prefill layer norms: QK-RMSNorm Q,K [8192,5120] N=4 (one launch) + "
                      "RMSNorm+MXFP8, MXNorm p=1, MXNorm p=2 of [65536,4096] B=32 E4M3"),
         "qk": {"T": QK_T, "H": QK_H, "N": QK_N, "tensors": ["Q", "K"], "eps": EPS,
                "x": "bf16 N(0,1), 1% of channels x20", "gamma": "fp32 N(1,0.1)"},
@@ -228,14 +228,14 @@ def run_gpu(args):
     X, _ = workloads.mx_inputs(MX_T, MX_D, seed=4000 + MX_T, device=dev)
     Yq, Yk = torch.empty_like(Q), torch.empty_like(K)
     outs = {}
-    for name in KERNELS[2:]:
+    for name in KERNELS[1:]:
         outs[name] = (torch.empty(MX_T, MX_D, dtype=torch.uint8, device=dev),
                       torch.empty(MX_T, MX_D // MX_B, dtype=torch.uint8, device=dev))
     stream = torch.cuda.current_stream()
 
     launches = [
-        ("qknorm_rms[Q]", lambda: nts.qknorm_rms(Q, gq, eps=EPS, N=QK_N, out=Yq)),
-        ("qknorm_rms[K]", lambda: nts.qknorm_rms(K, gk, eps=EPS, N=QK_N, out=Yk)),
+        ("qknorm_rms_qk[Q+K]", lambda: nts.qknorm_rms_qk(Q, gq, K, gk, eps=EPS, N=QK_N,
+                                                         out_q=Yq, out_k=Yk)),
         ("rmsnorm_mxcast", lambda: nts.rmsnorm_mxcast(
             X, None, eps=EPS, B=MX_B, fmt="e4m3", codes=outs["rmsnorm_mxcast"][0],
             scales=outs["rmsnorm_mxcast"][1])),
@@ -322,6 +322,8 @@ def run_gpu(args):
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world)
+    if not args.no_decode:
+        result["decode_qk_us_per_call"] = decode_latency(nts, torch, dev)
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
@@ -340,9 +342,9 @@ def run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world):
     Xd = torch.empty_like(X)
     Qd, Kd = torch.empty_like(Q), torch.empty_like(K)
     Yqd, Ykd = torch.empty_like(Q), torch.empty_like(K)
-    codes_h = {n: torch.empty(MX_T, MX_D, dtype=torch.uint8).pin_memory() for n in KERNELS[2:]}
+    codes_h = {n: torch.empty(MX_T, MX_D, dtype=torch.uint8).pin_memory() for n in KERNELS[1:]}
     scales_h = {n: torch.empty(MX_T, MX_D // MX_B, dtype=torch.uint8).pin_memory()
-                for n in KERNELS[2:]}
+                for n in KERNELS[1:]}
     codes_d = torch.empty(MX_T, MX_D, dtype=torch.uint8, device=dev)
     scales_d = torch.empty(MX_T, MX_D // MX_B, dtype=torch.uint8, device=dev)
 
@@ -377,6 +379,37 @@ def run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(elapsed / steps * 1e3, 4),
             "path": "nts_*_host C ABI entry points, pinned host buffers"}
+
+
+def decode_latency(nts, torch, dev):
+    """Decode-shaped QK-Norm (Q and K each [T, 4096], 7B-like): GPU time per
+    fused Q+K call, from CUDA-graph replays of 20 back-to-back calls (the
+    host's launch cost is outside the graph)."""
+    import workloads
+    out = {}
+    for N in (1, 2, 4, 8):
+        for T in (1, 8, 64, 256):
+            Q, gq = workloads.qk_inputs(T, 4096, seed=T, device=dev)
+            K, gk = workloads.qk_inputs(T, 4096, seed=T + 1, device=dev)
+            Yq, Yk = torch.empty_like(Q), torch.empty_like(K)
+            call = lambda: nts.qknorm_rms_qk(Q, gq, K, gk, eps=EPS, N=N, out_q=Yq, out_k=Yk)
+            call()                                  # fills the launch-shape caches
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for _ in range(20):
+                    call()
+            graph.replay()
+            torch.cuda.synchronize()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(10):
+                graph.replay()
+            e.record()
+            torch.cuda.synchronize()
+            out[f"N={N},T={T}"] = round(s.elapsed_time(e) * 1e3 / 200, 2)
+    nts.check_status()
+    return out
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -473,6 +506,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["nts", "reference"], default="nts")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

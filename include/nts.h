@@ -99,6 +99,22 @@ NTS_API int nts_qknorm_rms(const void *X_dev, const float *gamma_dev, void *Y_de
                    void *stream);
 
 /*
+ * nts_qknorm_rms_qk -- nts_qknorm_rms of a token batch's Q and K in ONE
+ * launch (one persistent grid walks the tiles of both tensors).  Q and K may
+ * have different widths (Hq, Hk: e.g. grouped-query attention, where K is
+ * narrower) and their own gains; they share T, eps and N.  Each tensor obeys
+ * the argument rules of nts_qknorm_rms (in-place Yq == Q, Yk == K allowed;
+ * rinv_* nullable); the same errors apply.  Layerwise QK-Norm normalizes Q
+ * and K separately (SwiftQK Sec. II.A); fusing the two calls halves the
+ * launches, which dominate at decode sizes.
+ */
+NTS_API int nts_qknorm_rms_qk(const void *Q_dev, const float *gamma_q_dev, void *Yq_dev,
+                              float *rinv_q_dev, const void *K_dev,
+                              const float *gamma_k_dev, void *Yk_dev, float *rinv_k_dev,
+                              int64_t T, int64_t Hq, int64_t Hk, float eps, int N,
+                              void *stream);
+
+/*
  * nts_rmsnorm_mxcast -- RMSNorm fused with the MX cast (MXNorm card,
  * Fig. 1 caption, left graph; Fig. 8 "normalization and casting fused into a
  * single kernel"):

@@ -15,22 +15,23 @@ struct MxShape {
   int G = 0;    // consumer threads per row
 };
 
-// One warp per row while a thread holds at most 8 blocks; wider rows take
-// more warps.  bpt is the smallest of {1, 2, 4, 8} that covers the row.
+int threads_for(int K, int bpt) { return ((K + bpt - 1) / bpt + 31) / 32 * 32; }
+
+// Blocks per thread: up to 4 (measured best on GB300: enough independent
+// blocks per thread for latency hiding without spilling); 8 only when a row
+// would otherwise need more than the CTA's consumer threads.
 MxShape choose_mx_shape(int K, int force_bpt) {
-  static const int opts[] = {1, 2, 4, 8};
-  MxShape best;
-  for (int bpt : opts) {
-    if (force_bpt > 0 && bpt != force_bpt) continue;
-    int G = (K + bpt - 1) / bpt;
-    G = (G + 31) / 32 * 32;
-    if (G > kMaxConsumers) continue;
-    if (best.G == 0 || G < best.G || (G == best.G && bpt < best.bpt)) {
-      best.bpt = bpt;
-      best.G = G;
-    }
+  MxShape sh;
+  if (force_bpt > 0) {
+    sh.bpt = force_bpt;
+  } else {
+    sh.bpt = 1;
+    while (sh.bpt < 4 && K > 32 * sh.bpt) sh.bpt *= 2;
+    if (threads_for(K, sh.bpt) > kMaxConsumers) sh.bpt = 8;
   }
-  return best;
+  sh.G = threads_for(K, sh.bpt);
+  if (sh.G > kMaxConsumers) sh.G = 0;
+  return sh;
 }
 
 }  // namespace
@@ -45,15 +46,19 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   const MxShape sh = choose_mx_shape(K, tune.force_vpt);
   if (sh.G == 0) return fail(NTS_ERR_UNSUPPORTED, "row too wide: D = %d", D);
 
-  // Rows per tile: about four consumer warps, and a ring of at least three
-  // stages inside the shared-memory budget; fewer rows when T is small.
+  // Rows per tile: about four consumer warps and at least 8 KB per stage;
+  // fewer rows when T is small so that the tiles spread over the GPU.
   int R = std::max(1, 128 / sh.G);
-  while (R > 1 && mx_layout(3, R, D, sh.G).total > (uint32_t)tune.smem_budget) R /= 2;
+  R = std::max(R, (8192 + 2 * D - 1) / (2 * D));
+  R = std::min(R, std::max(1, kMaxConsumers / sh.G));
   while (R > 1 && (rq.T + R - 1) / R < (int64_t)2 * dev.sm_count) R /= 2;
   if (tune.force_rows > 0) R = tune.force_rows;
   if (R * sh.G > kMaxConsumers) return fail(NTS_ERR_UNSUPPORTED, "tile of %d rows too large", R);
 
-  int S = 6;
+  // Ring depth: two large stages or up to four small ones (measured: more
+  // CTAs per SM beat deeper rings once a stage is 32 KB).
+  const int stage = R * D * 2;
+  int S = stage >= 32768 ? 2 : (stage >= 12288 ? 3 : 4);
   while (S > 2 && mx_layout(S, R, D, sh.G).total > (uint32_t)tune.smem_budget) --S;
   while (S > 1 && mx_layout(S, R, D, sh.G).total > (uint32_t)dev.max_smem_optin) --S;
   if (tune.force_stages > 0) S = tune.force_stages;

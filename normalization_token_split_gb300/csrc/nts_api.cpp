@@ -321,8 +321,22 @@ int nts_qknorm_rms(const void* X_dev, const float* gamma_dev, void* Y_dev, float
   int rc = validate_qk(X_dev, gamma_dev, Y_dev, rinv_dev, T, H, eps, N);
   if (rc != NTS_OK) return rc;
   if (T == 0) return NTS_OK;
-  return launch_qknorm(X_dev, gamma_dev, Y_dev, rinv_dev, T, (int)H, eps, N,
-                       static_cast<cudaStream_t>(stream), current_tuning());
+  const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, T, H};
+  return launch_qknorm(&rq, 1, eps, N, static_cast<cudaStream_t>(stream), current_tuning());
+}
+
+int nts_qknorm_rms_qk(const void* Q_dev, const float* gamma_q_dev, void* Yq_dev,
+                      float* rinv_q_dev, const void* K_dev, const float* gamma_k_dev,
+                      void* Yk_dev, float* rinv_k_dev, int64_t T, int64_t Hq, int64_t Hk,
+                      float eps, int N, void* stream) {
+  int rc = validate_qk(Q_dev, gamma_q_dev, Yq_dev, rinv_q_dev, T, Hq, eps, N);
+  if (rc != NTS_OK) return rc;
+  rc = validate_qk(K_dev, gamma_k_dev, Yk_dev, rinv_k_dev, T, Hk, eps, N);
+  if (rc != NTS_OK) return rc;
+  if (T == 0) return NTS_OK;
+  const QkRequest rq[2] = {{Q_dev, gamma_q_dev, Yq_dev, rinv_q_dev, T, Hq},
+                           {K_dev, gamma_k_dev, Yk_dev, rinv_k_dev, T, Hk}};
+  return launch_qknorm(rq, 2, eps, N, static_cast<cudaStream_t>(stream), current_tuning());
 }
 
 int nts_rmsnorm_mxcast(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,

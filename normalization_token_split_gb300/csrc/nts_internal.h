@@ -74,8 +74,18 @@ struct MxRequest {
   double corr;  // c(B, p) for MXNorm
 };
 
-int launch_qknorm(const void* X, const float* gamma, void* Y, float* rinv, int64_t T, int H,
-                  float eps, int N, cudaStream_t stream, const LaunchTuning& tune);
+struct QkRequest {
+  const void* X;
+  const float* gamma;
+  void* Y;
+  float* rinv;
+  int64_t T;
+  int64_t H;
+};
+
+// One launch normalizing 1 or 2 tensors (Q and K) with the same N.
+int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, cudaStream_t stream,
+                  const LaunchTuning& tune);
 int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune);
 
 int read_and_clear_qk_status(unsigned* out);

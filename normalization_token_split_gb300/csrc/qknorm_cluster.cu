@@ -40,27 +40,37 @@ namespace nts {
 
 __device__ unsigned int g_qk_status;  // kStatusTimeout bits, read by nts_check_status
 
-struct QkParams {
+// One tensor normalized by a launch (a launch covers one or two: Q and K).
+struct QkTensor {
   const __nv_bfloat16* X;
   const float* gamma;
   __nv_bfloat16* Y;
   float* rinv_out;
   int64_t T;
-  int64_t ntiles;
-  int H;        // full row width H_total
-  int W;        // H / N, the columns of one shard
-  int nvec;     // W / 8 16-byte vectors per shard row
-  int G;        // consumer threads per row (multiple of 32)
-  int R;        // rows per tile
-  int S;        // ring stages
+  int64_t ntiles;  // ceil(T / R)
+  int H;           // full row width H_total
+  int W;           // H / N, the columns of one shard
+  int nvec;        // W / 8 16-byte vectors per shard row
+  uint32_t gam;    // shared-memory offset of this tensor's staged gamma
+};
+
+struct QkParams {
+  QkTensor ten[2];
+  int ntensors;
+  int64_t ntiles;  // tiles of all tensors; tensor 0's come first
+  int Wmax;        // widest shard of the tensors
+  int G;           // consumer threads per row (multiple of 32)
+  int R;           // rows per tile
+  int S;           // ring stages
   float eps;
   uint64_t wait_limit_ns;
   uint32_t missing_tx;  // test hook: bytes expected on the first stage but never sent
 };
 
 // Shared memory layout (bytes, in order):
-//   ring  [S][R][W] bf16          the staged shard rows
-//   gam   [2][nvec] float4        gamma of this shard, halves of each vector
+//   ring  [S][R][Wmax] bf16       the staged shard rows
+//   gam   per tensor [2][nvec] float4: gamma of this shard, the low and
+//         high halves of each 8-value vector
 //   full  [S], empty [S]          ring mbarriers
 //   xbar  [2][R]                  exchange mbarriers (double-buffered by tile)
 //   part  [2][R][N][WPR] f32      partial sums received from every warp of
@@ -69,16 +79,27 @@ struct QkLayout {
   uint32_t ring, gam, full, empty, xbar, part, total;
 };
 
-__host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int W, int G) {
+__host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int Wsum, int G) {
   QkLayout L;
   L.ring = 0;
-  L.gam = L.ring + (uint32_t)S * R * W * 2;
-  L.full = L.gam + (uint32_t)W * 4;
+  L.gam = L.ring + (uint32_t)S * R * Wmax * 2;
+  L.full = L.gam + (uint32_t)Wsum * 4;
   L.empty = L.full + (uint32_t)S * 8;
   L.xbar = L.empty + (uint32_t)S * 8;
   L.part = L.xbar + (uint32_t)2 * R * 8;
   L.total = L.part + (uint32_t)2 * R * N * (G / 32) * 4;
   return L;
+}
+
+// Tensor and first row of the tile with global index `tile`.
+__device__ __forceinline__ int qk_tile(const QkParams& p, int64_t tile, int64_t* t0) {
+  const int k = (p.ntensors > 1 && tile >= p.ten[0].ntiles) ? 1 : 0;
+  *t0 = (tile - (k ? p.ten[0].ntiles : 0)) * p.R;
+  return k;
+}
+
+__device__ __forceinline__ void bar_sync_named(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 template <int N, int VPT>
@@ -91,21 +112,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
   const int nconsumer = p.R * p.G;
   const int lane = tid & 31;
   const int wpr = p.G >> 5;
-  const QkLayout L = qk_layout(N, p.S, p.R, p.W, p.G);
+  const int Wsum = p.ten[0].W + (p.ntensors > 1 ? p.ten[1].W : 0);
+  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, Wsum, p.G);
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t stage_bytes = (uint32_t)p.R * p.W * 2;
+  const uint32_t stage_bytes = (uint32_t)p.R * p.Wmax * 2;
   const int64_t my_tiles = cid < p.ntiles ? (p.ntiles - 1 - cid) / ncl + 1 : 0;
 
-  // gamma of this shard, split into the low and high halves of each
-  // 8-value vector so that consecutive lanes read consecutive 16 bytes
-  {
-    const float4* gsrc = reinterpret_cast<const float4*>(p.gamma + (size_t)rank * p.W);
-    float4* gam = reinterpret_cast<float4*>(smem + L.gam);
-    for (int q = tid; q < p.nvec; q += blockDim.x) {
-      gam[q] = __ldg(gsrc + 2 * q);
-      gam[p.nvec + q] = __ldg(gsrc + 2 * q + 1);
-    }
-  }
   if (tid == 0) {
     for (int s = 0; s < p.S; ++s) {
       mbar_init(sbase + L.full + 8 * s, 1);
@@ -115,20 +127,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
     fence_mbar_init();
   }
   __syncthreads();
-  // Every CTA of the cluster is running and has initialised its barriers
-  // before anyone stores into a peer's shared memory.
-  if (N > 1) {
-    cluster_arrive_release();
-    cluster_wait_acquire();
-  }
 
-  bool aborted = false;
   if (tid >= nconsumer) {
     // ------------------------------------------------------ producer warp
+    // It touches only this CTA's shared memory, so it starts the ring at
+    // once; its half of the cluster start-up barrier is completed later.
+    if (N > 1) cluster_arrive_relaxed();
     if (lane == 0) {
+      bool aborted = false;
       const uint64_t policy = l2_policy_evict_first();
-      const __nv_bfloat16* Xs = p.X + (size_t)rank * p.W;
-      const uint32_t row_bytes = (uint32_t)p.W * 2;
       for (int64_t j = 0; j < my_tiles; ++j) {
         const int s = (int)(j % p.S);
         if (j >= p.S &&
@@ -138,16 +145,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
           aborted = true;
           break;
         }
-        const int64_t t0 = (cid + j * ncl) * p.R;
-        const int nrows = (int)min64(p.R, p.T - t0);
+        int64_t t0;
+        const QkTensor& tn = p.ten[qk_tile(p, cid + j * ncl, &t0)];
+        const int nrows = (int)min64(p.R, tn.T - t0);
+        const uint32_t row_bytes = (uint32_t)tn.W * 2;
         const uint32_t bar = sbase + L.full + 8 * s;
         const uint32_t dst = sbase + L.ring + (uint32_t)s * stage_bytes;
+        const __nv_bfloat16* src = tn.X + (size_t)t0 * tn.H + (size_t)rank * tn.W;
         mbar_arrive_expect_tx(bar, nrows * row_bytes + (j == 0 ? p.missing_tx : 0u));
         if (N == 1) {
-          bulk_g2s(dst, Xs + (size_t)t0 * p.H, nrows * row_bytes, bar, policy);
+          bulk_g2s(dst, src, nrows * row_bytes, bar, policy);
         } else {
           for (int r = 0; r < nrows; ++r)
-            bulk_g2s(dst + r * row_bytes, Xs + (size_t)(t0 + r) * p.H, row_bytes, bar, policy);
+            bulk_g2s(dst + r * row_bytes, src + (size_t)r * tn.H, row_bytes, bar, policy);
         }
       }
       // let the last copies land before this CTA can retire
@@ -156,18 +166,40 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
                                 p.wait_limit_ns);
     }
     __syncwarp();
+    if (N > 1) cluster_wait_acquire();
   } else {
     // ------------------------------------------------------- consumer warps
+    // gamma of this shard, split into the low and high halves of each
+    // 8-value vector so that consecutive lanes read consecutive 16 bytes
+    for (int k = 0; k < p.ntensors; ++k) {
+      const QkTensor& tn = p.ten[k];
+      const float4* gsrc = reinterpret_cast<const float4*>(tn.gamma + (size_t)rank * tn.W);
+      float4* gam = reinterpret_cast<float4*>(smem + tn.gam);
+      for (int q = tid; q < tn.nvec; q += nconsumer) {
+        gam[q] = __ldg(gsrc + 2 * q);
+        gam[tn.nvec + q] = __ldg(gsrc + 2 * q + 1);
+      }
+    }
+    bar_sync_named(1, nconsumer);
+    // Every CTA of the cluster is running and has initialised its barriers
+    // before anyone stores into a peer's shared memory.
+    if (N > 1) {
+      cluster_arrive_release();
+      cluster_wait_acquire();
+    }
+
     const int row = tid / p.G;
     const int g = tid - row * p.G;
     const int wir = g >> 5;
     const bool exchange = (N > 1) || (wpr > 1);
-    const uint32_t gam_lo = sbase + L.gam;
-    const uint32_t gam_hi = gam_lo + (uint32_t)p.nvec * 16;
+    bool aborted = false;
     for (int64_t j = 0; j < my_tiles; ++j) {
       const int s = (int)(j % p.S);
-      const int64_t t = (cid + j * ncl) * p.R + row;
-      const bool valid = t < p.T;
+      int64_t t0;
+      const QkTensor& tn = p.ten[qk_tile(p, cid + j * ncl, &t0)];
+      const int64_t t = t0 + row;
+      const bool valid = t < tn.T;
+      const int nvec = tn.nvec;
 
       if (!mbar_wait_bounded(sbase + L.full + 8 * s, (uint32_t)((j / p.S) & 1),
                              aborted ? 0 : p.wait_limit_ns)) {
@@ -178,12 +210,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
       // ---- Phase A: this shard's sum of squares (fp32, packed pairs)
       uint4 xr[VPT];
       uint64_t acc = 0;  // {0.f, 0.f}
-      const uint32_t srow = sbase + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * p.W * 2;
+      const uint32_t srow = sbase + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * tn.W * 2;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = i * p.G + g;
         xr[i] = make_uint4(0, 0, 0, 0);
-        if (valid && v < p.nvec) xr[i] = ld_shared_v4(srow + v * 16);
+        if (valid && v < nvec) xr[i] = ld_shared_v4(srow + v * 16);
         const uint64_t a = bf16x2_to_f2(xr[i].x), b = bf16x2_to_f2(xr[i].y);
         const uint64_t c = bf16x2_to_f2(xr[i].z), d = bf16x2_to_f2(xr[i].w);
         acc = f2_fma(a, a, acc);
@@ -211,10 +243,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
       }
 
       // ---- Phase B (overlapping the exchange): w = x * gamma
+      const uint32_t gam_lo = sbase + tn.gam;
+      const uint32_t gam_hi = gam_lo + (uint32_t)nvec * 16;
       uint64_t w[VPT][4];
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
-        const int v = min(i * p.G + g, p.nvec - 1);
+        const int v = min(i * p.G + g, nvec - 1);
         const uint4 glo = ld_shared_v4(gam_lo + v * 16);
         const uint4 ghi = ld_shared_v4(gam_hi + v * 16);
         w[i][0] = f2_mul(bf16x2_to_f2(xr[i].x), f2(__uint_as_float(glo.x), __uint_as_float(glo.y)));
@@ -237,13 +271,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
 
       // ---- Phase C: scale and store the shard
       if (valid) {
-        const float rinv = 1.0f / sqrtf(S / (float)p.H + p.eps);
+        const float rinv = 1.0f / sqrtf(S / (float)tn.H + p.eps);
         const uint64_t rr = f2(rinv, rinv);
-        __nv_bfloat16* yrow = p.Y + (size_t)t * p.H + (size_t)rank * p.W;
+        __nv_bfloat16* yrow = tn.Y + (size_t)t * tn.H + (size_t)rank * tn.W;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
           const int v = i * p.G + g;
-          if (v < p.nvec) {
+          if (v < nvec) {
             uint4 o;
             const uint64_t y0 = f2_mul(w[i][0], rr), y1 = f2_mul(w[i][1], rr);
             const uint64_t y2 = f2_mul(w[i][2], rr), y3 = f2_mul(w[i][3], rr);
@@ -254,7 +288,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
             st_global_v4_stream(yrow + v * 8, o);
           }
         }
-        if (p.rinv_out != nullptr && rank == 0 && g == 0) p.rinv_out[t] = rinv;
+        if (tn.rinv_out != nullptr && rank == 0 && g == 0) tn.rinv_out[t] = rinv;
       }
     }
   }
@@ -298,53 +332,73 @@ QkKernel pick_qk(int N, int vpt) {
 
 }  // namespace
 
-int launch_qknorm(const void* X, const float* gamma, void* Y, float* rinv, int64_t T, int H,
-                  float eps, int N, cudaStream_t stream, const LaunchTuning& tune) {
-  const int W = H / N;
-  const int nvec = W / 8;
+int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, cudaStream_t stream,
+                  const LaunchTuning& tune) {
   const DeviceInfo& dev = device_info();
   if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
+  int Wmax = 0, Wsum = 0;
+  int64_t Tsum = 0;
+  for (int k = 0; k < ntensors; ++k) {
+    Wmax = std::max(Wmax, (int)(rq[k].H / N));
+    Wsum += (int)(rq[k].H / N);
+    Tsum += rq[k].T;
+  }
 
-  const RowShape rs = choose_row_shape(nvec, tune.force_vpt);
-  if (rs.G == 0) return fail(NTS_ERR_UNSUPPORTED, "shard row too wide: H/N = %d", W);
+  // The row shape (vectors per thread, threads per row) fits the widest
+  // shard; narrower shards leave the extra slots idle.
+  const RowShape rs = choose_row_shape(Wmax / 8, tune.force_vpt);
+  if (rs.G == 0) return fail(NTS_ERR_UNSUPPORTED, "shard row too wide: H/N = %d", Wmax);
 
-  // Rows per tile: about 256 consumer threads, fewer when T is small so
-  // that the tiles spread over the GPU.
-  int R = std::max(1, 256 / rs.G);
-  R = std::min(R, 16);
-  while (R > 1 && (T + R - 1) / R < (int64_t)2 * dev.sm_count / N) R /= 2;
+  // Rows per tile: up to four (at most 256 consumer threads: the kernel
+  // keeps about 120 registers per thread, so larger CTAs cost residency),
+  // fewer when there are few tokens so that the tiles spread over the GPU.
+  int R = std::max(1, std::min(4, 256 / rs.G));
+  while (R > 1 && (Tsum + R - 1) / R < (int64_t)2 * dev.sm_count / N) R /= 2;
   if (tune.force_rows > 0) R = tune.force_rows;
   if (R * rs.G > kMaxConsumers) return fail(NTS_ERR_UNSUPPORTED, "tile of %d rows too large", R);
 
-  // Ring depth: up to 6 stages within the shared-memory budget; the widest
+  // Ring depth: up to 4 stages within the shared-memory budget; the widest
   // shards (whose staged gamma alone is up to 120 KB) fall back to fewer.
-  int S = 6;
-  while (S > 2 && qk_layout(N, S, R, W, rs.G).total > (uint32_t)tune.smem_budget) --S;
-  while (S > 1 && qk_layout(N, S, R, W, rs.G).total > (uint32_t)dev.max_smem_optin) --S;
+  int S = 4;
+  while (S > 2 && qk_layout(N, S, R, Wmax, Wsum, rs.G).total > (uint32_t)tune.smem_budget) --S;
+  while (S > 1 && qk_layout(N, S, R, Wmax, Wsum, rs.G).total > (uint32_t)dev.max_smem_optin) --S;
   if (tune.force_stages > 0) S = tune.force_stages;
-  const size_t smem = qk_layout(N, S, R, W, rs.G).total;
+  const QkLayout L = qk_layout(N, S, R, Wmax, Wsum, rs.G);
+  const size_t smem = L.total;
   if (smem > (size_t)dev.max_smem_optin)
-    return fail(NTS_ERR_UNSUPPORTED, "shard row too wide for shared memory: H/N = %d", W);
+    return fail(NTS_ERR_UNSUPPORTED, "shard row too wide for shared memory: H/N = %d", Wmax);
 
   QkKernel kern = pick_qk(N, rs.vpt);
   if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for N=%d vpt=%d", N, rs.vpt);
 
-  QkParams prm;
-  prm.X = static_cast<const __nv_bfloat16*>(X);
-  prm.gamma = gamma;
-  prm.Y = static_cast<__nv_bfloat16*>(Y);
-  prm.rinv_out = rinv;
-  prm.T = T;
-  prm.ntiles = (T + R - 1) / R;
-  prm.H = H;
-  prm.W = W;
-  prm.nvec = nvec;
+  QkParams prm = {};
+  uint32_t gam = L.gam;
+  int64_t ntiles = 0;
+  for (int k = 0; k < ntensors; ++k) {
+    QkTensor& tn = prm.ten[k];
+    tn.X = static_cast<const __nv_bfloat16*>(rq[k].X);
+    tn.gamma = rq[k].gamma;
+    tn.Y = static_cast<__nv_bfloat16*>(rq[k].Y);
+    tn.rinv_out = rq[k].rinv;
+    tn.T = rq[k].T;
+    tn.ntiles = (rq[k].T + R - 1) / R;
+    tn.H = (int)rq[k].H;
+    tn.W = (int)(rq[k].H / N);
+    tn.nvec = tn.W / 8;
+    tn.gam = gam;
+    gam += (uint32_t)tn.W * 4;
+    ntiles += tn.ntiles;
+  }
+  prm.ntensors = ntensors;
+  prm.ntiles = ntiles;
+  prm.Wmax = Wmax;
   prm.G = rs.G;
   prm.R = R;
   prm.S = S;
   prm.eps = eps;
   prm.wait_limit_ns = tune.wait_limit_ns;
   prm.missing_tx = tune.missing_tx;
+  if (ntiles == 0) return NTS_OK;
 
   const int nthreads = R * rs.G + 32;  // consumers + producer warp
   int rc = prepare_kernel((const void*)kern, smem);
@@ -365,13 +419,13 @@ int launch_qknorm(const void* X, const float* gamma, void* Y, float* rinv, int64
   int64_t max_clusters = 0;
   rc = max_active_clusters((const void*)kern, cfg, N, &max_clusters);
   if (rc != NTS_OK) return rc;
-  int64_t ncl = std::min<int64_t>(prm.ntiles, max_clusters);
-  if (tune.force_grid > 0) ncl = std::min<int64_t>(prm.ntiles, tune.force_grid);
+  int64_t ncl = std::min<int64_t>(ntiles, max_clusters);
+  if (tune.force_grid > 0) ncl = std::min<int64_t>(ntiles, tune.force_grid);
   cfg.gridDim = dim3((unsigned)(ncl * N));
 
-  log_launch("qknorm_rms", "T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d smem=%zu clusters=%lld/%lld",
-             (long long)T, H, N, rs.vpt, rs.G, R, S, smem, (long long)ncl,
-             (long long)max_clusters);
+  log_launch("qknorm_rms", "tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d smem=%zu "
+             "clusters=%lld/%lld", ntensors, (long long)rq[0].T, (int)rq[0].H, N, rs.vpt, rs.G,
+             R, S, smem, (long long)ncl, (long long)max_clusters);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e != cudaSuccess) return fail_cuda(e, "launching qknorm_rms");
   return NTS_OK;

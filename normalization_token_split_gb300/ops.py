@@ -74,6 +74,31 @@ def qknorm_rms(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, N: int =
     return out, rinv
 
 
+def qknorm_rms_qk(q: torch.Tensor, gamma_q: torch.Tensor, k: torch.Tensor,
+                  gamma_k: torch.Tensor, eps: float = 1e-6, N: int = 1,
+                  out_q: Optional[torch.Tensor] = None, out_k: Optional[torch.Tensor] = None,
+                  rinv_q: Optional[torch.Tensor] = None, rinv_k: Optional[torch.Tensor] = None,
+                  want_rinv: bool = False, stream=None):
+    """Layerwise QK-RMSNorm of Q [T, Hq] and K [T, Hk] in one launch.
+    Returns (yq, yk, rinv_q or None, rinv_k or None)."""
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("gamma_q", gamma_q, torch.float32), ("gamma_k", gamma_k, torch.float32)):
+        _need_cuda(name, t, dt)
+    T, Hq = q.shape
+    Tk, Hk = k.shape
+    if Tk != T:
+        raise ValueError("q and k must have the same number of tokens")
+    out_q = torch.empty_like(q) if out_q is None else out_q
+    out_k = torch.empty_like(k) if out_k is None else out_k
+    if want_rinv:
+        rinv_q = torch.empty(T, device=q.device, dtype=torch.float32) if rinv_q is None else rinv_q
+        rinv_k = torch.empty(T, device=q.device, dtype=torch.float32) if rinv_k is None else rinv_k
+    check(lib().nts_qknorm_rms_qk(_ptr(q), _ptr(gamma_q), _ptr(out_q), _ptr(rinv_q), _ptr(k),
+                                  _ptr(gamma_k), _ptr(out_k), _ptr(rinv_k), T, Hq, Hk,
+                                  float(eps), int(N), _stream(stream)))
+    return out_q, out_k, rinv_q, rinv_k
+
+
 def _mx_outputs(x, D, B, fmt, codes, scales, rinv, amax, want_rinv, want_amax):
     T = x.shape[0]
     if codes is None:

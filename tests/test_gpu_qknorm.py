@@ -158,3 +158,47 @@ def test_host_buffer_form():
     nts.check_status()
     Yo, ro, _ = oracle.qknorm_rms(workloads.bf16_bits(X), g.numpy(), 1e-6, 4)
     check_qk(workloads.bf16_bits(Yh), rh.numpy(), Yo, ro, "host form")
+
+
+# ------------------------------------------------- fused Q+K single launch
+
+@pytest.mark.parametrize("Hq,Hk", [(4096, 4096), (5120, 1024), (2048, 2048), (1024, 5120)])
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+@pytest.mark.parametrize("T", [1, 8, 256, 1031])
+def test_fused_qk_matches_oracle(Hq, Hk, N, T):
+    Q, gq = workloads.qk_inputs(T, Hq, seed=T + Hq, device=DEV)
+    K, gk = workloads.qk_inputs(T, Hk, seed=T + Hk + 1, device=DEV)
+    yq, yk, rq, rk = nts.qknorm_rms_qk(Q, gq, K, gk, eps=1e-6, N=N, want_rinv=True)
+    nts.check_status()
+    for X, g, Y, r in ((Q, gq, yq, rq), (K, gk, yk, rk)):
+        Yo, ro, _ = oracle.qknorm_rms(workloads.bf16_bits(X), g.cpu().numpy(), 1e-6, N)
+        check_qk(workloads.bf16_bits(Y), r.cpu().numpy(), Yo, ro, f"fused T={T} {Hq},{Hk} N={N}")
+
+
+def test_fused_qk_prefill_full_size_equals_separate_calls():
+    Q, gq = workloads.qk_inputs(8192, 5120, seed=3000, outlier_frac=0.01, device=DEV)
+    K, gk = workloads.qk_inputs(8192, 5120, seed=3001, outlier_frac=0.01, device=DEV)
+    yq, yk, rq, rk = nts.qknorm_rms_qk(Q, gq, K, gk, eps=1e-6, N=4, want_rinv=True)
+    sq, srq = nts.qknorm_rms(Q, gq, eps=1e-6, N=4, want_rinv=True)
+    sk, srk = nts.qknorm_rms(K, gk, eps=1e-6, N=4, want_rinv=True)
+    nts.check_status()
+    # same kernel arithmetic, same summation order: bit-identical
+    assert torch.equal(yq, sq) and torch.equal(yk, sk)
+    assert torch.equal(rq, srq) and torch.equal(rk, srk)
+    Yo, ro, _ = oracle.qknorm_rms(workloads.bf16_bits(K), gk.cpu().numpy(), 1e-6, 4)
+    check_qk(workloads.bf16_bits(yk), rk.cpu().numpy(), Yo, ro, "fused prefill K")
+
+
+def test_fused_qk_in_place_and_zero_tokens():
+    Q, gq = workloads.qk_inputs(300, 2048, seed=21, device=DEV)
+    K, gk = workloads.qk_inputs(300, 1024, seed=22, device=DEV)
+    Qb, Kb = workloads.bf16_bits(Q), workloads.bf16_bits(K)
+    nts.qknorm_rms_qk(Q, gq, K, gk, eps=1e-6, N=2, out_q=Q, out_k=K, want_rinv=True)
+    nts.check_status()
+    for Xb, g, Y in ((Qb, gq, Q), (Kb, gk, K)):
+        Yo, ro, _ = oracle.qknorm_rms(Xb, g.cpu().numpy(), 1e-6, 2)
+        got, want = bf16_to_f64(workloads.bf16_bits(Y)), bf16_to_f64(Yo)
+        assert np.all(np.abs(got - want) <= 1e-3 + 1e-2 * np.abs(want))
+    E = torch.empty(0, 2048, dtype=torch.bfloat16, device=DEV)
+    nts.qknorm_rms_qk(E, gq, E, gq, N=2)
+    nts.check_status()
