@@ -45,10 +45,13 @@ MX_T, MX_D, MX_B = 65536, 4096, 32
 EPS = 1e-6
 
 KERNELS = ["qknorm_rms_qk[Q+K]", "rmsnorm_mxcast", "mxnorm_cast[p=1]", "mxnorm_cast[p=2]"]
-KERNEL_SOURCES = {
-    "qknorm_rms": "normalization_token_split_gb300/csrc/qknorm_cluster.cu",
-    "mx": "normalization_token_split_gb300/csrc/mx_norm_cast.cu",
+KERNEL_SOURCES = {   # files whose content the committed ncu traffic figures belong to
+    "qknorm_rms_qk[Q+K]": ["normalization_token_split_gb300/csrc/qknorm_cluster.cu"],
+    "rmsnorm_mxcast": ["normalization_token_split_gb300/csrc/mx_kernel.cuh",
+                       "normalization_token_split_gb300/csrc/mx_launch.cu"],
 }
+KERNEL_SOURCES["mxnorm_cast[p=1]"] = KERNEL_SOURCES["rmsnorm_mxcast"]
+KERNEL_SOURCES["mxnorm_cast[p=2]"] = KERNEL_SOURCES["rmsnorm_mxcast"]
 
 
 def qk_bytes(T, H):
@@ -185,23 +188,28 @@ def barrier(world: int):
 
 
 def kernel_traffic():
-    """dram bytes per launch from the committed ncu summaries, if they were
-    taken from the current kernel source (sha256 recorded in the summary)."""
-    out = {}
+    """dram read + write bytes per launch from the committed ncu summaries
+    (profiles/*.md lines "traffic_per_launch NAME BYTES source_sha256 H"),
+    kept only where H matches the kernel's current source files."""
     prof = os.path.join(ROOT, "profiles")
-    for key, src in KERNEL_SOURCES.items():
+    found = {}
+    if os.path.isdir(prof):
+        for fn in sorted(os.listdir(prof)):
+            if fn.endswith(".md"):
+                text = open(os.path.join(prof, fn)).read()
+                for m in re.finditer(r"traffic_per_launch\s+(\S+)\s+(\d+)\s+source_sha256\s+(\w+)",
+                                     text):
+                    found[m.group(1)] = (int(m.group(2)), m.group(3))
+    out = {}
+    for name, files in KERNEL_SOURCES.items():
+        h = hashlib.sha256()
         try:
-            h = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+            for f in files:
+                h.update(open(os.path.join(ROOT, f), "rb").read())
         except OSError:
             continue
-        for fn in sorted(os.listdir(prof)) if os.path.isdir(prof) else []:
-            if not fn.endswith(".md"):
-                continue
-            text = open(os.path.join(prof, fn)).read()
-            for m in re.finditer(r"traffic_per_launch\s+(\S+)\s+(\d+)\s+source_sha256\s+(\w+)", text):
-                name, val, sha = m.group(1), int(m.group(2)), m.group(3)
-                if sha == h and (name.startswith(key) or (key == "mx" and "mx" in name)):
-                    out[name] = val
+        if name in found and found[name][1] == h.hexdigest()[:16]:
+            out[name] = found[name][0]
     return out
 
 
@@ -298,13 +306,14 @@ def run_gpu(args):
                          "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
     dominant = max(KERNELS, key=lambda n: per_kernel_ms[n])
     traffic = kernel_traffic()
-    dom_key = dominant.replace("[", "_").replace("]", "").replace("=", "")
     roofline = {"bound": "hbm", "kernel": dominant,
                 "achieved": kernels[dominant]["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": round(kernels[dominant]["gbs"] / peak, 4),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
-                "traffic": traffic.get(dom_key)}
+                "traffic": traffic.get(dominant),
+                "traffic_note": "ncu dram read+write bytes of one launch (profiles/); writes still "
+                                "dirty in L2 at kernel end are not counted"}
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,

@@ -1,0 +1,74 @@
+"""Host-side logic of bench.py without a GPU: the max-over-ranks timing
+aggregation and barrier under a world-size-2 gloo process group, and the
+reference arm's JSON line (the CPU oracle on bounded samples)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+from conftest import ROOT
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    out[rank] = bench.max_over_ranks(10.0 + rank * 5.0, world)
+    bench.barrier(world)
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_2():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=120)
+            assert p.exitcode == 0
+        assert dict(out) == {0: 15.0, 1: 15.0}
+
+
+def test_single_rank_aggregation_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    bench.barrier(1)
+
+
+def _run_reference(env_extra):
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "1"], capture_output=True, text=True,
+                       env=env, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    return r.stdout.strip()
+
+
+def test_reference_arm_prints_one_json_line():
+    line = _run_reference({})
+    d = json.loads(line)
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["steps"] == 2 and d["higher_is_better"] is True
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    assert _run_reference({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == ""
