@@ -18,8 +18,13 @@
 //    memory fence sits in the token loop, so nothing waits for the previous
 //    tile's global stores;
 //  * Phase B is the window between those sends and the wait: every warp
-//    multiplies its registers by gamma (staged once in shared memory) with
-//    packed f32x2 instructions, then waits;
+//    multiplies its registers by gamma (one bulk copy into shared memory per
+//    CTA, split once into a bank-conflict-free layout) with packed f32x2
+//    instructions, then waits;
+//  * start-up stays off the critical path: the producer issues gamma and the
+//    first tiles at once, and consumers defer the cluster start-up wait to
+//    their first exchange (a timeline probe showed a blocking prologue cost
+//    ~4 us of a 60 us launch);
 //  * the block-level token pipeline of Sec. III.D is a persistent loop over
 //    tiles of R rows.  A producer warp keeps a ring of S shared-memory stages
 //    filled with bulk TMA copies; consumer warps release a stage (an
@@ -62,6 +67,7 @@ struct QkParams {
   int G;           // consumer threads per row (multiple of 32)
   int R;           // rows per tile
   int S;           // ring stages
+  int gsplit;      // 1: gamma re-laid out into split halves; 0: read as copied
   float eps;
   uint64_t wait_limit_ns;
   uint32_t missing_tx;  // test hook: bytes expected on the first stage but never sent
@@ -69,23 +75,30 @@ struct QkParams {
 
 // Shared memory layout (bytes, in order):
 //   ring  [S][R][Wmax] bf16       the staged shard rows
-//   gam   per tensor [2][nvec] float4: gamma of this shard, the low and
-//         high halves of each 8-value vector
+//   gstg  per tensor [W] f32      gamma of this shard as copied (one bulk
+//                                 copy); absent when gsplit == 0
+//   gam   per tensor [2][nvec] float4: the same, split into the low and high
+//         halves of each 8-value vector (conflict-free reads); when the
+//         shards are too wide for both copies, gam holds gamma as copied
 //   full  [S], empty [S]          ring mbarriers
+//   gbar                          gamma-arrival mbarrier
 //   xbar  [2][R]                  exchange mbarriers (double-buffered by tile)
 //   part  [2][R][N][WPR] f32      partial sums received from every warp of
 //                                 every shard of a row
 struct QkLayout {
-  uint32_t ring, gam, full, empty, xbar, part, total;
+  uint32_t ring, gstg, gam, full, empty, gbar, xbar, part, total;
 };
 
-__host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int Wsum, int G) {
+__host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int Wsum, int G,
+                                              int gsplit) {
   QkLayout L;
   L.ring = 0;
-  L.gam = L.ring + (uint32_t)S * R * Wmax * 2;
+  L.gstg = L.ring + (uint32_t)S * R * Wmax * 2;
+  L.gam = L.gstg + (gsplit ? (uint32_t)Wsum * 4 : 0u);
   L.full = L.gam + (uint32_t)Wsum * 4;
   L.empty = L.full + (uint32_t)S * 8;
-  L.xbar = L.empty + (uint32_t)S * 8;
+  L.gbar = L.empty + (uint32_t)S * 8;
+  L.xbar = L.gbar + 8;
   L.part = L.xbar + (uint32_t)2 * R * 8;
   L.total = L.part + (uint32_t)2 * R * N * (G / 32) * 4;
   return L;
@@ -96,10 +109,6 @@ __device__ __forceinline__ int qk_tile(const QkParams& p, int64_t tile, int64_t*
   const int k = (p.ntensors > 1 && tile >= p.ten[0].ntiles) ? 1 : 0;
   *t0 = (tile - (k ? p.ten[0].ntiles : 0)) * p.R;
   return k;
-}
-
-__device__ __forceinline__ void bar_sync_named(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 template <int N, int VPT>
@@ -113,7 +122,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
   const int lane = tid & 31;
   const int wpr = p.G >> 5;
   const int Wsum = p.ten[0].W + (p.ntensors > 1 ? p.ten[1].W : 0);
-  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, Wsum, p.G);
+  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, Wsum, p.G, p.gsplit);
   const uint32_t sbase = smem_addr(smem);
   const uint32_t stage_bytes = (uint32_t)p.R * p.Wmax * 2;
   const int64_t my_tiles = cid < p.ntiles ? (p.ntiles - 1 - cid) / ncl + 1 : 0;
@@ -124,6 +133,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
       mbar_init(sbase + L.empty + 8 * s, nconsumer / 32);
     }
     for (int b = 0; b < 2 * p.R; ++b) mbar_init(sbase + L.xbar + 8 * b, 1);
+    mbar_init(sbase + L.gbar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -135,6 +145,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
     if (N > 1) cluster_arrive_relaxed();
     if (lane == 0) {
       bool aborted = false;
+      // this shard's gamma first (every CTA re-reads it, so no evict hint)
+      mbar_arrive_expect_tx(sbase + L.gbar, (uint32_t)Wsum * 4);
+      for (int k = 0; k < p.ntensors; ++k)
+        bulk_g2s_plain(sbase + p.ten[k].gam - L.gam + L.gstg,
+                       p.ten[k].gamma + (size_t)rank * p.ten[k].W, (uint32_t)p.ten[k].W * 4,
+                       sbase + L.gbar);
       const uint64_t policy = l2_policy_evict_first();
       for (int64_t j = 0; j < my_tiles; ++j) {
         const int s = (int)(j % p.S);
@@ -164,29 +180,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
       for (int64_t j = max64(0, my_tiles - p.S); j < my_tiles && !aborted; ++j)
         (void)mbar_wait_bounded(sbase + L.full + 8 * (int)(j % p.S), (uint32_t)((j / p.S) & 1),
                                 p.wait_limit_ns);
+      (void)mbar_wait_bounded(sbase + L.gbar, 0, p.wait_limit_ns);
     }
     __syncwarp();
     if (N > 1) cluster_wait_acquire();
   } else {
     // ------------------------------------------------------- consumer warps
-    // gamma of this shard, split into the low and high halves of each
-    // 8-value vector so that consecutive lanes read consecutive 16 bytes
-    for (int k = 0; k < p.ntensors; ++k) {
-      const QkTensor& tn = p.ten[k];
-      const float4* gsrc = reinterpret_cast<const float4*>(tn.gamma + (size_t)rank * tn.W);
-      float4* gam = reinterpret_cast<float4*>(smem + tn.gam);
-      for (int q = tid; q < tn.nvec; q += nconsumer) {
-        gam[q] = __ldg(gsrc + 2 * q);
-        gam[tn.nvec + q] = __ldg(gsrc + 2 * q + 1);
-      }
-    }
-    bar_sync_named(1, nconsumer);
-    // Every CTA of the cluster is running and has initialised its barriers
-    // before anyone stores into a peer's shared memory.
-    if (N > 1) {
-      cluster_arrive_release();
-      cluster_wait_acquire();
-    }
+    // Every CTA of the cluster must be running, with its barriers
+    // initialised, before anyone stores into a peer's shared memory: arrive
+    // now, wait just before the first exchange (the first tile's loads and
+    // Phase A overlap the start-up).
+    if (N > 1) cluster_arrive_release();
+    bool started = (N == 1);
+    bool have_gamma = false;
 
     const int row = tid / p.G;
     const int g = tid - row * p.G;
@@ -207,31 +213,39 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         aborted = true;
       }
 
-      // ---- Phase A: this shard's sum of squares (fp32, packed pairs)
-      uint4 xr[VPT];
-      uint64_t acc = 0;  // {0.f, 0.f}
+      // ---- Phase A: this shard's sum of squares (fp32, packed pairs).  The
+      // values are converted once and kept as fp32 pairs in w; four
+      // independent accumulators keep the FMA chains short.
+      uint64_t w[VPT][4];
+      uint64_t acc[4] = {0, 0, 0, 0};  // {0.f, 0.f} each
       const uint32_t srow = sbase + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * tn.W * 2;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = i * p.G + g;
-        xr[i] = make_uint4(0, 0, 0, 0);
-        if (valid && v < nvec) xr[i] = ld_shared_v4(srow + v * 16);
-        const uint64_t a = bf16x2_to_f2(xr[i].x), b = bf16x2_to_f2(xr[i].y);
-        const uint64_t c = bf16x2_to_f2(xr[i].z), d = bf16x2_to_f2(xr[i].w);
-        acc = f2_fma(a, a, acc);
-        acc = f2_fma(b, b, acc);
-        acc = f2_fma(c, c, acc);
-        acc = f2_fma(d, d, acc);
+        uint4 xr = make_uint4(0, 0, 0, 0);
+        if (valid && v < nvec) xr = ld_shared_v4(srow + v * 16);
+        w[i][0] = bf16x2_to_f2(xr.x);
+        w[i][1] = bf16x2_to_f2(xr.y);
+        w[i][2] = bf16x2_to_f2(xr.z);
+        w[i][3] = bf16x2_to_f2(xr.w);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = f2_fma(w[i][q], w[i][q], acc[q]);
       }
       // the stage's data is in registers: hand it back to the producer
       __syncwarp();
       if (lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
-      const float ss = warp_sum(f2_lo(acc) + f2_hi(acc));
+      const uint64_t a01 = f2_add(acc[0], acc[1]), a23 = f2_add(acc[2], acc[3]);
+      const uint64_t a = f2_add(a01, a23);
+      const float ss = warp_sum(f2_lo(a) + f2_hi(a));
 
       // ---- exchange: send this warp's partial to every shard of the row
       const int b = (int)(j & 1);
       const uint32_t xbar = sbase + L.xbar + 8 * (b * p.R + row);
       const uint32_t slot0 = sbase + L.part + 4 * (uint32_t)((b * p.R + row) * N * wpr);
+      if (!started) {
+        cluster_wait_acquire();
+        started = true;
+      }
       if (exchange) {
         if (g == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(N * wpr * 4));
         if (lane == 0) {
@@ -242,19 +256,40 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         }
       }
 
-      // ---- Phase B (overlapping the exchange): w = x * gamma
+      // ---- Phase B (overlapping the exchange): w = x * gamma, in place
+      if (!have_gamma) {
+        // once: wait for the copied gamma and split it into the layout the
+        // loop reads (consecutive lanes, consecutive 16 bytes)
+        if (!mbar_wait_bounded(sbase + L.gbar, 0, aborted ? 0 : p.wait_limit_ns)) {
+          if (!aborted) atomicOr(&g_qk_status, kStatusTimeout);
+          aborted = true;
+        }
+        for (int k = 0; k < p.ntensors && p.gsplit; ++k) {
+          const QkTensor& tk = p.ten[k];
+          const float4* src = reinterpret_cast<const float4*>(smem + tk.gam - L.gam + L.gstg);
+          float4* dst = reinterpret_cast<float4*>(smem + tk.gam);
+          for (int q = tid; q < tk.nvec; q += nconsumer) {
+            dst[q] = src[2 * q];
+            dst[tk.nvec + q] = src[2 * q + 1];
+          }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(nconsumer) : "memory");
+        have_gamma = true;
+      }
+      // split layout: halves nvec*16 bytes apart, vectors 16 apart; as
+      // copied: halves 16 apart, vectors 32 apart
       const uint32_t gam_lo = sbase + tn.gam;
-      const uint32_t gam_hi = gam_lo + (uint32_t)nvec * 16;
-      uint64_t w[VPT][4];
+      const uint32_t gam_hi = gam_lo + (p.gsplit ? (uint32_t)nvec * 16 : 16u);
+      const uint32_t gstride = p.gsplit ? 16u : 32u;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = min(i * p.G + g, nvec - 1);
-        const uint4 glo = ld_shared_v4(gam_lo + v * 16);
-        const uint4 ghi = ld_shared_v4(gam_hi + v * 16);
-        w[i][0] = f2_mul(bf16x2_to_f2(xr[i].x), f2(__uint_as_float(glo.x), __uint_as_float(glo.y)));
-        w[i][1] = f2_mul(bf16x2_to_f2(xr[i].y), f2(__uint_as_float(glo.z), __uint_as_float(glo.w)));
-        w[i][2] = f2_mul(bf16x2_to_f2(xr[i].z), f2(__uint_as_float(ghi.x), __uint_as_float(ghi.y)));
-        w[i][3] = f2_mul(bf16x2_to_f2(xr[i].w), f2(__uint_as_float(ghi.z), __uint_as_float(ghi.w)));
+        const uint4 glo = ld_shared_v4(gam_lo + v * gstride);
+        const uint4 ghi = ld_shared_v4(gam_hi + v * gstride);
+        w[i][0] = f2_mul(w[i][0], f2(__uint_as_float(glo.x), __uint_as_float(glo.y)));
+        w[i][1] = f2_mul(w[i][1], f2(__uint_as_float(glo.z), __uint_as_float(glo.w)));
+        w[i][2] = f2_mul(w[i][2], f2(__uint_as_float(ghi.x), __uint_as_float(ghi.y)));
+        w[i][3] = f2_mul(w[i][3], f2(__uint_as_float(ghi.z), __uint_as_float(ghi.w)));
       }
 
       // ---- combine in rank order (then warp order within a shard)
@@ -291,6 +326,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         if (tn.rinv_out != nullptr && rank == 0 && g == 0) tn.rinv_out[t] = rinv;
       }
     }
+    if (!started) cluster_wait_acquire();  // a CTA without tiles
   }
 
   // No CTA leaves while a peer may still store into its shared memory.
@@ -359,11 +395,15 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, cudaStrea
 
   // Ring depth: up to 4 stages within the shared-memory budget; the widest
   // shards (whose staged gamma alone is up to 120 KB) fall back to fewer.
+  // gamma is split into the conflict-free layout when both copies fit.
+  int gsplit = 1;
   int S = 4;
-  while (S > 2 && qk_layout(N, S, R, Wmax, Wsum, rs.G).total > (uint32_t)tune.smem_budget) --S;
-  while (S > 1 && qk_layout(N, S, R, Wmax, Wsum, rs.G).total > (uint32_t)dev.max_smem_optin) --S;
+  while (S > 2 && qk_layout(N, S, R, Wmax, Wsum, rs.G, 1).total > (uint32_t)tune.smem_budget) --S;
+  if (qk_layout(N, S, R, Wmax, Wsum, rs.G, 1).total > (uint32_t)dev.max_smem_optin) gsplit = 0;
+  while (S > 1 && qk_layout(N, S, R, Wmax, Wsum, rs.G, gsplit).total > (uint32_t)dev.max_smem_optin)
+    --S;
   if (tune.force_stages > 0) S = tune.force_stages;
-  const QkLayout L = qk_layout(N, S, R, Wmax, Wsum, rs.G);
+  const QkLayout L = qk_layout(N, S, R, Wmax, Wsum, rs.G, gsplit);
   const size_t smem = L.total;
   if (smem > (size_t)dev.max_smem_optin)
     return fail(NTS_ERR_UNSUPPORTED, "shard row too wide for shared memory: H/N = %d", Wmax);
@@ -395,6 +435,7 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, cudaStrea
   prm.G = rs.G;
   prm.R = R;
   prm.S = S;
+  prm.gsplit = gsplit;
   prm.eps = eps;
   prm.wait_limit_ns = tune.wait_limit_ns;
   prm.missing_tx = tune.missing_tx;
@@ -423,9 +464,9 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, cudaStrea
   if (tune.force_grid > 0) ncl = std::min<int64_t>(ntiles, tune.force_grid);
   cfg.gridDim = dim3((unsigned)(ncl * N));
 
-  log_launch("qknorm_rms", "tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d smem=%zu "
-             "clusters=%lld/%lld", ntensors, (long long)rq[0].T, (int)rq[0].H, N, rs.vpt, rs.G,
-             R, S, smem, (long long)ncl, (long long)max_clusters);
+  log_launch("qknorm_rms", "tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d gsplit=%d "
+             "smem=%zu clusters=%lld/%lld", ntensors, (long long)rq[0].T, (int)rq[0].H, N, rs.vpt,
+             rs.G, R, S, gsplit, smem, (long long)ncl, (long long)max_clusters);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e != cudaSuccess) return fail_cuda(e, "launching qknorm_rms");
   return NTS_OK;
