@@ -99,6 +99,24 @@ NTS_API int nts_qknorm_rms(const void *X_dev, const float *gamma_dev, void *Y_de
                    void *stream);
 
 /*
+ * nts_qknorm_rms_heads -- headwise QK-Norm (SwiftQK Sec. II.A: one
+ * normalization factor per attention head instead of one per projected
+ * vector).  X holds T tokens of H = nheads * head_dim values, the heads one
+ * after another; head h of token t is normalized over its own head_dim
+ * values:  rinv[t][h] = 1/sqrt((1/head_dim) sum x^2 + eps),
+ * y = bf16_rne((x * gamma) * rinv), with gamma of head_dim entries shared by
+ * all heads.  N splits every head across the CTAs of a cluster exactly as in
+ * nts_qknorm_rms (head_dim % N == 0, (head_dim / N) % 8 == 0).
+ *   X_dev, Y_dev  bf16 [T, H] (in place allowed); gamma_dev fp32 [head_dim];
+ *   rinv_dev      fp32 [T, H/head_dim] or NULL.
+ * Errors: as nts_qknorm_rms, plus INVALID_ARG for head_dim <= 0 or
+ * H % head_dim != 0.
+ */
+NTS_API int nts_qknorm_rms_heads(const void *X_dev, const float *gamma_dev, void *Y_dev,
+                                 float *rinv_dev, int64_t T, int64_t H, int64_t head_dim,
+                                 float eps, int N, void *stream);
+
+/*
  * nts_qknorm_rms_qk -- nts_qknorm_rms of a token batch's Q and K in ONE
  * launch (one persistent grid walks the tiles of both tensors).  Q and K may
  * have different widths (Hq, Hk: e.g. grouped-query attention, where K is
@@ -166,6 +184,20 @@ NTS_API int nts_mxnorm_cast(const void *X_dev, const float *gamma_dev,
                     uint8_t *codes_dev, uint8_t *scales_dev, float *rinv_dev,
                     float *amax_dev, int64_t T, int64_t D, float eps, int B,
                     int fmt, int p, void *stream);
+
+/*
+ * nts_mxnorm_postround_cast -- the "post-round" MXNorm scheme (MXNorm card,
+ * Fig. A.4, which names it and reports it trains unstably; reading): the RMS
+ * estimate takes every block absmax after the E8M0 power-of-two rounding,
+ *     rho~ = c(B, p) * ((1/K) sum_k (2^round(log2 amax_k))^p)^(1/p),
+ * with the same c(B, p); the cast (scales and codes from amax_k * rinv) is
+ * that of nts_mxnorm_cast.  Arguments, layouts and errors as
+ * nts_mxnorm_cast.
+ */
+NTS_API int nts_mxnorm_postround_cast(const void *X_dev, const float *gamma_dev,
+                                      uint8_t *codes_dev, uint8_t *scales_dev,
+                                      float *rinv_dev, float *amax_dev, int64_t T, int64_t D,
+                                      float eps, int B, int fmt, int p, void *stream);
 
 /*
  * nts_mxnorm_correction -- the correction factor c(B, p) used by

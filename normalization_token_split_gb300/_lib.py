@@ -32,8 +32,10 @@ def _declare(lib):
         "nts_last_error": ([], ctypes.c_char_p),
         "nts_qknorm_rms": ([P, P, P, P, i64, i64, f32, i32, P], i32),
         "nts_qknorm_rms_qk": ([P, P, P, P, P, P, P, P, i64, i64, i64, f32, i32, P], i32),
+        "nts_qknorm_rms_heads": ([P, P, P, P, i64, i64, i64, f32, i32, P], i32),
         "nts_rmsnorm_mxcast": ([P, P, P, P, P, P, i64, i64, f32, i32, i32, P], i32),
         "nts_mxnorm_cast": ([P, P, P, P, P, P, i64, i64, f32, i32, i32, i32, P], i32),
+        "nts_mxnorm_postround_cast": ([P, P, P, P, P, P, i64, i64, f32, i32, i32, i32, P], i32),
         "nts_mxnorm_correction": ([i32, i32, ctypes.POINTER(ctypes.c_double)], i32),
         "nts_check_status": ([P], i32),
         "nts_qknorm_rms_host": ([P, P, P, P, P, P, P, i64, i64, f32, i32, P], i32),

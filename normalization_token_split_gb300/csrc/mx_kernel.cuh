@@ -59,6 +59,7 @@ struct MxParams {
   int S;                // ring stages
   float eps;
   float corr;           // MXNorm: c(B,1) for p = 1, c(B,2)^2 for p = 2
+  int post;             // MXNorm: 1 = statistic from E8M0-rounded absmaxes (post-round)
   uint64_t wait_limit_ns;
   uint32_t missing_tx;  // test hook: bytes expected on the first stage but never sent
 };
@@ -92,6 +93,26 @@ __device__ __forceinline__ int e8m0_exponent(float ay, int emax) {
   if (field == 0) return -127;
   const int e = field - 127 + ((b & 0x7FFFFFu) >= 0x3504F4u ? 1 : 0) - emax;
   return max(-127, min(127, e));
+}
+
+// 2^round(log2 a) for a >= 0 (0 for a == 0): the power of two the E8M0
+// rounding picks for a block absmax a, subnormal a included.
+__device__ __forceinline__ float round_pow2(float a) {
+  const uint32_t b = __float_as_uint(a);
+  const int field = (int)(b >> 23);
+  const uint32_t m = b & 0x7FFFFFu;
+  int k;
+  if (field == 0) {
+    if (m == 0) return 0.f;
+    const int msb = 31 - __clz(m);                       // a = m * 2^-149
+    const uint32_t frac = (m << (23 - msb)) & 0x7FFFFFu;  // significand of a, 23 bits
+    k = msb - 149 + (frac >= 0x3504F4u ? 1 : 0);
+  } else {
+    k = field - 127 + (m >= 0x3504F4u ? 1 : 0);
+  }
+  if (k >= 128) return __uint_as_float(0x7F800000u);     // beyond fp32
+  if (k >= -126) return __uint_as_float((uint32_t)(k + 127) << 23);
+  return __uint_as_float(1u << (k + 149));
 }
 
 // 8 bf16 values (one vector) times an fp32 gain vector at `gp`, as four
@@ -230,8 +251,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
           }
           am[i] = mf;
         }
-        if (STAT == kStatMxP1) stat += am[i];
-        if (STAT == kStatMxP2) stat = fmaf(am[i], am[i], stat);
+        const float a = (STAT != kStatRms && p.post) ? round_pow2(am[i]) : am[i];
+        if (STAT == kStatMxP1) stat += a;
+        if (STAT == kStatMxP2) stat = fmaf(a, a, stat);
       }
     }
     if (STAT == kStatRms) stat = f2_lo(acc) + f2_hi(acc);

@@ -89,6 +89,7 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   prm.corr = 0.f;
   if (rq.p == 1) prm.corr = (float)rq.corr;
   if (rq.p == 2) prm.corr = (float)(rq.corr * rq.corr);
+  prm.post = rq.post;
   prm.wait_limit_ns = tune.wait_limit_ns;
   prm.missing_tx = tune.missing_tx;
 
@@ -103,7 +104,7 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   int64_t grid = std::min<int64_t>(prm.ntiles, (int64_t)per_sm * dev.sm_count);
   if (tune.force_grid > 0) grid = std::min<int64_t>(prm.ntiles, tune.force_grid);
 
-  log_launch(rq.p == 0 ? "rmsnorm_mxcast" : "mxnorm_cast",
+  log_launch(rq.p == 0 ? "rmsnorm_mxcast" : (rq.post ? "mxnorm_postround_cast" : "mxnorm_cast"),
              "T=%lld D=%d B=%d fmt=%d p=%d bpt=%d G=%d R=%d S=%d smem=%zu grid=%lld (%d/SM)",
              (long long)rq.T, D, rq.B, rq.fmt, rq.p, sh.bpt, sh.G, R, S, smem, (long long)grid,
              per_sm);

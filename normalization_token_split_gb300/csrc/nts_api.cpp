@@ -292,11 +292,11 @@ int validate_mx(const void* X, const float* gamma, const uint8_t* codes, const u
 
 int run_mx(const void* X, const float* gamma, uint8_t* codes, uint8_t* scales, float* rinv,
            float* amax, int64_t T, int64_t D, float eps, int B, int fmt, int p, bool mxnorm,
-           void* stream) {
+           void* stream, int post = 0) {
   int rc = validate_mx(X, gamma, codes, scales, rinv, amax, T, D, eps, B, fmt, p, mxnorm);
   if (rc != NTS_OK) return rc;
   if (T == 0) return NTS_OK;
-  MxRequest rq{X, gamma, codes, scales, rinv, amax, T, D, eps, B, fmt, mxnorm ? p : 0, 0.0};
+  MxRequest rq{X, gamma, codes, scales, rinv, amax, T, D, eps, B, fmt, mxnorm ? p : 0, 0.0, post};
   if (mxnorm) {
     rc = nts_mxnorm_correction(B, p, &rq.corr);
     if (rc != NTS_OK) return rc;
@@ -322,6 +322,23 @@ int nts_qknorm_rms(const void* X_dev, const float* gamma_dev, void* Y_dev, float
   if (rc != NTS_OK) return rc;
   if (T == 0) return NTS_OK;
   const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, T, H};
+  return launch_qknorm(&rq, 1, eps, N, static_cast<cudaStream_t>(stream), current_tuning());
+}
+
+int nts_qknorm_rms_heads(const void* X_dev, const float* gamma_dev, void* Y_dev,
+                         float* rinv_dev, int64_t T, int64_t H, int64_t head_dim, float eps,
+                         int N, void* stream) {
+  if (head_dim <= 0) return fail(NTS_ERR_INVALID_ARG, "head_dim must be > 0");
+  if (H <= 0 || H % head_dim != 0)
+    return fail(NTS_ERR_INVALID_ARG, "H (%lld) must be a positive multiple of head_dim (%lld)",
+                (long long)H, (long long)head_dim);
+  if (T < 0) return fail(NTS_ERR_INVALID_ARG, "T must be >= 0, got %lld", (long long)T);
+  // Row-major [T, H] is row-major [T * nheads, head_dim]: one row per head.
+  const int64_t rows = T * (H / head_dim);
+  int rc = validate_qk(X_dev, gamma_dev, Y_dev, rinv_dev, rows, head_dim, eps, N);
+  if (rc != NTS_OK) return rc;
+  if (rows == 0) return NTS_OK;
+  const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, rows, head_dim};
   return launch_qknorm(&rq, 1, eps, N, static_cast<cudaStream_t>(stream), current_tuning());
 }
 
@@ -351,6 +368,13 @@ int nts_mxnorm_cast(const void* X_dev, const float* gamma_dev, uint8_t* codes_de
                     float eps, int B, int fmt, int p, void* stream) {
   return run_mx(X_dev, gamma_dev, codes_dev, scales_dev, rinv_dev, amax_dev, T, D, eps, B, fmt,
                 p, true, stream);
+}
+
+int nts_mxnorm_postround_cast(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,
+                              uint8_t* scales_dev, float* rinv_dev, float* amax_dev, int64_t T,
+                              int64_t D, float eps, int B, int fmt, int p, void* stream) {
+  return run_mx(X_dev, gamma_dev, codes_dev, scales_dev, rinv_dev, amax_dev, T, D, eps, B, fmt,
+                p, true, stream, 1);
 }
 
 int nts_check_status(void* stream) {

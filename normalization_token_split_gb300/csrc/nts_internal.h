@@ -72,6 +72,7 @@ struct MxRequest {
   int fmt;
   int p;        // 0 = RMSNorm statistic, 1 or 2 = MXNorm
   double corr;  // c(B, p) for MXNorm
+  int post;     // MXNorm from E8M0-rounded absmaxes (post-round)
 };
 
 struct QkRequest {

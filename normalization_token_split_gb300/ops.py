@@ -74,6 +74,26 @@ def qknorm_rms(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, N: int =
     return out, rinv
 
 
+def qknorm_rms_heads(x: torch.Tensor, gamma: torch.Tensor, head_dim: int, eps: float = 1e-6,
+                     N: int = 1, out: Optional[torch.Tensor] = None,
+                     rinv: Optional[torch.Tensor] = None, want_rinv: bool = False, stream=None):
+    """Headwise QK-Norm of x [T, H] (H = nheads * head_dim) with gamma
+    [head_dim] shared by the heads.  Returns (y, rinv [T, nheads] or None)."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("gamma", gamma, torch.float32)
+    T, H = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _need_cuda("out", out, torch.bfloat16)
+    if rinv is None and want_rinv:
+        rinv = torch.empty(T, H // head_dim, device=x.device, dtype=torch.float32)
+    if rinv is not None:
+        _need_cuda("rinv", rinv, torch.float32)
+    check(lib().nts_qknorm_rms_heads(_ptr(x), _ptr(gamma), _ptr(out), _ptr(rinv), T, H,
+                                     int(head_dim), float(eps), int(N), _stream(stream)))
+    return out, rinv
+
+
 def qknorm_rms_qk(q: torch.Tensor, gamma_q: torch.Tensor, k: torch.Tensor,
                   gamma_k: torch.Tensor, eps: float = 1e-6, N: int = 1,
                   out_q: Optional[torch.Tensor] = None, out_k: Optional[torch.Tensor] = None,
@@ -150,6 +170,24 @@ def mxnorm_cast(x: torch.Tensor, gamma: Optional[torch.Tensor] = None, eps: floa
     check(lib().nts_mxnorm_cast(_ptr(x), _ptr(gamma), _ptr(codes), _ptr(scales), _ptr(rinv),
                                 _ptr(amax), T, D, float(eps), int(B), f, int(p),
                                 _stream(stream)))
+    return MxOut(codes, scales, rinv, amax)
+
+
+def mxnorm_postround_cast(x: torch.Tensor, gamma: Optional[torch.Tensor] = None,
+                          eps: float = 1e-6, B: int = 32, fmt="e4m3", p: int = 2, codes=None,
+                          scales=None, rinv=None, amax=None, want_rinv: bool = False,
+                          want_amax: bool = False, stream=None) -> MxOut:
+    """Post-round MXNorm: the RMS estimate from E8M0-rounded block absmaxes."""
+    _need_cuda("x", x, torch.bfloat16)
+    if gamma is not None:
+        _need_cuda("gamma", gamma, torch.float32)
+    T, D = x.shape
+    f = _fmt(fmt)
+    codes, scales, rinv, amax = _mx_outputs(x, D, B, f, codes, scales, rinv, amax,
+                                            want_rinv, want_amax)
+    check(lib().nts_mxnorm_postround_cast(_ptr(x), _ptr(gamma), _ptr(codes), _ptr(scales),
+                                          _ptr(rinv), _ptr(amax), T, D, float(eps), int(B), f,
+                                          int(p), _stream(stream)))
     return MxOut(codes, scales, rinv, amax)
 
 

@@ -11,9 +11,13 @@ through ctypes.  Each wrapper names the passage its C function follows:
 * ``qknorm_rms``       -- SwiftQK, Eq. (1) evaluated in the phases of
                           Algorithm 1 (split-H partial sums, combine, x*gamma,
                           final scaling).
+* ``qknorm_rms_heads`` -- SwiftQK Sec. II.A: headwise QK-Norm, one factor per
+                          head, gamma shared by the heads.
 * ``rmsnorm_mxcast``   -- MXNorm card, Fig. 1 caption: RMSNorm then MXCast.
 * ``mxnorm_cast``      -- MXNorm card, abstract and Fig. 1 caption: RMS
                           estimated from the block absmaxes, c(B, p).
+* ``mxnorm_postround_cast`` -- MXNorm card, Fig. A.4 (reading): the estimate
+                          from E8M0-rounded absmaxes.
 * ``mx_cast_given_rinv`` -- the MX block stage with a given fp32 factor.
 * ``mx_correction``    -- c(B, p) by quadrature.
 
@@ -63,8 +67,11 @@ def _load():
         P = ctypes.c_void_p
         i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
         lib.oracle_qknorm_rms.argtypes = [P, P, P, P, P, i64, i64, dbl, i32]
+        lib.oracle_qknorm_rms_heads.argtypes = [P, P, P, P, i64, i64, i64, dbl]
         lib.oracle_rmsnorm_mxcast.argtypes = [P, P, P, P, P, P, P, i64, i64, dbl, i32, i32]
         lib.oracle_mxnorm_cast.argtypes = [P, P, P, P, P, P, P, i64, i64, dbl, i32, i32, i32, dbl]
+        lib.oracle_mxnorm_postround_cast.argtypes = [P, P, P, P, P, P, P, i64, i64, dbl, i32, i32,
+                                                     i32, dbl]
         lib.oracle_mx_cast_given_rinv.argtypes = [P, P, P, P, P, P, P, i64, i64, i32, i32]
         lib.oracle_mx_correction.argtypes = [i32, i32]
         lib.oracle_mx_correction.restype = dbl
@@ -120,6 +127,21 @@ def qknorm_rms(X, gamma, eps: float, N: int):
     return Y, rinv, part
 
 
+def qknorm_rms_heads(X, gamma, eps: float, head_dim: int):
+    """Headwise QK-Norm: returns (Y bf16 bits [T,H], rinv f64 [T, H/head_dim]);
+    gamma has head_dim entries."""
+    X = _bf16_bits(X)
+    T, H = X.shape
+    if head_dim < 1 or H % head_dim:
+        raise ValueError("H must be a multiple of head_dim")
+    g = _gamma(gamma, head_dim)
+    Y = np.empty_like(X)
+    rinv = np.empty((T, H // head_dim), np.float64)
+    _load().oracle_qknorm_rms_heads(_ptr(X), _ptr(g), _ptr(Y), _ptr(rinv), T, H, head_dim,
+                                    float(eps))
+    return Y, rinv
+
+
 def _mx_out(T, D, B, fmt):
     codes = np.empty((T, codes_row_bytes(D, fmt)), np.uint8)
     scales = np.empty((T, D // B), np.uint8)
@@ -153,6 +175,21 @@ def mxnorm_cast(X, gamma, eps: float, B: int, fmt: int, p: int):
     _load().oracle_mxnorm_cast(_ptr(X), _ptr(g), _ptr(codes), _ptr(scales),
                                _ptr(rinv), _ptr(amax), _ptr(work), T, D,
                                float(eps), B, fmt, p, c)
+    return codes, scales, rinv, amax
+
+
+def mxnorm_postround_cast(X, gamma, eps: float, B: int, fmt: int, p: int):
+    """Post-round MXNorm. Returns (codes, scales, rinv f64 [T], amax f32 [T,K])."""
+    X = _bf16_bits(X)
+    T, D = X.shape
+    g = _gamma(gamma, D)
+    codes, scales, amax = _mx_out(T, D, B, fmt)
+    rinv = np.empty(T, np.float64)
+    work = np.empty(D, np.float32)
+    c = mx_correction(B, p)
+    _load().oracle_mxnorm_postround_cast(_ptr(X), _ptr(g), _ptr(codes), _ptr(scales),
+                                         _ptr(rinv), _ptr(amax), _ptr(work), T, D,
+                                         float(eps), B, fmt, p, c)
     return codes, scales, rinv, amax
 
 

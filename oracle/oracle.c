@@ -188,6 +188,35 @@ ORACLE_EXPORT void oracle_qknorm_rms(const uint16_t *X, const float *gamma,
     }
 }
 
+/* Headwise QK-Norm ([SQK] Sec. II.A): one normalization factor per attention
+ * head instead of one per projected vector.  A token row of H = nheads *
+ * head_dim values holds the heads one after another; head h of token t is
+ * normalized over its own head_dim values,
+ *     y_j = x_j / sqrt((1/head_dim) sum_{j in head} x_j^2 + eps) * gamma_j',
+ * where gamma has head_dim entries shared by all heads (j' = j mod head_dim).
+ * rinv: [T][nheads] (nullable). */
+ORACLE_EXPORT void oracle_qknorm_rms_heads(const uint16_t *X, const float *gamma,
+                                           uint16_t *Y, double *rinv, int64_t T,
+                                           int64_t H, int64_t head_dim, double eps) {
+    int64_t nheads = H / head_dim;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < nheads; ++h) {
+            const uint16_t *x = X + t * H + h * head_dim;
+            double S = 0.0;
+            for (int64_t j = 0; j < head_dim; ++j) {
+                double xj = oracle_bf16_to_double(x[j]);
+                S += xj * xj;
+            }
+            double r = 1.0 / sqrt(S / (double)head_dim + eps);
+            if (rinv) rinv[t * nheads + h] = r;
+            for (int64_t j = 0; j < head_dim; ++j) {
+                double w = oracle_bf16_to_double(x[j]) * (double)gamma[j];
+                Y[t * H + h * head_dim + j] = oracle_double_to_bf16(w * r);
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Path 2: RMSNorm + MX cast, and MXNorm                                     */
 /* ------------------------------------------------------------------------ */
@@ -330,11 +359,10 @@ ORACLE_EXPORT void oracle_rmsnorm_mxcast(const uint16_t *X, const float *gamma,
  * estimated mean square).  The output is the MX cast of w * r, whose block
  * absmaxes are a_k * r, so no second reduction is needed.  `c` is the
  * correction factor (oracle_mx_correction(B, p)). */
-ORACLE_EXPORT void oracle_mxnorm_cast(const uint16_t *X, const float *gamma,
-                                      uint8_t *codes, uint8_t *scales,
-                                      double *rinv, float *amax, float *work,
-                                      int64_t T, int64_t D, double eps, int B,
-                                      int fmt, int p, double c) {
+static void mxnorm_rows(const uint16_t *X, const float *gamma, uint8_t *codes,
+                        uint8_t *scales, double *rinv, float *amax, float *work,
+                        int64_t T, int64_t D, double eps, int B, int fmt, int p,
+                        double c, int post_round) {
     int64_t K = D / B, cb = codes_row_bytes(D, fmt);
     for (int64_t t = 0; t < T; ++t) {
         weight_row(X + t * D, gamma, D, work);
@@ -345,6 +373,8 @@ ORACLE_EXPORT void oracle_mxnorm_cast(const uint16_t *X, const float *gamma,
                 double v = fabs((double)work[k * B + b]);
                 if (v > a) a = v;
             }
+            /* post-round: the block absmax as its E8M0 power of two */
+            if (post_round && a > 0.0) a = ldexp(1.0, oracle_round_log2(a));
             acc += p == 1 ? a : a * a;
         }
         double Mp = p == 1 ? acc / (double)K : sqrt(acc / (double)K);
@@ -354,6 +384,26 @@ ORACLE_EXPORT void oracle_mxnorm_cast(const uint16_t *X, const float *gamma,
         mx_cast_row(work, D, r, 0, B, fmt, codes + t * cb, scales + t * K,
                     amax ? amax + t * K : NULL);
     }
+}
+
+ORACLE_EXPORT void oracle_mxnorm_cast(const uint16_t *X, const float *gamma,
+                                      uint8_t *codes, uint8_t *scales,
+                                      double *rinv, float *amax, float *work,
+                                      int64_t T, int64_t D, double eps, int B,
+                                      int fmt, int p, double c) {
+    mxnorm_rows(X, gamma, codes, scales, rinv, amax, work, T, D, eps, B, fmt, p, c, 0);
+}
+
+/* Post-round MXNorm ([MXN] Fig. A.4 names the scheme; reading): the RMS
+ * estimate takes each block absmax after the E8M0 power-of-two rounding,
+ * a_k -> 2^round(log2 a_k), with the same c(B, p); the cast itself is the
+ * block stage above, on the unrounded absmaxes. */
+ORACLE_EXPORT void oracle_mxnorm_postround_cast(const uint16_t *X, const float *gamma,
+                                                uint8_t *codes, uint8_t *scales,
+                                                double *rinv, float *amax, float *work,
+                                                int64_t T, int64_t D, double eps,
+                                                int B, int fmt, int p, double c) {
+    mxnorm_rows(X, gamma, codes, scales, rinv, amax, work, T, D, eps, B, fmt, p, c, 1);
 }
 
 /* The block stage alone with a given fp32 normalization factor per row,

@@ -144,3 +144,16 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _lib.lib()
+
+
+def test_headwise_argument_checks(lib):
+    f = lambda **k: lib.nts_qknorm_rms_heads(k.get("X", A16), A16, A16, None, k.get("T", 4),
+                                             k.get("H", 512), k.get("hd", 128), 1e-6,
+                                             k.get("N", 1), None)
+    assert f(hd=0) == INVALID
+    assert f(H=500) == INVALID
+    assert f(T=-1) == INVALID
+    assert f(X=None) == INVALID
+    assert f(N=3) == INVALID
+    assert f(hd=32, H=512, N=8) == UNSUPPORTED       # 4-value shards
+    assert f(T=0, X=None) == OK

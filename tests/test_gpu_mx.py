@@ -29,6 +29,9 @@ def gpu_call(kind, X, gamma, eps, B, fmt, p):
     gd = None if gamma is None else gamma.to(DEV)
     if kind == "rms":
         out = nts.rmsnorm_mxcast(Xd, gd, eps=eps, B=B, fmt=fmt, want_rinv=True, want_amax=True)
+    elif kind == "post":
+        out = nts.mxnorm_postround_cast(Xd, gd, eps=eps, B=B, fmt=fmt, p=p, want_rinv=True,
+                                        want_amax=True)
     else:
         out = nts.mxnorm_cast(Xd, gd, eps=eps, B=B, fmt=fmt, p=p, want_rinv=True, want_amax=True)
     nts.check_status()
@@ -38,6 +41,8 @@ def gpu_call(kind, X, gamma, eps, B, fmt, p):
 def oracle_call(kind, Xb, g, eps, B, fmt, p):
     if kind == "rms":
         return oracle.rmsnorm_mxcast(Xb, g, eps, B, fmt)
+    if kind == "post":
+        return oracle.mxnorm_postround_cast(Xb, g, eps, B, fmt, p)
     return oracle.mxnorm_cast(Xb, g, eps, B, fmt, p)
 
 
@@ -177,3 +182,33 @@ def test_host_buffer_form(kind):
     nts.check_status()
     dev = gpu_call(kind, X, None, 1e-6, B, "e4m3", 2)
     assert torch.equal(ch, dev.codes.cpu()) and torch.equal(sh, dev.scales.cpu())
+
+
+# ------------------------------------------------------ post-round MXNorm
+
+@pytest.mark.parametrize("p", [1, 2])
+@pytest.mark.parametrize("B", [16, 32, 64])
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+@pytest.mark.parametrize("with_gamma", [False, True])
+def test_postround_small_complete(p, B, fmt, with_gamma):
+    X, g = workloads.mx_inputs(257, 2048, seed=B * 3 + p, t_frac=0.1, with_gamma=with_gamma)
+    compare("post", X, g, 1e-6, B, fmt, p, what=f"post p={p} B={B} {fmt} gamma={with_gamma}")
+
+
+def test_postround_full_size_sampled():
+    X, _ = workloads.mx_inputs(65536, 4096, seed=4100, device=DEV)
+    rows = sample_rows(65536, 2048, 7).to(DEV)
+    for p in (1, 2):
+        compare("post", X, None, 1e-6, 32, "e4m3", p, rows=rows, what=f"post full p={p}")
+
+
+def test_postround_subnormal_and_degenerate_blocks():
+    X, _ = workloads.mx_inputs(32, 512, seed=43)
+    X[0] = 0
+    X[1, :32] = 3.0e-39                # bf16 subnormal block absmax
+    X[2, 32:64] = 7.0e-40
+    X[3] = 2.0e-38                     # a whole row of tiny values
+    X[4, ::2] = -0.0
+    for p in (1, 2):
+        for fmt in ("e4m3", "e2m1"):
+            compare("post", X, None, 1e-6, 32, fmt, p, what=f"post degenerate p={p} {fmt}")

@@ -202,3 +202,16 @@ def test_fused_qk_in_place_and_zero_tokens():
     E = torch.empty(0, 2048, dtype=torch.bfloat16, device=DEV)
     nts.qknorm_rms_qk(E, gq, E, gq, N=2)
     nts.check_status()
+
+
+# ------------------------------------------------------- headwise QK-Norm
+
+@pytest.mark.parametrize("T,H,hd,N", [(1, 4096, 128, 1), (37, 4096, 128, 1), (256, 2048, 64, 1),
+                                      (129, 5120, 128, 2), (64, 1024, 256, 4), (8, 3072, 96, 1)])
+def test_headwise_matches_oracle(T, H, hd, N):
+    X, _ = workloads.qk_inputs(T, H, seed=T + H + hd)
+    g = workloads.gamma_vector(hd, seed=hd)
+    y, r = nts.qknorm_rms_heads(X.to(DEV), g.to(DEV), hd, eps=1e-6, N=N, want_rinv=True)
+    nts.check_status()
+    Yo, ro = oracle.qknorm_rms_heads(workloads.bf16_bits(X), g.numpy(), 1e-6, hd)
+    check_qk(workloads.bf16_bits(y), r.cpu().numpy().ravel(), Yo, ro.ravel(), f"heads {T},{H},{hd},{N}")

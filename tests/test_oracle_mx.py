@@ -211,3 +211,45 @@ def test_degenerate_rows():
         assert np.all(codes == 0) and np.all(scales == 0) and np.all(amax == 0)
     out = oracle.mxnorm_cast(np.zeros((0, 64), np.uint16), None, 1e-6, 32, 0, 2)
     assert out[0].shape == (0, 64)
+
+
+# ----------------------------------------------------- post-round MXNorm
+
+@pytest.mark.parametrize("p", [1, 2])
+@pytest.mark.parametrize("fmt", [oracle.FMT_E4M3, oracle.FMT_E2M1])
+def test_postround_equals_preround_on_power_of_two_absmaxes(p, fmt):
+    # blocks whose absmax is already a power of two are unchanged by rounding
+    T, D, B = 12, 256, 32
+    g = torch.Generator().manual_seed(41)
+    powers = 2.0 ** torch.randint(-4, 5, (T, D // B), generator=g).float()
+    u = (torch.rand(T, D // B, B, generator=g) * 1.8 - 0.9) * powers[..., None]
+    u[..., 0] = powers * torch.where(torch.rand(T, D // B, generator=g) < 0.5, -1.0, 1.0)
+    Xb = workloads.bf16_bits(u.reshape(T, D).to(torch.bfloat16))
+    a = oracle.mxnorm_cast(Xb, None, 1e-6, B, fmt, p)
+    b = oracle.mxnorm_postround_cast(Xb, None, 1e-6, B, fmt, p)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+@pytest.mark.parametrize("p", [1, 2])
+def test_postround_constant_rows_closed_form(p):
+    # |c| = 3 rounds to 4 (3 > 2 sqrt 2); 1.25 to 1; 0.75 to 1 (> sqrt(2)/2);
+    # 0.6875 to 0.5 (< sqrt(2)/2); 6 to 8
+    cs = [3.0, -1.25, 0.75, 0.6875, 6.0]
+    rounded = [4.0, 1.0, 1.0, 0.5, 8.0]
+    Xb = workloads.bf16_bits(workloads.constant_rows(len(cs), 128, cs))
+    cB = oracle.mx_correction(32, p)
+    _, _, rinv, amax = oracle.mxnorm_postround_cast(Xb, None, 1e-6, 32, oracle.FMT_E4M3, p)
+    for t, (c, a_hat) in enumerate(zip(cs, rounded)):
+        assert np.all(amax[t] == abs(c))
+        assert rinv[t] == pytest.approx(1 / math.sqrt((cB * a_hat) ** 2 + 1e-6), rel=1e-14)
+
+
+def test_postround_estimate_within_sqrt2_of_preround():
+    X, _ = workloads.mx_inputs(256, 1024, seed=42, t_frac=0.2)
+    Xb = workloads.bf16_bits(X)
+    for p in (1, 2):
+        _, _, r_pre, _ = oracle.mxnorm_cast(Xb, None, 0.0, 32, oracle.FMT_E4M3, p)
+        _, _, r_post, _ = oracle.mxnorm_postround_cast(Xb, None, 0.0, 32, oracle.FMT_E4M3, p)
+        ratio = r_pre / r_post                      # = rho_post / rho_pre
+        assert np.all(ratio >= 2 ** -0.5 * (1 - 1e-12)) and np.all(ratio <= 2 ** 0.5 * (1 + 1e-12))
+        assert not np.allclose(ratio, 1.0)          # the rounding does change the estimate

@@ -114,3 +114,35 @@ def test_degenerate_rows():
     # T = 0 is a no-op
     Y0, r0, p0 = oracle.qknorm_rms(np.zeros((0, 16), np.uint16), np.ones(16, np.float32), 1e-6, 2)
     assert Y0.shape == (0, 16) and r0.shape == (0,)
+
+
+# ------------------------------------------------------- headwise QK-Norm
+
+def test_headwise_single_head_is_layerwise():
+    # with one head the headwise factor is the layerwise one (Sec. II.A)
+    X, g = workloads.qk_inputs(16, 256, seed=31)
+    Xb = workloads.bf16_bits(X)
+    Yh, rh = oracle.qknorm_rms_heads(Xb, g.numpy(), 1e-6, 256)
+    Yl, rl, _ = oracle.qknorm_rms(Xb, g.numpy(), 1e-6, 1)
+    assert np.array_equal(Yh, Yl) and np.array_equal(rh[:, 0], rl)
+
+
+def test_headwise_heads_are_independent_and_closed_form():
+    T, hd, nh = 4, 32, 5
+    g = workloads.gamma_vector(hd, seed=2).numpy()
+    cs = np.array([[1.0, -2.0, 0.5, 4.0, 0.0], [3.0, 3.0, -0.25, 1.0, 8.0],
+                   [0.125, 2.0, 2.0, -1.0, 1.0], [6.0, -6.0, 1.5, 0.75, -3.0]])
+    x = np.repeat(cs, hd, axis=1)                      # every head constant
+    Xb = workloads.bf16_bits(torch.tensor(x, dtype=torch.float32).to(torch.bfloat16))
+    Y, r = oracle.qknorm_rms_heads(Xb, g, 1e-6, hd)
+    assert np.allclose(r, 1 / np.sqrt(cs ** 2 + 1e-6), rtol=1e-14)
+    want = (np.tile(g.astype(np.float64), nh) * x * np.repeat(r, hd, axis=1))
+    got = _decode(Y.ravel()).reshape(Y.shape)
+    assert np.all(np.abs(got - want) <= np.abs(want) * 2.0 ** -8 + 1e-300)
+    # changing one head leaves the others bit-identical
+    x2 = x.copy(); x2[:, 2 * hd:3 * hd] *= 3
+    X2 = workloads.bf16_bits(torch.tensor(x2, dtype=torch.float32).to(torch.bfloat16))
+    Y2, r2 = oracle.qknorm_rms_heads(X2, g, 1e-6, hd)
+    keep = np.ones(nh * hd, bool); keep[2 * hd:3 * hd] = False
+    assert np.array_equal(Y2[:, keep], Y[:, keep])
+    assert np.array_equal(np.delete(r2, 2, axis=1), np.delete(r, 2, axis=1))
