@@ -46,7 +46,8 @@ EPS = 1e-6
 
 KERNELS = ["qknorm_rms_qk[Q+K]", "rmsnorm_mxcast", "mxnorm_cast[p=1]", "mxnorm_cast[p=2]"]
 KERNEL_SOURCES = {   # files whose content the committed ncu traffic figures belong to
-    "qknorm_rms_qk[Q+K]": ["normalization_token_split_gb300/csrc/qknorm_cluster.cu"],
+    "qknorm_rms_qk[Q+K]": ["normalization_token_split_gb300/csrc/qk_kernel.cuh",
+                           "normalization_token_split_gb300/csrc/qk_launch.cu"],
     "rmsnorm_mxcast": ["normalization_token_split_gb300/csrc/mx_kernel.cuh",
                        "normalization_token_split_gb300/csrc/mx_launch.cu"],
 }

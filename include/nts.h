@@ -99,6 +99,19 @@ NTS_API int nts_qknorm_rms(const void *X_dev, const float *gamma_dev, void *Y_de
                    void *stream);
 
 /*
+ * nts_qknorm_rms_fp8 -- nts_qknorm_rms on FP8-E4M3 activations (SwiftQK
+ * Sec. IV.C evaluates bf16 and FP8-E4M3 activations; the squares and the
+ * combine stay fp32).  X_dev holds OCP E4M3 codes, uint8 [T, H]; the
+ * activation is code * x_scale (a per-tensor dequantization scale, > 0 and
+ * finite).  gamma, Y (bf16), rinv, N and the errors are those of
+ * nts_qknorm_rms, plus UNSUPPORTED when (H / N) % 16 != 0 (a shard's row must
+ * be a whole number of 16-byte vectors).  Y must not overlap X.
+ */
+NTS_API int nts_qknorm_rms_fp8(const void *X_dev, float x_scale, const float *gamma_dev,
+                               void *Y_dev, float *rinv_dev, int64_t T, int64_t H, float eps,
+                               int N, void *stream);
+
+/*
  * nts_qknorm_rms_heads -- headwise QK-Norm (SwiftQK Sec. II.A: one
  * normalization factor per attention head instead of one per projected
  * vector).  X holds T tokens of H = nheads * head_dim values, the heads one

@@ -322,7 +322,23 @@ int nts_qknorm_rms(const void* X_dev, const float* gamma_dev, void* Y_dev, float
   if (rc != NTS_OK) return rc;
   if (T == 0) return NTS_OK;
   const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, T, H};
-  return launch_qknorm(&rq, 1, eps, N, static_cast<cudaStream_t>(stream), current_tuning());
+  return launch_qknorm(&rq, 1, eps, N, 0, 1.0f, static_cast<cudaStream_t>(stream),
+                       current_tuning());
+}
+
+int nts_qknorm_rms_fp8(const void* X_dev, float x_scale, const float* gamma_dev, void* Y_dev,
+                       float* rinv_dev, int64_t T, int64_t H, float eps, int N, void* stream) {
+  int rc = validate_qk(X_dev, gamma_dev, Y_dev, rinv_dev, T, H, eps, N);
+  if (rc != NTS_OK) return rc;
+  if (!(x_scale > 0.f) || !std::isfinite(x_scale))
+    return fail(NTS_ERR_INVALID_ARG, "x_scale must be positive and finite");
+  if ((H / N) % 16 != 0)
+    return fail(NTS_ERR_UNSUPPORTED, "H/N (%lld) must be a multiple of 16 for E4M3 rows",
+                (long long)(H / N));
+  if (T == 0) return NTS_OK;
+  const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, T, H};
+  return launch_qknorm(&rq, 1, eps, N, 1, x_scale, static_cast<cudaStream_t>(stream),
+                       current_tuning());
 }
 
 int nts_qknorm_rms_heads(const void* X_dev, const float* gamma_dev, void* Y_dev,
@@ -339,7 +355,8 @@ int nts_qknorm_rms_heads(const void* X_dev, const float* gamma_dev, void* Y_dev,
   if (rc != NTS_OK) return rc;
   if (rows == 0) return NTS_OK;
   const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, rows, head_dim};
-  return launch_qknorm(&rq, 1, eps, N, static_cast<cudaStream_t>(stream), current_tuning());
+  return launch_qknorm(&rq, 1, eps, N, 0, 1.0f, static_cast<cudaStream_t>(stream),
+                       current_tuning());
 }
 
 int nts_qknorm_rms_qk(const void* Q_dev, const float* gamma_q_dev, void* Yq_dev,
@@ -353,7 +370,8 @@ int nts_qknorm_rms_qk(const void* Q_dev, const float* gamma_q_dev, void* Yq_dev,
   if (T == 0) return NTS_OK;
   const QkRequest rq[2] = {{Q_dev, gamma_q_dev, Yq_dev, rinv_q_dev, T, Hq},
                            {K_dev, gamma_k_dev, Yk_dev, rinv_k_dev, T, Hk}};
-  return launch_qknorm(rq, 2, eps, N, static_cast<cudaStream_t>(stream), current_tuning());
+  return launch_qknorm(rq, 2, eps, N, 0, 1.0f, static_cast<cudaStream_t>(stream),
+                       current_tuning());
 }
 
 int nts_rmsnorm_mxcast(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,

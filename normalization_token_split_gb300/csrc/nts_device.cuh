@@ -138,6 +138,12 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
 // 16-byte store that does not allocate in L1 and streams through L2.
 __device__ __forceinline__ void st_global_v4_stream(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
@@ -258,6 +264,19 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
 // bf16 pair (low half = element 0) -> the two fp32 values, exactly.
 __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t v) {
   return f2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// Two E4M3 codes (low byte = element 0) -> their exact fp32 values, via the
+// hardware's exact E4M3 -> f16 conversion.
+__device__ __forceinline__ uint64_t e4m3x2_to_f2(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  return f2(lo, hi);
 }
 
 // max(|a|, |b|) lane-wise on bf16 pairs; the sign bits of the result are the

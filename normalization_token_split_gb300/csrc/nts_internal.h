@@ -84,9 +84,10 @@ struct QkRequest {
   int64_t H;
 };
 
-// One launch normalizing 1 or 2 tensors (Q and K) with the same N.
-int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, cudaStream_t stream,
-                  const LaunchTuning& tune);
+// One launch normalizing 1 or 2 tensors (Q and K) with the same N; the
+// activations are bf16, or E4M3 codes whose values are code * x_scale.
+int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4m3,
+                  float x_scale, cudaStream_t stream, const LaunchTuning& tune);
 int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune);
 
 int read_and_clear_qk_status(unsigned* out);

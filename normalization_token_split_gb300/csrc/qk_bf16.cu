@@ -1,0 +1,12 @@
+// qk_bf16.cu -- instantiates the split-H QK-RMSNorm kernels (qk_kernel.cuh)
+// for bfloat16 activations; a unit of its own so the input types compile
+// in parallel.
+#include "qk_kernel.cuh"
+
+namespace nts {
+
+QkKernel pick_qk_bf16(int N, int vpt) { return pick_qk_input<kInBf16>(N, vpt); }
+
+int read_and_clear_qk_bf16_status(unsigned* out) { return read_and_clear_local_qk_status(out); }
+
+}  // namespace nts

@@ -1,4 +1,4 @@
-// qknorm_cluster.cu -- layerwise QK-RMSNorm with split-H scalar partial sums
+// qk_kernel.cuh -- layerwise QK-RMSNorm with split-H scalar partial sums
 // on one GB300: the N shards of a row are the N CTAs of a thread-block
 // cluster, and the per-shard sums of squares travel through distributed
 // shared memory.
@@ -34,20 +34,25 @@
 //    grid is still sized from the cluster occupancy query, for throughput.
 //    Every wait in the kernel is bounded in time (an expired wait sets the
 //    status word and the kernel finishes with undefined outputs).
-#include <cuda_runtime.h>
+#pragma once
 
-#include <algorithm>
+#include <cuda_runtime.h>
 
 #include "nts_device.cuh"
 #include "nts_internal.h"
 
 namespace nts {
 
-__device__ unsigned int g_qk_status;  // kStatusTimeout bits, read by nts_check_status
+// kStatusTimeout bits of the QK kernels of the including translation unit;
+// every unit has its own word (no relocatable device code).
+static __device__ unsigned int g_qk_status;
+
+// Element type of the activations read by a launch.
+enum { kInBf16 = 0, kInE4M3 = 1 };
 
 // One tensor normalized by a launch (a launch covers one or two: Q and K).
 struct QkTensor {
-  const __nv_bfloat16* X;
+  const void* X;   // bf16 or E4M3 codes [T, H]
   const float* gamma;
   __nv_bfloat16* Y;
   float* rinv_out;
@@ -69,12 +74,13 @@ struct QkParams {
   int S;           // ring stages
   int gsplit;      // 1: gamma re-laid out into split halves; 0: read as copied
   float eps;
+  float x_scale;   // E4M3 input: value = code * x_scale
   uint64_t wait_limit_ns;
   uint32_t missing_tx;  // test hook: bytes expected on the first stage but never sent
 };
 
 // Shared memory layout (bytes, in order):
-//   ring  [S][R][Wmax] bf16       the staged shard rows
+//   ring  [S][R][Wmax] elements   the staged shard rows (2 or 1 bytes each)
 //   gstg  per tensor [W] f32      gamma of this shard as copied (one bulk
 //                                 copy); absent when gsplit == 0
 //   gam   per tensor [2][nvec] float4: the same, split into the low and high
@@ -90,10 +96,10 @@ struct QkLayout {
 };
 
 __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int Wsum, int G,
-                                              int gsplit) {
+                                              int gsplit, int esize) {
   QkLayout L;
   L.ring = 0;
-  L.gstg = L.ring + (uint32_t)S * R * Wmax * 2;
+  L.gstg = L.ring + (uint32_t)S * R * Wmax * esize;
   L.gam = L.gstg + (gsplit ? (uint32_t)Wsum * 4 : 0u);
   L.full = L.gam + (uint32_t)Wsum * 4;
   L.empty = L.full + (uint32_t)S * 8;
@@ -111,8 +117,32 @@ __device__ __forceinline__ int qk_tile(const QkParams& p, int64_t tile, int64_t*
   return k;
 }
 
-template <int N, int VPT>
+// Eight activations of vector v of a staged row as four fp32 pairs; zeros
+// when !inb (the load is predicated, the conversion is not).
+template <int IN>
+__device__ __forceinline__ void load_vector(uint32_t srow, int v, bool inb, float x_scale,
+                                            uint64_t (&w)[4]) {
+  if (IN == kInBf16) {
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (inb) x = ld_shared_v4(srow + v * 16);
+    w[0] = bf16x2_to_f2(x.x);
+    w[1] = bf16x2_to_f2(x.y);
+    w[2] = bf16x2_to_f2(x.z);
+    w[3] = bf16x2_to_f2(x.w);
+  } else {
+    uint2 x = make_uint2(0, 0);
+    if (inb) x = ld_shared_v2(srow + v * 8);
+    const uint64_t sc = f2(x_scale, x_scale);
+    w[0] = f2_mul(e4m3x2_to_f2((uint16_t)(x.x & 0xFFFFu)), sc);
+    w[1] = f2_mul(e4m3x2_to_f2((uint16_t)(x.x >> 16)), sc);
+    w[2] = f2_mul(e4m3x2_to_f2((uint16_t)(x.y & 0xFFFFu)), sc);
+    w[3] = f2_mul(e4m3x2_to_f2((uint16_t)(x.y >> 16)), sc);
+  }
+}
+
+template <int N, int VPT, int IN>
 __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const QkParams p) {
+  constexpr int ES = (IN == kInBf16) ? 2 : 1;  // bytes per activation
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t rank = (N > 1) ? cluster_ctarank() : 0u;
   const int64_t cid = cluster_id_x();
@@ -122,9 +152,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
   const int lane = tid & 31;
   const int wpr = p.G >> 5;
   const int Wsum = p.ten[0].W + (p.ntensors > 1 ? p.ten[1].W : 0);
-  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, Wsum, p.G, p.gsplit);
+  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, Wsum, p.G, p.gsplit, ES);
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t stage_bytes = (uint32_t)p.R * p.Wmax * 2;
+  const uint32_t stage_bytes = (uint32_t)p.R * p.Wmax * ES;
   const int64_t my_tiles = cid < p.ntiles ? (p.ntiles - 1 - cid) / ncl + 1 : 0;
 
   if (tid == 0) {
@@ -164,16 +194,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         int64_t t0;
         const QkTensor& tn = p.ten[qk_tile(p, cid + j * ncl, &t0)];
         const int nrows = (int)min64(p.R, tn.T - t0);
-        const uint32_t row_bytes = (uint32_t)tn.W * 2;
+        const uint32_t row_bytes = (uint32_t)tn.W * ES;
         const uint32_t bar = sbase + L.full + 8 * s;
         const uint32_t dst = sbase + L.ring + (uint32_t)s * stage_bytes;
-        const __nv_bfloat16* src = tn.X + (size_t)t0 * tn.H + (size_t)rank * tn.W;
+        const char* src = static_cast<const char*>(tn.X) +
+                          ((size_t)t0 * tn.H + (size_t)rank * tn.W) * ES;
         mbar_arrive_expect_tx(bar, nrows * row_bytes + (j == 0 ? p.missing_tx : 0u));
         if (N == 1) {
           bulk_g2s(dst, src, nrows * row_bytes, bar, policy);
         } else {
           for (int r = 0; r < nrows; ++r)
-            bulk_g2s(dst + r * row_bytes, src + (size_t)r * tn.H, row_bytes, bar, policy);
+            bulk_g2s(dst + r * row_bytes, src + (size_t)r * tn.H * ES, row_bytes, bar, policy);
         }
       }
       // let the last copies land before this CTA can retire
@@ -218,16 +249,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
       // independent accumulators keep the FMA chains short.
       uint64_t w[VPT][4];
       uint64_t acc[4] = {0, 0, 0, 0};  // {0.f, 0.f} each
-      const uint32_t srow = sbase + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * tn.W * 2;
+      const uint32_t srow = sbase + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * tn.W * ES;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = i * p.G + g;
-        uint4 xr = make_uint4(0, 0, 0, 0);
-        if (valid && v < nvec) xr = ld_shared_v4(srow + v * 16);
-        w[i][0] = bf16x2_to_f2(xr.x);
-        w[i][1] = bf16x2_to_f2(xr.y);
-        w[i][2] = bf16x2_to_f2(xr.z);
-        w[i][3] = bf16x2_to_f2(xr.w);
+        load_vector<IN>(srow, v, valid && v < nvec, p.x_scale, w[i]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = f2_fma(w[i][q], w[i][q], acc[q]);
       }
@@ -336,150 +362,48 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
   }
 }
 
-// ------------------------------------------------------------------ launch
-
-namespace {
-
 using QkKernel = void (*)(QkParams);
 
-template <int N>
-QkKernel pick_qk_kernel(int vpt) {
+template <int N, int IN>
+QkKernel pick_qk_vpt(int vpt) {
   switch (vpt) {
-    case 1: return qknorm_cluster_kernel<N, 1>;
-    case 2: return qknorm_cluster_kernel<N, 2>;
-    case 3: return qknorm_cluster_kernel<N, 3>;
-    case 4: return qknorm_cluster_kernel<N, 4>;
-    case 5: return qknorm_cluster_kernel<N, 5>;
-    case 6: return qknorm_cluster_kernel<N, 6>;
-    case 8: return qknorm_cluster_kernel<N, 8>;
+    case 1: return qknorm_cluster_kernel<N, 1, IN>;
+    case 2: return qknorm_cluster_kernel<N, 2, IN>;
+    case 3: return qknorm_cluster_kernel<N, 3, IN>;
+    case 4: return qknorm_cluster_kernel<N, 4, IN>;
+    case 5: return qknorm_cluster_kernel<N, 5, IN>;
+    case 6: return qknorm_cluster_kernel<N, 6, IN>;
+    case 8: return qknorm_cluster_kernel<N, 8, IN>;
     default: return nullptr;
   }
 }
 
-QkKernel pick_qk(int N, int vpt) {
+// Instantiates every QK kernel for input type IN in the calling unit.
+template <int IN>
+QkKernel pick_qk_input(int N, int vpt) {
   switch (N) {
-    case 1: return pick_qk_kernel<1>(vpt);
-    case 2: return pick_qk_kernel<2>(vpt);
-    case 4: return pick_qk_kernel<4>(vpt);
-    case 8: return pick_qk_kernel<8>(vpt);
+    case 1: return pick_qk_vpt<1, IN>(vpt);
+    case 2: return pick_qk_vpt<2, IN>(vpt);
+    case 4: return pick_qk_vpt<4, IN>(vpt);
+    case 8: return pick_qk_vpt<8, IN>(vpt);
     default: return nullptr;
   }
 }
 
-}  // namespace
-
-int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, cudaStream_t stream,
-                  const LaunchTuning& tune) {
-  const DeviceInfo& dev = device_info();
-  if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
-  int Wmax = 0, Wsum = 0;
-  int64_t Tsum = 0;
-  for (int k = 0; k < ntensors; ++k) {
-    Wmax = std::max(Wmax, (int)(rq[k].H / N));
-    Wsum += (int)(rq[k].H / N);
-    Tsum += rq[k].T;
-  }
-
-  // The row shape (vectors per thread, threads per row) fits the widest
-  // shard; narrower shards leave the extra slots idle.
-  const RowShape rs = choose_row_shape(Wmax / 8, tune.force_vpt);
-  if (rs.G == 0) return fail(NTS_ERR_UNSUPPORTED, "shard row too wide: H/N = %d", Wmax);
-
-  // Rows per tile: up to four (at most 256 consumer threads: the kernel
-  // keeps about 120 registers per thread, so larger CTAs cost residency),
-  // fewer when there are few tokens so that the tiles spread over the GPU.
-  int R = std::max(1, std::min(4, 256 / rs.G));
-  while (R > 1 && (Tsum + R - 1) / R < (int64_t)2 * dev.sm_count / N) R /= 2;
-  if (tune.force_rows > 0) R = tune.force_rows;
-  if (R * rs.G > kMaxConsumers) return fail(NTS_ERR_UNSUPPORTED, "tile of %d rows too large", R);
-
-  // Ring depth: up to 4 stages within the shared-memory budget; the widest
-  // shards (whose staged gamma alone is up to 120 KB) fall back to fewer.
-  // gamma is split into the conflict-free layout when both copies fit.
-  int gsplit = 1;
-  int S = 4;
-  while (S > 2 && qk_layout(N, S, R, Wmax, Wsum, rs.G, 1).total > (uint32_t)tune.smem_budget) --S;
-  if (qk_layout(N, S, R, Wmax, Wsum, rs.G, 1).total > (uint32_t)dev.max_smem_optin) gsplit = 0;
-  while (S > 1 && qk_layout(N, S, R, Wmax, Wsum, rs.G, gsplit).total > (uint32_t)dev.max_smem_optin)
-    --S;
-  if (tune.force_stages > 0) S = tune.force_stages;
-  const QkLayout L = qk_layout(N, S, R, Wmax, Wsum, rs.G, gsplit);
-  const size_t smem = L.total;
-  if (smem > (size_t)dev.max_smem_optin)
-    return fail(NTS_ERR_UNSUPPORTED, "shard row too wide for shared memory: H/N = %d", Wmax);
-
-  QkKernel kern = pick_qk(N, rs.vpt);
-  if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for N=%d vpt=%d", N, rs.vpt);
-
-  QkParams prm = {};
-  uint32_t gam = L.gam;
-  int64_t ntiles = 0;
-  for (int k = 0; k < ntensors; ++k) {
-    QkTensor& tn = prm.ten[k];
-    tn.X = static_cast<const __nv_bfloat16*>(rq[k].X);
-    tn.gamma = rq[k].gamma;
-    tn.Y = static_cast<__nv_bfloat16*>(rq[k].Y);
-    tn.rinv_out = rq[k].rinv;
-    tn.T = rq[k].T;
-    tn.ntiles = (rq[k].T + R - 1) / R;
-    tn.H = (int)rq[k].H;
-    tn.W = (int)(rq[k].H / N);
-    tn.nvec = tn.W / 8;
-    tn.gam = gam;
-    gam += (uint32_t)tn.W * 4;
-    ntiles += tn.ntiles;
-  }
-  prm.ntensors = ntensors;
-  prm.ntiles = ntiles;
-  prm.Wmax = Wmax;
-  prm.G = rs.G;
-  prm.R = R;
-  prm.S = S;
-  prm.gsplit = gsplit;
-  prm.eps = eps;
-  prm.wait_limit_ns = tune.wait_limit_ns;
-  prm.missing_tx = tune.missing_tx;
-  if (ntiles == 0) return NTS_OK;
-
-  const int nthreads = R * rs.G + 32;  // consumers + producer warp
-  int rc = prepare_kernel((const void*)kern, smem);
-  if (rc != NTS_OK) return rc;
-
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = N;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(nthreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-
-  int64_t max_clusters = 0;
-  rc = max_active_clusters((const void*)kern, cfg, N, &max_clusters);
-  if (rc != NTS_OK) return rc;
-  int64_t ncl = std::min<int64_t>(ntiles, max_clusters);
-  if (tune.force_grid > 0) ncl = std::min<int64_t>(ntiles, tune.force_grid);
-  cfg.gridDim = dim3((unsigned)(ncl * N));
-
-  log_launch("qknorm_rms", "tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d gsplit=%d "
-             "smem=%zu clusters=%lld/%lld", ntensors, (long long)rq[0].T, (int)rq[0].H, N, rs.vpt,
-             rs.G, R, S, gsplit, smem, (long long)ncl, (long long)max_clusters);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
-  if (e != cudaSuccess) return fail_cuda(e, "launching qknorm_rms");
-  return NTS_OK;
-}
-
-int read_and_clear_qk_status(unsigned* out) {
+static inline int read_and_clear_local_qk_status(unsigned* out) {
   unsigned v = 0, zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_qk_status, sizeof(v));
-  if (e != cudaSuccess) return fail_cuda(e, "reading the qknorm status word");
+  if (e != cudaSuccess) return fail_cuda(e, "reading a QK status word");
   e = cudaMemcpyToSymbol(g_qk_status, &zero, sizeof(zero));
-  if (e != cudaSuccess) return fail_cuda(e, "clearing the qknorm status word");
+  if (e != cudaSuccess) return fail_cuda(e, "clearing a QK status word");
   *out = v;
   return NTS_OK;
 }
+
+// Defined by qk_bf16.cu and qk_e4m3.cu.
+QkKernel pick_qk_bf16(int N, int vpt);
+QkKernel pick_qk_e4m3(int N, int vpt);
+int read_and_clear_qk_bf16_status(unsigned* out);
+int read_and_clear_qk_e4m3_status(unsigned* out);
 
 }  // namespace nts

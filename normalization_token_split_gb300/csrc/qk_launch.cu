@@ -1,0 +1,127 @@
+// qk_launch.cu -- launch-shape selection and launch of the split-H
+// QK-RMSNorm kernels (qk_kernel.cuh).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "qk_kernel.cuh"
+
+namespace nts {
+
+int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4m3,
+                  float x_scale, cudaStream_t stream, const LaunchTuning& tune) {
+  const int ES = in_e4m3 ? 1 : 2;
+  const DeviceInfo& dev = device_info();
+  if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
+  int Wmax = 0, Wsum = 0;
+  int64_t Tsum = 0;
+  for (int k = 0; k < ntensors; ++k) {
+    Wmax = std::max(Wmax, (int)(rq[k].H / N));
+    Wsum += (int)(rq[k].H / N);
+    Tsum += rq[k].T;
+  }
+
+  // The row shape (vectors per thread, threads per row) fits the widest
+  // shard; narrower shards leave the extra slots idle.
+  const RowShape rs = choose_row_shape(Wmax / 8, tune.force_vpt);
+  if (rs.G == 0) return fail(NTS_ERR_UNSUPPORTED, "shard row too wide: H/N = %d", Wmax);
+
+  // Rows per tile: up to four (at most 256 consumer threads: the kernel
+  // keeps about 120 registers per thread, so larger CTAs cost residency),
+  // fewer when there are few tokens so that the tiles spread over the GPU.
+  int R = std::max(1, std::min(4, 256 / rs.G));
+  while (R > 1 && (Tsum + R - 1) / R < (int64_t)2 * dev.sm_count / N) R /= 2;
+  if (tune.force_rows > 0) R = tune.force_rows;
+  if (R * rs.G > kMaxConsumers) return fail(NTS_ERR_UNSUPPORTED, "tile of %d rows too large", R);
+
+  // Ring depth: up to 4 stages within the shared-memory budget; the widest
+  // shards (whose staged gamma alone is up to 120 KB) fall back to fewer.
+  // gamma is split into the conflict-free layout when both copies fit.
+  int gsplit = 1;
+  int S = 4;
+  while (S > 2 && qk_layout(N, S, R, Wmax, Wsum, rs.G, 1, ES).total > (uint32_t)tune.smem_budget) --S;
+  if (qk_layout(N, S, R, Wmax, Wsum, rs.G, 1, ES).total > (uint32_t)dev.max_smem_optin) gsplit = 0;
+  while (S > 1 && qk_layout(N, S, R, Wmax, Wsum, rs.G, gsplit, ES).total > (uint32_t)dev.max_smem_optin)
+    --S;
+  if (tune.force_stages > 0) S = tune.force_stages;
+  const QkLayout L = qk_layout(N, S, R, Wmax, Wsum, rs.G, gsplit, ES);
+  const size_t smem = L.total;
+  if (smem > (size_t)dev.max_smem_optin)
+    return fail(NTS_ERR_UNSUPPORTED, "shard row too wide for shared memory: H/N = %d", Wmax);
+
+  QkKernel kern = in_e4m3 ? pick_qk_e4m3(N, rs.vpt) : pick_qk_bf16(N, rs.vpt);
+  if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for N=%d vpt=%d", N, rs.vpt);
+
+  QkParams prm = {};
+  uint32_t gam = L.gam;
+  int64_t ntiles = 0;
+  for (int k = 0; k < ntensors; ++k) {
+    QkTensor& tn = prm.ten[k];
+    tn.X = rq[k].X;
+    tn.gamma = rq[k].gamma;
+    tn.Y = static_cast<__nv_bfloat16*>(rq[k].Y);
+    tn.rinv_out = rq[k].rinv;
+    tn.T = rq[k].T;
+    tn.ntiles = (rq[k].T + R - 1) / R;
+    tn.H = (int)rq[k].H;
+    tn.W = (int)(rq[k].H / N);
+    tn.nvec = tn.W / 8;
+    tn.gam = gam;
+    gam += (uint32_t)tn.W * 4;
+    ntiles += tn.ntiles;
+  }
+  prm.ntensors = ntensors;
+  prm.ntiles = ntiles;
+  prm.Wmax = Wmax;
+  prm.G = rs.G;
+  prm.R = R;
+  prm.S = S;
+  prm.gsplit = gsplit;
+  prm.eps = eps;
+  prm.x_scale = x_scale;
+  prm.wait_limit_ns = tune.wait_limit_ns;
+  prm.missing_tx = tune.missing_tx;
+  if (ntiles == 0) return NTS_OK;
+
+  const int nthreads = R * rs.G + 32;  // consumers + producer warp
+  int rc = prepare_kernel((const void*)kern, smem);
+  if (rc != NTS_OK) return rc;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = N;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(nthreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+
+  int64_t max_clusters = 0;
+  rc = max_active_clusters((const void*)kern, cfg, N, &max_clusters);
+  if (rc != NTS_OK) return rc;
+  int64_t ncl = std::min<int64_t>(ntiles, max_clusters);
+  if (tune.force_grid > 0) ncl = std::min<int64_t>(ntiles, tune.force_grid);
+  cfg.gridDim = dim3((unsigned)(ncl * N));
+
+  log_launch("qknorm_rms", "tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d gsplit=%d "
+             "smem=%zu clusters=%lld/%lld", ntensors, (long long)rq[0].T, (int)rq[0].H, N, rs.vpt,
+             rs.G, R, S, gsplit, smem, (long long)ncl, (long long)max_clusters);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
+  if (e != cudaSuccess) return fail_cuda(e, "launching qknorm_rms");
+  return NTS_OK;
+}
+
+int read_and_clear_qk_status(unsigned* out) {
+  unsigned a = 0, b = 0;
+  int rc = read_and_clear_qk_bf16_status(&a);
+  if (rc != NTS_OK) return rc;
+  rc = read_and_clear_qk_e4m3_status(&b);
+  if (rc != NTS_OK) return rc;
+  *out = a | b;
+  return NTS_OK;
+}
+
+}  // namespace nts

@@ -74,6 +74,28 @@ def qknorm_rms(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, N: int =
     return out, rinv
 
 
+def qknorm_rms_fp8(x_codes: torch.Tensor, x_scale: float, gamma: torch.Tensor,
+                   eps: float = 1e-6, N: int = 1, out: Optional[torch.Tensor] = None,
+                   rinv: Optional[torch.Tensor] = None, want_rinv: bool = False, stream=None):
+    """QK-RMSNorm of FP8-E4M3 activations: x_codes uint8 (or float8_e4m3fn)
+    [T, H], value = code * x_scale.  Returns (y bf16 [T, H], rinv or None)."""
+    if x_codes.dtype == torch.float8_e4m3fn:
+        x_codes = x_codes.view(torch.uint8)
+    _need_cuda("x_codes", x_codes, torch.uint8)
+    _need_cuda("gamma", gamma, torch.float32)
+    T, H = x_codes.shape
+    if out is None:
+        out = torch.empty(T, H, device=x_codes.device, dtype=torch.bfloat16)
+    _need_cuda("out", out, torch.bfloat16)
+    if rinv is None and want_rinv:
+        rinv = torch.empty(T, device=x_codes.device, dtype=torch.float32)
+    if rinv is not None:
+        _need_cuda("rinv", rinv, torch.float32)
+    check(lib().nts_qknorm_rms_fp8(_ptr(x_codes), float(x_scale), _ptr(gamma), _ptr(out),
+                                   _ptr(rinv), T, H, float(eps), int(N), _stream(stream)))
+    return out, rinv
+
+
 def qknorm_rms_heads(x: torch.Tensor, gamma: torch.Tensor, head_dim: int, eps: float = 1e-6,
                      N: int = 1, out: Optional[torch.Tensor] = None,
                      rinv: Optional[torch.Tensor] = None, want_rinv: bool = False, stream=None):

@@ -11,6 +11,7 @@ through ctypes.  Each wrapper names the passage its C function follows:
 * ``qknorm_rms``       -- SwiftQK, Eq. (1) evaluated in the phases of
                           Algorithm 1 (split-H partial sums, combine, x*gamma,
                           final scaling).
+* ``qknorm_rms_fp8``   -- SwiftQK Sec. IV.C: the same on FP8-E4M3 activations.
 * ``qknorm_rms_heads`` -- SwiftQK Sec. II.A: headwise QK-Norm, one factor per
                           head, gamma shared by the heads.
 * ``rmsnorm_mxcast``   -- MXNorm card, Fig. 1 caption: RMSNorm then MXCast.
@@ -67,6 +68,7 @@ def _load():
         P = ctypes.c_void_p
         i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
         lib.oracle_qknorm_rms.argtypes = [P, P, P, P, P, i64, i64, dbl, i32]
+        lib.oracle_qknorm_rms_fp8.argtypes = [P, dbl, P, P, P, P, i64, i64, dbl, i32]
         lib.oracle_qknorm_rms_heads.argtypes = [P, P, P, P, i64, i64, i64, dbl]
         lib.oracle_rmsnorm_mxcast.argtypes = [P, P, P, P, P, P, P, i64, i64, dbl, i32, i32]
         lib.oracle_mxnorm_cast.argtypes = [P, P, P, P, P, P, P, i64, i64, dbl, i32, i32, i32, dbl]
@@ -124,6 +126,22 @@ def qknorm_rms(X, gamma, eps: float, N: int):
     part = np.empty((T, N), np.float64)
     _load().oracle_qknorm_rms(_ptr(X), _ptr(g), _ptr(Y), _ptr(rinv), _ptr(part),
                               T, H, float(eps), N)
+    return Y, rinv, part
+
+
+def qknorm_rms_fp8(X_codes, x_scale: float, gamma, eps: float, N: int):
+    """QK-RMSNorm of E4M3 activations (value = code * x_scale).
+    Returns (Y bf16 bits [T,H], rinv f64 [T], partial sums f64 [T,N])."""
+    X = np.ascontiguousarray(X_codes, dtype=np.uint8)
+    T, H = X.shape
+    if N < 1 or H % N:
+        raise ValueError("H must be a multiple of N")
+    g = _gamma(gamma, H)
+    Y = np.empty((T, H), np.uint16)
+    rinv = np.empty(T, np.float64)
+    part = np.empty((T, N), np.float64)
+    _load().oracle_qknorm_rms_fp8(_ptr(X), float(x_scale), _ptr(g), _ptr(Y), _ptr(rinv),
+                                  _ptr(part), T, H, float(eps), N)
     return Y, rinv, part
 
 

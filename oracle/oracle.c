@@ -188,6 +188,36 @@ ORACLE_EXPORT void oracle_qknorm_rms(const uint16_t *X, const float *gamma,
     }
 }
 
+/* QK-RMSNorm of FP8-E4M3 activations ([SQK] Sec. IV.C evaluates bf16 and
+ * FP8-E4M3 activations with fp32 accumulation).  X holds E4M3 codes; the
+ * activation is code * x_scale (a per-tensor dequantization scale).  The
+ * phases and outputs are those of oracle_qknorm_rms. */
+ORACLE_EXPORT void oracle_qknorm_rms_fp8(const uint8_t *X, double x_scale,
+                                         const float *gamma, uint16_t *Y, double *rinv,
+                                         double *partials, int64_t T, int64_t H,
+                                         double eps, int N) {
+    int64_t W = H / N;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint8_t *x = X + t * H;
+        double S = 0.0;
+        for (int k = 0; k < N; ++k) {                       /* Phase A */
+            double Sk = 0.0;
+            for (int64_t j = k * W; j < (k + 1) * W; ++j) {
+                double xj = oracle_e4m3_to_double(x[j]) * x_scale;
+                Sk += xj * xj;
+            }
+            if (partials) partials[t * N + k] = Sk;
+            S += Sk;                                        /* combine */
+        }
+        double r = 1.0 / sqrt(S / (double)H + eps);
+        if (rinv) rinv[t] = r;
+        for (int64_t j = 0; j < H; ++j) {                   /* Phases B, C */
+            double w = oracle_e4m3_to_double(x[j]) * x_scale * (double)gamma[j];
+            Y[t * H + j] = oracle_double_to_bf16(w * r);
+        }
+    }
+}
+
 /* Headwise QK-Norm ([SQK] Sec. II.A): one normalization factor per attention
  * head instead of one per projected vector.  A token row of H = nheads *
  * head_dim values holds the heads one after another; head h of token t is

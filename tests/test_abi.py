@@ -157,3 +157,15 @@ def test_headwise_argument_checks(lib):
     assert f(N=3) == INVALID
     assert f(hd=32, H=512, N=8) == UNSUPPORTED       # 4-value shards
     assert f(T=0, X=None) == OK
+
+
+def test_fp8_argument_checks(lib):
+    f = lambda **k: lib.nts_qknorm_rms_fp8(k.get("X", A16), k.get("s", 1.0), A16, A16, None,
+                                           k.get("T", 4), k.get("H", 512), 1e-6, k.get("N", 2),
+                                           None)
+    assert f(s=0.0) == INVALID
+    assert f(s=float("nan")) == INVALID
+    assert f(X=None) == INVALID
+    assert f(H=24, N=1) == UNSUPPORTED          # 24-byte E4M3 rows
+    assert f(H=48, N=2) == UNSUPPORTED
+    assert f(T=0, X=None) == OK

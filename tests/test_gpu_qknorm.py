@@ -215,3 +215,26 @@ def test_headwise_matches_oracle(T, H, hd, N):
     nts.check_status()
     Yo, ro = oracle.qknorm_rms_heads(workloads.bf16_bits(X), g.numpy(), 1e-6, hd)
     check_qk(workloads.bf16_bits(y), r.cpu().numpy().ravel(), Yo, ro.ravel(), f"heads {T},{H},{hd},{N}")
+
+
+# ------------------------------------------------- FP8-E4M3 activations
+
+@pytest.mark.parametrize("T,H,N", [(1, 4096, 1), (64, 1024, 2), (257, 4096, 4), (33, 5120, 8),
+                                   (8192, 5120, 4), (5, 16, 1), (100, 30720, 1)])
+def test_fp8_input_matches_oracle(T, H, N):
+    dev = DEV if T * H > 1 << 22 else "cpu"
+    codes, scale, g = workloads.qk_inputs_fp8(T, H, seed=T + H, outlier_frac=0.01, device=dev)
+    y, r = nts.qknorm_rms_fp8(codes.to(DEV), scale, g.to(DEV), eps=1e-6, N=N, want_rinv=True)
+    nts.check_status()
+    Yo, ro, _ = oracle.qknorm_rms_fp8(codes.cpu().numpy(), scale, g.cpu().numpy(), 1e-6, N)
+    check_qk(workloads.bf16_bits(y), r.cpu().numpy(), Yo, ro, f"fp8 T={T} H={H} N={N}")
+
+
+def test_fp8_equals_bf16_kernel_on_the_same_values():
+    # E4M3 values are bf16 values: the FP8 kernel must match the bf16 kernel
+    codes, scale, g = workloads.qk_inputs_fp8(512, 4096, seed=61, device=DEV)
+    vals = (codes.view(torch.float8_e4m3fn).float() * scale).to(torch.bfloat16)
+    y8, r8 = nts.qknorm_rms_fp8(codes, scale, g, eps=1e-6, N=4, want_rinv=True)
+    yb, rb = nts.qknorm_rms(vals, g, eps=1e-6, N=4, want_rinv=True)
+    nts.check_status()
+    assert torch.equal(r8, rb) and torch.equal(y8, yb)

@@ -146,3 +146,33 @@ def test_headwise_heads_are_independent_and_closed_form():
     keep = np.ones(nh * hd, bool); keep[2 * hd:3 * hd] = False
     assert np.array_equal(Y2[:, keep], Y[:, keep])
     assert np.array_equal(np.delete(r2, 2, axis=1), np.delete(r, 2, axis=1))
+
+
+# ------------------------------------------------- FP8-E4M3 activations
+
+def test_fp8_input_equals_bf16_path_on_the_same_values():
+    # every E4M3 value is exactly a bf16 value: the FP8 oracle must equal the
+    # (pinned) bf16 oracle fed the decoded values
+    codes, scale, g = workloads.qk_inputs_fp8(32, 1024, seed=51)
+    vals = codes.view(torch.float8_e4m3fn).float() * scale
+    Xb = workloads.bf16_bits(vals.to(torch.bfloat16))
+    assert np.array_equal(_decode(Xb.ravel()), vals.numpy().astype(np.float64).ravel())
+    for N in (1, 2, 4):
+        Y8, r8, p8 = oracle.qknorm_rms_fp8(codes.numpy(), scale, g.numpy(), 1e-6, N)
+        Yb, rb, pb = oracle.qknorm_rms(Xb, g.numpy(), 1e-6, N)
+        assert np.array_equal(Y8, Yb) and np.array_equal(r8, rb) and np.array_equal(p8, pb)
+
+
+def test_fp8_scale_invariance_and_pages_error_report():
+    codes, scale, g = workloads.qk_inputs_fp8(64, 1024, seed=52)
+    Y1, _, _ = oracle.qknorm_rms_fp8(codes.numpy(), scale, g.numpy(), 0.0, 2)
+    Y2, _, _ = oracle.qknorm_rms_fp8(codes.numpy(), scale * 8.0, g.numpy(), 0.0, 2)
+    assert np.array_equal(Y1, Y2)
+    # SwiftQK Sec. IV.C: FP8-E4M3 activations, max abs error 5.0e-1 vs FP64
+    # gold; here the gold is Eq. (1) on the bf16 activations the FP8 codes
+    # approximate
+    X, gamma = workloads.qk_inputs(64, 1024, seed=52)
+    Yo, _, _ = oracle.qknorm_rms(workloads.bf16_bits(X), gamma.numpy(), 1e-6, 2)
+    Y8, _, _ = oracle.qknorm_rms_fp8(codes.numpy(), scale, g.numpy(), 1e-6, 2)
+    err = np.abs(_decode(Y8.ravel()) - _decode(Yo.ravel()))
+    assert err.max() < 5.0e-1 and err.mean() < 2.5e-2 * 2

@@ -92,3 +92,16 @@ def constant_rows(T: int, D: int, values, device="cpu") -> torch.Tensor:
     """Rows x = c * 1 (one constant per row), as bf16."""
     c = torch.as_tensor(values, dtype=torch.float32, device=device).reshape(T, 1)
     return (c * torch.ones(T, D, device=device)).to(torch.bfloat16)
+
+
+def qk_inputs_fp8(T: int, H: int, seed: int, outlier_frac: float = 0.0, device="cpu"):
+    """(X E4M3 codes uint8 [T,H], x_scale, gamma fp32 [H]) for the FP8-input
+    QK-Norm: the bf16 recipe of qk_inputs divided by a per-tensor scale
+    (absmax / 448, rounded to a power of two) and cast with torch's
+    float8_e4m3fn conversion."""
+    x, gamma = qk_inputs(T, H, seed, outlier_frac=outlier_frac, device=device)
+    xf = x.float()
+    amax = float(xf.abs().max()) if xf.numel() else 1.0
+    scale = 2.0 ** np.ceil(np.log2(max(amax, 1e-30) / 448.0))
+    codes = (xf / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, float(scale), gamma
