@@ -12,6 +12,8 @@ through ctypes.  Each wrapper names the passage its C function follows:
                           Algorithm 1 (split-H partial sums, combine, x*gamma,
                           final scaling).
 * ``qknorm_rms_fp8``   -- SwiftQK Sec. IV.C: the same on FP8-E4M3 activations.
+* ``layernorm_split``  -- SwiftQK notes Sec. 5e: LayerNorm with its two
+                          additive statistics split over H.
 * ``qknorm_rms_heads`` -- SwiftQK Sec. II.A: headwise QK-Norm, one factor per
                           head, gamma shared by the heads.
 * ``rmsnorm_mxcast``   -- MXNorm card, Fig. 1 caption: RMSNorm then MXCast.
@@ -69,6 +71,7 @@ def _load():
         i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
         lib.oracle_qknorm_rms.argtypes = [P, P, P, P, P, i64, i64, dbl, i32]
         lib.oracle_qknorm_rms_fp8.argtypes = [P, dbl, P, P, P, P, i64, i64, dbl, i32]
+        lib.oracle_layernorm_split.argtypes = [P, P, P, P, P, P, P, i64, i64, dbl, i32]
         lib.oracle_qknorm_rms_heads.argtypes = [P, P, P, P, i64, i64, i64, dbl]
         lib.oracle_rmsnorm_mxcast.argtypes = [P, P, P, P, P, P, P, i64, i64, dbl, i32, i32]
         lib.oracle_mxnorm_cast.argtypes = [P, P, P, P, P, P, P, i64, i64, dbl, i32, i32, i32, dbl]
@@ -143,6 +146,25 @@ def qknorm_rms_fp8(X_codes, x_scale: float, gamma, eps: float, N: int):
     _load().oracle_qknorm_rms_fp8(_ptr(X), float(x_scale), _ptr(g), _ptr(Y), _ptr(rinv),
                                   _ptr(part), T, H, float(eps), N)
     return Y, rinv, part
+
+
+def layernorm_split(X, gamma, beta, eps: float, N: int):
+    """LayerNorm over H split into N shards.  Returns (Y bf16 bits [T,H],
+    mean f64 [T], rstd f64 [T], partials f64 [T,N,2] = per-shard (sum x,
+    sum x^2))."""
+    X = _bf16_bits(X)
+    T, H = X.shape
+    if N < 1 or H % N:
+        raise ValueError("H must be a multiple of N")
+    g = _gamma(gamma, H)
+    b = _gamma(beta, H)
+    Y = np.empty_like(X)
+    mean = np.empty(T, np.float64)
+    rstd = np.empty(T, np.float64)
+    part = np.empty((T, N, 2), np.float64)
+    _load().oracle_layernorm_split(_ptr(X), _ptr(g), _ptr(b), _ptr(Y), _ptr(mean), _ptr(rstd),
+                                   _ptr(part), T, H, float(eps), N)
+    return Y, mean, rstd, part
 
 
 def qknorm_rms_heads(X, gamma, eps: float, head_dim: int):

@@ -218,6 +218,53 @@ ORACLE_EXPORT void oracle_qknorm_rms_fp8(const uint8_t *X, double x_scale,
     }
 }
 
+/* LayerNorm split over H ([SQKN] Sec. 5e: LayerNorm's statistics reduce to
+ * two additive scalars per shard, sum x and sum x^2, exchanged and combined
+ * like the single sum of squares):
+ *     mu = (1/H) sum_j x_j,   var = (1/H) sum_j (x_j - mu)^2,
+ *     y_j = (x_j - mu) / sqrt(var + eps) * gamma_j + beta_j.
+ * The oracle takes the definition (mean first, then the centred sum, in
+ * double); partials [T][N][2] are each shard's (sum x, sum x^2).  beta is
+ * nullable (zero); mean / rstd are [T] (nullable). */
+ORACLE_EXPORT void oracle_layernorm_split(const uint16_t *X, const float *gamma,
+                                          const float *beta, uint16_t *Y, double *mean,
+                                          double *rstd, double *partials, int64_t T,
+                                          int64_t H, double eps, int N) {
+    int64_t W = H / N;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t *x = X + t * H;
+        double S1 = 0.0;
+        for (int k = 0; k < N; ++k) {
+            double s1 = 0.0, s2 = 0.0;
+            for (int64_t j = k * W; j < (k + 1) * W; ++j) {
+                double xj = oracle_bf16_to_double(x[j]);
+                s1 += xj;
+                s2 += xj * xj;
+            }
+            if (partials) {
+                partials[(t * N + k) * 2] = s1;
+                partials[(t * N + k) * 2 + 1] = s2;
+            }
+            S1 += s1;
+        }
+        double mu = S1 / (double)H;
+        double var = 0.0;
+        for (int64_t j = 0; j < H; ++j) {
+            double d = oracle_bf16_to_double(x[j]) - mu;
+            var += d * d;
+        }
+        var /= (double)H;
+        double r = 1.0 / sqrt(var + eps);
+        if (mean) mean[t] = mu;
+        if (rstd) rstd[t] = r;
+        for (int64_t j = 0; j < H; ++j) {
+            double y = (oracle_bf16_to_double(x[j]) - mu) * r * (double)gamma[j];
+            if (beta) y += (double)beta[j];
+            Y[t * H + j] = oracle_double_to_bf16(y);
+        }
+    }
+}
+
 /* Headwise QK-Norm ([SQK] Sec. II.A): one normalization factor per attention
  * head instead of one per projected vector.  A token row of H = nheads *
  * head_dim values holds the heads one after another; head h of token t is
