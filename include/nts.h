@@ -130,6 +130,35 @@ NTS_API int nts_qknorm_rms_heads(const void *X_dev, const float *gamma_dev, void
                                  float eps, int N, void *stream);
 
 /*
+ * nts_layernorm_split -- LayerNorm with the split-H statistic exchange
+ * (SwiftQK reading notes, Sec. 5e: the variance is (1/H) sum x^2 - mu^2, so
+ * a shard needs only two additive scalars, its sum and its sum of squares,
+ * and the Phase A/B/C structure of nts_qknorm_rms carries over with two
+ * scalars per shard instead of one):
+ *
+ *     s1_k, s2_k = sums over shard k of x_j and x_j^2            (fp32)
+ *     mu    = (s1_0 + ... + s1_{N-1}) / H
+ *     var   = max((s2_0 + ... + s2_{N-1}) / H - mu^2, 0)
+ *     rstd  = 1 / sqrt(var + eps)
+ *     y_j   = bf16_rne((x_j * gamma_j) * rstd + (beta_j - mu * rstd * gamma_j))
+ *
+ * which is (x_j - mu) * rstd * gamma_j + beta_j.  The one-pass variance
+ * loses relative accuracy when |mu| is large against the spread of the row
+ * (fp32 cancellation in s2/H - mu^2); the pages' formulation is kept.
+ *   X_dev      bf16 [T, H], read.     gamma_dev  fp32 [H], read.
+ *   beta_dev   fp32 [H], read, or NULL (no shift).
+ *   Y_dev      bf16 [T, H], written (Y == X allowed).
+ *   mean_dev   fp32 [T], written, or NULL.   rstd_dev  fp32 [T], or NULL.
+ *   Limits as nts_qknorm_rms, except H / N <= 20480 when beta is given (the
+ *   shard's gamma and beta both stay in shared memory).
+ * Errors: as nts_qknorm_rms.
+ */
+NTS_API int nts_layernorm_split(const void *X_dev, const float *gamma_dev,
+                                const float *beta_dev, void *Y_dev, float *mean_dev,
+                                float *rstd_dev, int64_t T, int64_t H, float eps, int N,
+                                void *stream);
+
+/*
  * nts_qknorm_rms_qk -- nts_qknorm_rms of a token batch's Q and K in ONE
  * launch (one persistent grid walks the tiles of both tensors).  Q and K may
  * have different widths (Hq, Hk: e.g. grouped-query attention, where K is

@@ -322,7 +322,7 @@ int nts_qknorm_rms(const void* X_dev, const float* gamma_dev, void* Y_dev, float
   if (rc != NTS_OK) return rc;
   if (T == 0) return NTS_OK;
   const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, T, H};
-  return launch_qknorm(&rq, 1, eps, N, 0, 1.0f, static_cast<cudaStream_t>(stream),
+  return launch_qknorm(&rq, 1, eps, N, 0, 1.0f, 0, static_cast<cudaStream_t>(stream),
                        current_tuning());
 }
 
@@ -337,7 +337,7 @@ int nts_qknorm_rms_fp8(const void* X_dev, float x_scale, const float* gamma_dev,
                 (long long)(H / N));
   if (T == 0) return NTS_OK;
   const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, T, H};
-  return launch_qknorm(&rq, 1, eps, N, 1, x_scale, static_cast<cudaStream_t>(stream),
+  return launch_qknorm(&rq, 1, eps, N, 1, x_scale, 0, static_cast<cudaStream_t>(stream),
                        current_tuning());
 }
 
@@ -355,7 +355,26 @@ int nts_qknorm_rms_heads(const void* X_dev, const float* gamma_dev, void* Y_dev,
   if (rc != NTS_OK) return rc;
   if (rows == 0) return NTS_OK;
   const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, rows, head_dim};
-  return launch_qknorm(&rq, 1, eps, N, 0, 1.0f, static_cast<cudaStream_t>(stream),
+  return launch_qknorm(&rq, 1, eps, N, 0, 1.0f, 0, static_cast<cudaStream_t>(stream),
+                       current_tuning());
+}
+
+int nts_layernorm_split(const void* X_dev, const float* gamma_dev, const float* beta_dev,
+                        void* Y_dev, float* mean_dev, float* rstd_dev, int64_t T, int64_t H,
+                        float eps, int N, void* stream) {
+  int rc = validate_qk(X_dev, gamma_dev, Y_dev, rstd_dev, T, H, eps, N);
+  if (rc != NTS_OK) return rc;
+  if (beta_dev != nullptr && !aligned(beta_dev, 16))
+    return fail(NTS_ERR_UNSUPPORTED, "beta must be 16-byte aligned");
+  if (mean_dev != nullptr && !aligned(mean_dev, 4))
+    return fail(NTS_ERR_UNSUPPORTED, "mean must be 4-byte aligned");
+  if (beta_dev != nullptr && H / N > 20480)
+    return fail(NTS_ERR_UNSUPPORTED, "H/N (%lld) exceeds 20480 with beta", (long long)(H / N));
+  if (T == 0) return NTS_OK;
+  QkRequest rq{X_dev, gamma_dev, Y_dev, rstd_dev, T, H};
+  rq.beta = beta_dev;
+  rq.mean = mean_dev;
+  return launch_qknorm(&rq, 1, eps, N, 0, 1.0f, 1, static_cast<cudaStream_t>(stream),
                        current_tuning());
 }
 
@@ -370,7 +389,7 @@ int nts_qknorm_rms_qk(const void* Q_dev, const float* gamma_q_dev, void* Yq_dev,
   if (T == 0) return NTS_OK;
   const QkRequest rq[2] = {{Q_dev, gamma_q_dev, Yq_dev, rinv_q_dev, T, Hq},
                            {K_dev, gamma_k_dev, Yk_dev, rinv_k_dev, T, Hk}};
-  return launch_qknorm(rq, 2, eps, N, 0, 1.0f, static_cast<cudaStream_t>(stream),
+  return launch_qknorm(rq, 2, eps, N, 0, 1.0f, 0, static_cast<cudaStream_t>(stream),
                        current_tuning());
 }
 

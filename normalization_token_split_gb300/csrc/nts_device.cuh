@@ -218,6 +218,17 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint
       : "memory");
 }
 
+// Two 32-bit values (8 bytes) into a cluster CTA's shared memory, completing
+// 8 transaction bytes on its mbarrier (address 8-byte aligned).
+__device__ __forceinline__ void st_async_f32x2(uint32_t remote_addr, float a, float b,
+                                               uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+          remote_addr),
+      "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(remote_bar)
+      : "memory");
+}
+
 // 1-D bulk copy global -> shared without an L2 hint (for re-read data).
 __device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void* src, uint32_t bytes,
                                                uint32_t bar) {

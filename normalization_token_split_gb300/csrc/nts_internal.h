@@ -82,12 +82,15 @@ struct QkRequest {
   float* rinv;
   int64_t T;
   int64_t H;
+  const float* beta = nullptr;  // LayerNorm only (nullable)
+  float* mean = nullptr;        // LayerNorm only (nullable)
 };
 
 // One launch normalizing 1 or 2 tensors (Q and K) with the same N; the
 // activations are bf16, or E4M3 codes whose values are code * x_scale.
+// layernorm = 1 selects the LayerNorm statistic (bf16 input only).
 int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4m3,
-                  float x_scale, cudaStream_t stream, const LaunchTuning& tune);
+                  float x_scale, int layernorm, cudaStream_t stream, const LaunchTuning& tune);
 int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune);
 
 int read_and_clear_qk_status(unsigned* out);

@@ -49,19 +49,25 @@ static __device__ unsigned int g_qk_status;
 
 // Element type of the activations read by a launch.
 enum { kInBf16 = 0, kInE4M3 = 1 };
+// Statistic: RMSNorm (one sum of squares) or LayerNorm (sum and sum of
+// squares, the SwiftQK notes' two additive scalars, Sec. 5e).
+enum { kQkRms = 0, kQkLn = 1 };
 
 // One tensor normalized by a launch (a launch covers one or two: Q and K).
 struct QkTensor {
   const void* X;   // bf16 or E4M3 codes [T, H]
   const float* gamma;
+  const float* beta;     // LayerNorm shift (nullable)
   __nv_bfloat16* Y;
-  float* rinv_out;
+  float* rinv_out;       // RMSNorm: 1/rms; LayerNorm: 1/sqrt(var + eps)
+  float* mean_out;       // LayerNorm mean (nullable)
   int64_t T;
   int64_t ntiles;  // ceil(T / R)
   int H;           // full row width H_total
   int W;           // H / N, the columns of one shard
   int nvec;        // W / 8 16-byte vectors per shard row
   uint32_t gam;    // shared-memory offset of this tensor's staged gamma
+  uint32_t bet;    // ... and of its staged beta (0 when beta is NULL)
 };
 
 struct QkParams {
@@ -73,6 +79,7 @@ struct QkParams {
   int R;           // rows per tile
   int S;           // ring stages
   int gsplit;      // 1: gamma re-laid out into split halves; 0: read as copied
+  int psum;        // fp32 parameters staged per CTA (gamma, and beta, of every tensor)
   float eps;
   float x_scale;   // E4M3 input: value = code * x_scale
   uint64_t wait_limit_ns;
@@ -81,22 +88,22 @@ struct QkParams {
 
 // Shared memory layout (bytes, in order):
 //   ring  [S][R][Wmax] elements   the staged shard rows (2 or 1 bytes each)
-//   gstg  per tensor [W] f32      gamma of this shard as copied (one bulk
-//                                 copy); absent when gsplit == 0
+//   gstg  per tensor [W] f32      gamma (and beta) of this shard as copied
+//                                 (bulk copies); absent when gsplit == 0
 //   gam   per tensor [2][nvec] float4: the same, split into the low and high
 //         halves of each 8-value vector (conflict-free reads); when the
-//         shards are too wide for both copies, gam holds gamma as copied
+//         shards are too wide for both copies, gam holds them as copied
 //   full  [S], empty [S]          ring mbarriers
 //   gbar                          gamma-arrival mbarrier
 //   xbar  [2][R]                  exchange mbarriers (double-buffered by tile)
-//   part  [2][R][N][WPR] f32      partial sums received from every warp of
-//                                 every shard of a row
+//   part  [2][R][N][WPR][NS] f32  partial sums received from every warp of
+//                                 every shard of a row (NS = 1 RMS, 2 LN)
 struct QkLayout {
   uint32_t ring, gstg, gam, full, empty, gbar, xbar, part, total;
 };
 
 __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int Wsum, int G,
-                                              int gsplit, int esize) {
+                                              int gsplit, int esize, int ns) {
   QkLayout L;
   L.ring = 0;
   L.gstg = L.ring + (uint32_t)S * R * Wmax * esize;
@@ -106,7 +113,7 @@ __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int
   L.gbar = L.empty + (uint32_t)S * 8;
   L.xbar = L.gbar + 8;
   L.part = L.xbar + (uint32_t)2 * R * 8;
-  L.total = L.part + (uint32_t)2 * R * N * (G / 32) * 4;
+  L.total = L.part + (uint32_t)2 * R * N * (G / 32) * 4 * ns;
   return L;
 }
 
@@ -140,9 +147,10 @@ __device__ __forceinline__ void load_vector(uint32_t srow, int v, bool inb, floa
   }
 }
 
-template <int N, int VPT, int IN>
+template <int N, int VPT, int IN, int STAT>
 __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const QkParams p) {
   constexpr int ES = (IN == kInBf16) ? 2 : 1;  // bytes per activation
+  constexpr int NS = (STAT == kQkLn) ? 2 : 1;  // scalars exchanged per warp
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t rank = (N > 1) ? cluster_ctarank() : 0u;
   const int64_t cid = cluster_id_x();
@@ -151,8 +159,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
   const int nconsumer = p.R * p.G;
   const int lane = tid & 31;
   const int wpr = p.G >> 5;
-  const int Wsum = p.ten[0].W + (p.ntensors > 1 ? p.ten[1].W : 0);
-  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, Wsum, p.G, p.gsplit, ES);
+  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, p.psum, p.G, p.gsplit, ES, NS);
   const uint32_t sbase = smem_addr(smem);
   const uint32_t stage_bytes = (uint32_t)p.R * p.Wmax * ES;
   const int64_t my_tiles = cid < p.ntiles ? (p.ntiles - 1 - cid) / ncl + 1 : 0;
@@ -175,12 +182,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
     if (N > 1) cluster_arrive_relaxed();
     if (lane == 0) {
       bool aborted = false;
-      // this shard's gamma first (every CTA re-reads it, so no evict hint)
-      mbar_arrive_expect_tx(sbase + L.gbar, (uint32_t)Wsum * 4);
-      for (int k = 0; k < p.ntensors; ++k)
-        bulk_g2s_plain(sbase + p.ten[k].gam - L.gam + L.gstg,
-                       p.ten[k].gamma + (size_t)rank * p.ten[k].W, (uint32_t)p.ten[k].W * 4,
-                       sbase + L.gbar);
+      // this shard's gamma (and beta) first (every CTA re-reads them, so no
+      // evict hint)
+      mbar_arrive_expect_tx(sbase + L.gbar, (uint32_t)p.psum * 4);
+      for (int k = 0; k < p.ntensors; ++k) {
+        const QkTensor& tk = p.ten[k];
+        bulk_g2s_plain(sbase + tk.gam - L.gam + L.gstg, tk.gamma + (size_t)rank * tk.W,
+                       (uint32_t)tk.W * 4, sbase + L.gbar);
+        if (STAT == kQkLn && tk.beta != nullptr)
+          bulk_g2s_plain(sbase + tk.bet - L.gam + L.gstg, tk.beta + (size_t)rank * tk.W,
+                         (uint32_t)tk.W * 4, sbase + L.gbar);
+      }
       const uint64_t policy = l2_policy_evict_first();
       for (int64_t j = 0; j < my_tiles; ++j) {
         const int s = (int)(j % p.S);
@@ -244,11 +256,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         aborted = true;
       }
 
-      // ---- Phase A: this shard's sum of squares (fp32, packed pairs).  The
-      // values are converted once and kept as fp32 pairs in w; four
-      // independent accumulators keep the FMA chains short.
+      // ---- Phase A: this shard's sum of squares (and, for LayerNorm, its
+      // sum) in fp32 packed pairs.  The values are converted once and kept
+      // as fp32 pairs in w; independent accumulators keep chains short.
       uint64_t w[VPT][4];
       uint64_t acc[4] = {0, 0, 0, 0};  // {0.f, 0.f} each
+      uint64_t sum2[2] = {0, 0};
       const uint32_t srow = sbase + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * tn.W * ES;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
@@ -256,6 +269,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         load_vector<IN>(srow, v, valid && v < nvec, p.x_scale, w[i]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = f2_fma(w[i][q], w[i][q], acc[q]);
+        if (STAT == kQkLn) {
+          sum2[0] = f2_add(sum2[0], f2_add(w[i][0], w[i][1]));
+          sum2[1] = f2_add(sum2[1], f2_add(w[i][2], w[i][3]));
+        }
       }
       // the stage's data is in registers: hand it back to the producer
       __syncwarp();
@@ -263,22 +280,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
       const uint64_t a01 = f2_add(acc[0], acc[1]), a23 = f2_add(acc[2], acc[3]);
       const uint64_t a = f2_add(a01, a23);
       const float ss = warp_sum(f2_lo(a) + f2_hi(a));
+      float s1 = 0.f;
+      if (STAT == kQkLn) {
+        const uint64_t c = f2_add(sum2[0], sum2[1]);
+        s1 = warp_sum(f2_lo(c) + f2_hi(c));
+      }
 
       // ---- exchange: send this warp's partial to every shard of the row
       const int b = (int)(j & 1);
       const uint32_t xbar = sbase + L.xbar + 8 * (b * p.R + row);
-      const uint32_t slot0 = sbase + L.part + 4 * (uint32_t)((b * p.R + row) * N * wpr);
+      const uint32_t slot0 = sbase + L.part + 4 * NS * (uint32_t)((b * p.R + row) * N * wpr);
       if (!started) {
         cluster_wait_acquire();
         started = true;
       }
       if (exchange) {
-        if (g == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(N * wpr * 4));
+        if (g == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(N * wpr * 4 * NS));
         if (lane == 0) {
-          const uint32_t slot = slot0 + 4 * (rank * wpr + wir);
+          const uint32_t slot = slot0 + 4 * NS * (rank * wpr + wir);
 #pragma unroll
-          for (int k = 0; k < N; ++k)
-            st_async_f32(map_to_rank(slot, k), ss, map_to_rank(xbar, k));
+          for (int k = 0; k < N; ++k) {
+            if (STAT == kQkLn)
+              st_async_f32x2(map_to_rank(slot, k), ss, s1, map_to_rank(xbar, k));
+            else
+              st_async_f32(map_to_rank(slot, k), ss, map_to_rank(xbar, k));
+          }
         }
       }
 
@@ -292,11 +318,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         }
         for (int k = 0; k < p.ntensors && p.gsplit; ++k) {
           const QkTensor& tk = p.ten[k];
-          const float4* src = reinterpret_cast<const float4*>(smem + tk.gam - L.gam + L.gstg);
-          float4* dst = reinterpret_cast<float4*>(smem + tk.gam);
-          for (int q = tid; q < tk.nvec; q += nconsumer) {
-            dst[q] = src[2 * q];
-            dst[tk.nvec + q] = src[2 * q + 1];
+          for (int par = 0; par < ((STAT == kQkLn && tk.beta != nullptr) ? 2 : 1); ++par) {
+            const uint32_t off = par ? tk.bet : tk.gam;
+            const float4* src = reinterpret_cast<const float4*>(smem + off - L.gam + L.gstg);
+            float4* dst = reinterpret_cast<float4*>(smem + off);
+            for (int q = tid; q < tk.nvec; q += nconsumer) {
+              dst[q] = src[2 * q];
+              dst[tk.nvec + q] = src[2 * q + 1];
+            }
           }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(nconsumer) : "memory");
@@ -319,7 +348,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
       }
 
       // ---- combine in rank order (then warp order within a shard)
-      float S = ss;
+      float S = ss, S1 = s1;
       if (exchange) {
         if (!mbar_wait_bounded(xbar, (uint32_t)((j >> 1) & 1), aborted ? 0 : p.wait_limit_ns)) {
           if (!aborted) atomicOr(&g_qk_status, kStatusTimeout);
@@ -327,21 +356,62 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         }
         const float* sl = reinterpret_cast<const float*>(smem + (slot0 - sbase));
         S = 0.f;
-        for (int k = 0; k < N * wpr; ++k) S += sl[k];
+        S1 = 0.f;
+        for (int k = 0; k < N * wpr; ++k) {
+          S += sl[NS * k];
+          if (STAT == kQkLn) S1 += sl[NS * k + 1];
+        }
       }
 
-      // ---- Phase C: scale and store the shard
+      // ---- Phase C: scale (and for LayerNorm centre and shift), store
       if (valid) {
-        const float rinv = 1.0f / sqrtf(S / (float)tn.H + p.eps);
+        float rinv, mu = 0.f;
+        if (STAT == kQkLn) {
+          mu = S1 / (float)tn.H;
+          const float var = fmaxf(S / (float)tn.H - mu * mu, 0.f);
+          rinv = 1.0f / sqrtf(var + p.eps);
+        } else {
+          rinv = 1.0f / sqrtf(S / (float)tn.H + p.eps);
+        }
         const uint64_t rr = f2(rinv, rinv);
+        const float nmr = -mu * rinv;
         __nv_bfloat16* yrow = tn.Y + (size_t)t * tn.H + (size_t)rank * tn.W;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
           const int v = i * p.G + g;
           if (v < nvec) {
             uint4 o;
-            const uint64_t y0 = f2_mul(w[i][0], rr), y1 = f2_mul(w[i][1], rr);
-            const uint64_t y2 = f2_mul(w[i][2], rr), y3 = f2_mul(w[i][3], rr);
+            uint64_t y0, y1, y2, y3;
+            if (STAT == kQkLn) {
+              // y = (x - mu) rinv gamma + beta = w rinv + (beta - mu rinv gamma)
+              const uint4 glo = ld_shared_v4(gam_lo + v * gstride);
+              const uint4 ghi = ld_shared_v4(gam_hi + v * gstride);
+              uint4 blo = make_uint4(0, 0, 0, 0), bhi = make_uint4(0, 0, 0, 0);
+              if (tn.beta != nullptr) {
+                const uint32_t bet_lo = sbase + tn.bet;
+                const uint32_t bet_hi = bet_lo + (p.gsplit ? (uint32_t)nvec * 16 : 16u);
+                blo = ld_shared_v4(bet_lo + v * gstride);
+                bhi = ld_shared_v4(bet_hi + v * gstride);
+              }
+              const uint64_t m2 = f2(nmr, nmr);
+              const uint64_t c0 = f2_fma(m2, f2(__uint_as_float(glo.x), __uint_as_float(glo.y)),
+                                         f2(__uint_as_float(blo.x), __uint_as_float(blo.y)));
+              const uint64_t c1 = f2_fma(m2, f2(__uint_as_float(glo.z), __uint_as_float(glo.w)),
+                                         f2(__uint_as_float(blo.z), __uint_as_float(blo.w)));
+              const uint64_t c2 = f2_fma(m2, f2(__uint_as_float(ghi.x), __uint_as_float(ghi.y)),
+                                         f2(__uint_as_float(bhi.x), __uint_as_float(bhi.y)));
+              const uint64_t c3 = f2_fma(m2, f2(__uint_as_float(ghi.z), __uint_as_float(ghi.w)),
+                                         f2(__uint_as_float(bhi.z), __uint_as_float(bhi.w)));
+              y0 = f2_fma(w[i][0], rr, c0);
+              y1 = f2_fma(w[i][1], rr, c1);
+              y2 = f2_fma(w[i][2], rr, c2);
+              y3 = f2_fma(w[i][3], rr, c3);
+            } else {
+              y0 = f2_mul(w[i][0], rr);
+              y1 = f2_mul(w[i][1], rr);
+              y2 = f2_mul(w[i][2], rr);
+              y3 = f2_mul(w[i][3], rr);
+            }
             o.x = pack_bf16x2_rn(f2_lo(y0), f2_hi(y0));
             o.y = pack_bf16x2_rn(f2_lo(y1), f2_hi(y1));
             o.z = pack_bf16x2_rn(f2_lo(y2), f2_hi(y2));
@@ -350,6 +420,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
           }
         }
         if (tn.rinv_out != nullptr && rank == 0 && g == 0) tn.rinv_out[t] = rinv;
+        if (STAT == kQkLn && tn.mean_out != nullptr && rank == 0 && g == 0) tn.mean_out[t] = mu;
       }
     }
     if (!started) cluster_wait_acquire();  // a CTA without tiles
@@ -364,28 +435,29 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
 
 using QkKernel = void (*)(QkParams);
 
-template <int N, int IN>
+template <int N, int IN, int STAT>
 QkKernel pick_qk_vpt(int vpt) {
   switch (vpt) {
-    case 1: return qknorm_cluster_kernel<N, 1, IN>;
-    case 2: return qknorm_cluster_kernel<N, 2, IN>;
-    case 3: return qknorm_cluster_kernel<N, 3, IN>;
-    case 4: return qknorm_cluster_kernel<N, 4, IN>;
-    case 5: return qknorm_cluster_kernel<N, 5, IN>;
-    case 6: return qknorm_cluster_kernel<N, 6, IN>;
-    case 8: return qknorm_cluster_kernel<N, 8, IN>;
+    case 1: return qknorm_cluster_kernel<N, 1, IN, STAT>;
+    case 2: return qknorm_cluster_kernel<N, 2, IN, STAT>;
+    case 3: return qknorm_cluster_kernel<N, 3, IN, STAT>;
+    case 4: return qknorm_cluster_kernel<N, 4, IN, STAT>;
+    case 5: return qknorm_cluster_kernel<N, 5, IN, STAT>;
+    case 6: return qknorm_cluster_kernel<N, 6, IN, STAT>;
+    case 8: return qknorm_cluster_kernel<N, 8, IN, STAT>;
     default: return nullptr;
   }
 }
 
-// Instantiates every QK kernel for input type IN in the calling unit.
-template <int IN>
+// Instantiates every QK kernel for input type IN and statistic STAT in the
+// calling unit.
+template <int IN, int STAT>
 QkKernel pick_qk_input(int N, int vpt) {
   switch (N) {
-    case 1: return pick_qk_vpt<1, IN>(vpt);
-    case 2: return pick_qk_vpt<2, IN>(vpt);
-    case 4: return pick_qk_vpt<4, IN>(vpt);
-    case 8: return pick_qk_vpt<8, IN>(vpt);
+    case 1: return pick_qk_vpt<1, IN, STAT>(vpt);
+    case 2: return pick_qk_vpt<2, IN, STAT>(vpt);
+    case 4: return pick_qk_vpt<4, IN, STAT>(vpt);
+    case 8: return pick_qk_vpt<8, IN, STAT>(vpt);
     default: return nullptr;
   }
 }
@@ -400,10 +472,12 @@ static inline int read_and_clear_local_qk_status(unsigned* out) {
   return NTS_OK;
 }
 
-// Defined by qk_bf16.cu and qk_e4m3.cu.
+// Defined by qk_bf16.cu, qk_e4m3.cu and qk_ln.cu.
 QkKernel pick_qk_bf16(int N, int vpt);
 QkKernel pick_qk_e4m3(int N, int vpt);
+QkKernel pick_qk_ln(int N, int vpt);
 int read_and_clear_qk_bf16_status(unsigned* out);
 int read_and_clear_qk_e4m3_status(unsigned* out);
+int read_and_clear_qk_ln_status(unsigned* out);
 
 }  // namespace nts

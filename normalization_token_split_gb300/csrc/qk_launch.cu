@@ -1,5 +1,5 @@
 // qk_launch.cu -- launch-shape selection and launch of the split-H
-// QK-RMSNorm kernels (qk_kernel.cuh).
+// QK-RMSNorm and LayerNorm kernels (qk_kernel.cuh).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -9,15 +9,19 @@
 namespace nts {
 
 int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4m3,
-                  float x_scale, cudaStream_t stream, const LaunchTuning& tune) {
+                  float x_scale, int layernorm, cudaStream_t stream, const LaunchTuning& tune) {
   const int ES = in_e4m3 ? 1 : 2;
+  const int NS = layernorm ? 2 : 1;
+  if (layernorm && in_e4m3) return fail(NTS_ERR_UNSUPPORTED, "LayerNorm of E4M3 input");
   const DeviceInfo& dev = device_info();
   if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
-  int Wmax = 0, Wsum = 0;
+  // psum: fp32 parameters staged per CTA (gamma, and beta when given)
+  int Wmax = 0, psum = 0;
   int64_t Tsum = 0;
   for (int k = 0; k < ntensors; ++k) {
-    Wmax = std::max(Wmax, (int)(rq[k].H / N));
-    Wsum += (int)(rq[k].H / N);
+    const int W = (int)(rq[k].H / N);
+    Wmax = std::max(Wmax, W);
+    psum += W * ((layernorm && rq[k].beta != nullptr) ? 2 : 1);
     Tsum += rq[k].T;
   }
 
@@ -39,17 +43,19 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4
   // gamma is split into the conflict-free layout when both copies fit.
   int gsplit = 1;
   int S = 4;
-  while (S > 2 && qk_layout(N, S, R, Wmax, Wsum, rs.G, 1, ES).total > (uint32_t)tune.smem_budget) --S;
-  if (qk_layout(N, S, R, Wmax, Wsum, rs.G, 1, ES).total > (uint32_t)dev.max_smem_optin) gsplit = 0;
-  while (S > 1 && qk_layout(N, S, R, Wmax, Wsum, rs.G, gsplit, ES).total > (uint32_t)dev.max_smem_optin)
-    --S;
+  auto layout = [&](int s, int split) { return qk_layout(N, s, R, Wmax, psum, rs.G, split, ES, NS); };
+  while (S > 2 && layout(S, 1).total > (uint32_t)tune.smem_budget) --S;
+  if (layout(S, 1).total > (uint32_t)dev.max_smem_optin) gsplit = 0;
+  while (S > 1 && layout(S, gsplit).total > (uint32_t)dev.max_smem_optin) --S;
   if (tune.force_stages > 0) S = tune.force_stages;
-  const QkLayout L = qk_layout(N, S, R, Wmax, Wsum, rs.G, gsplit, ES);
+  const QkLayout L = layout(S, gsplit);
   const size_t smem = L.total;
   if (smem > (size_t)dev.max_smem_optin)
     return fail(NTS_ERR_UNSUPPORTED, "shard row too wide for shared memory: H/N = %d", Wmax);
 
-  QkKernel kern = in_e4m3 ? pick_qk_e4m3(N, rs.vpt) : pick_qk_bf16(N, rs.vpt);
+  QkKernel kern = layernorm ? pick_qk_ln(N, rs.vpt)
+                 : in_e4m3 ? pick_qk_e4m3(N, rs.vpt)
+                           : pick_qk_bf16(N, rs.vpt);
   if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for N=%d vpt=%d", N, rs.vpt);
 
   QkParams prm = {};
@@ -59,6 +65,8 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4
     QkTensor& tn = prm.ten[k];
     tn.X = rq[k].X;
     tn.gamma = rq[k].gamma;
+    tn.beta = layernorm ? rq[k].beta : nullptr;
+    tn.mean_out = layernorm ? rq[k].mean : nullptr;
     tn.Y = static_cast<__nv_bfloat16*>(rq[k].Y);
     tn.rinv_out = rq[k].rinv;
     tn.T = rq[k].T;
@@ -68,6 +76,10 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4
     tn.nvec = tn.W / 8;
     tn.gam = gam;
     gam += (uint32_t)tn.W * 4;
+    if (tn.beta != nullptr) {
+      tn.bet = gam;
+      gam += (uint32_t)tn.W * 4;
+    }
     ntiles += tn.ntiles;
   }
   prm.ntensors = ntensors;
@@ -77,6 +89,7 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4
   prm.R = R;
   prm.S = S;
   prm.gsplit = gsplit;
+  prm.psum = psum;
   prm.eps = eps;
   prm.x_scale = x_scale;
   prm.wait_limit_ns = tune.wait_limit_ns;
@@ -106,21 +119,23 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4
   if (tune.force_grid > 0) ncl = std::min<int64_t>(ntiles, tune.force_grid);
   cfg.gridDim = dim3((unsigned)(ncl * N));
 
-  log_launch("qknorm_rms", "tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d gsplit=%d "
+  log_launch(layernorm ? "layernorm_split" : "qknorm_rms", "tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d gsplit=%d "
              "smem=%zu clusters=%lld/%lld", ntensors, (long long)rq[0].T, (int)rq[0].H, N, rs.vpt,
              rs.G, R, S, gsplit, smem, (long long)ncl, (long long)max_clusters);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
-  if (e != cudaSuccess) return fail_cuda(e, "launching qknorm_rms");
+  if (e != cudaSuccess) return fail_cuda(e, layernorm ? "launching layernorm_split" : "launching qknorm_rms");
   return NTS_OK;
 }
 
 int read_and_clear_qk_status(unsigned* out) {
-  unsigned a = 0, b = 0;
+  unsigned a = 0, b = 0, c = 0;
   int rc = read_and_clear_qk_bf16_status(&a);
   if (rc != NTS_OK) return rc;
   rc = read_and_clear_qk_e4m3_status(&b);
   if (rc != NTS_OK) return rc;
-  *out = a | b;
+  rc = read_and_clear_qk_ln_status(&c);
+  if (rc != NTS_OK) return rc;
+  *out = a | b | c;
   return NTS_OK;
 }
 

@@ -116,6 +116,32 @@ def qknorm_rms_heads(x: torch.Tensor, gamma: torch.Tensor, head_dim: int, eps: f
     return out, rinv
 
 
+def layernorm_split(x: torch.Tensor, gamma: torch.Tensor, beta: Optional[torch.Tensor] = None,
+                    eps: float = 1e-5, N: int = 1, out: Optional[torch.Tensor] = None,
+                    mean: Optional[torch.Tensor] = None, rstd: Optional[torch.Tensor] = None,
+                    want_stats: bool = False, stream=None):
+    """LayerNorm of x [T, H] (bf16) with gain gamma and optional shift beta
+    (fp32 [H]), the statistics exchanged as per-shard (sum, sum of squares)
+    between N cluster shards.  Returns (y, mean or None, rstd or None)."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("gamma", gamma, torch.float32)
+    if beta is not None:
+        _need_cuda("beta", beta, torch.float32)
+    T, H = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _need_cuda("out", out, torch.bfloat16)
+    if want_stats:
+        mean = torch.empty(T, device=x.device, dtype=torch.float32) if mean is None else mean
+        rstd = torch.empty(T, device=x.device, dtype=torch.float32) if rstd is None else rstd
+    for name, t in (("mean", mean), ("rstd", rstd)):
+        if t is not None:
+            _need_cuda(name, t, torch.float32)
+    check(lib().nts_layernorm_split(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(out), _ptr(mean),
+                                    _ptr(rstd), T, H, float(eps), int(N), _stream(stream)))
+    return out, mean, rstd
+
+
 def qknorm_rms_qk(q: torch.Tensor, gamma_q: torch.Tensor, k: torch.Tensor,
                   gamma_k: torch.Tensor, eps: float = 1e-6, N: int = 1,
                   out_q: Optional[torch.Tensor] = None, out_k: Optional[torch.Tensor] = None,

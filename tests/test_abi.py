@@ -169,3 +169,20 @@ def test_fp8_argument_checks(lib):
     assert f(H=24, N=1) == UNSUPPORTED          # 24-byte E4M3 rows
     assert f(H=48, N=2) == UNSUPPORTED
     assert f(T=0, X=None) == OK
+
+
+def test_layernorm_argument_checks(lib):
+    def f(**k):
+        return lib.nts_layernorm_split(k.get("X", A16), k.get("g", A16), k.get("b", None), A16,
+                                       k.get("m", None), None, k.get("T", 4), k.get("H", 512),
+                                       k.get("eps", 1e-5), k.get("N", 2), None)
+    assert f(X=None) == INVALID
+    assert f(g=None) == INVALID
+    assert f(T=-1) == INVALID
+    assert f(N=3) == INVALID
+    assert f(eps=0.0) == INVALID
+    assert f(H=8, N=2) == UNSUPPORTED               # 4-value shards
+    assert f(b=MIS) == UNSUPPORTED
+    assert f(m=P((1 << 20) + 2)) == UNSUPPORTED
+    assert f(b=A16, H=20488 * 2, N=2) == UNSUPPORTED  # gamma and beta do not fit on chip
+    assert f(T=0, X=None, g=None) == OK

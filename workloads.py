@@ -57,6 +57,12 @@ def qk_inputs(T: int, H: int, seed: int, outlier_frac: float = 0.0,
     return x.to(torch.bfloat16), gamma_vector(H, seed, device)
 
 
+def beta_vector(H: int, seed: int, device="cpu") -> torch.Tensor:
+    """LayerNorm shift beta fp32 [H]: small values around zero."""
+    g = _gen(seed * 7 + 3, device)
+    return 0.1 * torch.randn(H, generator=g, device=device, dtype=torch.float32)
+
+
 def outlier_columns(H: int, seed: int, outlier_frac: float) -> np.ndarray:
     """The columns qk_inputs scales for the given seed (for reporting)."""
     gc = _gen(seed * 31 + 5, "cpu")
