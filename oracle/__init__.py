@@ -25,7 +25,8 @@ through ctypes.  Each wrapper names the passage its C function follows:
 * ``mx_correction``    -- c(B, p) by quadrature.
 
 Parity status of every function is recorded in the test files that pin it
-(tests/test_oracle_*.py).  Formats: ``fmt`` 0 = E4M3, 1 = E2M1.
+(tests/test_oracle_*.py).  Formats: ``fmt`` 0 = E4M3, 1 = E2M1 (both with
+E8M0 block scales), 2 = NVFP4 (E2M1 values, B = 16, E4M3 block scales).
 """
 from __future__ import annotations
 
@@ -45,6 +46,7 @@ _lib = None
 
 FMT_E4M3 = 0
 FMT_E2M1 = 1
+FMT_NVFP4 = 2
 
 
 def build(force: bool = False) -> str:
@@ -182,6 +184,13 @@ def qknorm_rms_heads(X, gamma, eps: float, head_dim: int):
     return Y, rinv
 
 
+def _check_fmt(fmt: int, B: int, post: bool = False):
+    if fmt not in (FMT_E4M3, FMT_E2M1, FMT_NVFP4):
+        raise ValueError(f"unknown format {fmt}")
+    if fmt == FMT_NVFP4 and (B != 16 or post):
+        raise ValueError("NVFP4 has 16-value blocks and E4M3 scales (no post-round form)")
+
+
 def _mx_out(T, D, B, fmt):
     codes = np.empty((T, codes_row_bytes(D, fmt)), np.uint8)
     scales = np.empty((T, D // B), np.uint8)
@@ -191,6 +200,7 @@ def _mx_out(T, D, B, fmt):
 
 def rmsnorm_mxcast(X, gamma, eps: float, B: int, fmt: int):
     """Returns (codes, scales, rinv f64 [T], amax f32 [T,K])."""
+    _check_fmt(fmt, B)
     X = _bf16_bits(X)
     T, D = X.shape
     g = _gamma(gamma, D)
@@ -205,6 +215,7 @@ def rmsnorm_mxcast(X, gamma, eps: float, B: int, fmt: int):
 
 def mxnorm_cast(X, gamma, eps: float, B: int, fmt: int, p: int):
     """Returns (codes, scales, rinv f64 [T], amax f32 [T,K])."""
+    _check_fmt(fmt, B)
     X = _bf16_bits(X)
     T, D = X.shape
     g = _gamma(gamma, D)
@@ -220,6 +231,7 @@ def mxnorm_cast(X, gamma, eps: float, B: int, fmt: int, p: int):
 
 def mxnorm_postround_cast(X, gamma, eps: float, B: int, fmt: int, p: int):
     """Post-round MXNorm. Returns (codes, scales, rinv f64 [T], amax f32 [T,K])."""
+    _check_fmt(fmt, B, post=True)
     X = _bf16_bits(X)
     T, D = X.shape
     g = _gamma(gamma, D)
@@ -235,6 +247,7 @@ def mxnorm_postround_cast(X, gamma, eps: float, B: int, fmt: int, p: int):
 
 def mx_cast_given_rinv(X, gamma, rinv_f32, B: int, fmt: int):
     """Block stage with given fp32 factors. Returns (codes, scales, amax)."""
+    _check_fmt(fmt, B)
     X = _bf16_bits(X)
     T, D = X.shape
     g = _gamma(gamma, D)

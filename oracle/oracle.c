@@ -360,6 +360,35 @@ ORACLE_EXPORT double oracle_mx_correction(int B, int p) {
  *      fp32 r is known (integer codes decided in the same precision).
  * Output layout: codes row-major (E4M3 one byte per element; E2M1 two per
  * byte, element 2i in the low nibble), scales [K] bytes, amax [K] floats. */
+/* NVFP4 block (fmt 2; a reading: the MXNorm card names NVFP4 among its
+ * kernel cases, Table 4, without its rules): B = 16 E2M1 values share one
+ * E4M3 scale
+ *     s_k    = E4M3(amax_k * r / 6)        (6 = largest E2M1 magnitude;
+ *                                            RNE, saturating at 448)
+ *     code_kb = E2M1(w_kb * r / s_k)        (code 0 when s_k == 0),
+ * with no second, per-tensor scale: the normalized absmaxes lie far inside
+ * the E4M3 range.  In fp32 mode every step is an fp32 operation:
+ * fl32(fl32(amax*r)/6), then fl32(fl32(w*r) * fl32(1/s)). */
+static void nvfp4_cast_block(const float *w, int B, double r, int in_float,
+                             double amax, uint8_t *codes, int64_t j0,
+                             uint8_t *scale) {
+    double v = in_float ? (double)(float)(amax * r) : amax * r;
+    double sv = in_float ? (double)(float)(v / 6.0) : v / 6.0;
+    uint8_t sc = oracle_double_to_e4m3(sv);
+    double s = oracle_e4m3_to_double(sc);
+    double inv = 0.0;
+    if (s > 0.0) inv = in_float ? (double)(float)(1.0 / s) : 1.0 / s;
+    *scale = sc;
+    for (int b = 0; b < B; ++b) {
+        int64_t j = j0 + b;
+        double y = in_float ? (double)(float)((double)w[b] * r) : (double)w[b] * r;
+        uint8_t c = 0;
+        if (s > 0.0) c = oracle_double_to_e2m1(in_float ? (double)(float)(y * inv) : y / s);
+        if ((j & 1) == 0) codes[j / 2] = c;
+        else codes[j / 2] = (uint8_t)(codes[j / 2] | (c << 4));
+    }
+}
+
 static void mx_cast_row(const float *w, int64_t D, double r, int in_float,
                         int B, int fmt, uint8_t *codes, uint8_t *scales,
                         float *amax_out) {
@@ -372,6 +401,10 @@ static void mx_cast_row(const float *w, int64_t D, double r, int in_float,
             if (a > amax) amax = a;
         }
         if (amax_out) amax_out[k] = (float)amax;
+        if (fmt == 2) {
+            nvfp4_cast_block(w + k * B, B, r, in_float, amax, codes, k * B, scales + k);
+            continue;
+        }
         double v = in_float ? (double)(float)(amax * r) : amax * r;
         int e = oracle_e8m0_exponent(v, emax);
         scales[k] = (uint8_t)(e + 127);
