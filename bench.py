@@ -334,6 +334,8 @@ def run_gpu(args):
         result["e2e"] = run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world)
     if not args.no_decode:
         result["decode_qk_us_per_call"] = decode_latency(nts, torch, dev)
+    if not args.no_variants:
+        result["variants"] = variant_rates(nts, torch, dev, Q, gq, X, peak)
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
@@ -389,6 +391,63 @@ def run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(elapsed / steps * 1e3, 4),
             "path": "nts_*_host C ABI entry points, pinned host buffers"}
+
+
+def variant_rates(nts, torch, dev, Q, gq, X, peak, reps=20):
+    """The widened paths outside the step, each at the step's sizes: device
+    time per launch (CUDA events around `reps` back-to-back launches on the
+    launching stream, after 3 warm-up launches) and algorithmic GB/s."""
+    import workloads
+    T, H = Q.shape
+    Tm, D = X.shape
+    codes8, scale8, g8 = workloads.qk_inputs_fp8(T, H, seed=3000, outlier_frac=0.01, device=dev)
+    beta = workloads.beta_vector(H, seed=3000, device=dev)
+    ghd = workloads.gamma_vector(128, seed=128, device=dev)
+    Y = torch.empty_like(Q)
+    codes = torch.empty(Tm, D, dtype=torch.uint8, device=dev)
+    codes4 = torch.empty(Tm, D // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(Tm, D // MX_B, dtype=torch.uint8, device=dev)
+    scales16 = torch.empty(Tm, D // 16, dtype=torch.uint8, device=dev)
+    cases = {
+        f"qknorm_rms_heads[{T}x{H},head_dim=128,N=1]": (
+            4 * T * H, lambda: nts.qknorm_rms_heads(Q, ghd, 128, eps=EPS, N=1, out=Y)),
+        f"qknorm_rms_fp8[{T}x{H},N={QK_N}]": (
+            3 * T * H, lambda: nts.qknorm_rms_fp8(codes8, scale8, g8, eps=EPS, N=QK_N, out=Y)),
+        f"qknorm_rms[{T}x{H},N={QK_N}]": (
+            4 * T * H, lambda: nts.qknorm_rms(Q, gq, eps=EPS, N=QK_N, out=Y)),
+        f"layernorm_split[{T}x{H},N={QK_N},beta]": (
+            4 * T * H, lambda: nts.layernorm_split(Q, gq, beta, eps=1e-5, N=QK_N, out=Y)),
+        f"mxnorm_postround_cast[{Tm}x{D},B={MX_B},p=2,e4m3]": (
+            mx_bytes(Tm, D, MX_B), lambda: nts.mxnorm_postround_cast(
+                X, None, eps=EPS, B=MX_B, fmt="e4m3", p=2, codes=codes, scales=scales)),
+        f"mxnorm_cast[{Tm}x{D},B=16,p=2,nvfp4]": (
+            Tm * (2 * D + D // 2 + D // 16), lambda: nts.mxnorm_cast(
+                X, None, eps=EPS, B=16, fmt="nvfp4", p=2, codes=codes4, scales=scales16)),
+        f"rmsnorm_mxcast[{Tm}x{D},B=16,nvfp4]": (
+            Tm * (2 * D + D // 2 + D // 16), lambda: nts.rmsnorm_mxcast(
+                X, None, eps=EPS, B=16, fmt="nvfp4", codes=codes4, scales=scales16)),
+        f"rmsnorm_mxcast[{Tm}x{D},B={MX_B},e2m1]": (
+            Tm * (2 * D + D // 2 + D // MX_B), lambda: nts.rmsnorm_mxcast(
+                X, None, eps=EPS, B=MX_B, fmt="e2m1", codes=codes4, scales=scales)),
+    }
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name, (nbytes, fn) in cases.items():
+        for _ in range(3):
+            fn()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s.record(stream)
+        for _ in range(reps):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e) / reps
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 5), "bytes": nbytes, "gbs": round(gbs, 1),
+                     "frac_of_measured": round(gbs / peak, 4)}
+    nts.check_status()
+    return out
 
 
 def decode_latency(nts, torch, dev):
@@ -517,6 +576,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

@@ -56,8 +56,9 @@ typedef enum {
 } nts_status;
 
 typedef enum {
-    NTS_FMT_E4M3 = 0, /* OCP E4M3: 1 byte per element, max 448 (MXFP8) */
-    NTS_FMT_E2M1 = 1  /* OCP E2M1: 4 bits per element, max 6 (MXFP4) */
+    NTS_FMT_E4M3 = 0, /* OCP E4M3: 1 byte per element, max 448; E8M0 scales (MXFP8) */
+    NTS_FMT_E2M1 = 1, /* OCP E2M1: 4 bits per element, max 6; E8M0 scales (MXFP4) */
+    NTS_FMT_NVFP4 = 2 /* E2M1 elements, B = 16, one E4M3 scale per block (NVFP4) */
 } nts_elem_fmt;
 
 /* Library version, major*10000 + minor*100 + patch. */
@@ -197,9 +198,17 @@ NTS_API int nts_qknorm_rms_qk(const void *Q_dev, const float *gamma_q_dev, void 
  *               of w (before normalization) or NULL.
  *   T >= 0; D % B == 0; B in {16, 32, 64}; D <= 32768; eps > 0 and finite;
  *   fmt in nts_elem_fmt.
+ *
+ * fmt = NTS_FMT_NVFP4 (B must be 16; the MXNorm card lists NVFP4 among its
+ * kernel cases, Table 4, without its rules; this is the reading taken):
+ *     s_k      = E4M3_rne_satfinite(fp32(fp32(amax_k * rinv) / 6))
+ *     scale_k  = the E4M3 code of s_k
+ *     code_j   = E2M1_rne_satfinite(fp32(fp32(w_j * rinv) * fp32(1 / s_k))),
+ *                or 0 for every element of a block whose s_k is 0;
+ * codes are laid out as for E2M1; no per-tensor second-level scale.
  * Errors: INVALID_ARG (null X/codes/scales, T < 0, D <= 0, D % B, bad B,
- *         eps or fmt), UNSUPPORTED (row too wide, unaligned pointer),
- *         CUDA (launch failure).
+ *         eps or fmt, NVFP4 with B != 16), UNSUPPORTED (row too wide,
+ *         unaligned pointer), CUDA (launch failure).
  */
 NTS_API int nts_rmsnorm_mxcast(const void *X_dev, const float *gamma_dev,
                        uint8_t *codes_dev, uint8_t *scales_dev,
@@ -234,7 +243,8 @@ NTS_API int nts_mxnorm_cast(const void *X_dev, const float *gamma_dev,
  *     rho~ = c(B, p) * ((1/K) sum_k (2^round(log2 amax_k))^p)^(1/p),
  * with the same c(B, p); the cast (scales and codes from amax_k * rinv) is
  * that of nts_mxnorm_cast.  Arguments, layouts and errors as
- * nts_mxnorm_cast.
+ * nts_mxnorm_cast; the rounding is that of E8M0 scales, so fmt =
+ * NTS_FMT_NVFP4 is INVALID_ARG here.
  */
 NTS_API int nts_mxnorm_postround_cast(const void *X_dev, const float *gamma_dev,
                                       uint8_t *codes_dev, uint8_t *scales_dev,

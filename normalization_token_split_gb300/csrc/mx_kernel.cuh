@@ -4,7 +4,8 @@
 // Method (MXNorm paper card, abstract, Fig. 1 caption and Fig. A.1):
 //   a row of D values is cut into K = D/B blocks of B contiguous values; each
 //   block is stored as B element codes (E4M3 or E2M1) sharing one E8M0 scale
-//   2^round(log2(normalized absmax / 2^emax)).  RMSNorm + MXCast takes the
+//   2^round(log2(normalized absmax / 2^emax)), or (NVFP4, Table 4's second
+//   format) 16 E2M1 codes sharing one E4M3 scale, normalized absmax / 6.  RMSNorm + MXCast takes the
 //   RMS from sum x^2 over the row; MXNorm estimates it from the block
 //   absmaxes the cast computes anyway, rho~ = c(B,p) * M_p(absmax), a
 //   reduction B times smaller.  Both are fused into one kernel (Fig. 8).
@@ -296,10 +297,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
       for (int i = 0; i < BPT; ++i) {
         const int b = i * p.G + g;
         if (b < p.K) {
-          const int e = e8m0_exponent(am[i] * rinv, kEmax);
-          const float is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+          float is;                 // multiplier taking w*rinv to the element grid
+          uint32_t keep = ~0u;      // NVFP4: 0 for a block whose scale is zero
+          if (FMT == NTS_FMT_NVFP4) {
+            const uint32_t sc = cvt_e4m3x2(__fdiv_rn(am[i] * rinv, 6.0f), 0.f) & 0xFFu;
+            is = sc != 0 ? __frcp_rn(f2_lo(e4m3x2_to_f2((uint16_t)sc))) : 0.f;
+            keep = sc != 0 ? ~0u : 0u;
+            p.scales[(size_t)t * p.K + b] = (uint8_t)sc;
+          } else {
+            const int e = e8m0_exponent(am[i] * rinv, kEmax);
+            is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+            p.scales[(size_t)t * p.K + b] = (uint8_t)(e + 127);
+          }
           const uint64_t ss = f2(is, is);
-          p.scales[(size_t)t * p.K + b] = (uint8_t)(e + 127);
           if (p.amax_out != nullptr) p.amax_out[(size_t)t * p.K + b] = am[i];
           const uint32_t base = srow + (uint32_t)b * kB * 2;
 #pragma unroll
@@ -329,7 +339,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
                                  (cvt_e2m1x2(f2_lo(q[1]), f2_hi(q[1])) << 8) |
                                  (cvt_e2m1x2(f2_lo(q[2]), f2_hi(q[2])) << 16) |
                                  (cvt_e2m1x2(f2_lo(q[3]), f2_hi(q[3])) << 24);
-              st_global_u32(crow + (size_t)b * (kB / 2) + u * 4, c);
+              st_global_u32(crow + (size_t)b * (kB / 2) + u * 4, c & keep);
             }
           }
         }
@@ -385,10 +395,12 @@ static inline int read_and_clear_local_mx_status(unsigned* out) {
   return NTS_OK;
 }
 
-// Defined by mx_e4m3.cu and mx_e2m1.cu.
+// Defined by mx_e4m3.cu, mx_e2m1.cu and mx_nvfp4.cu.
 MxKernel pick_mx_e4m3(int stat, int B, int bpt);
 MxKernel pick_mx_e2m1(int stat, int B, int bpt);
+MxKernel pick_mx_nvfp4(int stat, int B, int bpt);
 int read_and_clear_mx_e4m3_status(unsigned* out);
 int read_and_clear_mx_e2m1_status(unsigned* out);
+int read_and_clear_mx_nvfp4_status(unsigned* out);
 
 }  // namespace nts

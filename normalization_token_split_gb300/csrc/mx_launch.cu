@@ -67,8 +67,9 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
     return fail(NTS_ERR_UNSUPPORTED, "row too wide for shared memory: D = %d", D);
 
   const int stat = rq.p == 0 ? kStatRms : (rq.p == 1 ? kStatMxP1 : kStatMxP2);
-  MxKernel kern = rq.fmt == NTS_FMT_E4M3 ? pick_mx_e4m3(stat, rq.B, sh.bpt)
-                                         : pick_mx_e2m1(stat, rq.B, sh.bpt);
+  MxKernel kern = rq.fmt == NTS_FMT_E4M3   ? pick_mx_e4m3(stat, rq.B, sh.bpt)
+                 : rq.fmt == NTS_FMT_E2M1 ? pick_mx_e2m1(stat, rq.B, sh.bpt)
+                                          : pick_mx_nvfp4(stat, rq.B, sh.bpt);
   if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for B=%d bpt=%d", rq.B, sh.bpt);
 
   MxParams prm;
@@ -115,12 +116,14 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
 }
 
 int read_and_clear_mx_status(unsigned* out) {
-  unsigned a = 0, b = 0;
+  unsigned a = 0, b = 0, c = 0;
   int rc = read_and_clear_mx_e4m3_status(&a);
   if (rc != NTS_OK) return rc;
   rc = read_and_clear_mx_e2m1_status(&b);
   if (rc != NTS_OK) return rc;
-  *out = a | b;
+  rc = read_and_clear_mx_nvfp4_status(&c);
+  if (rc != NTS_OK) return rc;
+  *out = a | b | c;
   return NTS_OK;
 }
 

@@ -278,8 +278,10 @@ int validate_mx(const void* X, const float* gamma, const uint8_t* codes, const u
     return fail(NTS_ERR_INVALID_ARG, "B must be 16, 32 or 64, got %d", B);
   if (D % B != 0)
     return fail(NTS_ERR_INVALID_ARG, "D (%lld) must be a multiple of B (%d)", (long long)D, B);
-  if (fmt != NTS_FMT_E4M3 && fmt != NTS_FMT_E2M1)
+  if (fmt != NTS_FMT_E4M3 && fmt != NTS_FMT_E2M1 && fmt != NTS_FMT_NVFP4)
     return fail(NTS_ERR_INVALID_ARG, "unknown element format %d", fmt);
+  if (fmt == NTS_FMT_NVFP4 && B != 16)
+    return fail(NTS_ERR_INVALID_ARG, "NVFP4 blocks have 16 elements, got B = %d", B);
   if (mxnorm && p != 1 && p != 2) return fail(NTS_ERR_INVALID_ARG, "p must be 1 or 2, got %d", p);
   if (!(eps > 0.f) || !std::isfinite(eps))
     return fail(NTS_ERR_INVALID_ARG, "eps must be positive and finite");
@@ -295,6 +297,8 @@ int run_mx(const void* X, const float* gamma, uint8_t* codes, uint8_t* scales, f
            void* stream, int post = 0) {
   int rc = validate_mx(X, gamma, codes, scales, rinv, amax, T, D, eps, B, fmt, p, mxnorm);
   if (rc != NTS_OK) return rc;
+  if (post && fmt == NTS_FMT_NVFP4)
+    return fail(NTS_ERR_INVALID_ARG, "post-round MXNorm rounds to E8M0 scales, not NVFP4");
   if (T == 0) return NTS_OK;
   MxRequest rq{X, gamma, codes, scales, rinv, amax, T, D, eps, B, fmt, mxnorm ? p : 0, 0.0, post};
   if (mxnorm) {

@@ -14,7 +14,9 @@ from ._lib import check, lib
 
 FMT_E4M3 = 0
 FMT_E2M1 = 1
-_FMT_NAMES = {"e4m3": FMT_E4M3, "e2m1": FMT_E2M1, FMT_E4M3: FMT_E4M3, FMT_E2M1: FMT_E2M1}
+FMT_NVFP4 = 2   # E2M1 elements, B = 16, E4M3 block scales
+_FMT_NAMES = {"e4m3": FMT_E4M3, "e2m1": FMT_E2M1, "nvfp4": FMT_NVFP4,
+              FMT_E4M3: FMT_E4M3, FMT_E2M1: FMT_E2M1, FMT_NVFP4: FMT_NVFP4}
 
 
 class MxOut(NamedTuple):

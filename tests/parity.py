@@ -8,7 +8,8 @@ hot-path contract:
   oracle's block stage fed the device's own fp32 factors): bit-exact;
 * against the oracle's double-precision definition: scales exact except +-1
   where the oracle's normalized absmax lies within 1e-6 (relative) of a
-  power-of-two rounding boundary sqrt(2) 2^n; codes exact except one code step
+  power-of-two rounding boundary sqrt(2) 2^n (NVFP4: where absmax/6 lies
+  within 1e-6 of an E4M3 rounding midpoint); codes exact except one code step
   where the oracle's pre-cast value lies within 1e-6 of a rounding midpoint.
 """
 from __future__ import annotations
@@ -43,7 +44,14 @@ def check_qk(Y_gpu_bits, rinv_gpu, Y_or_bits, rinv_or, what=""):
 def _format_values(fmt):
     if fmt == oracle.FMT_E4M3:
         return np.array([oracle.decode(c, fmt) for c in range(0x7F)])
-    return np.array([oracle.decode(c, fmt) for c in range(8)])
+    return np.array([oracle.decode(c, oracle.FMT_E2M1) for c in range(8)])
+
+
+def _near_midpoint(v, fmt):
+    """Relative distance of |v| to the nearest rounding midpoint of fmt."""
+    vals = _format_values(fmt)
+    mids = (vals[:-1] + vals[1:]) / 2
+    return np.min(np.abs(np.abs(v)[:, None] / mids[None, :] - 1), axis=1)
 
 
 def _near_boundary_log2(v):
@@ -83,13 +91,15 @@ def check_mx(X_bits, gamma, B, fmt, gpu, ref, rinv_gpu, eps, what=""):
     assert nbad_c == 0, f"{what} {nbad_c} code bytes differ from the fp32 block stage"
 
     # (2) against the double definition: exceptions only at boundaries
-    emax = 8 if fmt == oracle.FMT_E4M3 else 2
+    nvfp4 = fmt == oracle.FMT_NVFP4
     diff_s = scales_g != scales_o
     stats["scale_boundary_exceptions"] = int(diff_s.sum())
     if diff_s.any():
         v = (amax_o.astype(np.float64) * rinv_o[:, None])[diff_s]
         assert np.all(np.abs(scales_g[diff_s].astype(int) - scales_o[diff_s].astype(int)) == 1)
-        assert np.all(_near_boundary_log2(v) <= NEAR), f"{what} scale differs away from a boundary"
+        near = (_near_midpoint(v / 6.0, oracle.FMT_E4M3) if nvfp4
+                else _near_boundary_log2(v))
+        assert np.all(near <= NEAR), f"{what} scale differs away from a boundary"
     cg = unpack_codes(codes_g, fmt, D)
     co = unpack_codes(codes_o, fmt, D)
     same_scale = np.repeat(~diff_s, B, axis=1)
@@ -101,8 +111,13 @@ def check_mx(X_bits, gamma, B, fmt, gpu, ref, rinv_gpu, eps, what=""):
         rows, cols = np.nonzero(diff_c)
         x = bf16_to_f64(X_bits[rows, cols])
         w = x if gamma is None else (x.astype(np.float32) * gamma[cols]).astype(np.float64)
-        e = scales_o[rows, cols // B].astype(np.float64) - 127
-        q = np.abs(w * rinv_o[rows] * np.exp2(-e))
+        if nvfp4:
+            sc = scales_o[rows, cols // B]
+            q = np.abs(w * rinv_o[rows] / np.array([oracle.decode(int(c), oracle.FMT_E4M3)
+                                                    for c in sc]))
+        else:
+            e = scales_o[rows, cols // B].astype(np.float64) - 127
+            q = np.abs(w * rinv_o[rows] * np.exp2(-e))
         near = np.min(np.abs(q[:, None] / mids[None, :] - 1), axis=1) <= NEAR
         sign_mask = 0x7F if fmt == oracle.FMT_E4M3 else 0x7
         step = np.abs((cg[rows, cols] & sign_mask).astype(int) - (co[rows, cols] & sign_mask).astype(int))

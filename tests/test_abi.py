@@ -186,3 +186,17 @@ def test_layernorm_argument_checks(lib):
     assert f(m=P((1 << 20) + 2)) == UNSUPPORTED
     assert f(b=A16, H=20488 * 2, N=2) == UNSUPPORTED  # gamma and beta do not fit on chip
     assert f(T=0, X=None, g=None) == OK
+
+
+def test_nvfp4_argument_checks(lib):
+    NV = 2
+    assert lib.nts_rmsnorm_mxcast(A16, None, A16, A16, None, None, 4, 256, 1e-6, 32, NV,
+                                  None) == INVALID
+    assert lib.nts_mxnorm_cast(A16, None, A16, A16, None, None, 4, 256, 1e-6, 64, NV, 2,
+                               None) == INVALID
+    assert lib.nts_mxnorm_postround_cast(A16, None, A16, A16, None, None, 4, 256, 1e-6, 16, NV,
+                                         2, None) == INVALID
+    assert lib.nts_rmsnorm_mxcast(A16, None, A16, A16, None, None, 4, 256, 1e-6, 16, 3,
+                                  None) == INVALID
+    assert lib.nts_rmsnorm_mxcast(A16, None, A16, A16, None, None, 0, 256, 1e-6, 16, NV,
+                                  None) == OK

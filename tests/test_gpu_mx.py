@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 nts = pytest.importorskip("normalization_token_split_gb300")
 DEV = "cuda:0"
-FMTS = {"e4m3": oracle.FMT_E4M3, "e2m1": oracle.FMT_E2M1}
+FMTS = {"e4m3": oracle.FMT_E4M3, "e2m1": oracle.FMT_E2M1, "nvfp4": oracle.FMT_NVFP4}
 
 
 def gpu_call(kind, X, gamma, eps, B, fmt, p):
@@ -212,3 +212,55 @@ def test_postround_subnormal_and_degenerate_blocks():
     for p in (1, 2):
         for fmt in ("e4m3", "e2m1"):
             compare("post", X, None, 1e-6, 32, fmt, p, what=f"post degenerate p={p} {fmt}")
+
+
+# ------------------------------------------- NVFP4 (E2M1, B = 16, E4M3 scales)
+
+@pytest.mark.parametrize("kind,p", KINDS)
+@pytest.mark.parametrize("with_gamma", [False, True])
+def test_nvfp4_small_complete(kind, p, with_gamma):
+    X, g = workloads.mx_inputs(333, 1024, seed=900 + p, t_frac=0.1, with_gamma=with_gamma)
+    compare(kind, X, g, 1e-6, 16, "nvfp4", p, what=f"nvfp4 {kind}{p} gamma={with_gamma}")
+
+
+@pytest.mark.parametrize("kind,p", KINDS)
+@pytest.mark.parametrize("D", [4096, 7168, 16384])
+def test_nvfp4_full_size_sampled(kind, p, D):
+    X, _ = workloads.mx_inputs(65536, D, seed=910 + D, t_frac=0.05, device=DEV)
+    rows = sample_rows(65536, max(256, 4 * 1024 * 1024 // D), D + p)
+    trows = torch.from_numpy(workloads.student_t_rows(65536, 910 + D, 0.05)[:64])
+    rows = torch.unique(torch.cat([rows, trows])).to(DEV)
+    compare(kind, X, None, 1e-6, 16, "nvfp4", p, rows=rows, what=f"nvfp4 {kind}{p} D={D}")
+
+
+@pytest.mark.parametrize("D", [16, 48, 1040, 8192, 32768])
+@pytest.mark.parametrize("T", [1, 5, 129])
+def test_nvfp4_row_widths_and_ragged_tails(D, T):
+    X, g = workloads.mx_inputs(T, D, seed=920 + D + T, with_gamma=True)
+    for kind, p in KINDS:
+        compare(kind, X, g, 1e-6, 16, "nvfp4", p, what=f"nvfp4 {kind}{p} T={T} D={D}")
+
+
+def test_nvfp4_degenerate_blocks():
+    X, _ = workloads.mx_inputs(64, 512, seed=930)
+    X[0] = 0                          # all-zero row: zero scales and codes
+    X[1, :16] = 0                     # one zero block
+    X[2, 32:48] = 1e-30               # block whose scale underflows to zero
+    X[3, 64:80] = -1.0e17             # large values
+    X[4, ::2] = -0.0
+    X[5, 96:112] = torch.linspace(-3, 3, 16)
+    for kind, p in KINDS:
+        out = gpu_call(kind, X, None, 1e-6, 16, "nvfp4", p)
+        compare(kind, X, None, 1e-6, 16, "nvfp4", p, what=f"nvfp4 degenerate {kind}{p}")
+        sc = out.scales.cpu().numpy()
+        assert np.all(sc[0] == 0) and sc[1, 0] == 0 and sc[2, 2] == 0
+        assert np.all(out.codes[0].cpu().numpy() == 0)
+        assert np.all(out.codes[2, 16:24].cpu().numpy() == 0)
+
+
+def test_nvfp4_rejects_other_blocks_and_post_round():
+    X, _ = workloads.mx_inputs(4, 256, seed=931, device=DEV)
+    with pytest.raises(nts.NtsError, match="INVALID_ARG"):
+        nts.rmsnorm_mxcast(X, None, B=32, fmt="nvfp4")
+    with pytest.raises(nts.NtsError, match="INVALID_ARG"):
+        nts.mxnorm_postround_cast(X, None, B=16, fmt="nvfp4")
