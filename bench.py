@@ -408,6 +408,10 @@ def variant_rates(nts, torch, dev, Q, gq, X, peak, reps=20):
     codes4 = torch.empty(Tm, D // 2, dtype=torch.uint8, device=dev)
     scales = torch.empty(Tm, D // MX_B, dtype=torch.uint8, device=dev)
     scales16 = torch.empty(Tm, D // 16, dtype=torch.uint8, device=dev)
+    qcodes = torch.empty(T, H, dtype=torch.uint8, device=dev)
+    qcodes4 = torch.empty(T, H // 2, dtype=torch.uint8, device=dev)
+    qscales = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+    qscales16 = torch.empty(T, H // 16, dtype=torch.uint8, device=dev)
     cases = {
         f"qknorm_rms_heads[{T}x{H},head_dim=128,N=1]": (
             4 * T * H, lambda: nts.qknorm_rms_heads(Q, ghd, 128, eps=EPS, N=1, out=Y)),
@@ -415,6 +419,12 @@ def variant_rates(nts, torch, dev, Q, gq, X, peak, reps=20):
             3 * T * H, lambda: nts.qknorm_rms_fp8(codes8, scale8, g8, eps=EPS, N=QK_N, out=Y)),
         f"qknorm_rms[{T}x{H},N={QK_N}]": (
             4 * T * H, lambda: nts.qknorm_rms(Q, gq, eps=EPS, N=QK_N, out=Y)),
+        f"qknorm_rms_mxcast[{T}x{H},N={QK_N},B=32,e4m3]": (
+            T * H * 3 + T * (H // 32), lambda: nts.qknorm_rms_mxcast(
+                Q, gq, eps=EPS, N=QK_N, B=32, fmt="e4m3", codes=qcodes, scales=qscales)),
+        f"qknorm_rms_mxcast[{T}x{H},N={QK_N},B=16,nvfp4]": (
+            T * H * 2 + T * H // 2 + T * (H // 16), lambda: nts.qknorm_rms_mxcast(
+                Q, gq, eps=EPS, N=QK_N, B=16, fmt="nvfp4", codes=qcodes4, scales=qscales16)),
         f"layernorm_split[{T}x{H},N={QK_N},beta]": (
             4 * T * H, lambda: nts.layernorm_split(Q, gq, beta, eps=1e-5, N=QK_N, out=Y)),
         f"mxnorm_postround_cast[{Tm}x{D},B={MX_B},p=2,e4m3]": (

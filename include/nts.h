@@ -176,6 +176,31 @@ NTS_API int nts_qknorm_rms_qk(const void *Q_dev, const float *gamma_q_dev, void 
                               void *stream);
 
 /*
+ * nts_qknorm_rms_mxcast -- layerwise QK-RMSNorm with the split-H exchange of
+ * nts_qknorm_rms, whose normalized rows leave as an MX (or NVFP4) block cast
+ * instead of bf16: the QK path's Phase C feeds the block stage of
+ * nts_rmsnorm_mxcast (SwiftQK Sec. III.C writes only the final normalized
+ * shard; the MXNorm card, Fig. 8, fuses normalization and cast into one
+ * kernel).  With w_j = fp32(x_j * gamma_j) and rinv = 1/sqrt(S/H + eps),
+ * S = S_0 + ... + S_{N-1} in rank order as in nts_qknorm_rms, the scales and
+ * codes are exactly those nts_rmsnorm_mxcast defines for this w and rinv
+ * (E8M0 scales for E4M3/E2M1, E4M3 scales for NVFP4).  Each block's absmax
+ * is taken while the exchange is in flight; blocks never straddle shards.
+ *   X_dev       bf16 [T, H], read.         gamma_dev  fp32 [H], read.
+ *   codes_dev   uint8 [T, H] (E4M3) or [T, H/2] (E2M1, NVFP4), written,
+ *               16-byte aligned.
+ *   scales_dev  uint8 [T, H/B], written.   rinv_dev   fp32 [T] or NULL.
+ *   Limits of nts_qknorm_rms, plus B in {16, 32, 64} (16 for NVFP4) and
+ *   (H / N) % B == 0.
+ * Errors: as nts_qknorm_rms; INVALID_ARG also for a null scales_dev, a bad
+ *         B or fmt; UNSUPPORTED for (H / N) % B != 0.
+ */
+NTS_API int nts_qknorm_rms_mxcast(const void *X_dev, const float *gamma_dev,
+                                  uint8_t *codes_dev, uint8_t *scales_dev, float *rinv_dev,
+                                  int64_t T, int64_t H, float eps, int N, int B, int fmt,
+                                  void *stream);
+
+/*
  * nts_rmsnorm_mxcast -- RMSNorm fused with the MX cast (MXNorm card,
  * Fig. 1 caption, left graph; Fig. 8 "normalization and casting fused into a
  * single kernel"):

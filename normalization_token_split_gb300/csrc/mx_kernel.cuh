@@ -84,18 +84,6 @@ __host__ __device__ inline MxLayout mx_layout(int S, int R, int D, int G) {
   return L;
 }
 
-// E8M0 exponent of a block whose normalized absmax is `ay` (>= 0):
-// round(log2 ay) - emax, where the log2 rounding goes up exactly when the
-// fp32 significand is >= the first fp32 value above sqrt(2) (0x3504F4 in the
-// mantissa field); zero and subnormal absmaxes give the smallest scale.
-__device__ __forceinline__ int e8m0_exponent(float ay, int emax) {
-  const uint32_t b = __float_as_uint(ay);
-  const int field = (int)(b >> 23);
-  if (field == 0) return -127;
-  const int e = field - 127 + ((b & 0x7FFFFFu) >= 0x3504F4u ? 1 : 0) - emax;
-  return max(-127, min(127, e));
-}
-
 // 2^round(log2 a) for a >= 0 (0 for a == 0): the power of two the E8M0
 // rounding picks for a block absmax a, subnormal a included.
 __device__ __forceinline__ float round_pow2(float a) {
@@ -157,11 +145,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
     if (lane == 0) {
       bool aborted = false;
       const uint64_t policy = l2_policy_evict_first();
+      // ring stage s of tile j and the parity of its pass, (j / S) & 1, kept
+      // incrementally (no 64-bit division in the loop)
+      int s = 0;
+      uint32_t ph = 0;
       for (int64_t j = 0; j < my_tiles; ++j) {
-        const int s = (int)(j % p.S);
         if (j >= p.S &&
-            !mbar_wait_bounded(sbase + L.empty + 8 * s, (uint32_t)((j / p.S - 1) & 1),
-                               p.wait_limit_ns)) {
+            !mbar_wait_bounded(sbase + L.empty + 8 * s, ph ^ 1u, p.wait_limit_ns)) {
           atomicOr(&g_mx_status, kStatusTimeout);
           aborted = true;
           break;
@@ -172,6 +162,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
         mbar_arrive_expect_tx(bar, bytes + (j == 0 ? p.missing_tx : 0u));
         bulk_g2s(sbase + L.ring + (uint32_t)s * stage_bytes, p.X + (size_t)t0 * p.D, bytes, bar,
                  policy);
+        if (++s == p.S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       for (int64_t j = max64(0, my_tiles - p.S); j < my_tiles && !aborted; ++j)
         (void)mbar_wait_bounded(sbase + L.full + 8 * (int)(j % p.S), (uint32_t)((j / p.S) & 1),
@@ -189,12 +183,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
   const size_t cbytes = (FMT == NTS_FMT_E4M3) ? (size_t)p.D : (size_t)p.D / 2;
   bool aborted = false;
 
+  int s = 0;          // ring stage of tile j
+  uint32_t ph = 0;    // (j / S) & 1
   for (int64_t j = 0; j < my_tiles; ++j) {
-    const int s = (int)(j % p.S);
     const int64_t t = (cta + j * ncta) * p.R + row;
     const bool valid = t < p.T;
-    if (!mbar_wait_bounded(sbase + L.full + 8 * s, (uint32_t)((j / p.S) & 1),
-                           aborted ? 0 : p.wait_limit_ns)) {
+    if (!mbar_wait_bounded(sbase + L.full + 8 * s, ph, aborted ? 0 : p.wait_limit_ns)) {
       if (!aborted) atomicOr(&g_mx_status, kStatusTimeout);
       aborted = true;
     }
@@ -300,8 +294,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
           float is;                 // multiplier taking w*rinv to the element grid
           uint32_t keep = ~0u;      // NVFP4: 0 for a block whose scale is zero
           if (FMT == NTS_FMT_NVFP4) {
-            const uint32_t sc = cvt_e4m3x2(__fdiv_rn(am[i] * rinv, 6.0f), 0.f) & 0xFFu;
-            is = sc != 0 ? __frcp_rn(f2_lo(e4m3x2_to_f2((uint16_t)sc))) : 0.f;
+            const uint32_t sc = nvfp4_scale(am[i] * rinv, &is);
             keep = sc != 0 ? ~0u : 0u;
             p.scales[(size_t)t * p.K + b] = (uint8_t)sc;
           } else {
@@ -348,6 +341,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
     // every read of stage s by this warp is done
     __syncwarp();
     if (lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
+    if (++s == p.S) {
+      s = 0;
+      ph ^= 1u;
+    }
   }
 }
 

@@ -326,7 +326,7 @@ int nts_qknorm_rms(const void* X_dev, const float* gamma_dev, void* Y_dev, float
   if (rc != NTS_OK) return rc;
   if (T == 0) return NTS_OK;
   const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, T, H};
-  return launch_qknorm(&rq, 1, eps, N, 0, 1.0f, 0, static_cast<cudaStream_t>(stream),
+  return launch_qknorm(&rq, 1, eps, N, QkOptions{}, static_cast<cudaStream_t>(stream),
                        current_tuning());
 }
 
@@ -341,8 +341,10 @@ int nts_qknorm_rms_fp8(const void* X_dev, float x_scale, const float* gamma_dev,
                 (long long)(H / N));
   if (T == 0) return NTS_OK;
   const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, T, H};
-  return launch_qknorm(&rq, 1, eps, N, 1, x_scale, 0, static_cast<cudaStream_t>(stream),
-                       current_tuning());
+  QkOptions opt;
+  opt.in_e4m3 = 1;
+  opt.x_scale = x_scale;
+  return launch_qknorm(&rq, 1, eps, N, opt, static_cast<cudaStream_t>(stream), current_tuning());
 }
 
 int nts_qknorm_rms_heads(const void* X_dev, const float* gamma_dev, void* Y_dev,
@@ -359,7 +361,7 @@ int nts_qknorm_rms_heads(const void* X_dev, const float* gamma_dev, void* Y_dev,
   if (rc != NTS_OK) return rc;
   if (rows == 0) return NTS_OK;
   const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, rows, head_dim};
-  return launch_qknorm(&rq, 1, eps, N, 0, 1.0f, 0, static_cast<cudaStream_t>(stream),
+  return launch_qknorm(&rq, 1, eps, N, QkOptions{}, static_cast<cudaStream_t>(stream),
                        current_tuning());
 }
 
@@ -378,8 +380,9 @@ int nts_layernorm_split(const void* X_dev, const float* gamma_dev, const float* 
   QkRequest rq{X_dev, gamma_dev, Y_dev, rstd_dev, T, H};
   rq.beta = beta_dev;
   rq.mean = mean_dev;
-  return launch_qknorm(&rq, 1, eps, N, 0, 1.0f, 1, static_cast<cudaStream_t>(stream),
-                       current_tuning());
+  QkOptions opt;
+  opt.layernorm = 1;
+  return launch_qknorm(&rq, 1, eps, N, opt, static_cast<cudaStream_t>(stream), current_tuning());
 }
 
 int nts_qknorm_rms_qk(const void* Q_dev, const float* gamma_q_dev, void* Yq_dev,
@@ -393,8 +396,33 @@ int nts_qknorm_rms_qk(const void* Q_dev, const float* gamma_q_dev, void* Yq_dev,
   if (T == 0) return NTS_OK;
   const QkRequest rq[2] = {{Q_dev, gamma_q_dev, Yq_dev, rinv_q_dev, T, Hq},
                            {K_dev, gamma_k_dev, Yk_dev, rinv_k_dev, T, Hk}};
-  return launch_qknorm(rq, 2, eps, N, 0, 1.0f, 0, static_cast<cudaStream_t>(stream),
+  return launch_qknorm(rq, 2, eps, N, QkOptions{}, static_cast<cudaStream_t>(stream),
                        current_tuning());
+}
+
+int nts_qknorm_rms_mxcast(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,
+                          uint8_t* scales_dev, float* rinv_dev, int64_t T, int64_t H, float eps,
+                          int N, int B, int fmt, void* stream) {
+  int rc = validate_qk(X_dev, gamma_dev, codes_dev, rinv_dev, T, H, eps, N);
+  if (rc != NTS_OK) return rc;
+  if (T > 0 && scales_dev == nullptr) return fail(NTS_ERR_INVALID_ARG, "scales must be non-NULL");
+  if (B != 16 && B != 32 && B != 64)
+    return fail(NTS_ERR_INVALID_ARG, "B must be 16, 32 or 64, got %d", B);
+  if (fmt != NTS_FMT_E4M3 && fmt != NTS_FMT_E2M1 && fmt != NTS_FMT_NVFP4)
+    return fail(NTS_ERR_INVALID_ARG, "unknown element format %d", fmt);
+  if (fmt == NTS_FMT_NVFP4 && B != 16)
+    return fail(NTS_ERR_INVALID_ARG, "NVFP4 blocks have 16 elements, got B = %d", B);
+  if ((H / N) % B != 0)
+    return fail(NTS_ERR_UNSUPPORTED, "H/N (%lld) must be a multiple of B (%d)",
+                (long long)(H / N), B);
+  if (T == 0) return NTS_OK;
+  QkRequest rq{X_dev, gamma_dev, nullptr, rinv_dev, T, H};
+  rq.codes = codes_dev;
+  rq.scales = scales_dev;
+  QkOptions opt;
+  opt.out_fmt = fmt;
+  opt.B = B;
+  return launch_qknorm(&rq, 1, eps, N, opt, static_cast<cudaStream_t>(stream), current_tuning());
 }
 
 int nts_rmsnorm_mxcast(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,

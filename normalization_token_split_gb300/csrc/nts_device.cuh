@@ -239,6 +239,20 @@ __device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void* src, ui
       : "memory");
 }
 
+// ------------------------------------------------------- MX block scales
+
+// E8M0 exponent of a block whose normalized absmax is `ay` (>= 0):
+// round(log2 ay) - emax, where the log2 rounding goes up exactly when the
+// fp32 significand is >= the first fp32 value above sqrt(2) (0x3504F4 in the
+// mantissa field); zero and subnormal absmaxes give the smallest scale.
+__device__ __forceinline__ int e8m0_exponent(float ay, int emax) {
+  const uint32_t b = __float_as_uint(ay);
+  const int field = (int)(b >> 23);
+  if (field == 0) return -127;
+  const int e = field - 127 + ((b & 0x7FFFFFu) >= 0x3504F4u ? 1 : 0) - emax;
+  return max(-127, min(127, e));
+}
+
 // ------------------------------------------------------- packed fp32 math
 // Two fp32 lanes in one 64-bit register pair (Blackwell f32x2 pipes).
 
@@ -247,16 +261,8 @@ __device__ __forceinline__ uint64_t f2(float lo, float hi) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
-__device__ __forceinline__ float f2_lo(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return lo;
-}
-__device__ __forceinline__ float f2_hi(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return hi;
-}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
@@ -316,6 +322,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
   return v;
+}
+
+// NVFP4 block scale of a block whose normalized absmax is `ay` (>= 0): the
+// E4M3 code of fp32(ay / 6) (RNE, saturating at 448; 6 is the largest E2M1
+// magnitude) and, in *inv, the fp32 reciprocal of that code's value (0 for
+// a zero scale).
+__device__ __forceinline__ uint32_t nvfp4_scale(float ay, float* inv) {
+  const uint32_t sc = cvt_e4m3x2(__fdiv_rn(ay, 6.0f), 0.f) & 0xFFu;
+  *inv = sc != 0 ? __frcp_rn(f2_lo(e4m3x2_to_f2((uint16_t)sc))) : 0.f;
+  return sc;
 }
 
 }  // namespace nts

@@ -84,13 +84,23 @@ struct QkRequest {
   int64_t H;
   const float* beta = nullptr;  // LayerNorm only (nullable)
   float* mean = nullptr;        // LayerNorm only (nullable)
+  uint8_t* codes = nullptr;     // block-cast output (replaces Y)
+  uint8_t* scales = nullptr;
 };
 
-// One launch normalizing 1 or 2 tensors (Q and K) with the same N; the
-// activations are bf16, or E4M3 codes whose values are code * x_scale.
-// layernorm = 1 selects the LayerNorm statistic (bf16 input only).
-int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4m3,
-                  float x_scale, int layernorm, cudaStream_t stream, const LaunchTuning& tune);
+// What a QK launch reads, computes and writes beyond the common case (bf16
+// in, RMSNorm, bf16 out).
+struct QkOptions {
+  int in_e4m3 = 0;      // activations are E4M3 codes, value = code * x_scale
+  float x_scale = 1.f;
+  int layernorm = 0;    // LayerNorm statistic (bf16 input only)
+  int out_fmt = -1;     // >= 0: block-cast output in this nts_elem_fmt (RMSNorm only)
+  int B = 0;            // ... with blocks of B elements
+};
+
+// One launch normalizing 1 or 2 tensors (Q and K) with the same N.
+int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkOptions& opt,
+                  cudaStream_t stream, const LaunchTuning& tune);
 int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune);
 
 int read_and_clear_qk_status(unsigned* out);

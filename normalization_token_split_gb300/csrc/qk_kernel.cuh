@@ -52,6 +52,9 @@ enum { kInBf16 = 0, kInE4M3 = 1 };
 // Statistic: RMSNorm (one sum of squares) or LayerNorm (sum and sum of
 // squares, the SwiftQK notes' two additive scalars, Sec. 5e).
 enum { kQkRms = 0, kQkLn = 1 };
+// Output: bf16 rows, or the block cast of the normalized rows (MX E4M3 or
+// E2M1 codes with E8M0 scales, or NVFP4) written in place of them.
+enum { kOutBf16 = 0, kOutE4M3 = 1, kOutE2M1 = 2, kOutNvfp4 = 3 };
 
 // One tensor normalized by a launch (a launch covers one or two: Q and K).
 struct QkTensor {
@@ -59,6 +62,8 @@ struct QkTensor {
   const float* gamma;
   const float* beta;     // LayerNorm shift (nullable)
   __nv_bfloat16* Y;
+  uint8_t* codes;        // block-cast output: element codes [T, H] or [T, H/2]
+  uint8_t* scales;       // ... and block scales [T, H/B]
   float* rinv_out;       // RMSNorm: 1/rms; LayerNorm: 1/sqrt(var + eps)
   float* mean_out;       // LayerNorm mean (nullable)
   int64_t T;
@@ -80,6 +85,8 @@ struct QkParams {
   int S;           // ring stages
   int gsplit;      // 1: gamma re-laid out into split halves; 0: read as copied
   int psum;        // fp32 parameters staged per CTA (gamma, and beta, of every tensor)
+  int bv;          // block-cast output: 16-byte vectors per block (B / 8)
+  int bshift;      // ... and log2(B)
   float eps;
   float x_scale;   // E4M3 input: value = code * x_scale
   uint64_t wait_limit_ns;
@@ -147,7 +154,7 @@ __device__ __forceinline__ void load_vector(uint32_t srow, int v, bool inb, floa
   }
 }
 
-template <int N, int VPT, int IN, int STAT>
+template <int N, int VPT, int IN, int STAT, int OUT>
 __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const QkParams p) {
   constexpr int ES = (IN == kInBf16) ? 2 : 1;  // bytes per activation
   constexpr int NS = (STAT == kQkLn) ? 2 : 1;  // scalars exchanged per warp
@@ -194,11 +201,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
                          (uint32_t)tk.W * 4, sbase + L.gbar);
       }
       const uint64_t policy = l2_policy_evict_first();
+      // ring stage s of tile j and the parity of its pass, (j / S) & 1, kept
+      // incrementally (no 64-bit division in the loop)
+      int s = 0;
+      uint32_t ph = 0;
       for (int64_t j = 0; j < my_tiles; ++j) {
-        const int s = (int)(j % p.S);
         if (j >= p.S &&
-            !mbar_wait_bounded(sbase + L.empty + 8 * s, (uint32_t)((j / p.S - 1) & 1),
-                               p.wait_limit_ns)) {
+            !mbar_wait_bounded(sbase + L.empty + 8 * s, ph ^ 1u, p.wait_limit_ns)) {
           atomicOr(&g_qk_status, kStatusTimeout);
           aborted = true;
           break;
@@ -217,6 +226,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         } else {
           for (int r = 0; r < nrows; ++r)
             bulk_g2s(dst + r * row_bytes, src + (size_t)r * tn.H * ES, row_bytes, bar, policy);
+        }
+        if (++s == p.S) {
+          s = 0;
+          ph ^= 1u;
         }
       }
       // let the last copies land before this CTA can retire
@@ -242,16 +255,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
     const int wir = g >> 5;
     const bool exchange = (N > 1) || (wpr > 1);
     bool aborted = false;
+    int s = 0;          // ring stage of tile j
+    uint32_t ph = 0;    // (j / S) & 1
     for (int64_t j = 0; j < my_tiles; ++j) {
-      const int s = (int)(j % p.S);
       int64_t t0;
       const QkTensor& tn = p.ten[qk_tile(p, cid + j * ncl, &t0)];
       const int64_t t = t0 + row;
       const bool valid = t < tn.T;
       const int nvec = tn.nvec;
 
-      if (!mbar_wait_bounded(sbase + L.full + 8 * s, (uint32_t)((j / p.S) & 1),
-                             aborted ? 0 : p.wait_limit_ns)) {
+      if (!mbar_wait_bounded(sbase + L.full + 8 * s, ph, aborted ? 0 : p.wait_limit_ns)) {
         if (!aborted) atomicOr(&g_qk_status, kStatusTimeout);
         aborted = true;
       }
@@ -346,6 +359,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         w[i][2] = f2_mul(w[i][2], f2(__uint_as_float(ghi.x), __uint_as_float(ghi.y)));
         w[i][3] = f2_mul(w[i][3], f2(__uint_as_float(ghi.z), __uint_as_float(ghi.w)));
       }
+      // block-cast output: each block's absmax of x*gamma, still before the
+      // combine (a block is bv consecutive vectors, i.e. bv adjacent lanes)
+      float am[OUT != kOutBf16 ? VPT : 1];
+      if (OUT != kOutBf16) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          float m = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            m = fmaxf(m, fmaxf(fabsf(f2_lo(w[i][q])), fabsf(f2_hi(w[i][q]))));
+          for (int o = 1; o < p.bv; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+          am[i] = m;
+        }
+      }
 
       // ---- combine in rank order (then warp order within a shard)
       float S = ss, S1 = s1;
@@ -379,6 +406,42 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
           const int v = i * p.G + g;
+          if (OUT != kOutBf16) {
+            if (v < nvec) {
+              // scale of this vector's block, then its eight codes
+              const int64_t col = (int64_t)rank * tn.W + 8 * v;
+              float is;
+              uint32_t keep = ~0u, sbyte;
+              if (OUT == kOutNvfp4) {
+                sbyte = nvfp4_scale(am[i] * rinv, &is);
+                keep = sbyte != 0 ? ~0u : 0u;
+              } else {
+                const int e = e8m0_exponent(am[i] * rinv, OUT == kOutE4M3 ? 8 : 2);
+                is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+                sbyte = (uint32_t)(e + 127);
+              }
+              if ((g & (p.bv - 1)) == 0)
+                tn.scales[((size_t)t * tn.H + col) >> p.bshift] = (uint8_t)sbyte;
+              const uint64_t ss = f2(is, is);
+              uint64_t q[4];
+#pragma unroll
+              for (int h = 0; h < 4; ++h) q[h] = f2_mul(f2_mul(w[i][h], rr), ss);
+              if (OUT == kOutE4M3) {
+                const uint32_t lo = cvt_e4m3x2(f2_lo(q[0]), f2_hi(q[0])) |
+                                    (cvt_e4m3x2(f2_lo(q[1]), f2_hi(q[1])) << 16);
+                const uint32_t hi = cvt_e4m3x2(f2_lo(q[2]), f2_hi(q[2])) |
+                                    (cvt_e4m3x2(f2_lo(q[3]), f2_hi(q[3])) << 16);
+                st_global_v2(tn.codes + (size_t)t * tn.H + col, lo, hi);
+              } else {
+                const uint32_t c = cvt_e2m1x2(f2_lo(q[0]), f2_hi(q[0])) |
+                                   (cvt_e2m1x2(f2_lo(q[1]), f2_hi(q[1])) << 8) |
+                                   (cvt_e2m1x2(f2_lo(q[2]), f2_hi(q[2])) << 16) |
+                                   (cvt_e2m1x2(f2_lo(q[3]), f2_hi(q[3])) << 24);
+                st_global_u32(tn.codes + ((size_t)t * tn.H + col) / 2, c & keep);
+              }
+            }
+            continue;
+          }
           if (v < nvec) {
             uint4 o;
             uint64_t y0, y1, y2, y3;
@@ -422,6 +485,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         if (tn.rinv_out != nullptr && rank == 0 && g == 0) tn.rinv_out[t] = rinv;
         if (STAT == kQkLn && tn.mean_out != nullptr && rank == 0 && g == 0) tn.mean_out[t] = mu;
       }
+      if (++s == p.S) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     if (!started) cluster_wait_acquire();  // a CTA without tiles
   }
@@ -435,29 +502,29 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
 
 using QkKernel = void (*)(QkParams);
 
-template <int N, int IN, int STAT>
+template <int N, int IN, int STAT, int OUT>
 QkKernel pick_qk_vpt(int vpt) {
   switch (vpt) {
-    case 1: return qknorm_cluster_kernel<N, 1, IN, STAT>;
-    case 2: return qknorm_cluster_kernel<N, 2, IN, STAT>;
-    case 3: return qknorm_cluster_kernel<N, 3, IN, STAT>;
-    case 4: return qknorm_cluster_kernel<N, 4, IN, STAT>;
-    case 5: return qknorm_cluster_kernel<N, 5, IN, STAT>;
-    case 6: return qknorm_cluster_kernel<N, 6, IN, STAT>;
-    case 8: return qknorm_cluster_kernel<N, 8, IN, STAT>;
+    case 1: return qknorm_cluster_kernel<N, 1, IN, STAT, OUT>;
+    case 2: return qknorm_cluster_kernel<N, 2, IN, STAT, OUT>;
+    case 3: return qknorm_cluster_kernel<N, 3, IN, STAT, OUT>;
+    case 4: return qknorm_cluster_kernel<N, 4, IN, STAT, OUT>;
+    case 5: return qknorm_cluster_kernel<N, 5, IN, STAT, OUT>;
+    case 6: return qknorm_cluster_kernel<N, 6, IN, STAT, OUT>;
+    case 8: return qknorm_cluster_kernel<N, 8, IN, STAT, OUT>;
     default: return nullptr;
   }
 }
 
-// Instantiates every QK kernel for input type IN and statistic STAT in the
-// calling unit.
-template <int IN, int STAT>
+// Instantiates every QK kernel for input type IN, statistic STAT and output
+// OUT in the calling unit.
+template <int IN, int STAT, int OUT = kOutBf16>
 QkKernel pick_qk_input(int N, int vpt) {
   switch (N) {
-    case 1: return pick_qk_vpt<1, IN, STAT>(vpt);
-    case 2: return pick_qk_vpt<2, IN, STAT>(vpt);
-    case 4: return pick_qk_vpt<4, IN, STAT>(vpt);
-    case 8: return pick_qk_vpt<8, IN, STAT>(vpt);
+    case 1: return pick_qk_vpt<1, IN, STAT, OUT>(vpt);
+    case 2: return pick_qk_vpt<2, IN, STAT, OUT>(vpt);
+    case 4: return pick_qk_vpt<4, IN, STAT, OUT>(vpt);
+    case 8: return pick_qk_vpt<8, IN, STAT, OUT>(vpt);
     default: return nullptr;
   }
 }
@@ -472,12 +539,18 @@ static inline int read_and_clear_local_qk_status(unsigned* out) {
   return NTS_OK;
 }
 
-// Defined by qk_bf16.cu, qk_e4m3.cu and qk_ln.cu.
+// Defined by qk_bf16.cu, qk_e4m3.cu, qk_ln.cu and qk_mx_*.cu.
 QkKernel pick_qk_bf16(int N, int vpt);
 QkKernel pick_qk_e4m3(int N, int vpt);
 QkKernel pick_qk_ln(int N, int vpt);
+QkKernel pick_qk_mx_e4m3(int N, int vpt);
+QkKernel pick_qk_mx_e2m1(int N, int vpt);
+QkKernel pick_qk_mx_nvfp4(int N, int vpt);
 int read_and_clear_qk_bf16_status(unsigned* out);
 int read_and_clear_qk_e4m3_status(unsigned* out);
 int read_and_clear_qk_ln_status(unsigned* out);
+int read_and_clear_qk_mx_e4m3_status(unsigned* out);
+int read_and_clear_qk_mx_e2m1_status(unsigned* out);
+int read_and_clear_qk_mx_nvfp4_status(unsigned* out);
 
 }  // namespace nts

@@ -8,11 +8,15 @@
 
 namespace nts {
 
-int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4m3,
-                  float x_scale, int layernorm, cudaStream_t stream, const LaunchTuning& tune) {
-  const int ES = in_e4m3 ? 1 : 2;
+int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkOptions& opt,
+                  cudaStream_t stream, const LaunchTuning& tune) {
+  const int layernorm = opt.layernorm;
+  const int ES = opt.in_e4m3 ? 1 : 2;
   const int NS = layernorm ? 2 : 1;
-  if (layernorm && in_e4m3) return fail(NTS_ERR_UNSUPPORTED, "LayerNorm of E4M3 input");
+  const bool mx_out = opt.out_fmt >= 0;
+  if (layernorm && opt.in_e4m3) return fail(NTS_ERR_UNSUPPORTED, "LayerNorm of E4M3 input");
+  if (mx_out && (layernorm || opt.in_e4m3))
+    return fail(NTS_ERR_UNSUPPORTED, "block-cast output of LayerNorm or E4M3 input");
   const DeviceInfo& dev = device_info();
   if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
   // psum: fp32 parameters staged per CTA (gamma, and beta when given)
@@ -53,9 +57,15 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4
   if (smem > (size_t)dev.max_smem_optin)
     return fail(NTS_ERR_UNSUPPORTED, "shard row too wide for shared memory: H/N = %d", Wmax);
 
-  QkKernel kern = layernorm ? pick_qk_ln(N, rs.vpt)
-                 : in_e4m3 ? pick_qk_e4m3(N, rs.vpt)
-                           : pick_qk_bf16(N, rs.vpt);
+  QkKernel kern;
+  if (mx_out)
+    kern = opt.out_fmt == NTS_FMT_E4M3   ? pick_qk_mx_e4m3(N, rs.vpt)
+           : opt.out_fmt == NTS_FMT_E2M1 ? pick_qk_mx_e2m1(N, rs.vpt)
+                                         : pick_qk_mx_nvfp4(N, rs.vpt);
+  else
+    kern = layernorm    ? pick_qk_ln(N, rs.vpt)
+           : opt.in_e4m3 ? pick_qk_e4m3(N, rs.vpt)
+                         : pick_qk_bf16(N, rs.vpt);
   if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for N=%d vpt=%d", N, rs.vpt);
 
   QkParams prm = {};
@@ -68,6 +78,8 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4
     tn.beta = layernorm ? rq[k].beta : nullptr;
     tn.mean_out = layernorm ? rq[k].mean : nullptr;
     tn.Y = static_cast<__nv_bfloat16*>(rq[k].Y);
+    tn.codes = rq[k].codes;
+    tn.scales = rq[k].scales;
     tn.rinv_out = rq[k].rinv;
     tn.T = rq[k].T;
     tn.ntiles = (rq[k].T + R - 1) / R;
@@ -90,8 +102,11 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4
   prm.S = S;
   prm.gsplit = gsplit;
   prm.psum = psum;
+  prm.bv = mx_out ? opt.B / 8 : 1;
+  prm.bshift = 0;
+  while (mx_out && (1 << prm.bshift) < opt.B) ++prm.bshift;   // B = 2^bshift
   prm.eps = eps;
-  prm.x_scale = x_scale;
+  prm.x_scale = opt.x_scale;
   prm.wait_limit_ns = tune.wait_limit_ns;
   prm.missing_tx = tune.missing_tx;
   if (ntiles == 0) return NTS_OK;
@@ -119,7 +134,8 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4
   if (tune.force_grid > 0) ncl = std::min<int64_t>(ntiles, tune.force_grid);
   cfg.gridDim = dim3((unsigned)(ncl * N));
 
-  log_launch(layernorm ? "layernorm_split" : "qknorm_rms", "tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d gsplit=%d "
+  log_launch(layernorm ? "layernorm_split" : (mx_out ? "qknorm_rms_mxcast" : "qknorm_rms"),
+             "tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d gsplit=%d "
              "smem=%zu clusters=%lld/%lld", ntensors, (long long)rq[0].T, (int)rq[0].H, N, rs.vpt,
              rs.G, R, S, gsplit, smem, (long long)ncl, (long long)max_clusters);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
@@ -128,14 +144,18 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, int in_e4
 }
 
 int read_and_clear_qk_status(unsigned* out) {
-  unsigned a = 0, b = 0, c = 0;
-  int rc = read_and_clear_qk_bf16_status(&a);
-  if (rc != NTS_OK) return rc;
-  rc = read_and_clear_qk_e4m3_status(&b);
-  if (rc != NTS_OK) return rc;
-  rc = read_and_clear_qk_ln_status(&c);
-  if (rc != NTS_OK) return rc;
-  *out = a | b | c;
+  int (*const readers[])(unsigned*) = {
+      read_and_clear_qk_bf16_status,    read_and_clear_qk_e4m3_status,
+      read_and_clear_qk_ln_status,      read_and_clear_qk_mx_e4m3_status,
+      read_and_clear_qk_mx_e2m1_status, read_and_clear_qk_mx_nvfp4_status};
+  unsigned all = 0;
+  for (auto* read : readers) {
+    unsigned v = 0;
+    const int rc = read(&v);
+    if (rc != NTS_OK) return rc;
+    all |= v;
+  }
+  *out = all;
   return NTS_OK;
 }
 

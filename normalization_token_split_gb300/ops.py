@@ -144,6 +144,24 @@ def layernorm_split(x: torch.Tensor, gamma: torch.Tensor, beta: Optional[torch.T
     return out, mean, rstd
 
 
+def qknorm_rms_mxcast(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, N: int = 1,
+                      B: int = 32, fmt="e4m3", codes=None, scales=None, rinv=None,
+                      want_rinv: bool = False, stream=None) -> "MxOut":
+    """Layerwise QK-RMSNorm of x [T, H] split into N cluster shards, written
+    as an MX / NVFP4 block cast (codes, scales) instead of bf16 rows.
+    Returns MxOut(codes, scales, rinv or None, None)."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("gamma", gamma, torch.float32)
+    T, H = x.shape
+    f = _fmt(fmt)
+    codes, scales, rinv, _ = _mx_outputs(x, H, B, f, codes, scales, rinv, None, want_rinv,
+                                         False)
+    check(lib().nts_qknorm_rms_mxcast(_ptr(x), _ptr(gamma), _ptr(codes), _ptr(scales),
+                                      _ptr(rinv), T, H, float(eps), int(N), int(B), f,
+                                      _stream(stream)))
+    return MxOut(codes, scales, rinv, None)
+
+
 def qknorm_rms_qk(q: torch.Tensor, gamma_q: torch.Tensor, k: torch.Tensor,
                   gamma_k: torch.Tensor, eps: float = 1e-6, N: int = 1,
                   out_q: Optional[torch.Tensor] = None, out_k: Optional[torch.Tensor] = None,

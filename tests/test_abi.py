@@ -200,3 +200,18 @@ def test_nvfp4_argument_checks(lib):
                                   None) == INVALID
     assert lib.nts_rmsnorm_mxcast(A16, None, A16, A16, None, None, 0, 256, 1e-6, 16, NV,
                                   None) == OK
+
+
+def test_qk_mxcast_argument_checks(lib):
+    def f(**k):
+        return lib.nts_qknorm_rms_mxcast(k.get("X", A16), A16, k.get("c", A16), k.get("s", A16),
+                                         None, k.get("T", 4), k.get("H", 1024), 1e-6,
+                                         k.get("N", 2), k.get("B", 32), k.get("fmt", 0), None)
+    assert f(s=None) == INVALID
+    assert f(c=None) == INVALID
+    assert f(B=8) == INVALID
+    assert f(fmt=3) == INVALID
+    assert f(fmt=2, B=32) == INVALID
+    assert f(H=1040, B=16) == UNSUPPORTED      # 520-value shards
+    assert f(c=MIS) == UNSUPPORTED
+    assert f(T=0, X=None, c=None, s=None) == OK
