@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
       if (!aborted) atomicOr(&g_mx_status, kStatusTimeout);
       aborted = true;
     }
-    const uint32_t srow = sbase + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * p.D * 2;
+    const unsigned char* srow = smem + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * p.D * 2;
 
     // ---- pass 1: block absmaxes (of w = x or x*gamma) and the statistic
     float am[BPT];
@@ -203,13 +203,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
       const int b = i * p.G + g;
       am[i] = 0.f;
       if (valid && b < p.K) {
-        const uint32_t base = srow + (uint32_t)b * kB * 2;
+        const unsigned char* base = srow + (uint32_t)b * kB * 2;
         if (p.gamma == nullptr) {
           uint32_t m = 0;
 #pragma unroll
           for (int k = 0; k < VB; ++k) {
             const int u = (k + sig) & (VB - 1);
-            const uint4 v = ld_shared_v4(base + u * 16);
+            const uint4 v = lds128(base + u * 16);
             m = bf16x2_absmax(m, v.x);
             m = bf16x2_absmax(m, v.y);
             m = bf16x2_absmax(m, v.z);
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
 #pragma unroll
           for (int k = 0; k < VB; ++k) {
             const int u = (k + sig) & (VB - 1);
-            const uint4 v = ld_shared_v4(base + u * 16);
+            const uint4 v = lds128(base + u * 16);
             if (STAT == kStatRms) {
               const uint64_t a = bf16x2_to_f2(v.x), c = bf16x2_to_f2(v.y);
               const uint64_t d = bf16x2_to_f2(v.z), e = bf16x2_to_f2(v.w);
@@ -304,11 +304,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
           }
           const uint64_t ss = f2(is, is);
           if (p.amax_out != nullptr) p.amax_out[(size_t)t * p.K + b] = am[i];
-          const uint32_t base = srow + (uint32_t)b * kB * 2;
+          const unsigned char* base = srow + (uint32_t)b * kB * 2;
 #pragma unroll
           for (int k = 0; k < VB; ++k) {
             const int u = (k + sig) & (VB - 1);
-            const uint4 v = ld_shared_v4(base + u * 16);
+            const uint4 v = lds128(base + u * 16);
             uint64_t w[4];
             if (p.gamma == nullptr) {
               w[0] = bf16x2_to_f2(v.x);

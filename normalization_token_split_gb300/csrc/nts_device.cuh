@@ -130,33 +130,23 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 
 // ------------------------------------------------------------ data movement
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
+// Loads from this CTA's shared memory and stores of results to global
+// memory as ordinary C++ accesses, not asm: the compiler then knows the
+// address spaces and may interleave the loads of one vector with the stores
+// of earlier ones.  The mbarrier operations' asm carries a memory clobber
+// and so still orders the loads against the TMA writes that fill a stage and
+// against the release of the stage to the producer.
+__device__ __forceinline__ uint4 lds128(const unsigned char* p) {
+  return *reinterpret_cast<const uint4*>(p);
 }
 
-__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
+__device__ __forceinline__ uint2 lds64(const unsigned char* p) {
+  return *reinterpret_cast<const uint2*>(p);
 }
 
-// 16-byte store that does not allocate in L1 and streams through L2.
+// 16-byte store that streams through L2 (evict-first, st.global.cs).
 __device__ __forceinline__ void st_global_v4_stream(void* p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-__device__ __forceinline__ void st_global_v2_stream(void* p, uint32_t a, uint32_t b) {
-  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
-}
-
-__device__ __forceinline__ void st_global_u32_stream(void* p, uint32_t a) {
-  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+  __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
 // 8 bf16 (one 16-byte vector) -> 8 floats, element order preserved.
@@ -311,11 +301,11 @@ __device__ __forceinline__ float bf16x2_hmax_abs(uint32_t m) {
 }
 
 __device__ __forceinline__ void st_global_v2(void* p, uint32_t a, uint32_t b) {
-  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+  *reinterpret_cast<uint2*>(p) = make_uint2(a, b);
 }
 
 __device__ __forceinline__ void st_global_u32(void* p, uint32_t a) {
-  asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+  *reinterpret_cast<uint32_t*>(p) = a;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

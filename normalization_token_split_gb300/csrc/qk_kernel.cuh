@@ -134,18 +134,18 @@ __device__ __forceinline__ int qk_tile(const QkParams& p, int64_t tile, int64_t*
 // Eight activations of vector v of a staged row as four fp32 pairs; zeros
 // when !inb (the load is predicated, the conversion is not).
 template <int IN>
-__device__ __forceinline__ void load_vector(uint32_t srow, int v, bool inb, float x_scale,
-                                            uint64_t (&w)[4]) {
+__device__ __forceinline__ void load_vector(const unsigned char* srow, int v, bool inb,
+                                            float x_scale, uint64_t (&w)[4]) {
   if (IN == kInBf16) {
     uint4 x = make_uint4(0, 0, 0, 0);
-    if (inb) x = ld_shared_v4(srow + v * 16);
+    if (inb) x = lds128(srow + v * 16);
     w[0] = bf16x2_to_f2(x.x);
     w[1] = bf16x2_to_f2(x.y);
     w[2] = bf16x2_to_f2(x.z);
     w[3] = bf16x2_to_f2(x.w);
   } else {
     uint2 x = make_uint2(0, 0);
-    if (inb) x = ld_shared_v2(srow + v * 8);
+    if (inb) x = lds64(srow + v * 8);
     const uint64_t sc = f2(x_scale, x_scale);
     w[0] = f2_mul(e4m3x2_to_f2((uint16_t)(x.x & 0xFFFFu)), sc);
     w[1] = f2_mul(e4m3x2_to_f2((uint16_t)(x.x >> 16)), sc);
@@ -275,7 +275,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
       uint64_t w[VPT][4];
       uint64_t acc[4] = {0, 0, 0, 0};  // {0.f, 0.f} each
       uint64_t sum2[2] = {0, 0};
-      const uint32_t srow = sbase + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * tn.W * ES;
+      const unsigned char* srow =
+          smem + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * tn.W * ES;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = i * p.G + g;
@@ -346,14 +347,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
       }
       // split layout: halves nvec*16 bytes apart, vectors 16 apart; as
       // copied: halves 16 apart, vectors 32 apart
-      const uint32_t gam_lo = sbase + tn.gam;
-      const uint32_t gam_hi = gam_lo + (p.gsplit ? (uint32_t)nvec * 16 : 16u);
+      const unsigned char* gam_lo = smem + tn.gam;
+      const unsigned char* gam_hi = gam_lo + (p.gsplit ? (uint32_t)nvec * 16 : 16u);
       const uint32_t gstride = p.gsplit ? 16u : 32u;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = min(i * p.G + g, nvec - 1);
-        const uint4 glo = ld_shared_v4(gam_lo + v * gstride);
-        const uint4 ghi = ld_shared_v4(gam_hi + v * gstride);
+        const uint4 glo = lds128(gam_lo + v * gstride);
+        const uint4 ghi = lds128(gam_hi + v * gstride);
         w[i][0] = f2_mul(w[i][0], f2(__uint_as_float(glo.x), __uint_as_float(glo.y)));
         w[i][1] = f2_mul(w[i][1], f2(__uint_as_float(glo.z), __uint_as_float(glo.w)));
         w[i][2] = f2_mul(w[i][2], f2(__uint_as_float(ghi.x), __uint_as_float(ghi.y)));
@@ -447,14 +448,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
             uint64_t y0, y1, y2, y3;
             if (STAT == kQkLn) {
               // y = (x - mu) rinv gamma + beta = w rinv + (beta - mu rinv gamma)
-              const uint4 glo = ld_shared_v4(gam_lo + v * gstride);
-              const uint4 ghi = ld_shared_v4(gam_hi + v * gstride);
+              const uint4 glo = lds128(gam_lo + v * gstride);
+              const uint4 ghi = lds128(gam_hi + v * gstride);
               uint4 blo = make_uint4(0, 0, 0, 0), bhi = make_uint4(0, 0, 0, 0);
               if (tn.beta != nullptr) {
-                const uint32_t bet_lo = sbase + tn.bet;
-                const uint32_t bet_hi = bet_lo + (p.gsplit ? (uint32_t)nvec * 16 : 16u);
-                blo = ld_shared_v4(bet_lo + v * gstride);
-                bhi = ld_shared_v4(bet_hi + v * gstride);
+                const unsigned char* bet_lo = smem + tn.bet;
+                const unsigned char* bet_hi = bet_lo + (p.gsplit ? (uint32_t)nvec * 16 : 16u);
+                blo = lds128(bet_lo + v * gstride);
+                bhi = lds128(bet_hi + v * gstride);
               }
               const uint64_t m2 = f2(nmr, nmr);
               const uint64_t c0 = f2_fma(m2, f2(__uint_as_float(glo.x), __uint_as_float(glo.y)),
