@@ -5,10 +5,11 @@
 //   a row of D values is cut into K = D/B blocks of B contiguous values; each
 //   block is stored as B element codes (E4M3 or E2M1) sharing one E8M0 scale
 //   2^round(log2(normalized absmax / 2^emax)), or (NVFP4, Table 4's second
-//   format) 16 E2M1 codes sharing one E4M3 scale, normalized absmax / 6.  RMSNorm + MXCast takes the
-//   RMS from sum x^2 over the row; MXNorm estimates it from the block
-//   absmaxes the cast computes anyway, rho~ = c(B,p) * M_p(absmax), a
-//   reduction B times smaller.  Both are fused into one kernel (Fig. 8).
+//   format) 16 E2M1 codes sharing one E4M3 scale, normalized absmax / 6.
+//   RMSNorm + MXCast takes the RMS from sum x^2 over the row; MXNorm
+//   estimates it from the block absmaxes the cast computes anyway,
+//   rho~ = c(B,p) * M_p(absmax), a reduction B times smaller.  Both are fused
+//   into one kernel (Fig. 8).
 //
 // GB300 mapping:
 //  * a persistent grid of CTAs walks tiles of R whole rows.  A producer warp
@@ -322,16 +323,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
 #pragma unroll
             for (int h = 0; h < 4; ++h) q[h] = f2_mul(f2_mul(w[h], rr), ss);
             if (FMT == NTS_FMT_E4M3) {
-              const uint32_t lo = cvt_e4m3x2(f2_lo(q[0]), f2_hi(q[0])) |
-                                  (cvt_e4m3x2(f2_lo(q[1]), f2_hi(q[1])) << 16);
-              const uint32_t hi = cvt_e4m3x2(f2_lo(q[2]), f2_hi(q[2])) |
-                                  (cvt_e4m3x2(f2_lo(q[3]), f2_hi(q[3])) << 16);
+              const uint32_t lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
+              const uint32_t hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
               st_global_v2(crow + (size_t)b * kB + u * 8, lo, hi);
             } else {
-              const uint32_t c = cvt_e2m1x2(f2_lo(q[0]), f2_hi(q[0])) |
-                                 (cvt_e2m1x2(f2_lo(q[1]), f2_hi(q[1])) << 8) |
-                                 (cvt_e2m1x2(f2_lo(q[2]), f2_hi(q[2])) << 16) |
-                                 (cvt_e2m1x2(f2_lo(q[3]), f2_hi(q[3])) << 24);
+              const uint32_t c = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]),
+                                            f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
               st_global_u32(crow + (size_t)b * (kB / 2) + u * 4, c & keep);
             }
           }

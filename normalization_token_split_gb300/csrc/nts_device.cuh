@@ -171,6 +171,35 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Four floats -> four E4M3 bytes in one word, f0 in bits 0-7 (RNE,
+// saturating); the two 16-bit conversions are packed by a register move.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float f0, float f1, float f2, float f3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(f0), "f"(f1), "f"(f2), "f"(f3));
+  return r;
+}
+
+// Eight floats -> eight E2M1 nibbles in one word, f0 in bits 0-3 (RNE,
+// saturating).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float f0, float f1, float f2, float f3, float f4,
+                                               float f5, float f6, float f7) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(f0), "f"(f1), "f"(f2), "f"(f3), "f"(f4), "f"(f5), "f"(f6), "f"(f7));
+  return r;
+}
+
 // Two floats -> two E2M1 nibbles in one byte (RNE, saturating); `lo` lands
 // in bits 0-3.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {

@@ -428,16 +428,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
 #pragma unroll
               for (int h = 0; h < 4; ++h) q[h] = f2_mul(f2_mul(w[i][h], rr), ss);
               if (OUT == kOutE4M3) {
-                const uint32_t lo = cvt_e4m3x2(f2_lo(q[0]), f2_hi(q[0])) |
-                                    (cvt_e4m3x2(f2_lo(q[1]), f2_hi(q[1])) << 16);
-                const uint32_t hi = cvt_e4m3x2(f2_lo(q[2]), f2_hi(q[2])) |
-                                    (cvt_e4m3x2(f2_lo(q[3]), f2_hi(q[3])) << 16);
+                const uint32_t lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
+                const uint32_t hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
                 st_global_v2(tn.codes + (size_t)t * tn.H + col, lo, hi);
               } else {
-                const uint32_t c = cvt_e2m1x2(f2_lo(q[0]), f2_hi(q[0])) |
-                                   (cvt_e2m1x2(f2_lo(q[1]), f2_hi(q[1])) << 8) |
-                                   (cvt_e2m1x2(f2_lo(q[2]), f2_hi(q[2])) << 16) |
-                                   (cvt_e2m1x2(f2_lo(q[3]), f2_hi(q[3])) << 24);
+                const uint32_t c = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]),
+                                              f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
                 st_global_u32(tn.codes + ((size_t)t * tn.H + col) / 2, c & keep);
               }
             }

@@ -123,6 +123,20 @@ def test_degenerate_blocks():
             compare(kind, X, None, 1e-6, 32, fmt, p, what=f"degenerate {kind}{p} {fmt}")
 
 
+def test_extreme_factors():
+    # rows so small that the mean square underflows and rinv = 1/sqrt(eps)
+    # is huge: rinv * 2^-e overflows fp32 for some blocks, so the kernel must
+    # take the two-product path there; other rows sit near its boundary
+    X, _ = workloads.mx_inputs(8, 1024, seed=78)
+    Xf = X.float()
+    for r, sc in enumerate((1e-36, 1e-34, 1e-30, 1e-25, 1e-20, 1e-12, 3e-39, 1.0)):
+        Xf[r] *= sc
+    X = Xf.to(torch.bfloat16)
+    for kind, p in KINDS:
+        for fmt in ("e4m3", "e2m1"):
+            compare(kind, X, None, 1e-38, 32, fmt, p, what=f"extreme {kind}{p} {fmt}")
+
+
 def test_zero_tokens_launches_nothing():
     X = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
     out = nts.mxnorm_cast(X, None, B=32)
