@@ -360,6 +360,11 @@ int nts_qknorm_rms_heads(const void* X_dev, const float* gamma_dev, void* Y_dev,
   int rc = validate_qk(X_dev, gamma_dev, Y_dev, rinv_dev, rows, head_dim, eps, N);
   if (rc != NTS_OK) return rc;
   if (rows == 0) return NTS_OK;
+  // Heads kept whole in one CTA when N == 1 (no statistic leaves a warp);
+  // otherwise every head is split across the N CTAs of a cluster.
+  if (heads_whole_path(H, head_dim, N))
+    return launch_heads(X_dev, gamma_dev, Y_dev, rinv_dev, T, H, head_dim, eps,
+                        static_cast<cudaStream_t>(stream), current_tuning());
   const QkRequest rq{X_dev, gamma_dev, Y_dev, rinv_dev, rows, head_dim};
   return launch_qknorm(&rq, 1, eps, N, QkOptions{}, static_cast<cudaStream_t>(stream),
                        current_tuning());

@@ -103,6 +103,13 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
                   cudaStream_t stream, const LaunchTuning& tune);
 int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune);
 
+// Headwise QK-Norm with every head inside one CTA (heads_kernel.cu): for
+// N == 1, head_dim in {8, 16, ..., 256} and H <= 30720.
+bool heads_whole_path(int64_t H, int64_t head_dim, int N);
+int launch_heads(const void* X, const float* gamma, void* Y, float* rinv, int64_t T, int64_t H,
+                 int64_t head_dim, float eps, cudaStream_t stream, const LaunchTuning& tune);
+int read_and_clear_heads_status(unsigned* out);
+
 int read_and_clear_qk_status(unsigned* out);
 int read_and_clear_mx_status(unsigned* out);
 

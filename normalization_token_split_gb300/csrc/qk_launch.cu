@@ -147,7 +147,8 @@ int read_and_clear_qk_status(unsigned* out) {
   int (*const readers[])(unsigned*) = {
       read_and_clear_qk_bf16_status,    read_and_clear_qk_e4m3_status,
       read_and_clear_qk_ln_status,      read_and_clear_qk_mx_e4m3_status,
-      read_and_clear_qk_mx_e2m1_status, read_and_clear_qk_mx_nvfp4_status};
+      read_and_clear_qk_mx_e2m1_status, read_and_clear_qk_mx_nvfp4_status,
+      read_and_clear_heads_status};
   unsigned all = 0;
   for (auto* read : readers) {
     unsigned v = 0;

@@ -217,6 +217,63 @@ def test_headwise_matches_oracle(T, H, hd, N):
     check_qk(workloads.bf16_bits(y), r.cpu().numpy().ravel(), Yo, ro.ravel(), f"heads {T},{H},{hd},{N}")
 
 
+@pytest.mark.parametrize("T,H,hd", [(1, 64, 8), (33, 512, 16), (100, 1024, 32), (513, 4096, 64),
+                                    (7, 2048, 256), (3, 32768, 128), (300, 24, 8)])
+def test_headwise_whole_heads_path(T, H, hd):
+    # N = 1 keeps every head inside one CTA (segmented warp reduction)
+    X, _ = workloads.qk_inputs(T, H, seed=T + 3 * H + hd, outlier_frac=0.02)
+    g = workloads.gamma_vector(hd, seed=hd + 1)
+    y, r = nts.qknorm_rms_heads(X.to(DEV), g.to(DEV), hd, eps=1e-6, N=1, want_rinv=True)
+    nts.check_status()
+    Yo, ro = oracle.qknorm_rms_heads(workloads.bf16_bits(X), g.numpy(), 1e-6, hd)
+    check_qk(workloads.bf16_bits(y), r.cpu().numpy().ravel(), Yo, ro.ravel(), f"heads {T},{H},{hd}")
+
+
+def test_headwise_prefill_full_size_sampled():
+    X, _ = workloads.qk_inputs(8192, 5120, seed=3100, outlier_frac=0.01, device=DEV)
+    g = workloads.gamma_vector(128, seed=128, device=DEV)
+    y, r = nts.qknorm_rms_heads(X, g, 128, eps=1e-6, N=1, want_rinv=True)
+    y2, r2 = nts.qknorm_rms_heads(X, g, 128, eps=1e-6, N=2, want_rinv=True)   # split heads
+    nts.check_status()
+    rows = torch.from_numpy(np.random.default_rng(5).choice(8192, 256, replace=False)).to(DEV)
+    Yo, ro = oracle.qknorm_rms_heads(workloads.bf16_bits(X[rows]), g.cpu().numpy(), 1e-6, 128)
+    check_qk(workloads.bf16_bits(y[rows]), r[rows].cpu().numpy().ravel(), Yo, ro.ravel(), "heads")
+    check_qk(workloads.bf16_bits(y2[rows]), r2[rows].cpu().numpy().ravel(), Yo, ro.ravel(), "split")
+
+
+@pytest.mark.parametrize("vpt,rows,stages,grid", [(1, 1, 1, 1), (2, 3, 2, 5), (8, 2, 4, 0),
+                                                  (4, 7, 3, 7)])
+def test_headwise_forced_launch_shapes(vpt, rows, stages, grid):
+    X, _ = workloads.qk_inputs(777, 2048, seed=17)
+    g = workloads.gamma_vector(128, seed=7)
+    try:
+        nts.set_tuning(vpt=vpt, rows=rows, stages=stages, grid=grid)
+        y, r = nts.qknorm_rms_heads(X.to(DEV), g.to(DEV), 128, eps=1e-6, N=1, want_rinv=True)
+        nts.check_status()
+    finally:
+        nts.set_tuning()
+    Yo, ro = oracle.qknorm_rms_heads(workloads.bf16_bits(X), g.numpy(), 1e-6, 128)
+    check_qk(workloads.bf16_bits(y), r.cpu().numpy().ravel(), Yo, ro.ravel(), "forced heads")
+
+
+def test_headwise_bounded_wait_reports_timeout():
+    X, _ = workloads.qk_inputs(64, 1024, seed=18)
+    g = workloads.gamma_vector(128, seed=8)
+    try:
+        nts.set_wait_limit_ns(20_000_000)
+        nts.set_missing_tx(16)
+        nts.qknorm_rms_heads(X.to(DEV), g.to(DEV), 128, N=1)
+        with pytest.raises(nts.NtsError, match="TIMEOUT"):
+            nts.check_status()
+    finally:
+        nts.set_missing_tx(0)
+        nts.set_wait_limit_ns(0)
+    y, r = nts.qknorm_rms_heads(X.to(DEV), g.to(DEV), 128, eps=1e-6, N=1, want_rinv=True)
+    nts.check_status()
+    Yo, ro = oracle.qknorm_rms_heads(workloads.bf16_bits(X), g.numpy(), 1e-6, 128)
+    check_qk(workloads.bf16_bits(y), r.cpu().numpy().ravel(), Yo, ro.ravel(), "after timeout")
+
+
 # ------------------------------------------------- FP8-E4M3 activations
 
 @pytest.mark.parametrize("T,H,N", [(1, 4096, 1), (64, 1024, 2), (257, 4096, 4), (33, 5120, 8),
