@@ -257,20 +257,21 @@ def run_gpu(args):
     ]
 
     def step(events=None):
+        # one event before each launch: launch i of step k runs between
+        # marks[k*n + i] and marks[k*n + i + 1] (the next launch's mark, or
+        # the closing mark), so no two event records sit between launches
         for i, (name, fn) in enumerate(launches):
             if events is not None:
-                events[i][0].record(stream)
+                events[i].record(stream)
             fn()
-            if events is not None:
-                events[i][1].record(stream)
 
     for _ in range(args.warmup):
         step()
     nts.check_status()
 
     # ---- timed region: K steps, per-launch events on the launching stream
-    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-           for _ in launches] for _ in range(args.steps)]
+    n = len(launches)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * n + 1)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
@@ -280,7 +281,8 @@ def run_gpu(args):
     w0 = time.time()
     t_start.record(stream)
     for k in range(args.steps):
-        step(ev[k])
+        step(marks[k * n:(k + 1) * n])
+    marks[-1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -291,7 +293,7 @@ def run_gpu(args):
 
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, world)
-    per_kernel_ms = {name: statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1])
+    per_kernel_ms = {name: statistics.mean(marks[k * n + i].elapsed_time(marks[k * n + i + 1])
                                            for k in range(args.steps))
                      for i, (name, _) in enumerate(launches)}
     ms_per_step = elapsed_ms / args.steps
