@@ -34,6 +34,13 @@ NTS_API int nts_debug_set_tuning(int vpt, int rows, int stages, int64_t grid, in
 NTS_API int nts_debug_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * Tile order of the persistent kernels: 1 (default) = every CTA takes its next
+ * tile from a per-stream counter; 0 = a fixed round-robin order.  Results do
+ * not depend on it.  Errors: INVALID_ARG for other values.
+ */
+NTS_API int nts_debug_set_schedule(int dynamic);
+
+/*
  * Test hook: every later launch tells its first ring stage to expect `bytes`
  * more than its copies deliver, so that stage's wait can only end by
  * expiring; the kernel then records NTS_ERR_TIMEOUT for nts_check_status and

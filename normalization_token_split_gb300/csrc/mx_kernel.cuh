@@ -64,14 +64,18 @@ struct MxParams {
   int post;             // MXNorm: 1 = statistic from E8M0-rounded absmaxes (post-round)
   uint64_t wait_limit_ns;
   uint32_t missing_tx;  // test hook: bytes expected on the first stage but never sent
+  unsigned int* sched;  // zeroed counter pair (next tile, CTAs done), or nullptr:
+                        // take tiles round-robin
 };
 
 enum { kStatRms = 0, kStatMxP1 = 1, kStatMxP2 = 2 };
 
 // Shared memory layout (bytes, in order):
-//   ring [S][R][D] bf16 | full[S] | empty[S] | rbar[2][R] | red[2][R][WPR] f32
+//   ring [S][R][D] bf16 | full[S] | empty[S] | tile[S] i64 | rbar[2][R] |
+//   red[2][R][WPR] f32
+// tile[s] is the tile the producer put in stage s, or -1: no more tiles.
 struct MxLayout {
-  uint32_t ring, full, empty, rbar, red, total;
+  uint32_t ring, full, empty, tile, rbar, red, total;
 };
 
 __host__ __device__ inline MxLayout mx_layout(int S, int R, int D, int G) {
@@ -79,7 +83,8 @@ __host__ __device__ inline MxLayout mx_layout(int S, int R, int D, int G) {
   L.ring = 0;
   L.full = L.ring + (uint32_t)S * R * D * 2;
   L.empty = L.full + (uint32_t)S * 8;
-  L.rbar = L.empty + (uint32_t)S * 8;
+  L.tile = L.empty + (uint32_t)S * 8;
+  L.rbar = L.tile + (uint32_t)S * 8;
   L.red = L.rbar + (uint32_t)2 * R * 8;
   L.total = L.red + (uint32_t)2 * R * (G / 32) * 4;
   return L;
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
   const uint32_t sbase = smem_addr(smem);
   const uint32_t stage_bytes = (uint32_t)p.R * p.D * 2;
   const int64_t cta = blockIdx.x, ncta = gridDim.x;
-  const int64_t my_tiles = cta < p.ntiles ? (p.ntiles - 1 - cta) / ncta + 1 : 0;
+  int64_t* tile_of = reinterpret_cast<int64_t*>(smem + L.tile);
 
   if (tid == 0) {
     for (int s = 0; s < p.S; ++s) {
@@ -150,27 +155,46 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
       // incrementally (no 64-bit division in the loop)
       int s = 0;
       uint32_t ph = 0;
-      for (int64_t j = 0; j < my_tiles; ++j) {
-        if (j >= p.S &&
-            !mbar_wait_bounded(sbase + L.empty + 8 * s, ph ^ 1u, p.wait_limit_ns)) {
+      int64_t n = 0;  // tiles issued
+      while (true) {
+        if (n >= p.S && !mbar_wait_bounded(sbase + L.empty + 8 * s, ph ^ 1u, p.wait_limit_ns)) {
           atomicOr(&g_mx_status, kStatusTimeout);
           aborted = true;
           break;
         }
-        const int64_t t0 = (cta + j * ncta) * p.R;
-        const uint32_t bytes = (uint32_t)min64(p.R, p.T - t0) * p.D * 2;
+        // next tile: from the launch's counter, or round-robin
+        const int64_t tile = p.sched != nullptr ? (int64_t)atomicAdd(p.sched, 1u) : cta + n * ncta;
         const uint32_t bar = sbase + L.full + 8 * s;
-        mbar_arrive_expect_tx(bar, bytes + (j == 0 ? p.missing_tx : 0u));
+        if (tile >= p.ntiles) {
+          tile_of[s] = -1;   // published by the arrive (release) below
+          mbar_arrive(bar);
+          break;
+        }
+        tile_of[s] = tile;
+        const int64_t t0 = tile * p.R;
+        const uint32_t bytes = (uint32_t)min64(p.R, p.T - t0) * p.D * 2;
+        mbar_arrive_expect_tx(bar, bytes + (n == 0 ? p.missing_tx : 0u));
         bulk_g2s(sbase + L.ring + (uint32_t)s * stage_bytes, p.X + (size_t)t0 * p.D, bytes, bar,
                  policy);
+        ++n;
         if (++s == p.S) {
           s = 0;
           ph ^= 1u;
         }
       }
-      for (int64_t j = max64(0, my_tiles - p.S); j < my_tiles && !aborted; ++j)
+      // Normally the consumers have waited for every copy before the CTA can
+      // retire; after an expired wait, let the copies in flight land first.
+      for (int64_t j = max64(0, n - p.S); j < n && aborted; ++j)
         (void)mbar_wait_bounded(sbase + L.full + 8 * (int)(j % p.S), (uint32_t)((j / p.S) & 1),
                                 p.wait_limit_ns);
+      // count this CTA out; the last one re-arms the pair for the next launch
+      if (p.sched != nullptr) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+          atomicExch(p.sched, 0u);
+          atomicExch(p.sched + 1, 0u);
+        }
+      }
     }
     __syncwarp();
     return;
@@ -184,15 +208,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
   const size_t cbytes = (FMT == NTS_FMT_E4M3) ? (size_t)p.D : (size_t)p.D / 2;
   bool aborted = false;
 
-  int s = 0;          // ring stage of tile j
+  int s = 0;          // ring stage of the j-th tile
   uint32_t ph = 0;    // (j / S) & 1
-  for (int64_t j = 0; j < my_tiles; ++j) {
-    const int64_t t = (cta + j * ncta) * p.R + row;
-    const bool valid = t < p.T;
-    if (!mbar_wait_bounded(sbase + L.full + 8 * s, ph, aborted ? 0 : p.wait_limit_ns)) {
-      if (!aborted) atomicOr(&g_mx_status, kStatusTimeout);
-      aborted = true;
+  for (int64_t j = 0;; ++j) {
+    if (!mbar_wait_bounded(sbase + L.full + 8 * s, ph, p.wait_limit_ns)) {
+      atomicOr(&g_mx_status, kStatusTimeout);
+      break;
     }
+    const int64_t tile = *reinterpret_cast<volatile int64_t*>(tile_of + s);
+    if (tile < 0 || tile >= p.ntiles) break;   // no more tiles
+    const int64_t t = tile * p.R + row;
+    const bool valid = t < p.T;
     const unsigned char* srow = smem + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * p.D * 2;
 
     // ---- pass 1: block absmaxes (of w = x or x*gamma) and the statistic
@@ -338,6 +364,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
     // every read of stage s by this warp is done
     __syncwarp();
     if (lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
+    if (aborted) break;
     if (++s == p.S) {
       s = 0;
       ph ^= 1u;

@@ -93,6 +93,7 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   prm.post = rq.post;
   prm.wait_limit_ns = tune.wait_limit_ns;
   prm.missing_tx = tune.missing_tx;
+  prm.sched = tune.dynamic ? sched_counters(stream) : nullptr;
 
   int rc = prepare_kernel((const void*)kern, smem);
   if (rc != NTS_OK) return rc;

@@ -549,6 +549,13 @@ int nts_debug_set_wait_limit_ns(uint64_t ns) {
   return NTS_OK;
 }
 
+int nts_debug_set_schedule(int dynamic) {
+  if (dynamic != 0 && dynamic != 1) return fail(NTS_ERR_INVALID_ARG, "dynamic must be 0 or 1");
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tune.dynamic = dynamic;
+  return NTS_OK;
+}
+
 int nts_debug_set_missing_tx(uint32_t bytes) {
   if (bytes % 16 != 0) return fail(NTS_ERR_INVALID_ARG, "bytes must be a multiple of 16");
   std::lock_guard<std::mutex> lk(g_tune_mu);

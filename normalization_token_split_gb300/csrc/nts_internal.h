@@ -26,9 +26,14 @@ struct LaunchTuning {
   int smem_budget = 102400;  // bytes of shared memory a CTA aims to stay under
   uint64_t wait_limit_ns = 1000000000ull;  // bounded mbarrier waits
   uint32_t missing_tx = 0;   // test hook, see nts_debug.h
+  int dynamic = 1;           // take tiles from a counter (0: round-robin order)
 };
 
 LaunchTuning current_tuning();
+
+// The zeroed counter pair of `stream` for a dynamically scheduled launch
+// (sched.cu), or nullptr: schedule round-robin.
+unsigned int* sched_counters(cudaStream_t stream);
 
 struct DeviceInfo {
   bool ok = false;

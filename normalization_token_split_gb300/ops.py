@@ -319,5 +319,9 @@ def set_wait_limit_ns(ns: int) -> None:
     check(lib().nts_debug_set_wait_limit_ns(int(ns)))
 
 
+def set_schedule(dynamic: bool) -> None:
+    check(lib().nts_debug_set_schedule(1 if dynamic else 0))
+
+
 def set_missing_tx(nbytes: int) -> None:
     check(lib().nts_debug_set_missing_tx(int(nbytes)))

@@ -278,3 +278,42 @@ def test_nvfp4_rejects_other_blocks_and_post_round():
         nts.rmsnorm_mxcast(X, None, B=32, fmt="nvfp4")
     with pytest.raises(nts.NtsError, match="INVALID_ARG"):
         nts.mxnorm_postround_cast(X, None, B=16, fmt="nvfp4")
+
+
+# ------------------------------------------------------------ tile order
+
+def test_dynamic_and_round_robin_tile_orders_agree():
+    # tiles taken from the per-stream counter or round-robin: same results,
+    # and the counter re-arms itself between back-to-back launches
+    X, _ = workloads.mx_inputs(5003, 2048, seed=950, t_frac=0.05, device=DEV)
+    outs = []
+    try:
+        for dyn in (True, False, True):
+            nts.set_schedule(dyn)
+            for _ in range(3):
+                out = nts.mxnorm_cast(X, None, B=32, p=2, want_rinv=True)
+            nts.check_status()
+            outs.append(out)
+    finally:
+        nts.set_schedule(True)
+    for o in outs[1:]:
+        assert torch.equal(o.codes, outs[0].codes) and torch.equal(o.scales, outs[0].scales)
+        assert torch.equal(o.rinv, outs[0].rinv)
+
+
+def test_launches_on_several_streams():
+    # each stream owns its counter pair: overlapping launches do not share one
+    Xs = [workloads.mx_inputs(T, 1024, seed=960 + T, device=DEV)[0] for T in (3001, 777, 4096)]
+    want = [nts.rmsnorm_mxcast(X, None, B=32) for X in Xs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in Xs]
+    got = [[None] * 4 for _ in Xs]
+    for rep in range(4):
+        for i, (X, st) in enumerate(zip(Xs, streams)):
+            with torch.cuda.stream(st):
+                got[i][rep] = nts.rmsnorm_mxcast(X, None, B=32, stream=st)
+    torch.cuda.synchronize()
+    nts.check_status()
+    for w, gs in zip(want, got):
+        for g in gs:
+            assert torch.equal(g.codes, w.codes) and torch.equal(g.scales, w.scales)
