@@ -51,11 +51,14 @@ struct HeadsParams {
   float inv_hd;         // 1 / head_dim (exact: head_dim is a power of two)
   uint64_t wait_limit_ns;
   uint32_t missing_tx;  // test hook: bytes expected on the first stage but never sent
+  unsigned int* sched;  // zeroed counter pair (next tile, CTAs done), or nullptr:
+                        // take tiles round-robin
 };
 
-// Shared memory layout (bytes): ring [S][R][H] bf16 | full[S] | empty[S]
+// Shared memory layout (bytes): ring [S][R][H] bf16 | full[S] | empty[S] |
+// tile[S] i64 (the tile in stage s, or -1: no more tiles)
 struct HeadsLayout {
-  uint32_t ring, full, empty, total;
+  uint32_t ring, full, empty, tile, total;
 };
 
 HeadsLayout heads_layout(int S, int R, int H) {
@@ -63,7 +66,8 @@ HeadsLayout heads_layout(int S, int R, int H) {
   L.ring = 0;
   L.full = (uint32_t)S * R * H * 2;
   L.empty = L.full + (uint32_t)S * 8;
-  L.total = L.empty + (uint32_t)S * 8;
+  L.tile = L.empty + (uint32_t)S * 8;
+  L.total = L.tile + (uint32_t)S * 8;
   return L;
 }
 
@@ -77,8 +81,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) heads_kernel(const HeadsParams
   const uint32_t stage_bytes = (uint32_t)p.R * p.H * 2;
   const uint32_t full0 = sbase + (uint32_t)p.S * stage_bytes;
   const uint32_t empty0 = full0 + (uint32_t)p.S * 8;
+  int64_t* tile_of = reinterpret_cast<int64_t*>(smem + (uint32_t)p.S * stage_bytes + 16 * p.S);
   const int64_t cta = blockIdx.x, ncta = gridDim.x;
-  const int64_t my_tiles = cta < p.ntiles ? (p.ntiles - 1 - cta) / ncta + 1 : 0;
 
   if (tid == 0) {
     for (int s = 0; s < p.S; ++s) {
@@ -95,27 +99,46 @@ __global__ void __launch_bounds__(kMaxThreads, 1) heads_kernel(const HeadsParams
       bool aborted = false;
       const uint64_t policy = l2_policy_evict_first();
       int s = 0;
-      uint32_t ph = 0;  // (j / S) & 1
-      for (int64_t j = 0; j < my_tiles; ++j) {
-        if (j >= p.S && !mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, p.wait_limit_ns)) {
+      uint32_t ph = 0;  // (n / S) & 1
+      int64_t n = 0;    // tiles issued
+      while (true) {
+        if (n >= p.S && !mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, p.wait_limit_ns)) {
           atomicOr(&g_heads_status, kStatusTimeout);
           aborted = true;
           break;
         }
-        const int64_t t0 = (cta + j * ncta) * p.R;
+        // next tile: from the launch's counter, or round-robin
+        const int64_t tile = p.sched != nullptr ? (int64_t)atomicAdd(p.sched, 1u) : cta + n * ncta;
+        if (tile >= p.ntiles) {
+          tile_of[s] = -1;   // published by the arrive (release) below
+          mbar_arrive(full0 + 8 * s);
+          break;
+        }
+        tile_of[s] = tile;
+        const int64_t t0 = tile * p.R;
         const uint32_t bytes = (uint32_t)min64(p.R, p.T - t0) * p.H * 2;
-        mbar_arrive_expect_tx(full0 + 8 * s, bytes + (j == 0 ? p.missing_tx : 0u));
+        mbar_arrive_expect_tx(full0 + 8 * s, bytes + (n == 0 ? p.missing_tx : 0u));
         bulk_g2s(sbase + (uint32_t)s * stage_bytes, p.X + (size_t)t0 * p.H, bytes, full0 + 8 * s,
                  policy);
+        ++n;
         if (++s == p.S) {
           s = 0;
           ph ^= 1u;
         }
       }
-      // let the last copies land before this CTA can retire
-      for (int64_t j = max64(0, my_tiles - p.S); j < my_tiles && !aborted; ++j)
+      // Normally the consumers have waited for every copy before the CTA can
+      // retire; after an expired wait, let the copies in flight land first.
+      for (int64_t j = max64(0, n - p.S); j < n && aborted; ++j)
         (void)mbar_wait_bounded(full0 + 8 * (int)(j % p.S), (uint32_t)((j / p.S) & 1),
                                 p.wait_limit_ns);
+      // count this CTA out; the last one re-arms the pair for the next launch
+      if (p.sched != nullptr) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+          atomicExch(p.sched, 0u);
+          atomicExch(p.sched + 1, 0u);
+        }
+      }
     }
     __syncwarp();
     return;
@@ -135,16 +158,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) heads_kernel(const HeadsParams
     gm[2] = f2(b.x, b.y);
     gm[3] = f2(b.z, b.w);
   }
-  bool aborted = false;
   int s = 0;
   uint32_t ph = 0;
-  for (int64_t j = 0; j < my_tiles; ++j) {
-    const int64_t t = (cta + j * ncta) * p.R + row;
-    const bool valid = t < p.T;
-    if (!mbar_wait_bounded(full0 + 8 * s, ph, aborted ? 0 : p.wait_limit_ns)) {
-      if (!aborted) atomicOr(&g_heads_status, kStatusTimeout);
-      aborted = true;
+  while (true) {
+    if (!mbar_wait_bounded(full0 + 8 * s, ph, p.wait_limit_ns)) {
+      atomicOr(&g_heads_status, kStatusTimeout);
+      break;
     }
+    const int64_t tile = *reinterpret_cast<volatile int64_t*>(tile_of + s);
+    if (tile < 0 || tile >= p.ntiles) break;   // no more tiles
+    const int64_t t = tile * p.R + row;
+    const bool valid = t < p.T;
     const unsigned char* srow = smem + (uint32_t)s * stage_bytes + (uint32_t)row * p.H * 2;
 
     // per vector: its sum of squares (fp32 pairs), values kept in registers
@@ -292,6 +316,7 @@ int launch_heads(const void* X, const float* gamma, void* Y, float* rinv, int64_
   prm.inv_hd = 1.0f / (float)head_dim;
   prm.wait_limit_ns = tune.wait_limit_ns;
   prm.missing_tx = tune.missing_tx;
+  prm.sched = tune.dynamic ? sched_counters(stream) : nullptr;
 
   int rc = prepare_kernel((const void*)kern, smem);
   if (rc != NTS_OK) return rc;

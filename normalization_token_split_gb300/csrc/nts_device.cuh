@@ -248,6 +248,17 @@ __device__ __forceinline__ void st_async_f32x2(uint32_t remote_addr, float a, fl
       : "memory");
 }
 
+// One 64-bit value into a cluster CTA's shared memory (8-byte aligned),
+// completing 8 transaction bytes on its mbarrier.
+__device__ __forceinline__ void st_async_u64(uint32_t remote_addr, uint64_t v,
+                                             uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+          remote_addr),
+      "r"((uint32_t)v), "r"((uint32_t)(v >> 32)), "r"(remote_bar)
+      : "memory");
+}
+
 // 1-D bulk copy global -> shared without an L2 hint (for re-read data).
 __device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void* src, uint32_t bytes,
                                                uint32_t bar) {

@@ -91,6 +91,8 @@ struct QkParams {
   float x_scale;   // E4M3 input: value = code * x_scale
   uint64_t wait_limit_ns;
   uint32_t missing_tx;  // test hook: bytes expected on the first stage but never sent
+  unsigned int* sched;  // zeroed counter pair (next tile, clusters done), or
+                        // nullptr: every tile in round-robin order
 };
 
 // Shared memory layout (bytes, in order):
@@ -103,10 +105,13 @@ struct QkParams {
 //   full  [S], empty [S]          ring mbarriers
 //   gbar                          gamma-arrival mbarrier
 //   xbar  [2][R]                  exchange mbarriers (double-buffered by tile)
+//   tbar  [S]                     tile-number mbarriers (dynamic order, N > 1)
+//   tile  [S] i64                 tile number sent by the cluster's rank 0
+//   tloc  [S] i64                 tile in stage s for the consumers (-1: done)
 //   part  [2][R][N][WPR][NS] f32  partial sums received from every warp of
 //                                 every shard of a row (NS = 1 RMS, 2 LN)
 struct QkLayout {
-  uint32_t ring, gstg, gam, full, empty, gbar, xbar, part, total;
+  uint32_t ring, gstg, gam, full, empty, gbar, xbar, tbar, tile, tloc, part, total;
 };
 
 __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int Wsum, int G,
@@ -119,7 +124,10 @@ __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int
   L.empty = L.full + (uint32_t)S * 8;
   L.gbar = L.empty + (uint32_t)S * 8;
   L.xbar = L.gbar + 8;
-  L.part = L.xbar + (uint32_t)2 * R * 8;
+  L.tbar = L.xbar + (uint32_t)2 * R * 8;
+  L.tile = L.tbar + (uint32_t)S * 8;
+  L.tloc = L.tile + (uint32_t)S * 8;
+  L.part = L.tloc + (uint32_t)S * 8;
   L.total = L.part + (uint32_t)2 * R * N * (G / 32) * 4 * ns;
   return L;
 }
@@ -169,12 +177,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
   const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, p.psum, p.G, p.gsplit, ES, NS);
   const uint32_t sbase = smem_addr(smem);
   const uint32_t stage_bytes = (uint32_t)p.R * p.Wmax * ES;
-  const int64_t my_tiles = cid < p.ntiles ? (p.ntiles - 1 - cid) / ncl + 1 : 0;
+  int64_t* tloc = reinterpret_cast<int64_t*>(smem + L.tloc);
+  // Tile order: the first S tiles of every cluster are fixed (cid + n * ncl,
+  // no start-up latency); later ones come from the launch's counter, taken
+  // by the cluster's rank 0 and sent to every CTA of the cluster.  Rank 0
+  // then hands a stage back only after the tile's combine, which every
+  // peer's producer has passed, so a tile number is never overwritten
+  // before it is read.
+  const bool dyn = p.sched != nullptr;
+  const bool hold = dyn && N > 1 && rank == 0;
 
   if (tid == 0) {
     for (int s = 0; s < p.S; ++s) {
       mbar_init(sbase + L.full + 8 * s, 1);
       mbar_init(sbase + L.empty + 8 * s, nconsumer / 32);
+      mbar_init(sbase + L.tbar + 8 * s, 1);
     }
     for (int b = 0; b < 2 * p.R; ++b) mbar_init(sbase + L.xbar + 8 * b, 1);
     mbar_init(sbase + L.gbar, 1);
@@ -205,38 +222,77 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
       // incrementally (no 64-bit division in the loop)
       int s = 0;
       uint32_t ph = 0;
-      for (int64_t j = 0; j < my_tiles; ++j) {
-        if (j >= p.S &&
-            !mbar_wait_bounded(sbase + L.empty + 8 * s, ph ^ 1u, p.wait_limit_ns)) {
+      int64_t n = 0;  // tiles issued
+      while (true) {
+        if (n >= p.S && !mbar_wait_bounded(sbase + L.empty + 8 * s, ph ^ 1u, p.wait_limit_ns)) {
           atomicOr(&g_qk_status, kStatusTimeout);
           aborted = true;
           break;
         }
+        int64_t tile;
+        if (n < p.S || !dyn) {
+          tile = cid + n * ncl;
+        } else if (N == 1) {
+          tile = ncl * p.S + (int64_t)atomicAdd(p.sched, 1u);
+        } else {
+          const uint32_t tb = sbase + L.tbar + 8 * s;
+          if (rank == 0) {
+            const int64_t tk = ncl * p.S + (int64_t)atomicAdd(p.sched, 1u);
+            const int64_t v = tk < p.ntiles ? tk : -1;
+            const uint32_t slot = sbase + L.tile + 8 * s;
+#pragma unroll
+            for (int k = 0; k < N; ++k)
+              st_async_u64(map_to_rank(slot, k), (uint64_t)v, map_to_rank(tb, k));
+          }
+          mbar_arrive_expect_tx(tb, 8);
+          if (!mbar_wait_bounded(tb, ph ^ 1u, p.wait_limit_ns)) {
+            atomicOr(&g_qk_status, kStatusTimeout);
+            aborted = true;
+            break;
+          }
+          tile = *reinterpret_cast<volatile int64_t*>(smem + L.tile + 8 * s);
+        }
+        const uint32_t bar = sbase + L.full + 8 * s;
+        if (tile < 0 || tile >= p.ntiles) {
+          tloc[s] = -1;   // published by the arrive (release) below
+          mbar_arrive(bar);
+          break;
+        }
+        tloc[s] = tile;
         int64_t t0;
-        const QkTensor& tn = p.ten[qk_tile(p, cid + j * ncl, &t0)];
+        const QkTensor& tn = p.ten[qk_tile(p, tile, &t0)];
         const int nrows = (int)min64(p.R, tn.T - t0);
         const uint32_t row_bytes = (uint32_t)tn.W * ES;
-        const uint32_t bar = sbase + L.full + 8 * s;
         const uint32_t dst = sbase + L.ring + (uint32_t)s * stage_bytes;
         const char* src = static_cast<const char*>(tn.X) +
                           ((size_t)t0 * tn.H + (size_t)rank * tn.W) * ES;
-        mbar_arrive_expect_tx(bar, nrows * row_bytes + (j == 0 ? p.missing_tx : 0u));
+        mbar_arrive_expect_tx(bar, nrows * row_bytes + (n == 0 ? p.missing_tx : 0u));
         if (N == 1) {
           bulk_g2s(dst, src, nrows * row_bytes, bar, policy);
         } else {
           for (int r = 0; r < nrows; ++r)
             bulk_g2s(dst + r * row_bytes, src + (size_t)r * tn.H * ES, row_bytes, bar, policy);
         }
+        ++n;
         if (++s == p.S) {
           s = 0;
           ph ^= 1u;
         }
       }
-      // let the last copies land before this CTA can retire
-      for (int64_t j = max64(0, my_tiles - p.S); j < my_tiles && !aborted; ++j)
+      // Normally the consumers have waited for every copy before the CTA can
+      // retire; after an expired wait, let the copies in flight land first.
+      for (int64_t j = max64(0, n - p.S); j < n && aborted; ++j)
         (void)mbar_wait_bounded(sbase + L.full + 8 * (int)(j % p.S), (uint32_t)((j / p.S) & 1),
                                 p.wait_limit_ns);
       (void)mbar_wait_bounded(sbase + L.gbar, 0, p.wait_limit_ns);
+      // rank 0 counts its cluster out; the last re-arms the pair
+      if (dyn && rank == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == (unsigned)(ncl - 1)) {
+          atomicExch(p.sched, 0u);
+          atomicExch(p.sched + 1, 0u);
+        }
+      }
     }
     __syncwarp();
     if (N > 1) cluster_wait_acquire();
@@ -255,19 +311,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
     const int wir = g >> 5;
     const bool exchange = (N > 1) || (wpr > 1);
     bool aborted = false;
-    int s = 0;          // ring stage of tile j
+    int s = 0;          // ring stage of the j-th tile
     uint32_t ph = 0;    // (j / S) & 1
-    for (int64_t j = 0; j < my_tiles; ++j) {
+    for (int64_t j = 0;; ++j) {
+      if (!mbar_wait_bounded(sbase + L.full + 8 * s, ph, p.wait_limit_ns)) {
+        atomicOr(&g_qk_status, kStatusTimeout);
+        break;
+      }
+      const int64_t tile = *reinterpret_cast<volatile int64_t*>(tloc + s);
+      if (tile < 0 || tile >= p.ntiles) break;   // no more tiles
       int64_t t0;
-      const QkTensor& tn = p.ten[qk_tile(p, cid + j * ncl, &t0)];
+      const QkTensor& tn = p.ten[qk_tile(p, tile, &t0)];
       const int64_t t = t0 + row;
       const bool valid = t < tn.T;
       const int nvec = tn.nvec;
-
-      if (!mbar_wait_bounded(sbase + L.full + 8 * s, ph, aborted ? 0 : p.wait_limit_ns)) {
-        if (!aborted) atomicOr(&g_qk_status, kStatusTimeout);
-        aborted = true;
-      }
 
       // ---- Phase A: this shard's sum of squares (and, for LayerNorm, its
       // sum) in fp32 packed pairs.  The values are converted once and kept
@@ -289,8 +346,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         }
       }
       // the stage's data is in registers: hand it back to the producer
+      // (rank 0 under the dynamic order: after the combine, see above)
       __syncwarp();
-      if (lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
+      if (!hold && lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
       const uint64_t a01 = f2_add(acc[0], acc[1]), a23 = f2_add(acc[2], acc[3]);
       const uint64_t a = f2_add(a01, a23);
       const float ss = warp_sum(f2_lo(a) + f2_hi(a));
@@ -482,6 +540,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknorm_cluster_kernel(const Qk
         if (tn.rinv_out != nullptr && rank == 0 && g == 0) tn.rinv_out[t] = rinv;
         if (STAT == kQkLn && tn.mean_out != nullptr && rank == 0 && g == 0) tn.mean_out[t] = mu;
       }
+      if (hold) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
+      }
+      if (aborted) break;
       if (++s == p.S) {
         s = 0;
         ph ^= 1u;

@@ -109,6 +109,7 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
   prm.x_scale = opt.x_scale;
   prm.wait_limit_ns = tune.wait_limit_ns;
   prm.missing_tx = tune.missing_tx;
+  prm.sched = tune.dynamic ? sched_counters(stream) : nullptr;
   if (ntiles == 0) return NTS_OK;
 
   const int nthreads = R * rs.G + 32;  // consumers + producer warp

@@ -295,3 +295,44 @@ def test_fp8_equals_bf16_kernel_on_the_same_values():
     yb, rb = nts.qknorm_rms(vals, g, eps=1e-6, N=4, want_rinv=True)
     nts.check_status()
     assert torch.equal(r8, rb) and torch.equal(y8, yb)
+
+
+def test_headwise_tile_orders_agree():
+    X, _ = workloads.qk_inputs(3001, 4096, seed=19, device=DEV)
+    g = workloads.gamma_vector(128, seed=9, device=DEV)
+    outs = []
+    try:
+        for dyn in (True, False, True):
+            nts.set_schedule(dyn)
+            for _ in range(3):
+                y, r = nts.qknorm_rms_heads(X, g, 128, N=1, want_rinv=True)
+            nts.check_status()
+            outs.append((y, r))
+    finally:
+        nts.set_schedule(True)
+    for y, r in outs[1:]:
+        assert torch.equal(y, outs[0][0]) and torch.equal(r, outs[0][1])
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+def test_cluster_tile_orders_agree(N):
+    # dynamic order (rank 0 of each cluster takes tiles from the counter and
+    # sends their numbers to its peers) and round-robin order: same results;
+    # several back-to-back launches check that the counter re-arms itself
+    Q, gq = workloads.qk_inputs(3001, 4096, seed=20 + N, device=DEV)
+    K, gk = workloads.qk_inputs(3001, 1024, seed=30 + N, device=DEV)
+    outs = []
+    try:
+        for dyn in (True, False, True):
+            nts.set_schedule(dyn)
+            for _ in range(3):
+                res = nts.qknorm_rms_qk(Q, gq, K, gk, eps=1e-6, N=N, want_rinv=True)
+                ln = nts.layernorm_split(Q, gq, None, N=N, want_stats=True)
+            nts.check_status()
+            outs.append(res + ln)
+    finally:
+        nts.set_schedule(True)
+    for o in outs[1:]:
+        assert all(torch.equal(a, b) for a, b in zip(o, outs[0]))
+    Yo, ro, _ = oracle.qknorm_rms(workloads.bf16_bits(K), gk.cpu().numpy(), 1e-6, N)
+    check_qk(workloads.bf16_bits(outs[0][1]), outs[0][3].cpu().numpy(), Yo, ro, f"dyn N={N}")
