@@ -321,6 +321,40 @@ NTS_API int nts_mxnorm_cast_host(const void *X_host, const float *gamma_dev,
                          int64_t T, int64_t D, float eps, int B, int fmt,
                          int p, void *stream);
 
+/*
+ * nts_mxnorm_cast_host_noalloc -- nts_mxnorm_cast_host with no caller-owned
+ * device buffers: the device staging for X, gamma, codes and scales is a
+ * fixed 16 MiB array inside the library (one per device).  The pages have
+ * no counterpart; it serves callers that cannot allocate device memory at
+ * the call: processes whose device memory another framework's pool has
+ * already reserved, latency-bound loops that must not call the allocator
+ * after start-up (cudaFree synchronizes the device, cudaMalloc may), and
+ * host-only callers with no device allocator.
+ *
+ *   X_host      bf16 [T, D], read.   gamma_host  fp32 [D], read, or NULL.
+ *   codes_host, scales_host: as nts_mxnorm_cast_host, written once the
+ *   stream reaches the end of the call's work.  Other arguments as
+ *   nts_mxnorm_cast.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (and fills the library's host-side launch caches: device facts, kernel
+ * attributes, c(B, p), the stream's tile counters).  Make that first call
+ * before any stream capture; later calls on that device and stream allocate
+ * nothing, host or device.
+ * Sharing: every call on a device uses the same array, so calls that overlap
+ * in time (other streams, unordered host threads) race and corrupt each
+ * other's staging; serialize them.  Nothing in the array needs to start at
+ * zero: each call copies in all the kernel reads.
+ * Errors: as nts_mxnorm_cast_host; UNSUPPORTED when the call needs more than
+ * 16 MiB of staging (2*T*D bytes of X, 4*D of gamma, T*D or T*D/2 of codes,
+ * T*D/B of scales, each rounded up to 256 bytes), or for a device ordinal
+ * of 64 or more.
+ */
+NTS_API int nts_mxnorm_cast_host_noalloc(const void *X_host, const float *gamma_host,
+                                         uint8_t *codes_host, uint8_t *scales_host, int64_t T,
+                                         int64_t D, float eps, int B, int fmt, int p,
+                                         void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -310,6 +310,19 @@ def mxnorm_cast_host(x_host, gamma_dev, codes_host, scales_host, x_dev, codes_de
 
 # ------------------------------------------------------------------ tuning
 
+def mxnorm_cast_host_noalloc(x_host, gamma_host, codes_host, scales_host, eps=1e-6, B=32,
+                             fmt="e4m3", p=2, stream=None) -> None:
+    """MXNorm of host rows with the library's fixed device staging (no
+    caller-owned device buffers; calls that overlap in time race)."""
+    _need_host("x_host", x_host)
+    T, D = x_host.shape
+    if gamma_host is not None:
+        _need_host("gamma_host", gamma_host)
+    check(lib().nts_mxnorm_cast_host_noalloc(_ptr(x_host), _ptr(gamma_host), _ptr(codes_host),
+                                             _ptr(scales_host), T, D, float(eps), int(B),
+                                             _fmt(fmt), int(p), _stream(stream)))
+
+
 def set_tuning(vpt=0, rows=0, stages=0, grid=0, smem_budget=0) -> None:
     check(lib().nts_debug_set_tuning(int(vpt), int(rows), int(stages), int(grid),
                                      int(smem_budget)))

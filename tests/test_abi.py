@@ -215,3 +215,17 @@ def test_qk_mxcast_argument_checks(lib):
     assert f(H=1040, B=16) == UNSUPPORTED      # 520-value shards
     assert f(c=MIS) == UNSUPPORTED
     assert f(T=0, X=None, c=None, s=None) == OK
+
+
+def test_noalloc_argument_checks(lib):
+    f = lambda **k: lib.nts_mxnorm_cast_host_noalloc(
+        k.get("X", A16), None, A16, A16, k.get("T", 4), k.get("D", 256), 1e-6, k.get("B", 32),
+        k.get("fmt", 0), k.get("p", 2), None)
+    assert f(X=None) == INVALID
+    assert f(B=8) == INVALID
+    assert f(p=3) == INVALID
+    assert f(fmt=5) == INVALID
+    assert f(T=-1) == INVALID
+    assert f(T=4096, D=4096) == UNSUPPORTED      # beyond the 16 MiB static scratch
+    assert b"static scratch" in lib.nts_last_error()
+    assert f(T=0, X=None) == OK
