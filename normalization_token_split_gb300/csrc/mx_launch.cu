@@ -17,16 +17,19 @@ struct MxShape {
 
 int threads_for(int K, int bpt) { return ((K + bpt - 1) / bpt + 31) / 32 * 32; }
 
-// Blocks per thread: up to 4 (measured best on GB300: enough independent
-// blocks per thread for latency hiding without spilling); 8 only when a row
-// would otherwise need more than the CTA's consumer threads.
-MxShape choose_mx_shape(int K, int force_bpt) {
+// Blocks per thread: as few as cover the row with one warp, up to 16
+// vectors per thread (4 blocks of 32, 8 of 16, 2 of 64: measured best on
+// GB300 -- a row in one warp needs no cross-warp exchange, and 16 vectors
+// give enough independent work without spilling); 8 only when a row would
+// otherwise need more than the CTA's consumer threads.
+MxShape choose_mx_shape(int K, int VB, int force_bpt) {
   MxShape sh;
   if (force_bpt > 0) {
     sh.bpt = force_bpt;
   } else {
+    const int cap = std::max(1, std::min(8, 16 / VB));
     sh.bpt = 1;
-    while (sh.bpt < 4 && K > 32 * sh.bpt) sh.bpt *= 2;
+    while (sh.bpt < cap && K > 32 * sh.bpt) sh.bpt *= 2;
     if (threads_for(K, sh.bpt) > kMaxConsumers) sh.bpt = 8;
   }
   sh.G = threads_for(K, sh.bpt);
@@ -43,7 +46,7 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
 
   // tune.force_vpt selects the blocks per thread for this kernel family
-  const MxShape sh = choose_mx_shape(K, tune.force_vpt);
+  const MxShape sh = choose_mx_shape(K, rq.B / 8, tune.force_vpt);
   if (sh.G == 0) return fail(NTS_ERR_UNSUPPORTED, "row too wide: D = %d", D);
 
   // Rows per tile: about four consumer warps and at least 8 KB per stage;
