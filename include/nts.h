@@ -295,9 +295,15 @@ NTS_API int nts_check_status(void *stream);
 
 /*
  * Host-buffer forms: the same operations for callers whose inputs and
- * outputs live in host memory.  Each enqueues on `stream`: the host->device
- * copy of the input rows, the kernel, and the device->host copies of the
- * outputs; the caller synchronizes the stream before reading *_host outputs.
+ * outputs live in host memory.  Each enqueues the host->device copy of the
+ * input rows, the kernel, and the device->host copies of the outputs, all
+ * ordered on `stream`: the caller synchronizes the stream before reading
+ * *_host outputs.  Calls of more than a few tens of MB move their rows in
+ * chunks through two internal copy streams (one per direction, created on
+ * the first such call on a device) while the kernels run on `stream`, so
+ * both copy directions and the kernels overlap; the enqueueing of such calls
+ * from several host threads is serialized.  Host buffers should be pinned
+ * for the copies to run asynchronously.
  * The device staging buffers (*_dev) are caller-owned and sized like the
  * corresponding host buffers; gamma stays a device pointer (a parameter,
  * uploaded once).  Optional outputs follow the device forms: a NULL *_host
@@ -338,9 +344,10 @@ NTS_API int nts_mxnorm_cast_host(const void *X_host, const float *gamma_dev,
  *
  * Set-up: the first call on each device looks up the array's device address
  * (and fills the library's host-side launch caches: device facts, kernel
- * attributes, c(B, p), the stream's tile counters).  Make that first call
- * before any stream capture; later calls on that device and stream allocate
- * nothing, host or device.
+ * attributes, c(B, p), the stream's tile counters, and for calls large
+ * enough to be split into chunks the internal copy streams).  Make that
+ * first call before any stream capture; later calls on that device and
+ * stream allocate nothing, host or device.
  * Sharing: every call on a device uses the same array, so calls that overlap
  * in time (other streams, unordered host threads) race and corrupt each
  * other's staging; serialize them.  Nothing in the array needs to start at

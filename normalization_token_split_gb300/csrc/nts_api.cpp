@@ -3,6 +3,7 @@
 // computation of the MXNorm correction factor c(B, p).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -316,6 +317,106 @@ int copy(void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, void* st
   return NTS_OK;
 }
 
+// ----------------------------------------------- host-buffer forms: pipeline
+//
+// A host-buffer call moves its rows in chunks through three streams: the
+// copies to the device on `in`, the kernels on the caller's stream, the
+// copies back on `out`, ordered chunk by chunk with events.  The two copy
+// directions then run at once (GB300 NVLink-C2C: ~210 GB/s either way
+// alone, ~330 GB/s both ways together) and the kernels hide behind them.
+// The caller's stream waits for the last copy back, so the call's effects
+// are ordered on that stream exactly as with one stream.
+
+constexpr int kMaxChunks = 8;
+constexpr size_t kChunkBytes = size_t(16) << 20;   // input bytes per chunk, at least
+constexpr int kChunkRows = 16;                     // chunk boundaries: multiples of 16 rows
+constexpr int kPipeDevices = 64;
+
+struct HostPipe {
+  bool ok = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, finished = nullptr;
+  cudaEvent_t loaded[kMaxChunks] = {}, done[kMaxChunks] = {};
+};
+
+// Serializes the enqueue sequences of host-buffer calls, which share the
+// per-device streams and events (a wait refers to the event's record at the
+// time it is enqueued, so reusing the events for the next call is safe).
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kPipeDevices];
+
+int host_pipe(HostPipe** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "querying the current device");
+  if (dev < 0 || dev >= kPipeDevices)
+    return fail(NTS_ERR_UNSUPPORTED, "device %d beyond the %d the host-buffer forms serve", dev,
+                kPipeDevices);
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ok) {
+    const unsigned ef = cudaEventDisableTiming;
+    e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, ef);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.finished, ef);
+    for (int k = 0; k < kMaxChunks && e == cudaSuccess; ++k) {
+      e = cudaEventCreateWithFlags(&hp.loaded[k], ef);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.done[k], ef);
+    }
+    if (e != cudaSuccess) return fail_cuda(e, "creating the host-buffer copy streams");
+    hp.ok = true;
+  }
+  *out = &hp;
+  return NTS_OK;
+}
+
+// Runs a host-buffer call over T rows: copy_in(r0, r1, stream) enqueues the
+// copies of rows [r0, r1) to the device, kernel(r0, r1, stream) the
+// computation, copy_out(r0, r1, stream) the copies back.  One chunk (small
+// calls) runs everything on the caller's stream.
+template <typename In, typename Kernel, typename Out>
+int run_host_pipeline(int64_t T, size_t in_bytes_per_row, void* stream, In copy_in,
+                      Kernel kernel, Out copy_out) {
+  int nchunks = (int)std::min<size_t>(kMaxChunks, (T * in_bytes_per_row) / kChunkBytes);
+  nchunks = std::max(1, std::min<int>(nchunks, (int)((T + kChunkRows - 1) / kChunkRows)));
+  if (nchunks == 1) {
+    int rc = copy_in(0, T, stream);
+    if (rc == NTS_OK) rc = kernel(0, T, stream);
+    if (rc == NTS_OK) rc = copy_out(0, T, stream);
+    return rc;
+  }
+  int64_t rows = (T + nchunks - 1) / nchunks;
+  rows = (rows + kChunkRows - 1) / kChunkRows * kChunkRows;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe* hp = nullptr;
+  int rc = host_pipe(&hp);
+  if (rc != NTS_OK) return rc;
+  cudaError_t e = cudaEventRecord(hp->start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->start, 0);
+  if (e != cudaSuccess) return fail_cuda(e, "ordering the copy streams after the caller's work");
+  int k = 0;
+  for (int64_t r0 = 0; r0 < T; r0 += rows, ++k) {
+    const int64_t r1 = std::min(T, r0 + rows);
+    rc = copy_in(r0, r1, hp->in);
+    if (rc != NTS_OK) return rc;
+    e = cudaEventRecord(hp->loaded[k], hp->in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->loaded[k], 0);
+    if (e != cudaSuccess) return fail_cuda(e, "ordering a chunk's kernel after its copy");
+    rc = kernel(r0, r1, stream);
+    if (rc != NTS_OK) return rc;
+    e = cudaEventRecord(hp->done[k], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->done[k], 0);
+    if (e != cudaSuccess) return fail_cuda(e, "ordering a chunk's copy back after its kernel");
+    rc = copy_out(r0, r1, hp->out);
+    if (rc != NTS_OK) return rc;
+  }
+  e = cudaEventRecord(hp->finished, hp->out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->finished, 0);
+  if (e != cudaSuccess) return fail_cuda(e, "ordering the caller's stream after the copies");
+  return NTS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -475,17 +576,27 @@ int nts_qknorm_rms_host(const void* X_host, const float* gamma_dev, void* Y_host
   int rc = validate_qk(X_dev, gamma_dev, Y_dev, rinv_k, T, H, eps, N);
   if (rc != NTS_OK) return rc;
   if (T == 0) return NTS_OK;
-  const size_t xb = (size_t)T * (size_t)H * 2;
-  rc = copy(X_dev, X_host, xb, cudaMemcpyHostToDevice, stream, "copying X to the device");
-  if (rc != NTS_OK) return rc;
-  rc = nts_qknorm_rms(X_dev, gamma_dev, Y_dev, rinv_k, T, H, eps, N, stream);
-  if (rc != NTS_OK) return rc;
-  rc = copy(Y_host, Y_dev, xb, cudaMemcpyDeviceToHost, stream, "copying Y to the host");
-  if (rc != NTS_OK) return rc;
-  if (rinv_host != nullptr)
-    rc = copy(rinv_host, rinv_dev, (size_t)T * 4, cudaMemcpyDeviceToHost, stream,
-              "copying rinv to the host");
-  return rc;
+  const size_t rb = (size_t)H * 2;  // bytes per row
+  auto at = [rb](const void* base, int64_t r) {
+    return static_cast<const char*>(base) + (size_t)r * rb;
+  };
+  auto in = [&](int64_t r0, int64_t r1, void* st) {
+    return copy(const_cast<char*>(at(X_dev, r0)), at(X_host, r0), (size_t)(r1 - r0) * rb,
+                cudaMemcpyHostToDevice, st, "copying X to the device");
+  };
+  auto kern = [&](int64_t r0, int64_t r1, void* st) {
+    return nts_qknorm_rms(at(X_dev, r0), gamma_dev, const_cast<char*>(at(Y_dev, r0)),
+                          rinv_k != nullptr ? rinv_k + r0 : nullptr, r1 - r0, H, eps, N, st);
+  };
+  auto out = [&](int64_t r0, int64_t r1, void* st) {
+    int c = copy(const_cast<char*>(at(Y_host, r0)), at(Y_dev, r0), (size_t)(r1 - r0) * rb,
+                 cudaMemcpyDeviceToHost, st, "copying Y to the host");
+    if (c == NTS_OK && rinv_host != nullptr)
+      c = copy(rinv_host + r0, rinv_dev + r0, (size_t)(r1 - r0) * 4, cudaMemcpyDeviceToHost, st,
+               "copying rinv to the host");
+    return c;
+  };
+  return run_host_pipeline(T, rb, stream, in, kern, out);
 }
 
 static int mx_host(const void* X_host, const float* gamma_dev, uint8_t* codes_host,
@@ -498,18 +609,26 @@ static int mx_host(const void* X_host, const float* gamma_dev, uint8_t* codes_ho
                        fmt, p, mxnorm);
   if (rc != NTS_OK) return rc;
   if (T == 0) return NTS_OK;
-  const size_t xb = (size_t)T * (size_t)D * 2;
-  const size_t cb = (size_t)T * (size_t)(fmt == NTS_FMT_E4M3 ? D : D / 2);
-  const size_t sb = (size_t)T * (size_t)(D / B);
-  rc = copy(X_dev, X_host, xb, cudaMemcpyHostToDevice, stream, "copying X to the device");
-  if (rc != NTS_OK) return rc;
-  rc = run_mx(X_dev, gamma_dev, codes_dev, scales_dev, nullptr, nullptr, T, D, eps, B, fmt, p,
-              mxnorm, stream);
-  if (rc != NTS_OK) return rc;
-  rc = copy(codes_host, codes_dev, cb, cudaMemcpyDeviceToHost, stream, "copying codes to the host");
-  if (rc != NTS_OK) return rc;
-  return copy(scales_host, scales_dev, sb, cudaMemcpyDeviceToHost, stream,
-              "copying scales to the host");
+  const size_t xr = (size_t)D * 2;                                   // bytes per row
+  const size_t cr = (size_t)(fmt == NTS_FMT_E4M3 ? D : D / 2);
+  const size_t sr = (size_t)(D / B);
+  auto in = [&](int64_t r0, int64_t r1, void* st) {
+    return copy(static_cast<char*>(X_dev) + r0 * xr, static_cast<const char*>(X_host) + r0 * xr,
+                (size_t)(r1 - r0) * xr, cudaMemcpyHostToDevice, st, "copying X to the device");
+  };
+  auto kern = [&](int64_t r0, int64_t r1, void* st) {
+    return run_mx(static_cast<const char*>(X_dev) + r0 * xr, gamma_dev, codes_dev + r0 * cr,
+                  scales_dev + r0 * sr, nullptr, nullptr, r1 - r0, D, eps, B, fmt, p, mxnorm, st);
+  };
+  auto out = [&](int64_t r0, int64_t r1, void* st) {
+    int c = copy(codes_host + r0 * cr, codes_dev + r0 * cr, (size_t)(r1 - r0) * cr,
+                 cudaMemcpyDeviceToHost, st, "copying codes to the host");
+    if (c == NTS_OK)
+      c = copy(scales_host + r0 * sr, scales_dev + r0 * sr, (size_t)(r1 - r0) * sr,
+               cudaMemcpyDeviceToHost, st, "copying scales to the host");
+    return c;
+  };
+  return run_host_pipeline(T, xr, stream, in, kern, out);
 }
 
 int nts_rmsnorm_mxcast_host(const void* X_host, const float* gamma_dev, uint8_t* codes_host,

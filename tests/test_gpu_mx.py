@@ -317,3 +317,25 @@ def test_launches_on_several_streams():
     for w, gs in zip(want, got):
         for g in gs:
             assert torch.equal(g.codes, w.codes) and torch.equal(g.scales, w.scales)
+
+
+@pytest.mark.parametrize("T,D,B,fmt", [(20011, 4096, 32, "e4m3"), (9000, 2048, 16, "nvfp4"),
+                                       (4133, 8192, 32, "e2m1")])
+def test_host_buffer_form_in_chunks(T, D, B, fmt):
+    # large enough to be split into chunks that flow through the copy-in,
+    # kernel and copy-out streams; the last chunk is ragged
+    X, _ = workloads.mx_inputs(T, D, seed=16 + T, t_frac=0.05)
+    Xh = X.pin_memory()
+    cb = D if fmt == "e4m3" else D // 2
+    ch = torch.empty(T, cb, dtype=torch.uint8).pin_memory()
+    sh = torch.empty(T, D // B, dtype=torch.uint8).pin_memory()
+    Xd = torch.empty_like(X, device=DEV)
+    cd = torch.empty(T, cb, dtype=torch.uint8, device=DEV)
+    sd = torch.empty(T, D // B, dtype=torch.uint8, device=DEV)
+    for rep in range(2):
+        nts.mxnorm_cast_host(Xh, None, ch, sh, Xd, cd, sd, eps=1e-6, B=B, fmt=fmt, p=2)
+        nts.check_status()
+        dev = nts.mxnorm_cast(X.to(DEV), None, eps=1e-6, B=B, fmt=fmt, p=2)
+        nts.check_status()
+        assert torch.equal(ch, dev.codes.cpu()) and torch.equal(sh, dev.scales.cpu())
+        ch.zero_()

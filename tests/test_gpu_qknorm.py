@@ -336,3 +336,21 @@ def test_cluster_tile_orders_agree(N):
         assert all(torch.equal(a, b) for a, b in zip(o, outs[0]))
     Yo, ro, _ = oracle.qknorm_rms(workloads.bf16_bits(K), gk.cpu().numpy(), 1e-6, N)
     check_qk(workloads.bf16_bits(outs[0][1]), outs[0][3].cpu().numpy(), Yo, ro, f"dyn N={N}")
+
+
+@pytest.mark.parametrize("T,H,N", [(8191, 5120, 4), (20000, 2048, 2)])
+def test_host_buffer_form_in_chunks(T, H, N):
+    X, g = workloads.qk_inputs(T, H, seed=T + H, outlier_frac=0.01)
+    Xh = X.pin_memory()
+    Yh = torch.empty_like(Xh).pin_memory()
+    rh = torch.empty(T, dtype=torch.float32).pin_memory()
+    Xd, Yd = torch.empty_like(X, device=DEV), torch.empty_like(X, device=DEV)
+    rd = torch.empty(T, dtype=torch.float32, device=DEV)
+    gd = g.to(DEV)
+    for rep in range(2):
+        nts.qknorm_rms_host(Xh, gd, Yh, Xd, Yd, eps=1e-6, N=N, rinv_host=rh, rinv_dev=rd)
+        nts.check_status()
+        y, r = nts.qknorm_rms(X.to(DEV), gd, eps=1e-6, N=N, want_rinv=True)
+        nts.check_status()
+        assert torch.equal(Yh, y.cpu()) and torch.equal(rh, r.cpu())
+        Yh.zero_()
