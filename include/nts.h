@@ -344,10 +344,11 @@ NTS_API int nts_mxnorm_cast_host(const void *X_host, const float *gamma_dev,
  *
  * Set-up: the first call on each device looks up the array's device address
  * (and fills the library's host-side launch caches: device facts, kernel
- * attributes, c(B, p), the stream's tile counters, and for calls large
- * enough to be split into chunks the internal copy streams).  Make that
- * first call before any stream capture; later calls on that device and
- * stream allocate nothing, host or device.
+ * attributes, c(B, p), the stream's tile counters).  Its staging is too
+ * small for the chunked copies of the other host-buffer forms, so it never
+ * creates their copy streams.  Make that first call before any stream
+ * capture; later calls on that device and stream allocate nothing, host or
+ * device.
  * Sharing: every call on a device uses the same array, so calls that overlap
  * in time (other streams, unordered host threads) race and corrupt each
  * other's staging; serialize them.  Nothing in the array needs to start at
