@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) heads_kernel(const HeadsParams
       for (int i = 0; i < VPT; ++i) {
         const int v = i * p.G + g;
         if (v < p.nvec) {
-          const float rinv = 1.0f / sqrtf(ss[i] * p.inv_hd + p.eps);
+          const float rinv = rsqrtf(fmaf(ss[i], p.inv_hd, p.eps));
           const uint64_t rr = f2(rinv, rinv);
           uint64_t y[4];
 #pragma unroll

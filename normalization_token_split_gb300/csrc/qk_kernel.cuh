@@ -69,6 +69,7 @@ struct QkTensor {
   int64_t T;
   int64_t ntiles;  // ceil(T / R)
   int H;           // full row width H_total
+  float inv_H;     // fp32(1 / H)
   int W;           // H / N, the columns of one shard
   int nvec;        // W / 8 16-byte vectors per shard row
   uint32_t gam;    // shared-memory offset of this tensor's staged gamma
@@ -458,11 +459,12 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
       if (valid) {
         float rinv, mu = 0.f;
         if (STAT == kQkLn) {
-          mu = S1 / (float)tn.H;
-          const float var = fmaxf(S / (float)tn.H - mu * mu, 0.f);
-          rinv = 1.0f / sqrtf(var + p.eps);
+          mu = S1 * tn.inv_H;
+          const float var = fmaxf(fmaf(S, tn.inv_H, -mu * mu), 0.f);
+          rinv = rsqrtf(var + p.eps);
         } else {
-          rinv = 1.0f / sqrtf(S / (float)tn.H + p.eps);
+          // the hardware reciprocal square root (a few 1e-8 relative error)
+          rinv = rsqrtf(fmaf(S, tn.inv_H, p.eps));
         }
         const uint64_t rr = f2(rinv, rinv);
         const float nmr = -mu * rinv;

@@ -84,6 +84,7 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
     tn.T = rq[k].T;
     tn.ntiles = (rq[k].T + R - 1) / R;
     tn.H = (int)rq[k].H;
+    tn.inv_H = (float)(1.0 / (double)rq[k].H);
     tn.W = (int)(rq[k].H / N);
     tn.nvec = tn.W / 8;
     tn.gam = gam;

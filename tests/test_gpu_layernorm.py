@@ -105,7 +105,8 @@ def test_constant_and_zero_rows():
     check_ln(X, Yg, mg, rg, Yo, mo, ro, "constant rows")
     for r, c in enumerate((1.5, -0.75, 3.0, 0.0)):
         assert mg[r] == np.float32(c)
-        assert rg[r] == np.float32(1.0) / np.sqrt(np.float32(1e-5))
+        # rstd = 1/sqrt(eps) up to the hardware rsqrt's rounding
+        assert abs(rg[r] * np.sqrt(np.float64(np.float32(1e-5))) - 1) < 4e-7
         want = bf16_to_f64(workloads.bf16_bits(b.to(torch.bfloat16)))
         assert np.all(np.abs(bf16_to_f64(Yg[r]) - want) <= 1e-3 + 1e-2 * np.abs(want))
 
