@@ -41,6 +41,16 @@ NTS_API int nts_debug_set_wait_limit_ns(uint64_t ns);
 NTS_API int nts_debug_set_schedule(int dynamic);
 
 /*
+ * Decode-sized QK-RMSNorm launches (bf16 in and out, every tile in one wave
+ * of single-tile clusters, no launch-shape override and no missing-bytes
+ * hook): 1 (default) = the
+ * single-tile kernel without producer warp or ring; 0 = the persistent
+ * kernel.  Results are identical either way.  Errors: INVALID_ARG for other
+ * values.
+ */
+NTS_API int nts_debug_set_direct(int on);
+
+/*
  * Test hook: every later launch tells its first ring stage to expect `bytes`
  * more than its copies deliver, so that stage's wait can only end by
  * expiring; the kernel then records NTS_ERR_TIMEOUT for nts_check_status and

@@ -49,6 +49,7 @@ def _declare(lib):
         "nts_debug_set_wait_limit_ns": ([ctypes.c_uint64], i32),
         "nts_debug_set_missing_tx": ([ctypes.c_uint32], i32),
         "nts_debug_set_schedule": ([i32], i32),
+        "nts_debug_set_direct": ([i32], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

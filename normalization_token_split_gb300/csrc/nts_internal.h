@@ -27,6 +27,7 @@ struct LaunchTuning {
   uint64_t wait_limit_ns = 1000000000ull;  // bounded mbarrier waits
   uint32_t missing_tx = 0;   // test hook, see nts_debug.h
   int dynamic = 1;           // take tiles from a counter (0: round-robin order)
+  int direct = 1;            // decode-sized QK launches use the single-tile kernel
 };
 
 LaunchTuning current_tuning();

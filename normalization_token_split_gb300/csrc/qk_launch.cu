@@ -113,6 +113,39 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
   prm.sched = tune.dynamic ? sched_counters(stream) : nullptr;
   if (ntiles == 0) return NTS_OK;
 
+  // Decode-sized launches (every tile in one wave of single-tile clusters):
+  // the kernel without producer, ring or mbarriers (qk_direct.cu).  It has
+  // no waits, so the missing-bytes test hook keeps the persistent kernel.
+  if (tune.direct && !mx_out && !layernorm && !opt.in_e4m3 && rs.vpt <= 5 &&
+      tune.force_rows == 0 && tune.force_stages == 0 && tune.force_grid == 0 &&
+      tune.missing_tx == 0) {
+    QkKernel dk = pick_qk_direct(N, rs.vpt);
+    const size_t dsmem = (size_t)R * N * (rs.G / 32) * 4;
+    cudaLaunchConfig_t dc = {};
+    cudaLaunchAttribute da[1];
+    da[0].id = cudaLaunchAttributeClusterDimension;
+    da[0].val.clusterDim.x = N;
+    da[0].val.clusterDim.y = 1;
+    da[0].val.clusterDim.z = 1;
+    dc.blockDim = dim3(R * rs.G);
+    dc.dynamicSmemBytes = dsmem;
+    dc.stream = stream;
+    dc.attrs = da;
+    dc.numAttrs = 1;
+    int64_t dmax = 0;
+    int rc = dk != nullptr ? max_active_clusters((const void*)dk, dc, N, &dmax) : NTS_OK;
+    if (rc != NTS_OK) return rc;
+    if (dk != nullptr && ntiles <= dmax) {
+      dc.gridDim = dim3((unsigned)(ntiles * N));
+      log_launch("qknorm_rms", "direct: tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d clusters=%lld",
+                 ntensors, (long long)rq[0].T, (int)rq[0].H, N, rs.vpt, rs.G, R,
+                 (long long)ntiles);
+      const cudaError_t e = cudaLaunchKernelEx(&dc, dk, prm);
+      if (e != cudaSuccess) return fail_cuda(e, "launching qknorm_rms");
+      return NTS_OK;
+    }
+  }
+
   const int nthreads = R * rs.G + 32;  // consumers + producer warp
   int rc = prepare_kernel((const void*)kern, smem);
   if (rc != NTS_OK) return rc;

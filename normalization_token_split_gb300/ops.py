@@ -336,5 +336,9 @@ def set_schedule(dynamic: bool) -> None:
     check(lib().nts_debug_set_schedule(1 if dynamic else 0))
 
 
+def set_direct(on: bool) -> None:
+    check(lib().nts_debug_set_direct(1 if on else 0))
+
+
 def set_missing_tx(nbytes: int) -> None:
     check(lib().nts_debug_set_missing_tx(int(nbytes)))

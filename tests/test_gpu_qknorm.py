@@ -354,3 +354,25 @@ def test_host_buffer_form_in_chunks(T, H, N):
         nts.check_status()
         assert torch.equal(Yh, y.cpu()) and torch.equal(rh, r.cpu())
         Yh.zero_()
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+@pytest.mark.parametrize("T", [1, 3, 64, 200])
+def test_decode_direct_kernel_equals_persistent(T, N):
+    # decode-sized launches take the single-tile kernel; it must give the
+    # persistent kernel's results bit for bit (same summation order)
+    Q, gq = workloads.qk_inputs(T, 4096, seed=40 + T, device=DEV)
+    K, gk = workloads.qk_inputs(T, 1024, seed=50 + T, device=DEV)
+    outs = []
+    try:
+        for direct in (True, False):
+            nts.set_direct(direct)
+            r1 = nts.qknorm_rms_qk(Q, gq, K, gk, eps=1e-6, N=N, want_rinv=True)
+            r2 = nts.qknorm_rms(Q, gq, eps=1e-6, N=N, want_rinv=True)
+            nts.check_status()
+            outs.append(r1 + r2)
+    finally:
+        nts.set_direct(True)
+    assert all(torch.equal(a, b) for a, b in zip(outs[0], outs[1]))
+    Yo, ro, _ = oracle.qknorm_rms(workloads.bf16_bits(Q), gq.cpu().numpy(), 1e-6, N)
+    check_qk(workloads.bf16_bits(outs[0][4]), outs[0][5].cpu().numpy(), Yo, ro, f"direct N={N}")
