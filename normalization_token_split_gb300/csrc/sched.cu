@@ -10,8 +10,11 @@
 //
 // The pairs live in a fixed device array (no allocation); each CUDA stream
 // gets its own pair on first use, so launches on different streams, which
-// may overlap, never share one.  When the pool is used up the launch falls
-// back to the round-robin order (a null pointer).
+// may overlap, never share one.  The round-robin order (a null pointer) is
+// kept where a stream handle does not identify one ordered stream of work:
+// launches recorded into a CUDA graph (a graph may be replayed on any
+// stream, alongside direct launches), the per-thread default stream (one
+// handle for every host thread's stream), and a used-up pool.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -31,6 +34,13 @@ __device__ __align__(256) unsigned int g_sched_pool[kSchedSlots][2];
 }  // namespace
 
 unsigned int* sched_counters(cudaStream_t stream) {
+  if (stream == cudaStreamPerThread) return nullptr;
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &capturing) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (capturing != cudaStreamCaptureStatusNone) return nullptr;
   static std::mutex mu;
   static std::map<int, unsigned int*> base;                  // device -> pool address
   static std::map<std::pair<int, cudaStream_t>, int> slot;   // (device, stream) -> pair

@@ -339,3 +339,30 @@ def test_host_buffer_form_in_chunks(T, D, B, fmt):
         nts.check_status()
         assert torch.equal(ch, dev.codes.cpu()) and torch.equal(sh, dev.scales.cpu())
         ch.zero_()
+
+
+def test_graph_replays_alongside_direct_launches():
+    # launches recorded into a CUDA graph take tiles in the fixed order (a
+    # graph may be replayed on any stream); direct launches on other streams
+    # keep their own counters, so the two never share one
+    X1, _ = workloads.mx_inputs(6000, 2048, seed=980, device=DEV)
+    X2, _ = workloads.mx_inputs(7000, 2048, seed=981, device=DEV)
+    ref1 = nts.mxnorm_cast(X1, None, B=32, p=2)
+    ref2 = nts.mxnorm_cast(X2, None, B=32, p=2)
+    c1 = torch.empty_like(ref1.codes)
+    s1 = torch.empty_like(ref1.scales)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        nts.mxnorm_cast(X1, None, B=32, p=2, codes=c1, scales=s1)
+    side = torch.cuda.Stream()
+    outs = []
+    for _ in range(4):
+        graph.replay()
+        with torch.cuda.stream(side):
+            outs.append(nts.mxnorm_cast(X2, None, B=32, p=2, stream=side))
+    torch.cuda.synchronize()
+    nts.check_status()
+    assert torch.equal(c1, ref1.codes) and torch.equal(s1, ref1.scales)
+    for o in outs:
+        assert torch.equal(o.codes, ref2.codes) and torch.equal(o.scales, ref2.scales)
