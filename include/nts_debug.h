@@ -41,9 +41,9 @@ NTS_API int nts_debug_set_wait_limit_ns(uint64_t ns);
 NTS_API int nts_debug_set_schedule(int dynamic);
 
 /*
- * Decode-sized QK-RMSNorm launches (bf16 in and out, every tile in one wave
- * of single-tile clusters, no launch-shape override and no missing-bytes
- * hook): 1 (default) = the
+ * Decode-sized QK-RMSNorm and LayerNorm launches (bf16 output, every tile
+ * in one wave of single-tile clusters, no launch-shape override and no
+ * missing-bytes hook): 1 (default) = the
  * single-tile kernel without producer warp or ring; 0 = the persistent
  * kernel.  Results are identical either way.  Errors: INVALID_ARG for other
  * values.

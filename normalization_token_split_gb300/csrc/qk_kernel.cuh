@@ -607,7 +607,7 @@ static inline int read_and_clear_local_qk_status(unsigned* out) {
 }
 
 // The single-tile kernel for decode-sized launches (qk_direct.cu).
-QkKernel pick_qk_direct(int N, int vpt);
+QkKernel pick_qk_direct(int N, int vpt, int in_e4m3, int layernorm);
 
 // Defined by qk_bf16.cu, qk_e4m3.cu, qk_ln.cu and qk_mx_*.cu.
 QkKernel pick_qk_bf16(int N, int vpt);

@@ -116,11 +116,10 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
   // Decode-sized launches (every tile in one wave of single-tile clusters):
   // the kernel without producer, ring or mbarriers (qk_direct.cu).  It has
   // no waits, so the missing-bytes test hook keeps the persistent kernel.
-  if (tune.direct && !mx_out && !layernorm && !opt.in_e4m3 && rs.vpt <= 5 &&
-      tune.force_rows == 0 && tune.force_stages == 0 && tune.force_grid == 0 &&
-      tune.missing_tx == 0) {
-    QkKernel dk = pick_qk_direct(N, rs.vpt);
-    const size_t dsmem = (size_t)R * N * (rs.G / 32) * 4;
+  if (tune.direct && !mx_out && rs.vpt <= 5 && tune.force_rows == 0 &&
+      tune.force_stages == 0 && tune.force_grid == 0 && tune.missing_tx == 0) {
+    QkKernel dk = pick_qk_direct(N, rs.vpt, opt.in_e4m3, layernorm);
+    const size_t dsmem = (size_t)R * N * (rs.G / 32) * 4 * NS;
     cudaLaunchConfig_t dc = {};
     cudaLaunchAttribute da[1];
     da[0].id = cudaLaunchAttributeClusterDimension;
@@ -137,7 +136,7 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
     if (rc != NTS_OK) return rc;
     if (dk != nullptr && ntiles <= dmax) {
       dc.gridDim = dim3((unsigned)(ntiles * N));
-      log_launch("qknorm_rms", "direct: tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d clusters=%lld",
+      log_launch(layernorm ? "layernorm_split" : "qknorm_rms", "direct: tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d clusters=%lld",
                  ntensors, (long long)rq[0].T, (int)rq[0].H, N, rs.vpt, rs.G, R,
                  (long long)ntiles);
       const cudaError_t e = cudaLaunchKernelEx(&dc, dk, prm);

@@ -376,3 +376,24 @@ def test_decode_direct_kernel_equals_persistent(T, N):
     assert all(torch.equal(a, b) for a, b in zip(outs[0], outs[1]))
     Yo, ro, _ = oracle.qknorm_rms(workloads.bf16_bits(Q), gq.cpu().numpy(), 1e-6, N)
     check_qk(workloads.bf16_bits(outs[0][4]), outs[0][5].cpu().numpy(), Yo, ro, f"direct N={N}")
+
+
+@pytest.mark.parametrize("N", [1, 4])
+@pytest.mark.parametrize("T", [1, 64])
+def test_decode_direct_kernel_fp8_and_layernorm(T, N):
+    codes, scale, g8 = workloads.qk_inputs_fp8(T, 4096, seed=60 + T, device=DEV)
+    X, g = workloads.qk_inputs(T, 4096, seed=70 + T, device=DEV)
+    b = workloads.beta_vector(4096, seed=70 + T, device=DEV)
+    outs = []
+    try:
+        for direct in (True, False):
+            nts.set_direct(direct)
+            r8 = nts.qknorm_rms_fp8(codes, scale, g8, eps=1e-6, N=N, want_rinv=True)
+            ln = nts.layernorm_split(X, g, b, N=N, want_stats=True)
+            nts.check_status()
+            outs.append(r8 + ln)
+    finally:
+        nts.set_direct(True)
+    assert all(torch.equal(a, c) for a, c in zip(outs[0], outs[1]))
+    Yo, ro, _ = oracle.qknorm_rms_fp8(codes.cpu().numpy(), scale, g8.cpu().numpy(), 1e-6, N)
+    check_qk(workloads.bf16_bits(outs[0][0]), outs[0][1].cpu().numpy(), Yo, ro, f"fp8 direct N={N}")
