@@ -161,8 +161,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) heads_kernel(const HeadsParams
   int s = 0;
   uint32_t ph = 0;
   while (true) {
-    if (!mbar_wait_bounded(full0 + 8 * s, ph, p.wait_limit_ns)) {
-      atomicOr(&g_heads_status, kStatusTimeout);
+    // a warp leaves together: an expired wait on one lane ends all 32 (the
+    // shuffles and barriers below need the whole warp)
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(full0 + 8 * s, ph, p.wait_limit_ns))) {
+      if (lane == 0) atomicOr(&g_heads_status, kStatusTimeout);
       break;
     }
     const int64_t tile = *reinterpret_cast<volatile int64_t*>(tile_of + s);

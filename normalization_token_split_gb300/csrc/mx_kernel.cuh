@@ -211,8 +211,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
   int s = 0;          // ring stage of the j-th tile
   uint32_t ph = 0;    // (j / S) & 1
   for (int64_t j = 0;; ++j) {
-    if (!mbar_wait_bounded(sbase + L.full + 8 * s, ph, p.wait_limit_ns)) {
-      atomicOr(&g_mx_status, kStatusTimeout);
+    // a warp leaves together: an expired wait on one lane ends all 32 (the
+    // shuffles and barriers below need the whole warp)
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(sbase + L.full + 8 * s, ph, p.wait_limit_ns))) {
+      if (lane == 0) atomicOr(&g_mx_status, kStatusTimeout);
       break;
     }
     const int64_t tile = *reinterpret_cast<volatile int64_t*>(tile_of + s);

@@ -106,8 +106,8 @@ struct QkParams {
 //   full  [S], empty [S]          ring mbarriers
 //   gbar                          gamma-arrival mbarrier
 //   xbar  [2][R]                  exchange mbarriers (double-buffered by tile)
-//   tbar  [S]                     tile-number mbarriers (dynamic order, N > 1)
-//   tile  [S] i64                 tile number sent by the cluster's rank 0
+//   tbar  [S+1]                   tile-number mbarriers (dynamic order, N > 1)
+//   tile  [S+1] i64               tile numbers sent by the cluster's rank 0
 //   tloc  [S] i64                 tile in stage s for the consumers (-1: done)
 //   part  [2][R][N][WPR][NS] f32  partial sums received from every warp of
 //                                 every shard of a row (NS = 1 RMS, 2 LN)
@@ -126,8 +126,8 @@ __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int
   L.gbar = L.empty + (uint32_t)S * 8;
   L.xbar = L.gbar + 8;
   L.tbar = L.xbar + (uint32_t)2 * R * 8;
-  L.tile = L.tbar + (uint32_t)S * 8;
-  L.tloc = L.tile + (uint32_t)S * 8;
+  L.tile = L.tbar + (uint32_t)(S + 1) * 8;
+  L.tloc = L.tile + (uint32_t)(S + 1) * 8;
   L.part = L.tloc + (uint32_t)S * 8;
   L.total = L.part + (uint32_t)2 * R * N * (G / 32) * 4 * ns;
   return L;
@@ -186,12 +186,13 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
   int64_t* tloc = reinterpret_cast<int64_t*>(smem + L.tloc);
   // Tile order: the first S tiles of every cluster are fixed (cid + n * ncl,
   // no start-up latency); later ones come from the launch's counter, taken
-  // by the cluster's rank 0 and sent to every CTA of the cluster.  Rank 0
-  // then hands a stage back only after the tile's combine, which every
-  // peer's producer has passed, so a tile number is never overwritten
-  // before it is read.
+  // by the cluster's rank 0 and sent to every CTA of the cluster through a
+  // ring of S + 1 slots.  Rank 0 writes the number of tile q only after its
+  // consumers have finished tile q - S - 1 (they released the stage of
+  // tile q - S, which they start only after tile q - S - 1's combine), and
+  // that combine needed every peer's partial sums of the tile, so every peer
+  // has read the number that the slot held.
   const bool dyn = p.sched != nullptr;
-  const bool hold = dyn && N > 1 && rank == 0;
 
   if (tid == 0) {
     for (int s = 0; s < p.S; ++s) {
@@ -199,6 +200,7 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
       mbar_init(sbase + L.empty + 8 * s, nconsumer / 32);
       mbar_init(sbase + L.tbar + 8 * s, 1);
     }
+    mbar_init(sbase + L.tbar + 8 * p.S, 1);
     for (int b = 0; b < 2 * p.R; ++b) mbar_init(sbase + L.xbar + 8 * b, 1);
     mbar_init(sbase + L.gbar, 1);
     fence_mbar_init();
@@ -228,7 +230,9 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
       // incrementally (no 64-bit division in the loop)
       int s = 0;
       uint32_t ph = 0;
-      int64_t n = 0;  // tiles issued
+      int64_t n = 0;      // tiles issued
+      int kd = 0;         // tile-number slot of the next dynamic tile
+      uint32_t pd = 0;    // its pass parity over the S + 1 slots
       while (true) {
         if (n >= p.S && !mbar_wait_bounded(sbase + L.empty + 8 * s, ph ^ 1u, p.wait_limit_ns)) {
           atomicOr(&g_qk_status, kStatusTimeout);
@@ -241,22 +245,29 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
         } else if (N == 1) {
           tile = ncl * p.S + (int64_t)atomicAdd(p.sched, 1u);
         } else {
-          const uint32_t tb = sbase + L.tbar + 8 * s;
+          const uint32_t tb = sbase + L.tbar + 8 * kd;
           if (rank == 0) {
+            // Every CTA of the cluster runs, its barriers initialised: this
+            // is pass S or later, so the consumers released stage 0, which
+            // they do only after the cluster start-up wait.
             const int64_t tk = ncl * p.S + (int64_t)atomicAdd(p.sched, 1u);
             const int64_t v = tk < p.ntiles ? tk : -1;
-            const uint32_t slot = sbase + L.tile + 8 * s;
+            const uint32_t slot = sbase + L.tile + 8 * kd;
 #pragma unroll
             for (int k = 0; k < N; ++k)
               st_async_u64(map_to_rank(slot, k), (uint64_t)v, map_to_rank(tb, k));
           }
           mbar_arrive_expect_tx(tb, 8);
-          if (!mbar_wait_bounded(tb, ph ^ 1u, p.wait_limit_ns)) {
+          if (!mbar_wait_bounded(tb, pd, p.wait_limit_ns)) {
             atomicOr(&g_qk_status, kStatusTimeout);
             aborted = true;
             break;
           }
-          tile = *reinterpret_cast<volatile int64_t*>(smem + L.tile + 8 * s);
+          tile = *reinterpret_cast<volatile int64_t*>(smem + L.tile + 8 * kd);
+          if (++kd == p.S + 1) {
+            kd = 0;
+            pd ^= 1u;
+          }
         }
         const uint32_t bar = sbase + L.full + 8 * s;
         if (tile < 0 || tile >= p.ntiles) {
@@ -306,8 +317,8 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
     // ------------------------------------------------------- consumer warps
     // Every CTA of the cluster must be running, with its barriers
     // initialised, before anyone stores into a peer's shared memory: arrive
-    // now, wait just before the first exchange (the first tile's loads and
-    // Phase A overlap the start-up).
+    // now, wait after the first tile's Phase A (its loads and Phase A
+    // overlap the start-up).
     if (N > 1) cluster_arrive_release();
     bool started = (N == 1);
     bool have_gamma = false;
@@ -320,8 +331,10 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
     int s = 0;          // ring stage of the j-th tile
     uint32_t ph = 0;    // (j / S) & 1
     for (int64_t j = 0;; ++j) {
-      if (!mbar_wait_bounded(sbase + L.full + 8 * s, ph, p.wait_limit_ns)) {
-        atomicOr(&g_qk_status, kStatusTimeout);
+      // a warp leaves together: an expired wait on one lane ends all 32 (the
+      // shuffles and barriers below need the whole warp)
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(sbase + L.full + 8 * s, ph, p.wait_limit_ns))) {
+        if (lane == 0) atomicOr(&g_qk_status, kStatusTimeout);
         break;
       }
       const int64_t tile = *reinterpret_cast<volatile int64_t*>(tloc + s);
@@ -351,10 +364,16 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
           sum2[1] = f2_add(sum2[1], f2_add(w[i][2], w[i][3]));
         }
       }
+      // The cluster start-up wait comes before the stage goes back: rank 0's
+      // producer sends tile numbers into the peers' shared memory only once
+      // stage 0 is back (pass S and later), so they are running by then.
+      if (!started) {
+        cluster_wait_acquire();
+        started = true;
+      }
       // the stage's data is in registers: hand it back to the producer
-      // (rank 0 under the dynamic order: after the combine, see above)
       __syncwarp();
-      if (!hold && lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
+      if (lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
       const uint64_t a01 = f2_add(acc[0], acc[1]), a23 = f2_add(acc[2], acc[3]);
       const uint64_t a = f2_add(a01, a23);
       const float ss = warp_sum(f2_lo(a) + f2_hi(a));
@@ -368,10 +387,6 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
       const int b = (int)(j & 1);
       const uint32_t xbar = sbase + L.xbar + 8 * (b * p.R + row);
       const uint32_t slot0 = sbase + L.part + 4 * NS * (uint32_t)((b * p.R + row) * N * wpr);
-      if (!started) {
-        cluster_wait_acquire();
-        started = true;
-      }
       if (exchange) {
         if (g == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(N * wpr * 4 * NS));
         if (lane == 0) {
@@ -546,10 +561,6 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
         }
         if (tn.rinv_out != nullptr && rank == 0 && g == 0) tn.rinv_out[t] = rinv;
         if (STAT == kQkLn && tn.mean_out != nullptr && rank == 0 && g == 0) tn.mean_out[t] = mu;
-      }
-      if (hold) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
       }
       if (aborted) break;
       if (++s == p.S) {
