@@ -193,10 +193,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) heads_kernel(const HeadsParams
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
 
-    // each head's sum over its hv lanes (segmented butterfly, all lanes)
+    // each head's sum over its hv lanes (segmented butterfly, all lanes;
+    // unrolled, each step guarded by the warp-uniform head size)
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
-      for (int o = 1; o < p.hv; o <<= 1) ss[i] += __shfl_xor_sync(0xFFFFFFFFu, ss[i], o);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1)
+        if (o < p.hv) ss[i] += __shfl_xor_sync(0xFFFFFFFFu, ss[i], o);
 
     if (valid) {
       __nv_bfloat16* yrow = p.Y + (size_t)t * p.H;

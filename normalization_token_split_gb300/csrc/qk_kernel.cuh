@@ -449,7 +449,11 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             m = fmaxf(m, fmaxf(fabsf(f2_lo(w[i][q])), fabsf(f2_hi(w[i][q]))));
-          for (int o = 1; o < p.bv; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+          // bv = B/8 is 2, 4 or 8: at most three steps, unrolled and guarded
+          // by the (warp-uniform) block size
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1)
+            if (o < p.bv) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
           am[i] = m;
         }
       }
@@ -484,13 +488,22 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
         const uint64_t rr = f2(rinv, rinv);
         const float nmr = -mu * rinv;
         __nv_bfloat16* yrow = tn.Y + (size_t)t * tn.H + (size_t)rank * tn.W;
+        // block-cast output: this shard's codes and scales of row t
+        uint8_t* crow = nullptr;
+        uint8_t* srow_sc = nullptr;
+        int vshift = 0;   // vector -> block: v >> vshift
+        if (OUT != kOutBf16) {
+          const size_t first = (size_t)t * tn.H + (size_t)rank * tn.W;  // element index
+          crow = OUT == kOutE4M3 ? tn.codes + first : tn.codes + first / 2;
+          srow_sc = tn.scales + (first >> p.bshift);
+          vshift = p.bshift - 3;
+        }
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
           const int v = i * p.G + g;
           if (OUT != kOutBf16) {
             if (v < nvec) {
               // scale of this vector's block, then its eight codes
-              const int64_t col = (int64_t)rank * tn.W + 8 * v;
               float is;
               uint32_t keep = ~0u, sbyte;
               if (OUT == kOutNvfp4) {
@@ -501,8 +514,7 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
                 is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
                 sbyte = (uint32_t)(e + 127);
               }
-              if ((g & (p.bv - 1)) == 0)
-                tn.scales[((size_t)t * tn.H + col) >> p.bshift] = (uint8_t)sbyte;
+              if ((g & (p.bv - 1)) == 0) srow_sc[v >> vshift] = (uint8_t)sbyte;
               const uint64_t ss = f2(is, is);
               uint64_t q[4];
 #pragma unroll
@@ -510,11 +522,11 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
               if (OUT == kOutE4M3) {
                 const uint32_t lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
                 const uint32_t hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
-                st_global_v2(tn.codes + (size_t)t * tn.H + col, lo, hi);
+                st_global_v2(crow + 8 * v, lo, hi);
               } else {
                 const uint32_t c = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]),
                                               f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
-                st_global_u32(tn.codes + ((size_t)t * tn.H + col) / 2, c & keep);
+                st_global_u32(crow + 4 * v, c & keep);
               }
             }
             continue;
