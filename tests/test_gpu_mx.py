@@ -366,3 +366,24 @@ def test_graph_replays_alongside_direct_launches():
     assert torch.equal(c1, ref1.codes) and torch.equal(s1, ref1.scales)
     for o in outs:
         assert torch.equal(o.codes, ref2.codes) and torch.equal(o.scales, ref2.scales)
+
+
+def test_boundary_exception_counts_are_a_handful(capsys):
+    # The double-precision definition and the kernel's fp32 decisions may
+    # differ only where a value sits within 1e-6 of a rounding boundary;
+    # count those exceptions over every row of the 65536 x 4096 config.
+    X, _ = workloads.mx_inputs(65536, 4096, seed=4000 + 65536, device=DEV)
+    report = {}
+    for kind, p in KINDS:
+        totals = {"scale_boundary_exceptions": 0, "code_boundary_exceptions": 0}
+        for r0 in range(0, 65536, 8192):
+            rows = torch.arange(r0, r0 + 8192, device=DEV)
+            st = compare(kind, X, None, 1e-6, 32, "e4m3", p, rows=rows, what=f"{kind}{p}")
+            for k in totals:
+                totals[k] += st[k]
+        report[f"{kind}{p}"] = totals
+        blocks = 65536 * 128
+        assert totals["scale_boundary_exceptions"] <= blocks * 1e-4
+        assert totals["code_boundary_exceptions"] <= blocks * 32 * 1e-5
+    with capsys.disabled():
+        print("\nMX boundary exceptions over 65536 x 4096 (B=32, E4M3):", report)
