@@ -141,9 +141,9 @@ NTS_API int nts_qknorm_rms_heads(const void *X_dev, const float *gamma_dev, void
  *     mu    = (s1_0 + ... + s1_{N-1}) / H
  *     var   = max((s2_0 + ... + s2_{N-1}) / H - mu^2, 0)
  *     rstd  = 1 / sqrt(var + eps)
- *     y_j   = bf16_rne((x_j * gamma_j) * rstd + (beta_j - mu * rstd * gamma_j))
+ *     y_j   = bf16_rne((x_j * rstd - mu * rstd) * gamma_j + beta_j)
  *
- * which is (x_j - mu) * rstd * gamma_j + beta_j.  The one-pass variance
+ * which is (x_j - mu) * rstd * gamma_j + beta_j (fp32 fused multiply-adds).  The one-pass variance
  * loses relative accuracy when |mu| is large against the spread of the row
  * (fp32 cancellation in s2/H - mu^2); the pages' formulation is kept.
  *   X_dev      bf16 [T, H], read.     gamma_dev  fp32 [H], read.

@@ -121,9 +121,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qk_direct_kernel(const QkParam
     s1 = warp_sum(f2_lo(c) + f2_hi(c));
   }
 
-  // Phase B: w = x * gamma
+  // Phase B: w = x * gamma (RMSNorm; LayerNorm multiplies after centring)
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
+  for (int i = 0; i < VPT && STAT != kQkLn; ++i) {
     w[i][0] = f2_mul(w[i][0], f2(g0[i].x, g0[i].y));
     w[i][1] = f2_mul(w[i][1], f2(g0[i].z, g0[i].w));
     w[i][2] = f2_mul(w[i][2], f2(g1[i].x, g1[i].y));
@@ -186,15 +186,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qk_direct_kernel(const QkParam
             b0 = __ldg(reinterpret_cast<const float4*>(brow + v * 8));
             b1 = __ldg(reinterpret_cast<const float4*>(brow + v * 8) + 1);
           }
+          // y = (x rinv - mu rinv) gamma + beta  (w still holds x)
           const uint64_t m2 = f2(nmr, nmr);
-          const uint64_t c0 = f2_fma(m2, f2(g0[i].x, g0[i].y), f2(b0.x, b0.y));
-          const uint64_t c1 = f2_fma(m2, f2(g0[i].z, g0[i].w), f2(b0.z, b0.w));
-          const uint64_t c2 = f2_fma(m2, f2(g1[i].x, g1[i].y), f2(b1.x, b1.y));
-          const uint64_t c3 = f2_fma(m2, f2(g1[i].z, g1[i].w), f2(b1.z, b1.w));
-          y0 = f2_fma(w[i][0], rr, c0);
-          y1 = f2_fma(w[i][1], rr, c1);
-          y2 = f2_fma(w[i][2], rr, c2);
-          y3 = f2_fma(w[i][3], rr, c3);
+          y0 = f2_fma(f2_fma(w[i][0], rr, m2), f2(g0[i].x, g0[i].y), f2(b0.x, b0.y));
+          y1 = f2_fma(f2_fma(w[i][1], rr, m2), f2(g0[i].z, g0[i].w), f2(b0.z, b0.w));
+          y2 = f2_fma(f2_fma(w[i][2], rr, m2), f2(g1[i].x, g1[i].y), f2(b1.x, b1.y));
+          y3 = f2_fma(f2_fma(w[i][3], rr, m2), f2(g1[i].z, g1[i].w), f2(b1.z, b1.w));
         } else {
           y0 = f2_mul(w[i][0], rr);
           y1 = f2_mul(w[i][1], rr);

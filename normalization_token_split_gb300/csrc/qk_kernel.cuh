@@ -105,6 +105,7 @@ struct QkParams {
 //         shards are too wide for both copies, gam holds them as copied
 //   full  [S], empty [S]          ring mbarriers
 //   gbar                          gamma-arrival mbarrier
+//   gsync                         consumers' mbarrier after the gamma relayout
 //   xbar  [2][R]                  exchange mbarriers (double-buffered by tile)
 //   tbar  [S+1]                   tile-number mbarriers (dynamic order, N > 1)
 //   tile  [S+1] i64               tile numbers sent by the cluster's rank 0
@@ -124,7 +125,7 @@ __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int
   L.full = L.gam + (uint32_t)Wsum * 4;
   L.empty = L.full + (uint32_t)S * 8;
   L.gbar = L.empty + (uint32_t)S * 8;
-  L.xbar = L.gbar + 8;
+  L.xbar = L.gbar + 16;   // gbar, then gsync
   L.tbar = L.xbar + (uint32_t)2 * R * 8;
   L.tile = L.tbar + (uint32_t)(S + 1) * 8;
   L.tloc = L.tile + (uint32_t)(S + 1) * 8;
@@ -203,6 +204,7 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
     mbar_init(sbase + L.tbar + 8 * p.S, 1);
     for (int b = 0; b < 2 * p.R; ++b) mbar_init(sbase + L.xbar + 8 * b, 1);
     mbar_init(sbase + L.gbar, 1);
+    mbar_init(sbase + L.gbar + 8, nconsumer / 32);   // gsync
     fence_mbar_init();
   }
   __syncthreads();
@@ -402,6 +404,7 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
       }
 
       // ---- Phase B (overlapping the exchange): w = x * gamma, in place
+      // (RMSNorm; LayerNorm multiplies by gamma after centring, Phase C)
       if (!have_gamma) {
         // once: wait for the copied gamma and split it into the layout the
         // loop reads (consecutive lanes, consecutive 16 bytes)
@@ -421,7 +424,14 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
             }
           }
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(nconsumer) : "memory");
+        // every consumer warp's share is written (a bounded wait, unlike a
+        // named barrier: a warp that left on an expired wait cannot hang it)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sbase + L.gbar + 8);
+        if (!mbar_wait_bounded(sbase + L.gbar + 8, 0, aborted ? 0 : p.wait_limit_ns)) {
+          if (!aborted) atomicOr(&g_qk_status, kStatusTimeout);
+          aborted = true;
+        }
         have_gamma = true;
       }
       // split layout: halves nvec*16 bytes apart, vectors 16 apart; as
@@ -430,7 +440,7 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
       const unsigned char* gam_hi = gam_lo + (p.gsplit ? (uint32_t)nvec * 16 : 16u);
       const uint32_t gstride = p.gsplit ? 16u : 32u;
 #pragma unroll
-      for (int i = 0; i < VPT; ++i) {
+      for (int i = 0; i < VPT && STAT != kQkLn; ++i) {
         const int v = min(i * p.G + g, nvec - 1);
         const uint4 glo = lds128(gam_lo + v * gstride);
         const uint4 ghi = lds128(gam_hi + v * gstride);
@@ -535,7 +545,7 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
             uint4 o;
             uint64_t y0, y1, y2, y3;
             if (STAT == kQkLn) {
-              // y = (x - mu) rinv gamma + beta = w rinv + (beta - mu rinv gamma)
+              // y = (x rinv - mu rinv) gamma + beta  (w still holds x)
               const uint4 glo = lds128(gam_lo + v * gstride);
               const uint4 ghi = lds128(gam_hi + v * gstride);
               uint4 blo = make_uint4(0, 0, 0, 0), bhi = make_uint4(0, 0, 0, 0);
@@ -546,18 +556,14 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
                 bhi = lds128(bet_hi + v * gstride);
               }
               const uint64_t m2 = f2(nmr, nmr);
-              const uint64_t c0 = f2_fma(m2, f2(__uint_as_float(glo.x), __uint_as_float(glo.y)),
-                                         f2(__uint_as_float(blo.x), __uint_as_float(blo.y)));
-              const uint64_t c1 = f2_fma(m2, f2(__uint_as_float(glo.z), __uint_as_float(glo.w)),
-                                         f2(__uint_as_float(blo.z), __uint_as_float(blo.w)));
-              const uint64_t c2 = f2_fma(m2, f2(__uint_as_float(ghi.x), __uint_as_float(ghi.y)),
-                                         f2(__uint_as_float(bhi.x), __uint_as_float(bhi.y)));
-              const uint64_t c3 = f2_fma(m2, f2(__uint_as_float(ghi.z), __uint_as_float(ghi.w)),
-                                         f2(__uint_as_float(bhi.z), __uint_as_float(bhi.w)));
-              y0 = f2_fma(w[i][0], rr, c0);
-              y1 = f2_fma(w[i][1], rr, c1);
-              y2 = f2_fma(w[i][2], rr, c2);
-              y3 = f2_fma(w[i][3], rr, c3);
+              y0 = f2_fma(f2_fma(w[i][0], rr, m2), f2(__uint_as_float(glo.x), __uint_as_float(glo.y)),
+                          f2(__uint_as_float(blo.x), __uint_as_float(blo.y)));
+              y1 = f2_fma(f2_fma(w[i][1], rr, m2), f2(__uint_as_float(glo.z), __uint_as_float(glo.w)),
+                          f2(__uint_as_float(blo.z), __uint_as_float(blo.w)));
+              y2 = f2_fma(f2_fma(w[i][2], rr, m2), f2(__uint_as_float(ghi.x), __uint_as_float(ghi.y)),
+                          f2(__uint_as_float(bhi.x), __uint_as_float(bhi.y)));
+              y3 = f2_fma(f2_fma(w[i][3], rr, m2), f2(__uint_as_float(ghi.z), __uint_as_float(ghi.w)),
+                          f2(__uint_as_float(bhi.z), __uint_as_float(bhi.w)));
             } else {
               y0 = f2_mul(w[i][0], rr);
               y1 = f2_mul(w[i][1], rr);
