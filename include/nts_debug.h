@@ -59,6 +59,22 @@ NTS_API int nts_debug_set_direct(int on);
  */
 NTS_API int nts_debug_set_missing_tx(uint32_t bytes);
 
+/*
+ * Self-check of the NVFP4 block scale (E4M3 code of fp32(amax/6), RNE,
+ * saturating, and the fp32 reciprocal of its value) as the kernels form it:
+ * the division by 6 by one multiply and two fmas (Brisebarre, Muller and
+ * Raina, IEEE Trans. Computers 53(8), 2004) and the reciprocal from a
+ * table.  Runs every non-negative fp32 absmax, 0 to +inf, on the current
+ * device, blocking until done (a few ms), and returns
+ *   *code_mismatches      absmaxes whose code or reciprocal differ from the
+ *                         ones taken through the IEEE quotient and the IEEE
+ *                         reciprocal (0 when the kernels are right);
+ *   *quotient_mismatches  absmaxes with a normal quotient (>= 2^-126) where
+ *                         the division differs from the IEEE quotient.
+ * Errors: INVALID_ARG for NULL outputs, CUDA for a failed launch or copy.
+ */
+NTS_API int nts_debug_check_nvfp4_scale(uint64_t* code_mismatches, uint64_t* quotient_mismatches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -75,10 +75,11 @@ enum { kStatRms = 0, kStatMxP1 = 1, kStatMxP2 = 2 };
 //   red[2][R][WPR] f32
 // tile[s] is the tile the producer put in stage s, or -1: no more tiles.
 struct MxLayout {
-  uint32_t ring, full, empty, tile, rbar, red, total;
+  uint32_t ring, full, empty, tile, rbar, red, rcp, total;
 };
 
-__host__ __device__ inline MxLayout mx_layout(int S, int R, int D, int G) {
+// rcp: the NVFP4 scale reciprocals (128 floats; empty for the E8M0 formats).
+__host__ __device__ inline MxLayout mx_layout(int S, int R, int D, int G, bool nvfp4) {
   MxLayout L;
   L.ring = 0;
   L.full = L.ring + (uint32_t)S * R * D * 2;
@@ -86,7 +87,8 @@ __host__ __device__ inline MxLayout mx_layout(int S, int R, int D, int G) {
   L.tile = L.empty + (uint32_t)S * 8;
   L.rbar = L.tile + (uint32_t)S * 8;
   L.red = L.rbar + (uint32_t)2 * R * 8;
-  L.total = L.red + (uint32_t)2 * R * (G / 32) * 4;
+  L.rcp = L.red + (uint32_t)2 * R * (G / 32) * 4;
+  L.total = L.rcp + (nvfp4 ? 128u * 4u : 0u);
   return L;
 }
 
@@ -130,7 +132,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
   const int lane = tid & 31;
   const int nconsumer = p.R * p.G;
   const int wpr = p.G >> 5;
-  const MxLayout L = mx_layout(p.S, p.R, p.D, p.G);
+  const MxLayout L = mx_layout(p.S, p.R, p.D, p.G, FMT == NTS_FMT_NVFP4);
   const uint32_t sbase = smem_addr(smem);
   const uint32_t stage_bytes = (uint32_t)p.R * p.D * 2;
   const int64_t cta = blockIdx.x, ncta = gridDim.x;
@@ -144,6 +146,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
     for (int b = 0; b < 2 * p.R; ++b) mbar_init(sbase + L.rbar + 8 * b, wpr);
     fence_mbar_init();
   }
+  float* rcp = reinterpret_cast<float*>(smem + L.rcp);
+  if (FMT == NTS_FMT_NVFP4) fill_e4m3_reciprocals(rcp, tid, (int)blockDim.x);
   __syncthreads();
 
   if (tid >= nconsumer) {
@@ -323,7 +327,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
           float is;                 // multiplier taking w*rinv to the element grid
           uint32_t keep = ~0u;      // NVFP4: 0 for a block whose scale is zero
           if (FMT == NTS_FMT_NVFP4) {
-            const uint32_t sc = nvfp4_scale(am[i] * rinv, &is);
+            const uint32_t sc = nvfp4_scale(am[i] * rinv, rcp, &is);
             keep = sc != 0 ? ~0u : 0u;
             p.scales[(size_t)t * p.K + b] = (uint8_t)sc;
           } else {

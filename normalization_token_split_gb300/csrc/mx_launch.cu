@@ -64,10 +64,11 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   // with two stages and three CTAs per SM than with three and two).
   const int stage = R * D * 2;
   int S = stage > 24576 ? 2 : (stage >= 12288 ? 3 : 4);
-  while (S > 2 && mx_layout(S, R, D, sh.G).total > (uint32_t)tune.smem_budget) --S;
-  while (S > 1 && mx_layout(S, R, D, sh.G).total > (uint32_t)dev.max_smem_optin) --S;
+  const bool nvfp4 = rq.fmt == NTS_FMT_NVFP4;
+  while (S > 2 && mx_layout(S, R, D, sh.G, nvfp4).total > (uint32_t)tune.smem_budget) --S;
+  while (S > 1 && mx_layout(S, R, D, sh.G, nvfp4).total > (uint32_t)dev.max_smem_optin) --S;
   if (tune.force_stages > 0) S = tune.force_stages;
-  const size_t smem = mx_layout(S, R, D, sh.G).total;
+  const size_t smem = mx_layout(S, R, D, sh.G, nvfp4).total;
   if (smem > (size_t)dev.max_smem_optin)
     return fail(NTS_ERR_UNSUPPORTED, "row too wide for shared memory: D = %d", D);
 

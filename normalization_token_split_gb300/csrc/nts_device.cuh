@@ -354,13 +354,39 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// NVFP4 block scale of a block whose normalized absmax is `ay` (>= 0): the
-// E4M3 code of fp32(ay / 6) (RNE, saturating at 448; 6 is the largest E2M1
-// magnitude) and, in *inv, the fp32 reciprocal of that code's value (0 for
-// a zero scale).
-__device__ __forceinline__ uint32_t nvfp4_scale(float ay, float* inv) {
-  const uint32_t sc = cvt_e4m3x2(__fdiv_rn(ay, 6.0f), 0.f) & 0xFFu;
-  *inv = sc != 0 ? __frcp_rn(f2_lo(e4m3x2_to_f2((uint16_t)sc))) : 0.f;
+// fp32(a / 6) for a >= 0 by one multiply and two fmas instead of a division
+// (Brisebarre, Muller and Raina, "Accelerating correctly rounded
+// floating-point division when the divisor is known in advance", IEEE Trans.
+// Computers 53(8), 2004): q = fl(a z) with z = fl(1/6), the remainder a - 6q
+// (exact in one fma), then fl(q + r z).  For every finite a >= 0 whose
+// quotient is a normal fp32 this is the IEEE quotient (checked for all such
+// a); a quotient below 2^-126 may be an ulp off.
+__device__ __forceinline__ float div6_rn(float a) {
+  const float z = 0x1.555556p-3f;
+  const float q = __fmul_rn(a, z);
+  const float r = __fmaf_rn(-q, 6.0f, a);
+  return __fmaf_rn(r, z, q);
+}
+
+// Reciprocals of the E4M3 scale values, for a shared-memory table that the
+// threads of a CTA fill before its first nvfp4_scale: rcp[c] = fp32(1 /
+// value of code c) for c = 1..126 and 0 for the zero code and the NaN code
+// 127.
+__device__ __forceinline__ void fill_e4m3_reciprocals(float* rcp, int tid, int nthreads) {
+  for (int c = tid; c < 128; c += nthreads)
+    rcp[c] = (c == 0 || c == 127) ? 0.f : __frcp_rn(f2_lo(e4m3x2_to_f2((uint16_t)c)));
+}
+
+// NVFP4 block scale of a block whose normalized absmax is `ay` (>= 0, not
+// NaN): the E4M3 code of fp32(ay / 6) (RNE, saturating at 448; 6 is the
+// largest E2M1 magnitude) and, in *inv, the fp32 reciprocal of that code's
+// value (0 for a zero scale), read from the table above.  The code equals
+// that of the IEEE quotient for every such ay: quotients below 2^-126 give
+// code 0 either way, and ay is clamped at 2^32, whose quotient already
+// saturates.
+__device__ __forceinline__ uint32_t nvfp4_scale(float ay, const float* rcp, float* inv) {
+  const uint32_t sc = cvt_e4m3x2(div6_rn(fminf(ay, 0x1p32f)), 0.f) & 0xFFu;
+  *inv = rcp[sc];
   return sc;
 }
 

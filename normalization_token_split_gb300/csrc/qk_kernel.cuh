@@ -113,11 +113,12 @@ struct QkParams {
 //   part  [2][R][N][WPR][NS] f32  partial sums received from every warp of
 //                                 every shard of a row (NS = 1 RMS, 2 LN)
 struct QkLayout {
-  uint32_t ring, gstg, gam, full, empty, gbar, xbar, tbar, tile, tloc, part, total;
+  uint32_t ring, gstg, gam, full, empty, gbar, xbar, tbar, tile, tloc, part, rcp, total;
 };
 
+// rcp: the NVFP4 scale reciprocals (128 floats; empty for other outputs).
 __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int Wsum, int G,
-                                              int gsplit, int esize, int ns) {
+                                              int gsplit, int esize, int ns, bool nvfp4) {
   QkLayout L;
   L.ring = 0;
   L.gstg = L.ring + (uint32_t)S * R * Wmax * esize;
@@ -130,7 +131,8 @@ __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int
   L.tile = L.tbar + (uint32_t)(S + 1) * 8;
   L.tloc = L.tile + (uint32_t)(S + 1) * 8;
   L.part = L.tloc + (uint32_t)S * 8;
-  L.total = L.part + (uint32_t)2 * R * N * (G / 32) * 4 * ns;
+  L.rcp = L.part + (uint32_t)2 * R * N * (G / 32) * 4 * ns;
+  L.total = L.rcp + (nvfp4 ? 128u * 4u : 0u);
   return L;
 }
 
@@ -181,7 +183,8 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
   const int nconsumer = p.R * p.G;
   const int lane = tid & 31;
   const int wpr = p.G >> 5;
-  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, p.psum, p.G, p.gsplit, ES, NS);
+  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, p.psum, p.G, p.gsplit, ES, NS,
+                               OUT == kOutNvfp4);
   const uint32_t sbase = smem_addr(smem);
   const uint32_t stage_bytes = (uint32_t)p.R * p.Wmax * ES;
   int64_t* tloc = reinterpret_cast<int64_t*>(smem + L.tloc);
@@ -207,6 +210,8 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
     mbar_init(sbase + L.gbar + 8, nconsumer / 32);   // gsync
     fence_mbar_init();
   }
+  float* rcp = reinterpret_cast<float*>(smem + L.rcp);
+  if (OUT == kOutNvfp4) fill_e4m3_reciprocals(rcp, tid, (int)blockDim.x);
   __syncthreads();
 
   if (tid >= nconsumer) {
@@ -517,7 +522,7 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
               float is;
               uint32_t keep = ~0u, sbyte;
               if (OUT == kOutNvfp4) {
-                sbyte = nvfp4_scale(am[i] * rinv, &is);
+                sbyte = nvfp4_scale(am[i] * rinv, rcp, &is);
                 keep = sbyte != 0 ? ~0u : 0u;
               } else {
                 const int e = e8m0_exponent(am[i] * rinv, OUT == kOutE4M3 ? 8 : 2);

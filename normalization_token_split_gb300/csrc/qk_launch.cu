@@ -47,7 +47,10 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
   // gamma is split into the conflict-free layout when both copies fit.
   int gsplit = 1;
   int S = 4;
-  auto layout = [&](int s, int split) { return qk_layout(N, s, R, Wmax, psum, rs.G, split, ES, NS); };
+  const bool nvfp4 = mx_out && opt.out_fmt == NTS_FMT_NVFP4;
+  auto layout = [&](int s, int split) {
+    return qk_layout(N, s, R, Wmax, psum, rs.G, split, ES, NS, nvfp4);
+  };
   while (S > 2 && layout(S, 1).total > (uint32_t)tune.smem_budget) --S;
   if (layout(S, 1).total > (uint32_t)dev.max_smem_optin) gsplit = 0;
   while (S > 1 && layout(S, gsplit).total > (uint32_t)dev.max_smem_optin) --S;

@@ -340,5 +340,14 @@ def set_direct(on: bool) -> None:
     check(lib().nts_debug_set_direct(1 if on else 0))
 
 
+def check_nvfp4_scale() -> tuple:
+    """(code mismatches, quotient mismatches) of the kernels' NVFP4 block
+    scale against the IEEE-division route over every non-negative fp32
+    absmax (nts_debug_check_nvfp4_scale); runs on the current device."""
+    a, b = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    check(lib().nts_debug_check_nvfp4_scale(ctypes.byref(a), ctypes.byref(b)))
+    return int(a.value), int(b.value)
+
+
 def set_missing_tx(nbytes: int) -> None:
     check(lib().nts_debug_set_missing_tx(int(nbytes)))

@@ -280,6 +280,16 @@ def test_nvfp4_rejects_other_blocks_and_post_round():
         nts.mxnorm_postround_cast(X, None, B=16, fmt="nvfp4")
 
 
+def test_nvfp4_scale_without_division_matches_ieee_route():
+    # Every non-negative fp32 absmax, 0 to +inf, on the device: the kernels'
+    # scale code and reciprocal (division by 6 without a divide, reciprocal
+    # from a table) equal those through the IEEE quotient and reciprocal, and
+    # the division is the IEEE quotient wherever that quotient is normal.
+    code_bad, quot_bad = nts.check_nvfp4_scale()
+    assert code_bad == 0, f"{code_bad} absmaxes with another scale or reciprocal"
+    assert quot_bad == 0, f"{quot_bad} normal quotients differ from IEEE division"
+
+
 # ------------------------------------------------------------ tile order
 
 def test_dynamic_and_round_robin_tile_orders_agree():
