@@ -8,13 +8,18 @@
 // The last CTA of a launch to finish puts both back to zero, so a pair is
 // ready again for the next launch on the same stream without any host work.
 //
-// The pairs live in a fixed device array (no allocation); each CUDA stream
+// The pairs live in a fixed device array (no allocation).  Each CUDA stream
 // gets its own pair on first use, so launches on different streams, which
-// may overlap, never share one.  The round-robin order (a null pointer) is
-// kept where a stream handle does not identify one ordered stream of work:
-// launches recorded into a CUDA graph (a graph may be replayed on any
-// stream, alongside direct launches), the per-thread default stream (one
-// handle for every host thread's stream), and a used-up pool.
+// may overlap, never share one.  A launch recorded into a CUDA graph gets a
+// pair of its own, kept for the life of the process: a graph may be replayed
+// on any stream, alongside direct launches, but the launches of one
+// instantiated graph are ordered behind each other, so that launch never
+// runs twice at once -- as long as the graph is not instantiated twice with
+// both instances running at the same time, the one case that needs the
+// round-robin order (nts_debug_set_schedule(0)) around its capture.  The
+// round-robin order (a null pointer) is also kept for the per-thread
+// default stream (one handle for every host thread's stream) and once the
+// pool is used up.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -27,7 +32,7 @@ namespace nts {
 
 namespace {
 
-constexpr int kSchedSlots = 4096;
+constexpr int kSchedSlots = 1 << 16;   // 512 KB of device memory
 
 __device__ __align__(256) unsigned int g_sched_pool[kSchedSlots][2];
 
@@ -40,7 +45,7 @@ unsigned int* sched_counters(cudaStream_t stream) {
     (void)cudaGetLastError();
     return nullptr;
   }
-  if (capturing != cudaStreamCaptureStatusNone) return nullptr;
+  if (capturing == cudaStreamCaptureStatusInvalidated) return nullptr;
   static std::mutex mu;
   static std::map<int, unsigned int*> base;                  // device -> pool address
   static std::map<std::pair<int, cudaStream_t>, int> slot;   // (device, stream) -> pair
@@ -57,10 +62,15 @@ unsigned int* sched_counters(cudaStream_t stream) {
     }
     b = base.emplace(dev, static_cast<unsigned int*>(p)).first;
   }
+  int& n = used[dev];
+  if (capturing == cudaStreamCaptureStatusActive) {
+    // a recorded launch: a pair for it alone
+    if (n >= kSchedSlots) return nullptr;
+    return b->second + 2 * n++;
+  }
   const auto key = std::make_pair(dev, stream);
   auto it = slot.find(key);
   if (it == slot.end()) {
-    int& n = used[dev];
     if (n >= kSchedSlots) return nullptr;
     it = slot.emplace(key, n++).first;
   }

@@ -352,30 +352,69 @@ def test_host_buffer_form_in_chunks(T, D, B, fmt):
 
 
 def test_graph_replays_alongside_direct_launches():
-    # launches recorded into a CUDA graph take tiles in the fixed order (a
-    # graph may be replayed on any stream); direct launches on other streams
-    # keep their own counters, so the two never share one
+    # a launch recorded into a CUDA graph owns its tile counters; direct
+    # launches on other streams keep theirs, so the two never share one.  The
+    # graph clears its outputs first, so a replay whose counters were not
+    # re-armed by the previous one would leave zeros behind.
     X1, _ = workloads.mx_inputs(6000, 2048, seed=980, device=DEV)
     X2, _ = workloads.mx_inputs(7000, 2048, seed=981, device=DEV)
     ref1 = nts.mxnorm_cast(X1, None, B=32, p=2)
     ref2 = nts.mxnorm_cast(X2, None, B=32, p=2)
     c1 = torch.empty_like(ref1.codes)
     s1 = torch.empty_like(ref1.scales)
+    c1b = torch.empty_like(ref1.codes)
+    s1b = torch.empty_like(ref1.scales)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
+        c1.zero_()
+        s1.zero_()
         nts.mxnorm_cast(X1, None, B=32, p=2, codes=c1, scales=s1)
+        c1b.zero_()
+        s1b.zero_()
+        nts.mxnorm_cast(X1, None, B=32, p=2, codes=c1b, scales=s1b)   # a second node
     side = torch.cuda.Stream()
     outs = []
-    for _ in range(4):
+    for _ in range(6):
         graph.replay()
         with torch.cuda.stream(side):
             outs.append(nts.mxnorm_cast(X2, None, B=32, p=2, stream=side))
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(c1, ref1.codes) and torch.equal(s1, ref1.scales)
+        assert torch.equal(c1b, ref1.codes) and torch.equal(s1b, ref1.scales)
     torch.cuda.synchronize()
     nts.check_status()
-    assert torch.equal(c1, ref1.codes) and torch.equal(s1, ref1.scales)
     for o in outs:
         assert torch.equal(o.codes, ref2.codes) and torch.equal(o.scales, ref2.scales)
+
+
+def test_graphs_replayed_on_two_streams_at_once():
+    # two captured graphs (each with its own counters) replayed concurrently
+    # on two streams, many times, with the QK kernel's counters in use too
+    X, _ = workloads.mx_inputs(9000, 4096, seed=982, device=DEV)
+    Q, gq = workloads.qk_inputs(3000, 5120, seed=983, device=DEV)
+    refm = nts.rmsnorm_mxcast(X, None, B=32)
+    refq, _ = nts.qknorm_rms(Q, gq, N=4)
+    cm, sm = torch.empty_like(refm.codes), torch.empty_like(refm.scales)
+    yq = torch.empty_like(refq)
+    torch.cuda.synchronize()
+    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1):
+        cm.zero_()
+        nts.rmsnorm_mxcast(X, None, B=32, codes=cm, scales=sm)
+    with torch.cuda.graph(g2):
+        yq.zero_()
+        nts.qknorm_rms(Q, gq, N=4, out=yq)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(5):
+        with torch.cuda.stream(s1):
+            g1.replay()
+        with torch.cuda.stream(s2):
+            g2.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(cm, refm.codes) and torch.equal(sm, refm.scales)
+        assert torch.equal(yq, refq)
+    nts.check_status()
 
 
 def test_boundary_exception_counts_are_a_handful(capsys):
