@@ -51,6 +51,15 @@ NTS_API int nts_debug_set_schedule(int dynamic);
 NTS_API int nts_debug_set_direct(int on);
 
 /*
+ * Programmatic dependent launch: 1 (default) = every kernel is launched with
+ * programmatic stream serialization, so it may be scheduled while the grid
+ * before it in the stream finishes (it waits for that grid's completion
+ * before its first global-memory access); 0 = plain stream order.  Results
+ * are identical either way.  Errors: INVALID_ARG for other values.
+ */
+NTS_API int nts_debug_set_pdl(int on);
+
+/*
  * Test hook: every later launch tells its first ring stage to expect `bytes`
  * more than its copies deliver, so that stage's wait can only end by
  * expiring; the kernel then records NTS_ERR_TIMEOUT for nts_check_status and

@@ -50,6 +50,7 @@ def _declare(lib):
         "nts_debug_set_missing_tx": ([ctypes.c_uint32], i32),
         "nts_debug_set_schedule": ([i32], i32),
         "nts_debug_set_direct": ([i32], i32),
+        "nts_debug_set_pdl": ([i32], i32),
         "nts_debug_check_nvfp4_scale": ([ctypes.POINTER(ctypes.c_uint64),
                                          ctypes.POINTER(ctypes.c_uint64)], i32),
     }

@@ -92,6 +92,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) heads_kernel(const HeadsParams
     fence_mbar_init();
   }
   __syncthreads();
+  // everything above touched shared memory only
+  grid_dependency_wait();
+  allow_dependent_launch();
 
   if (tid >= nconsumer) {
     // ------------------------------------------------------ producer warp
@@ -336,8 +339,15 @@ int launch_heads(const void* X, const float* gamma, void* Y, float* rinv, int64_
   log_launch("qknorm_rms_heads", "T=%lld H=%lld head_dim=%lld vpt=%d G=%d R=%d S=%d smem=%zu "
              "grid=%lld (%d/SM)", (long long)T, (long long)H, (long long)head_dim, rs.vpt, rs.G,
              R, S, smem, (long long)grid, per_sm);
-  kern<<<(unsigned)grid, nthreads, smem, stream>>>(prm);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(nthreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = tune.pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e != cudaSuccess) return fail_cuda(e, "launching the headwise kernel");
   return NTS_OK;
 }

@@ -149,6 +149,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
   float* rcp = reinterpret_cast<float*>(smem + L.rcp);
   if (FMT == NTS_FMT_NVFP4) fill_e4m3_reciprocals(rcp, tid, (int)blockDim.x);
   __syncthreads();
+  // everything above touched shared memory only
+  grid_dependency_wait();
+  allow_dependent_launch();
 
   if (tid >= nconsumer) {
     // ------------------------------------------------------ producer warp

@@ -116,8 +116,15 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
              "T=%lld D=%d B=%d fmt=%d p=%d bpt=%d G=%d R=%d S=%d smem=%zu grid=%lld (%d/SM)",
              (long long)rq.T, D, rq.B, rq.fmt, rq.p, sh.bpt, sh.G, R, S, smem, (long long)grid,
              per_sm);
-  kern<<<(unsigned)grid, nthreads, smem, stream>>>(prm);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(nthreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = tune.pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e != cudaSuccess) return fail_cuda(e, "launching the MX kernel");
   return NTS_OK;
 }

@@ -682,6 +682,13 @@ int nts_debug_set_direct(int on) {
   return NTS_OK;
 }
 
+int nts_debug_set_pdl(int on) {
+  if (on != 0 && on != 1) return fail(NTS_ERR_INVALID_ARG, "on must be 0 or 1");
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tune.pdl = on;
+  return NTS_OK;
+}
+
 int nts_debug_set_missing_tx(uint32_t bytes) {
   if (bytes % 16 != 0) return fail(NTS_ERR_INVALID_ARG, "bytes must be a multiple of 16");
   std::lock_guard<std::mutex> lk(g_tune_mu);

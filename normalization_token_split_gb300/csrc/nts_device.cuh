@@ -354,6 +354,23 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Programmatic dependent launch (PTX griddepcontrol, sm_90+).  A grid
+// launched with the programmatic-serialization attribute may start while
+// the grid before it in the stream is still running; it must wait here
+// before its first global-memory access, until that grid has completed and
+// its writes are visible.  For a launch without the attribute the wait
+// returns at once.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid of the stream (if launched with the attribute) be
+// scheduled once every CTA of this grid has called this or exited; that
+// grid still waits for this one's completion before touching memory.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // fp32(a / 6) for a >= 0 by one multiply and two fmas instead of a division
 // (Brisebarre, Muller and Raina, "Accelerating correctly rounded
 // floating-point division when the divisor is known in advance", IEEE Trans.

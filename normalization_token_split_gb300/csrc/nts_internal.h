@@ -28,7 +28,19 @@ struct LaunchTuning {
   uint32_t missing_tx = 0;   // test hook, see nts_debug.h
   int dynamic = 1;           // take tiles from a counter (0: round-robin order)
   int direct = 1;            // decode-sized QK launches use the single-tile kernel
+  int pdl = 1;               // launch with programmatic stream serialization
 };
+
+// The launch attribute that lets a grid be scheduled while the grid before
+// it in the stream finishes (programmatic dependent launch).  Every kernel
+// of the library waits (griddepcontrol.wait) before its first global-memory
+// access, so this changes timing only.
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
 
 LaunchTuning current_tuning();
 

@@ -8,8 +8,8 @@
 // Phase C writes (x*gamma)*rinv once.  What it leaves out is everything a
 // single tile does not need: no producer warp, no TMA ring, no mbarriers and
 // no gamma staging.  Every thread issues the global loads of its x and gamma
-// vectors at the very start, so their latency overlaps the cluster start-up
-// barrier; one more cluster barrier orders the partial sums.  The summation
+// vectors at the very start (after the dependent-launch wait), so their
+// latency overlaps the cluster start-up barrier; one more cluster barrier orders the partial sums.  The summation
 // order is the persistent kernel's, so the results are identical bit for bit.
 #include <cuda_runtime.h>
 
@@ -52,6 +52,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qk_direct_kernel(const QkParam
   const int g = tid - row * p.G;
   const int wir = g >> 5;
   if (N > 1) cluster_arrive_relaxed();  // start-up: peers must run before DSMEM stores
+  grid_dependency_wait();               // no global access before this
+  allow_dependent_launch();
 
   int64_t t0;
   const QkTensor& tn = p.ten[qk_tile(p, tile, &t0)];

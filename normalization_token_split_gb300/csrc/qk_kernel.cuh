@@ -213,6 +213,9 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
   float* rcp = reinterpret_cast<float*>(smem + L.rcp);
   if (OUT == kOutNvfp4) fill_e4m3_reciprocals(rcp, tid, (int)blockDim.x);
   __syncthreads();
+  // everything above touched shared memory only
+  grid_dependency_wait();
+  allow_dependent_launch();
 
   if (tid >= nconsumer) {
     // ------------------------------------------------------ producer warp

@@ -349,5 +349,11 @@ def check_nvfp4_scale() -> tuple:
     return int(a.value), int(b.value)
 
 
+def set_pdl(on: bool) -> None:
+    """Launch with programmatic stream serialization (default on); results
+    do not depend on it (nts_debug_set_pdl)."""
+    check(lib().nts_debug_set_pdl(1 if on else 0))
+
+
 def set_missing_tx(nbytes: int) -> None:
     check(lib().nts_debug_set_missing_tx(int(nbytes)))
