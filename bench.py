@@ -401,7 +401,37 @@ def run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world):
     return {"value": round(world * total * steps / elapsed / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(elapsed / steps * 1e3, 4),
-            "path": "nts_*_host C ABI entry points, pinned host buffers"}
+            "path": "nts_*_host C ABI entry points, pinned host buffers",
+            "copy_only_gbs": copy_ceiling(torch, dev, h2d, d2h, total)}
+
+
+def copy_ceiling(torch, dev, h2d, d2h, total, reps=4):
+    """The step's bytes moved by plain copies alone (host->device on one
+    stream, device->host on another, 32 MiB pieces, pinned buffers): the
+    ceiling for e2e on this link, in the step's GB/s."""
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    hin = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    din = torch.empty(h2d, dtype=torch.uint8, device=dev)
+    hout = torch.empty(d2h, dtype=torch.uint8).pin_memory()
+    dout = torch.empty(d2h, dtype=torch.uint8, device=dev)
+    piece = 32 << 20
+
+    def copies():
+        with torch.cuda.stream(s_in):
+            for o in range(0, h2d, piece):
+                din[o:o + piece].copy_(hin[o:o + piece], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for o in range(0, d2h, piece):
+                hout[o:o + piece].copy_(dout[o:o + piece], non_blocking=True)
+
+    copies()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        copies()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / reps
+    return round(total / dt / 1e9, 1)
 
 
 def variant_rates(nts, torch, dev, Q, gq, X, peak, reps=20):

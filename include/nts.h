@@ -298,7 +298,7 @@ NTS_API int nts_check_status(void *stream);
  * outputs live in host memory.  Each enqueues the host->device copy of the
  * input rows, the kernel, and the device->host copies of the outputs, all
  * ordered on `stream`: the caller synchronizes the stream before reading
- * *_host outputs.  Calls of more than a few tens of MB move their rows in
+ * *_host outputs.  Calls of more than 32 MB move their rows in up to 16
  * chunks through two internal copy streams (one per direction, created on
  * the first such call on a device) while the kernels run on `stream`, so
  * both copy directions and the kernels overlap; the enqueueing of such calls

@@ -51,6 +51,14 @@ NTS_API int nts_debug_set_schedule(int dynamic);
 NTS_API int nts_debug_set_direct(int on);
 
 /*
+ * Chunking of the host-buffer forms: a call moves its rows in at most
+ * max_chunks chunks (1..64) of at least min_chunk_bytes of input each; 0
+ * restores a default (16 chunks, 16 MiB).  Results do not depend on it.
+ * Errors: INVALID_ARG for values out of range.
+ */
+NTS_API int nts_debug_set_host_chunks(int max_chunks, int64_t min_chunk_bytes);
+
+/*
  * Programmatic dependent launch: 1 (default) = every kernel is launched with
  * programmatic stream serialization, so it may be scheduled while the grid
  * before it in the stream finishes (it waits for that grid's completion

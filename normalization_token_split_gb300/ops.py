@@ -349,6 +349,12 @@ def check_nvfp4_scale() -> tuple:
     return int(a.value), int(b.value)
 
 
+def set_host_chunks(max_chunks: int = 0, min_chunk_bytes: int = 0) -> None:
+    """Chunking of the host-buffer forms (0, 0 = defaults); results do not
+    depend on it (nts_debug_set_host_chunks)."""
+    check(lib().nts_debug_set_host_chunks(int(max_chunks), int(min_chunk_bytes)))
+
+
 def set_pdl(on: bool) -> None:
     """Launch with programmatic stream serialization (default on); results
     do not depend on it (nts_debug_set_pdl)."""

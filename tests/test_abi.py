@@ -124,6 +124,9 @@ def test_debug_hooks_validate(lib):
     assert lib.nts_debug_check_nvfp4_scale(None, None) == INVALID
     assert lib.nts_debug_set_pdl(2) == INVALID
     assert lib.nts_debug_set_pdl(1) == OK
+    assert lib.nts_debug_set_host_chunks(65, 0) == INVALID
+    assert lib.nts_debug_set_host_chunks(-1, 0) == INVALID
+    assert lib.nts_debug_set_host_chunks(0, 0) == OK
     assert lib.nts_debug_set_tuning(0, 0, 0, 0, 0) == OK
     assert lib.nts_debug_set_missing_tx(0) == OK
     assert lib.nts_debug_set_wait_limit_ns(0) == OK
