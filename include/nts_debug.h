@@ -92,6 +92,17 @@ NTS_API int nts_debug_set_missing_tx(uint32_t bytes);
  */
 NTS_API int nts_debug_check_nvfp4_scale(uint64_t* code_mismatches, uint64_t* quotient_mismatches);
 
+/*
+ * Self-check of the E8M0 block exponent as the kernels form it (one add and
+ * one shift: adding 0x4AFB0C to the fp32 bits of the normalized absmax
+ * carries into the exponent field exactly when the significand rounds the
+ * log2 up) against its definition field by field, for emax 8 (E4M3) and 2
+ * (E2M1), over every non-negative fp32 absmax, 0 to +inf, on the current
+ * device, blocking until done.  *mismatches = 0 when the kernels are right.
+ * Errors: INVALID_ARG for a NULL output, CUDA for a failed launch or copy.
+ */
+NTS_API int nts_debug_check_e8m0(uint64_t* mismatches);
+
 #ifdef __cplusplus
 }
 #endif

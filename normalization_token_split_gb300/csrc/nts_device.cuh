@@ -271,11 +271,22 @@ __device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void* src, ui
 
 // ------------------------------------------------------- MX block scales
 
-// E8M0 exponent of a block whose normalized absmax is `ay` (>= 0):
-// round(log2 ay) - emax, where the log2 rounding goes up exactly when the
-// fp32 significand is >= the first fp32 value above sqrt(2) (0x3504F4 in the
-// mantissa field); zero and subnormal absmaxes give the smallest scale.
+// E8M0 exponent of a block whose normalized absmax is `ay` (>= 0, not NaN):
+// round(log2 ay) - emax, clamped to [-127, 127], where the log2 rounding goes
+// up exactly when the fp32 significand is >= the first fp32 value above
+// sqrt(2) (0x3504F4 in the mantissa field); zero and subnormal absmaxes give
+// the smallest scale.  Adding 0x800000 - 0x3504F4 = 0x4AFB0C to the bits
+// carries into the exponent field exactly when the mantissa field is
+// >= 0x3504F4, so one add and one shift give field + [rounds up]; zero and
+// subnormal inputs land at or below -126 - emax and clamp to -127.
 __device__ __forceinline__ int e8m0_exponent(float ay, int emax) {
+  const int e = (int)((__float_as_uint(ay) + 0x4AFB0Cu) >> 23) - 127 - emax;
+  return max(-127, min(127, e));
+}
+
+// The same exponent by the plain definition (exponent field, mantissa
+// compare, zero/subnormal special case): the reference of the self-check.
+__device__ __forceinline__ int e8m0_exponent_by_fields(float ay, int emax) {
   const uint32_t b = __float_as_uint(ay);
   const int field = (int)(b >> 23);
   if (field == 0) return -127;

@@ -183,6 +183,10 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
   const int nconsumer = p.R * p.G;
   const int lane = tid & 31;
   const int wpr = p.G >> 5;
+  // block-cast output: vectors per block and log2 of the block size (NVFP4
+  // blocks are 16 values: fixed at compile time)
+  const int kBv = OUT == kOutNvfp4 ? 2 : p.bv;
+  const int kBshift = OUT == kOutNvfp4 ? 4 : p.bshift;
   const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, p.psum, p.G, p.gsplit, ES, NS,
                                OUT == kOutNvfp4);
   const uint32_t sbase = smem_addr(smem);
@@ -468,10 +472,10 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
           for (int q = 0; q < 4; ++q)
             m = fmaxf(m, fmaxf(fabsf(f2_lo(w[i][q])), fabsf(f2_hi(w[i][q]))));
           // bv = B/8 is 2, 4 or 8: at most three steps, unrolled and guarded
-          // by the (warp-uniform) block size
+          // by the (warp-uniform) block size; NVFP4 blocks are always 16
 #pragma unroll
           for (int o = 1; o < 8; o <<= 1)
-            if (o < p.bv) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if (o < kBv) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
           am[i] = m;
         }
       }
@@ -513,8 +517,8 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
         if (OUT != kOutBf16) {
           const size_t first = (size_t)t * tn.H + (size_t)rank * tn.W;  // element index
           crow = OUT == kOutE4M3 ? tn.codes + first : tn.codes + first / 2;
-          srow_sc = tn.scales + (first >> p.bshift);
-          vshift = p.bshift - 3;
+          srow_sc = tn.scales + (first >> kBshift);
+          vshift = kBshift - 3;
         }
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
@@ -532,7 +536,7 @@ __global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 1
                 is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
                 sbyte = (uint32_t)(e + 127);
               }
-              if ((g & (p.bv - 1)) == 0) srow_sc[v >> vshift] = (uint8_t)sbyte;
+              if ((g & (kBv - 1)) == 0) srow_sc[v >> vshift] = (uint8_t)sbyte;
               const uint64_t ss = f2(is, is);
               uint64_t q[4];
 #pragma unroll

@@ -361,5 +361,13 @@ def set_pdl(on: bool) -> None:
     check(lib().nts_debug_set_pdl(1 if on else 0))
 
 
+def check_e8m0() -> int:
+    """Absmaxes whose E8M0 exponent, as the kernels form it, differs from
+    the field-by-field definition (nts_debug_check_e8m0); 0 when right."""
+    a = ctypes.c_uint64(0)
+    check(lib().nts_debug_check_e8m0(ctypes.byref(a)))
+    return int(a.value)
+
+
 def set_missing_tx(nbytes: int) -> None:
     check(lib().nts_debug_set_missing_tx(int(nbytes)))

@@ -122,6 +122,7 @@ def test_debug_hooks_validate(lib):
     assert lib.nts_debug_set_tuning(-1, 0, 0, 0, 0) == INVALID
     assert lib.nts_debug_set_missing_tx(17) == INVALID
     assert lib.nts_debug_check_nvfp4_scale(None, None) == INVALID
+    assert lib.nts_debug_check_e8m0(None) == INVALID
     assert lib.nts_debug_set_pdl(2) == INVALID
     assert lib.nts_debug_set_pdl(1) == OK
     assert lib.nts_debug_set_host_chunks(65, 0) == INVALID

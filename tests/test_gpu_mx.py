@@ -290,6 +290,12 @@ def test_nvfp4_scale_without_division_matches_ieee_route():
     assert quot_bad == 0, f"{quot_bad} normal quotients differ from IEEE division"
 
 
+def test_e8m0_exponent_by_carry_matches_definition():
+    # every non-negative fp32 absmax, 0 to +inf, for E4M3 and E2M1: the
+    # kernels' one-add exponent equals the field-by-field definition
+    assert nts.check_e8m0() == 0
+
+
 # ------------------------------------------------------------ tile order
 
 def test_dynamic_and_round_robin_tile_orders_agree():
