@@ -56,7 +56,7 @@ struct MxParams {
   int64_t ntiles;
   int D;
   int K;                // D / B blocks per row
-  int G;                // consumer threads per row (multiple of 32)
+  int G;                // consumer threads per row: 16 (two rows per warp) or a multiple of 32
   int R;                // rows per tile
   int S;                // ring stages
   float eps;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int nconsumer = p.R * p.G;
-  const int wpr = p.G >> 5;
+  const int wpr = p.G >= 32 ? p.G >> 5 : 1;   // warps per row (G = 16: two rows per warp)
   const MxLayout L = mx_layout(p.S, p.R, p.D, p.G, FMT == NTS_FMT_NVFP4);
   const uint32_t sbase = smem_addr(smem);
   const uint32_t stage_bytes = (uint32_t)p.R * p.D * 2;
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
       }
     }
     if (STAT == kStatRms) stat = f2_lo(acc) + f2_hi(acc);
-    stat = warp_sum(stat);
+    stat = group_sum(stat, min(p.G, 32));
     if (wpr > 1) {
       // a row spans several warps: add their partials in warp order
       const int bsel = (int)(j & 1);

@@ -15,7 +15,12 @@ struct MxShape {
   int G = 0;    // consumer threads per row
 };
 
-int threads_for(int K, int bpt) { return ((K + bpt - 1) / bpt + 31) / 32 * 32; }
+// Threads for a row of K blocks, bpt each: 16 (half a warp, two rows per
+// warp) when that covers it, else whole warps.
+int threads_for(int K, int bpt) {
+  const int n = (K + bpt - 1) / bpt;
+  return n <= 16 ? 16 : (n + 31) / 32 * 32;
+}
 
 // Blocks per thread: as few as cover the row with one warp, up to 16
 // vectors per thread (4 blocks of 32, 8 of 16, 2 of 64: measured best on
@@ -55,8 +60,11 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   R = std::max(R, (8192 + 2 * D - 1) / (2 * D));
   R = std::min(R, std::max(1, kMaxConsumers / sh.G));
   while (R > 1 && (rq.T + R - 1) / R < (int64_t)2 * dev.sm_count) R /= 2;
+  if (sh.G < 32) R = (R + 1) / 2 * 2;   // whole warps: an even number of 16-thread rows
   if (tune.force_rows > 0) R = tune.force_rows;
   if (R * sh.G > kMaxConsumers) return fail(NTS_ERR_UNSUPPORTED, "tile of %d rows too large", R);
+  if ((R * sh.G) % 32 != 0)
+    return fail(NTS_ERR_UNSUPPORTED, "%d rows of %d threads are not whole warps", R, sh.G);
 
   // Ring depth: up to four small stages, three while three CTAs still fit
   // on an SM (a ring of at most 72 KB), else two (measured on GB300: more

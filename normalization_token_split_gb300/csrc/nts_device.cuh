@@ -365,6 +365,15 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Sum over aligned groups of `width` lanes (16 or 32, warp-uniform): for 32
+// the same steps in the same order as warp_sum.
+__device__ __forceinline__ float group_sum(float v, int width) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    if (o < width) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
 // Programmatic dependent launch (PTX griddepcontrol, sm_90+).  A grid
 // launched with the programmatic-serialization attribute may start while
 // the grid before it in the stream is still running; it must wait here

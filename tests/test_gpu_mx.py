@@ -165,6 +165,38 @@ def test_forced_launch_shapes(vpt, rows, stages, grid):
         nts.set_tuning()
 
 
+@pytest.mark.parametrize("D,B", [(1024, 64), (512, 32), (256, 16), (128, 64)])
+@pytest.mark.parametrize("T", [1, 3, 1000])
+def test_half_warp_rows(D, B, T):
+    # rows of at most 16 blocks take 16 threads: two rows per warp, each
+    # summed over its own half of the warp
+    X, g = workloads.mx_inputs(T, D, seed=D + B + T, t_frac=0.1, with_gamma=True)
+    for kind, p in KINDS:
+        for fmt in ("e4m3", "e2m1"):
+            compare(kind, X, g, 1e-6, B, fmt, p, what=f"half-warp {kind}{p} D={D} B={B} T={T}")
+            compare(kind, X, None, 1e-6, B, fmt, p, what=f"half-warp {kind}{p} D={D} B={B} T={T}")
+    if B == 16:
+        for kind, p in KINDS:
+            if kind != "post":
+                compare(kind, X, g, 1e-6, 16, "nvfp4", p, what=f"half-warp nvfp4 {kind}{p} D={D}")
+
+
+def test_half_warp_rows_need_whole_warps():
+    X, _ = workloads.mx_inputs(100, 1024, seed=97, device=DEV)
+    try:
+        nts.set_tuning(rows=3)            # 3 rows of 16 threads: not whole warps
+        with pytest.raises(nts.NtsError, match="UNSUPPORTED"):
+            nts.mxnorm_cast(X, None, B=64, p=2)
+        nts.set_tuning(rows=6)
+        a = nts.mxnorm_cast(X, None, B=64, p=2)
+        nts.set_tuning()
+        b = nts.mxnorm_cast(X, None, B=64, p=2)
+        nts.check_status()
+        assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+    finally:
+        nts.set_tuning()
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     X, _ = workloads.mx_inputs(64, 1024, seed=13)
     try:
