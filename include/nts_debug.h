@@ -20,12 +20,13 @@ extern "C" {
 /*
  * Override the automatic launch shape.  Each argument 0 means automatic.
  *   vpt        QK kernel: 16-byte vectors per thread, one of {1,2,3,4,5,6,8};
- *              MX kernels: MX blocks per thread, one of {1,2,4,8}
+ *              MX kernels: MX blocks per thread, 1..8 with at most 16
+ *              vectors per thread (blocks * B/8)
  *   rows       token rows per tile (rows * threads-per-row <= 480)
  *   stages     shared-memory ring stages (>= 1)
  *   grid       CTAs (MX kernels) or clusters (QK kernel) of the persistent grid
  *   smem_budget bytes a CTA's ring aims to stay under (default 102400)
- * Errors: INVALID_ARG for negative values or an unknown vpt.  A shape the
+ * Errors: INVALID_ARG for negative values or vpt > 8.  A shape the
  * device cannot run is reported by the next call as UNSUPPORTED or CUDA.
  */
 NTS_API int nts_debug_set_tuning(int vpt, int rows, int stages, int64_t grid, int smem_budget);

@@ -1,0 +1,11 @@
+// mx_e2m1_rms.cu -- instantiates the fused normalization + MX cast kernels
+// (mx_kernel.cuh) for E2M1 elements and the RMSNorm (sum of squares) statistic, every
+// block size and blocks-per-thread count; a unit of its own so that the
+// kernel families compile in parallel.
+#include "mx_kernel.cuh"
+
+namespace nts {
+
+NTS_MX_UNIT(mx_e2m1_rms, NTS_FMT_E2M1, kStatRms)
+
+}  // namespace nts

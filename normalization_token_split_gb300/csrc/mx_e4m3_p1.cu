@@ -1,0 +1,11 @@
+// mx_e4m3_p1.cu -- instantiates the fused normalization + MX cast kernels
+// (mx_kernel.cuh) for E4M3 elements and the MXNorm, p = 1 statistic, every
+// block size and blocks-per-thread count; a unit of its own so that the
+// kernel families compile in parallel.
+#include "mx_kernel.cuh"
+
+namespace nts {
+
+NTS_MX_UNIT(mx_e4m3_p1, NTS_FMT_E4M3, kStatMxP1)
+
+}  // namespace nts

@@ -383,13 +383,29 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
 
 using MxKernel = void (*)(MxParams);
 
+// The kernel for BPT blocks of VB vectors per thread, or nullptr where a
+// thread would hold more than 16 vectors (256 bytes) of its row (slower on
+// GB300 wherever measured; the launcher never picks them).
+template <int FMT, int STAT, int VB, int BPT>
+MxKernel mx_kernel_if_small() {
+  if constexpr (BPT * VB <= 16) {
+    return mx_norm_cast_kernel<VB, BPT, FMT, STAT>;
+  } else {
+    return nullptr;
+  }
+}
+
 template <int FMT, int STAT, int VB>
 MxKernel pick_mx_bpt(int bpt) {
   switch (bpt) {
-    case 1: return mx_norm_cast_kernel<VB, 1, FMT, STAT>;
-    case 2: return mx_norm_cast_kernel<VB, 2, FMT, STAT>;
-    case 4: return mx_norm_cast_kernel<VB, 4, FMT, STAT>;
-    case 8: return mx_norm_cast_kernel<VB, 8, FMT, STAT>;
+    case 1: return mx_kernel_if_small<FMT, STAT, VB, 1>();
+    case 2: return mx_kernel_if_small<FMT, STAT, VB, 2>();
+    case 3: return mx_kernel_if_small<FMT, STAT, VB, 3>();
+    case 4: return mx_kernel_if_small<FMT, STAT, VB, 4>();
+    case 5: return mx_kernel_if_small<FMT, STAT, VB, 5>();
+    case 6: return mx_kernel_if_small<FMT, STAT, VB, 6>();
+    case 7: return mx_kernel_if_small<FMT, STAT, VB, 7>();
+    case 8: return mx_kernel_if_small<FMT, STAT, VB, 8>();
     default: return nullptr;
   }
 }
@@ -404,17 +420,6 @@ MxKernel pick_mx_block(int B, int bpt) {
   }
 }
 
-// Instantiates every kernel of element format FMT in the calling unit.
-template <int FMT>
-MxKernel pick_mx_format(int stat, int B, int bpt) {
-  switch (stat) {
-    case kStatRms: return pick_mx_block<FMT, kStatRms>(B, bpt);
-    case kStatMxP1: return pick_mx_block<FMT, kStatMxP1>(B, bpt);
-    case kStatMxP2: return pick_mx_block<FMT, kStatMxP2>(B, bpt);
-    default: return nullptr;
-  }
-}
-
 static inline int read_and_clear_local_mx_status(unsigned* out) {
   unsigned v = 0, zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_mx_status, sizeof(v));
@@ -425,12 +430,26 @@ static inline int read_and_clear_local_mx_status(unsigned* out) {
   return NTS_OK;
 }
 
-// Defined by mx_e4m3.cu, mx_e2m1.cu and mx_nvfp4.cu.
-MxKernel pick_mx_e4m3(int stat, int B, int bpt);
-MxKernel pick_mx_e2m1(int stat, int B, int bpt);
+// One translation unit per element format and statistic (mx_e4m3_rms.cu,
+// ..., mx_e2m1_p2.cu; NVFP4 in mx_nvfp4.cu), so that they compile in
+// parallel; each has its own status word.
+#define NTS_MX_UNIT(NAME, FMT, STAT)                                              \
+  MxKernel pick_##NAME(int B, int bpt) { return pick_mx_block<FMT, STAT>(B, bpt); } \
+  int read_and_clear_##NAME##_status(unsigned* out) { return read_and_clear_local_mx_status(out); }
+
+MxKernel pick_mx_e4m3_rms(int B, int bpt);
+MxKernel pick_mx_e4m3_p1(int B, int bpt);
+MxKernel pick_mx_e4m3_p2(int B, int bpt);
+MxKernel pick_mx_e2m1_rms(int B, int bpt);
+MxKernel pick_mx_e2m1_p1(int B, int bpt);
+MxKernel pick_mx_e2m1_p2(int B, int bpt);
 MxKernel pick_mx_nvfp4(int stat, int B, int bpt);
-int read_and_clear_mx_e4m3_status(unsigned* out);
-int read_and_clear_mx_e2m1_status(unsigned* out);
+int read_and_clear_mx_e4m3_rms_status(unsigned* out);
+int read_and_clear_mx_e4m3_p1_status(unsigned* out);
+int read_and_clear_mx_e4m3_p2_status(unsigned* out);
+int read_and_clear_mx_e2m1_rms_status(unsigned* out);
+int read_and_clear_mx_e2m1_p1_status(unsigned* out);
+int read_and_clear_mx_e2m1_p2_status(unsigned* out);
 int read_and_clear_mx_nvfp4_status(unsigned* out);
 
 }  // namespace nts

@@ -22,24 +22,38 @@ int threads_for(int K, int bpt) {
   return n <= 16 ? 16 : (n + 31) / 32 * 32;
 }
 
-// Blocks per thread: as few as cover the row with one warp, up to 16
-// vectors per thread (4 blocks of 32, 8 of 16, 2 of 64: measured best on
-// GB300 -- a row in one warp needs no cross-warp exchange, and 16 vectors
-// give enough independent work without spilling); 8 only when a row would
-// otherwise need more than the CTA's consumer threads.
+// Threads per row: the fewest (16, or whole warps) that cover the row with
+// at most 16 vectors per thread (8 blocks of 16 values, 4 of 32, 2 of 64);
+// then blocks per thread: the fewest that still cover the row with those
+// threads, so the blocks spread over all of them.  Measured on GB300 over
+// D = 1024..16384 and B = 16..64: more than 16 vectors per thread, or more
+// warps per row than needed, cost up to 40 %; at D = 5120 this picks 3
+// blocks of 32 on 64 threads (6690 GB/s, against 6470 for 4 blocks and
+// 6390 for 5 blocks on 32 threads).
 MxShape choose_mx_shape(int K, int VB, int force_bpt) {
   MxShape sh;
   if (force_bpt > 0) {
     sh.bpt = force_bpt;
   } else {
     const int cap = std::max(1, std::min(8, 16 / VB));
-    sh.bpt = 1;
-    while (sh.bpt < cap && K > 32 * sh.bpt) sh.bpt *= 2;
-    if (threads_for(K, sh.bpt) > kMaxConsumers) sh.bpt = 8;
+    const int G = threads_for(K, cap);
+    sh.bpt = std::max(1, std::min(cap, (K + G - 1) / G));
   }
   sh.G = threads_for(K, sh.bpt);
   if (sh.G > kMaxConsumers) sh.G = 0;
   return sh;
+}
+
+// The kernel for element format fmt, statistic stat, block size B and bpt
+// blocks per thread (nullptr if none is built).
+MxKernel pick_mx(int fmt, int stat, int B, int bpt) {
+  if (fmt == NTS_FMT_NVFP4) return pick_mx_nvfp4(stat, B, bpt);
+  if (stat < kStatRms || stat > kStatMxP2 || (fmt != NTS_FMT_E4M3 && fmt != NTS_FMT_E2M1))
+    return nullptr;
+  MxKernel (*const table[2][3])(int, int) = {
+      {pick_mx_e4m3_rms, pick_mx_e4m3_p1, pick_mx_e4m3_p2},
+      {pick_mx_e2m1_rms, pick_mx_e2m1_p1, pick_mx_e2m1_p2}};
+  return table[fmt == NTS_FMT_E2M1 ? 1 : 0][stat](B, bpt);
 }
 
 }  // namespace
@@ -81,9 +95,7 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
     return fail(NTS_ERR_UNSUPPORTED, "row too wide for shared memory: D = %d", D);
 
   const int stat = rq.p == 0 ? kStatRms : (rq.p == 1 ? kStatMxP1 : kStatMxP2);
-  MxKernel kern = rq.fmt == NTS_FMT_E4M3   ? pick_mx_e4m3(stat, rq.B, sh.bpt)
-                 : rq.fmt == NTS_FMT_E2M1 ? pick_mx_e2m1(stat, rq.B, sh.bpt)
-                                          : pick_mx_nvfp4(stat, rq.B, sh.bpt);
+  MxKernel kern = pick_mx(rq.fmt, stat, rq.B, sh.bpt);
   if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for B=%d bpt=%d", rq.B, sh.bpt);
 
   MxParams prm;
@@ -138,14 +150,19 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
 }
 
 int read_and_clear_mx_status(unsigned* out) {
-  unsigned a = 0, b = 0, c = 0;
-  int rc = read_and_clear_mx_e4m3_status(&a);
-  if (rc != NTS_OK) return rc;
-  rc = read_and_clear_mx_e2m1_status(&b);
-  if (rc != NTS_OK) return rc;
-  rc = read_and_clear_mx_nvfp4_status(&c);
-  if (rc != NTS_OK) return rc;
-  *out = a | b | c;
+  int (*const readers[])(unsigned*) = {
+      read_and_clear_mx_e4m3_rms_status, read_and_clear_mx_e4m3_p1_status,
+      read_and_clear_mx_e4m3_p2_status,  read_and_clear_mx_e2m1_rms_status,
+      read_and_clear_mx_e2m1_p1_status,  read_and_clear_mx_e2m1_p2_status,
+      read_and_clear_mx_nvfp4_status};
+  unsigned all = 0;
+  for (auto read : readers) {
+    unsigned v = 0;
+    const int rc = read(&v);
+    if (rc != NTS_OK) return rc;
+    all |= v;
+  }
+  *out = all;
   return NTS_OK;
 }
 

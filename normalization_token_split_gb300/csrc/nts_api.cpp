@@ -658,7 +658,7 @@ int nts_mxnorm_cast_host(const void* X_host, const float* gamma_dev, uint8_t* co
 int nts_debug_set_tuning(int vpt, int rows, int stages, int64_t grid, int smem_budget) {
   if (vpt < 0 || rows < 0 || stages < 0 || grid < 0 || smem_budget < 0)
     return fail(NTS_ERR_INVALID_ARG, "tuning values must be >= 0");
-  if (vpt != 0 && (vpt > 8 || vpt == 7)) return fail(NTS_ERR_INVALID_ARG, "vpt %d unsupported", vpt);
+  if (vpt > 8) return fail(NTS_ERR_INVALID_ARG, "vpt %d unsupported", vpt);
   std::lock_guard<std::mutex> lk(g_tune_mu);
   g_tune.force_vpt = vpt;
   g_tune.force_rows = rows;

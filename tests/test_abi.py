@@ -118,7 +118,7 @@ def test_host_forms_argument_checks(lib):
 
 
 def test_debug_hooks_validate(lib):
-    assert lib.nts_debug_set_tuning(7, 0, 0, 0, 0) == INVALID
+    assert lib.nts_debug_set_tuning(9, 0, 0, 0, 0) == INVALID
     assert lib.nts_debug_set_tuning(-1, 0, 0, 0, 0) == INVALID
     assert lib.nts_debug_set_missing_tx(17) == INVALID
     assert lib.nts_debug_check_nvfp4_scale(None, None) == INVALID

@@ -153,7 +153,7 @@ def test_deterministic():
     assert torch.equal(a.rinv, b.rinv)
 
 
-@pytest.mark.parametrize("vpt,rows,stages,grid", [(1, 1, 1, 1), (2, 3, 2, 5), (8, 2, 4, 0),
+@pytest.mark.parametrize("vpt,rows,stages,grid", [(1, 1, 1, 1), (2, 3, 2, 5), (3, 2, 4, 0),
                                                   (4, 4, 3, 7), (0, 0, 1, 0)])
 def test_forced_launch_shapes(vpt, rows, stages, grid):
     X, g = workloads.mx_inputs(301, 2048, seed=99, with_gamma=True)
@@ -161,6 +161,34 @@ def test_forced_launch_shapes(vpt, rows, stages, grid):
         nts.set_tuning(vpt=vpt, rows=rows, stages=stages, grid=grid)
         for kind, p in KINDS:
             compare(kind, X, g, 1e-6, 32, "e4m3", p, what=f"forced {vpt},{rows},{stages},{grid}")
+    finally:
+        nts.set_tuning()
+
+
+@pytest.mark.parametrize("B,bpts", [(16, range(1, 9)), (32, range(1, 5)), (64, range(1, 3))])
+def test_every_blocks_per_thread_count(B, bpts):
+    # every instantiated blocks-per-thread count, on rows of 165 blocks of
+    # 16, 82 of 32 or 40 of 64 values, which most counts do not divide: the
+    # row's last thread holds fewer blocks and its last warp idles in part
+    D = 2640 if B == 16 else 2624 if B == 32 else 2560
+    X, g = workloads.mx_inputs(150, D, seed=B + D, t_frac=0.1, with_gamma=True)
+    try:
+        for bpt in bpts:
+            nts.set_tuning(vpt=bpt)
+            for kind, p in KINDS:
+                fmts = ("e4m3", "e2m1", "nvfp4") if B == 16 else ("e4m3", "e2m1")
+                for fmt in fmts:
+                    compare(kind, X, g, 1e-6, B, fmt, p, what=f"bpt={bpt} B={B} {kind}{p} {fmt}")
+    finally:
+        nts.set_tuning()
+
+
+def test_blocks_per_thread_beyond_16_vectors_are_unsupported():
+    X, _ = workloads.mx_inputs(64, 4096, seed=98, device=DEV)
+    try:
+        nts.set_tuning(vpt=5)             # 5 blocks of 32 = 20 vectors per thread
+        with pytest.raises(nts.NtsError, match="UNSUPPORTED"):
+            nts.mxnorm_cast(X, None, B=32, p=2)
     finally:
         nts.set_tuning()
 
