@@ -347,6 +347,8 @@ def run_gpu(args):
         result["decode_qk_us_per_call"] = decode_latency(nts, torch, dev)
     if not args.no_variants:
         result["variants"] = variant_rates(nts, torch, dev, Q, gq, X, peak)
+    if not args.no_sweep:
+        result["mxnorm_sweep_gbs"] = mxnorm_sweep(nts, torch, dev, peak)
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
@@ -432,6 +434,43 @@ def copy_ceiling(torch, dev, h2d, d2h, total, reps=4):
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / reps
     return round(total / dt / 1e9, 1)
+
+
+def mxnorm_sweep(nts, torch, dev, peak, reps=20):
+    """MXNorm p=2 over the sweep grid: T = 65536, D in {1024, 3072, 5120,
+    7168, 16384}, B in {16, 32, 64}, E4M3 and E2M1, rows N(0,1) with 5 %
+    Student-t(3).  Device time per launch over `reps` back-to-back launches
+    (3 warm-up), algorithmic GB/s; plus the fraction of measured and of
+    8 TB/s for each."""
+    import workloads
+    T = 65536
+    out = {}
+    for D in (1024, 3072, 5120, 7168, 16384):
+        X, _ = workloads.mx_inputs(T, D, seed=5000 + D, t_frac=0.05, device=dev)
+        codes = torch.empty(T * D, dtype=torch.uint8, device=dev)
+        scales = torch.empty(T * D // 16, dtype=torch.uint8, device=dev)
+        for fmt in ("e4m3", "e2m1"):
+            for B in (16, 32, 64):
+                cb = D if fmt == "e4m3" else D // 2
+                c = codes[:T * cb].view(T, cb)
+                sc = scales[:T * D // B].view(T, D // B)
+                fn = lambda: nts.mxnorm_cast(X, None, eps=EPS, B=B, fmt=fmt, p=2, codes=c, scales=sc)
+                for _ in range(3):
+                    fn()
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s0.record()
+                for _ in range(reps):
+                    fn()
+                s1.record()
+                torch.cuda.synchronize()
+                ms = s0.elapsed_time(s1) / reps
+                gbs = T * (2 * D + cb + D // B) / (ms * 1e-3) / 1e9
+                out[f"D={D},B={B},{fmt}"] = {"us": round(ms * 1e3, 1), "gbs": round(gbs, 1),
+                                             "frac_of_measured": round(gbs / peak, 4),
+                                             "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
+        del X, codes, scales
+    nts.check_status()
+    return out
 
 
 def variant_rates(nts, torch, dev, Q, gq, X, peak, reps=20):
@@ -628,6 +667,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

@@ -231,9 +231,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
     const unsigned char* srow = smem + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * p.D * 2;
 
     // ---- pass 1: block absmaxes (of w = x or x*gamma) and the statistic
+    // Four independent chains for every reduction (one per 32-bit lane of a
+    // vector), so that a block of 64 values is not one long dependency chain.
     float am[BPT];
     float stat = 0.f;
-    uint64_t acc = 0;  // RMSNorm: packed sum of x^2
+    uint64_t acc[4] = {0, 0, 0, 0};  // RMSNorm: packed sums of x^2
 #pragma unroll
     for (int i = 0; i < BPT; ++i) {
       const int b = i * p.G + g;
@@ -241,27 +243,28 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
       if (valid && b < p.K) {
         const unsigned char* base = srow + (uint32_t)b * kB * 2;
         if (p.gamma == nullptr) {
-          uint32_t m = 0;
+          uint32_t m[4] = {0, 0, 0, 0};
 #pragma unroll
           for (int k = 0; k < VB; ++k) {
             const int u = (k + sig) & (VB - 1);
             const uint4 v = lds128(base + u * 16);
-            m = bf16x2_absmax(m, v.x);
-            m = bf16x2_absmax(m, v.y);
-            m = bf16x2_absmax(m, v.z);
-            m = bf16x2_absmax(m, v.w);
+            m[0] = bf16x2_absmax(m[0], v.x);
+            m[1] = bf16x2_absmax(m[1], v.y);
+            m[2] = bf16x2_absmax(m[2], v.z);
+            m[3] = bf16x2_absmax(m[3], v.w);
             if (STAT == kStatRms) {
               const uint64_t a = bf16x2_to_f2(v.x), c = bf16x2_to_f2(v.y);
               const uint64_t d = bf16x2_to_f2(v.z), e = bf16x2_to_f2(v.w);
-              acc = f2_fma(a, a, acc);
-              acc = f2_fma(c, c, acc);
-              acc = f2_fma(d, d, acc);
-              acc = f2_fma(e, e, acc);
+              acc[0] = f2_fma(a, a, acc[0]);
+              acc[1] = f2_fma(c, c, acc[1]);
+              acc[2] = f2_fma(d, d, acc[2]);
+              acc[3] = f2_fma(e, e, acc[3]);
             }
           }
-          am[i] = bf16x2_hmax_abs(m);
+          am[i] = bf16x2_hmax_abs(bf16x2_absmax(bf16x2_absmax(m[0], m[1]),
+                                                bf16x2_absmax(m[2], m[3])));
         } else {
-          float mf = 0.f;
+          float mf[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int k = 0; k < VB; ++k) {
             const int u = (k + sig) & (VB - 1);
@@ -269,25 +272,28 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
             if (STAT == kStatRms) {
               const uint64_t a = bf16x2_to_f2(v.x), c = bf16x2_to_f2(v.y);
               const uint64_t d = bf16x2_to_f2(v.z), e = bf16x2_to_f2(v.w);
-              acc = f2_fma(a, a, acc);
-              acc = f2_fma(c, c, acc);
-              acc = f2_fma(d, d, acc);
-              acc = f2_fma(e, e, acc);
+              acc[0] = f2_fma(a, a, acc[0]);
+              acc[1] = f2_fma(c, c, acc[1]);
+              acc[2] = f2_fma(d, d, acc[2]);
+              acc[3] = f2_fma(e, e, acc[3]);
             }
             uint64_t w[4];
             weigh_vector(v, p.gamma + (size_t)b * kB + u * 8, w);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              mf = fmaxf(mf, fmaxf(fabsf(f2_lo(w[q])), fabsf(f2_hi(w[q]))));
+              mf[q] = fmaxf(mf[q], fmaxf(fabsf(f2_lo(w[q])), fabsf(f2_hi(w[q]))));
           }
-          am[i] = mf;
+          am[i] = fmaxf(fmaxf(mf[0], mf[1]), fmaxf(mf[2], mf[3]));
         }
         const float a = (STAT != kStatRms && p.post) ? round_pow2(am[i]) : am[i];
         if (STAT == kStatMxP1) stat += a;
         if (STAT == kStatMxP2) stat = fmaf(a, a, stat);
       }
     }
-    if (STAT == kStatRms) stat = f2_lo(acc) + f2_hi(acc);
+    if (STAT == kStatRms) {
+      const uint64_t a = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+      stat = f2_lo(a) + f2_hi(a);
+    }
     stat = group_sum(stat, min(p.G, 32));
     if (wpr > 1) {
       // a row spans several warps: add their partials in warp order
