@@ -404,27 +404,36 @@ def run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(elapsed / steps * 1e3, 4),
             "path": "nts_*_host C ABI entry points, pinned host buffers",
-            "copy_only_gbs": copy_ceiling(torch, dev, h2d, d2h, total)}
+            "copy_only_gbs": copy_ceiling(
+                torch,
+                [(Qd, Qh), (Kd, Kh)] + [(Xd, Xh)] * 3,
+                [(Yqh, Yqd), (Ykh, Ykd)] + [(codes_h[n], codes_d) for n in KERNELS[1:]]
+                + [(scales_h[n], scales_d) for n in KERNELS[1:]], total)}
 
 
-def copy_ceiling(torch, dev, h2d, d2h, total, reps=4):
-    """The step's bytes moved by plain copies alone (host->device on one
-    stream, device->host on another, 32 MiB pieces, pinned buffers): the
+def copy_ceiling(torch, ins, outs, total, reps=4):
+    """The step's bytes moved by plain copies alone, between the very host
+    and device buffers the e2e step uses (so the same pinned pages): every
+    (device, host) pair of `ins` host->device on one stream, every (host,
+    device) pair of `outs` device->host on another, in 32 MiB pieces.  The
     ceiling for e2e on this link, in the step's GB/s."""
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    hin = torch.empty(h2d, dtype=torch.uint8).pin_memory()
-    din = torch.empty(h2d, dtype=torch.uint8, device=dev)
-    hout = torch.empty(d2h, dtype=torch.uint8).pin_memory()
-    dout = torch.empty(d2h, dtype=torch.uint8, device=dev)
     piece = 32 << 20
+
+    def flat(t):
+        return t.view(-1).view(torch.uint8)
 
     def copies():
         with torch.cuda.stream(s_in):
-            for o in range(0, h2d, piece):
-                din[o:o + piece].copy_(hin[o:o + piece], non_blocking=True)
+            for d, h in ins:
+                d, h = flat(d), flat(h)
+                for o in range(0, h.numel(), piece):
+                    d[o:o + piece].copy_(h[o:o + piece], non_blocking=True)
         with torch.cuda.stream(s_out):
-            for o in range(0, d2h, piece):
-                hout[o:o + piece].copy_(dout[o:o + piece], non_blocking=True)
+            for h, d in outs:
+                h, d = flat(h), flat(d)
+                for o in range(0, d.numel(), piece):
+                    h[o:o + piece].copy_(d[o:o + piece], non_blocking=True)
 
     copies()
     torch.cuda.synchronize()
