@@ -346,7 +346,7 @@ def run_gpu(args):
     if not args.no_decode:
         result["decode_qk_us_per_call"] = decode_latency(nts, torch, dev)
     if not args.no_variants:
-        result["variants"] = variant_rates(nts, torch, dev, Q, gq, X, peak)
+        result["variants"] = variant_rates(nts, torch, dev, Q, gq, X, peak, K, gk)
     if not args.no_sweep:
         result["mxnorm_sweep_gbs"] = mxnorm_sweep(nts, torch, dev, peak)
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -482,7 +482,7 @@ def mxnorm_sweep(nts, torch, dev, peak, reps=20):
     return out
 
 
-def variant_rates(nts, torch, dev, Q, gq, X, peak, reps=20):
+def variant_rates(nts, torch, dev, Q, gq, X, peak, K, gk, reps=20):
     """The widened paths outside the step, each at the step's sizes: device
     time per launch (CUDA events around `reps` back-to-back launches on the
     launching stream, after 3 warm-up launches) and algorithmic GB/s."""
@@ -501,6 +501,8 @@ def variant_rates(nts, torch, dev, Q, gq, X, peak, reps=20):
     qcodes4 = torch.empty(T, H // 2, dtype=torch.uint8, device=dev)
     qscales = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
     qscales16 = torch.empty(T, H // 16, dtype=torch.uint8, device=dev)
+    outq = nts.MxOut(qcodes, qscales, None, None)
+    outk = nts.MxOut(torch.empty_like(qcodes), torch.empty_like(qscales), None, None)
     cases = {
         f"qknorm_rms_heads[{T}x{H},head_dim=128,N=1]": (
             4 * T * H, lambda: nts.qknorm_rms_heads(Q, ghd, 128, eps=EPS, N=1, out=Y)),
@@ -514,6 +516,9 @@ def variant_rates(nts, torch, dev, Q, gq, X, peak, reps=20):
         f"qknorm_rms_mxcast[{T}x{H},N={QK_N},B=16,nvfp4]": (
             T * H * 2 + T * H // 2 + T * (H // 16), lambda: nts.qknorm_rms_mxcast(
                 Q, gq, eps=EPS, N=QK_N, B=16, fmt="nvfp4", codes=qcodes4, scales=qscales16)),
+        f"qknorm_rms_qk_mxcast[Q+K {T}x{H},N={QK_N},B=32,e4m3]": (
+            2 * (T * H * 3 + T * (H // 32)), lambda: nts.qknorm_rms_qk_mxcast(
+                Q, gq, K, gk, eps=EPS, N=QK_N, B=32, fmt="e4m3", out_q=outq, out_k=outk)),
         f"layernorm_split[{T}x{H},N={QK_N},beta]": (
             4 * T * H, lambda: nts.layernorm_split(Q, gq, beta, eps=1e-5, N=QK_N, out=Y)),
         f"mxnorm_postround_cast[{Tm}x{D},B={MX_B},p=2,e4m3]": (

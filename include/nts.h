@@ -201,6 +201,26 @@ NTS_API int nts_qknorm_rms_mxcast(const void *X_dev, const float *gamma_dev,
                                   void *stream);
 
 /*
+ * nts_qknorm_rms_qk_mxcast -- nts_qknorm_rms_mxcast of a token batch's Q and
+ * K in ONE launch, as nts_qknorm_rms_qk fuses nts_qknorm_rms: Q and K may
+ * have different widths (Hq, Hk) and their own gains; they share T, eps, N,
+ * B and fmt.  Each tensor's codes, scales and rinv follow the definition of
+ * nts_qknorm_rms_mxcast.  Both tensors take the thread layout of the wider
+ * shard: with Hq == Hk every result equals that of a one-tensor call bit for
+ * bit; otherwise the narrower tensor's fp32 sum of squares may be added in
+ * another order (rinv within fp32 rounding of the one-tensor call; its scales
+ * and codes are decided with that rinv).  Each tensor obeys the argument
+ * rules of nts_qknorm_rms_mxcast, and the same errors apply, for either.
+ */
+NTS_API int nts_qknorm_rms_qk_mxcast(const void *Q_dev, const float *gamma_q_dev,
+                                     uint8_t *codes_q_dev, uint8_t *scales_q_dev,
+                                     float *rinv_q_dev, const void *K_dev,
+                                     const float *gamma_k_dev, uint8_t *codes_k_dev,
+                                     uint8_t *scales_k_dev, float *rinv_k_dev, int64_t T,
+                                     int64_t Hq, int64_t Hk, float eps, int N, int B, int fmt,
+                                     void *stream);
+
+/*
  * nts_rmsnorm_mxcast -- RMSNorm fused with the MX cast (MXNorm card,
  * Fig. 1 caption, left graph; Fig. 8 "normalization and casting fused into a
  * single kernel"):

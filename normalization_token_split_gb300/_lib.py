@@ -34,6 +34,8 @@ def _declare(lib):
         "nts_qknorm_rms_qk": ([P, P, P, P, P, P, P, P, i64, i64, i64, f32, i32, P], i32),
         "nts_layernorm_split": ([P, P, P, P, P, P, i64, i64, f32, i32, P], i32),
         "nts_qknorm_rms_mxcast": ([P, P, P, P, P, i64, i64, f32, i32, i32, i32, P], i32),
+        "nts_qknorm_rms_qk_mxcast": ([P, P, P, P, P, P, P, P, P, P, i64, i64, i64, f32, i32, i32,
+                                      i32, P], i32),
         "nts_qknorm_rms_fp8": ([P, f32, P, P, P, i64, i64, f32, i32, P], i32),
         "nts_qknorm_rms_heads": ([P, P, P, P, i64, i64, i64, f32, i32, P], i32),
         "nts_rmsnorm_mxcast": ([P, P, P, P, P, P, i64, i64, f32, i32, i32, P], i32),

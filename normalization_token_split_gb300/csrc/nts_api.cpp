@@ -512,9 +512,13 @@ int nts_qknorm_rms_qk(const void* Q_dev, const float* gamma_q_dev, void* Yq_dev,
                        current_tuning());
 }
 
-int nts_qknorm_rms_mxcast(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,
-                          uint8_t* scales_dev, float* rinv_dev, int64_t T, int64_t H, float eps,
-                          int N, int B, int fmt, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int validate_qk_mx(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,
+                   uint8_t* scales_dev, float* rinv_dev, int64_t T, int64_t H, float eps, int N,
+                   int B, int fmt) {
   int rc = validate_qk(X_dev, gamma_dev, codes_dev, rinv_dev, T, H, eps, N);
   if (rc != NTS_OK) return rc;
   if (T > 0 && scales_dev == nullptr) return fail(NTS_ERR_INVALID_ARG, "scales must be non-NULL");
@@ -527,6 +531,18 @@ int nts_qknorm_rms_mxcast(const void* X_dev, const float* gamma_dev, uint8_t* co
   if ((H / N) % B != 0)
     return fail(NTS_ERR_UNSUPPORTED, "H/N (%lld) must be a multiple of B (%d)",
                 (long long)(H / N), B);
+  return NTS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int nts_qknorm_rms_mxcast(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,
+                          uint8_t* scales_dev, float* rinv_dev, int64_t T, int64_t H, float eps,
+                          int N, int B, int fmt, void* stream) {
+  int rc = validate_qk_mx(X_dev, gamma_dev, codes_dev, scales_dev, rinv_dev, T, H, eps, N, B, fmt);
+  if (rc != NTS_OK) return rc;
   if (T == 0) return NTS_OK;
   QkRequest rq{X_dev, gamma_dev, nullptr, rinv_dev, T, H};
   rq.codes = codes_dev;
@@ -535,6 +551,30 @@ int nts_qknorm_rms_mxcast(const void* X_dev, const float* gamma_dev, uint8_t* co
   opt.out_fmt = fmt;
   opt.B = B;
   return launch_qknorm(&rq, 1, eps, N, opt, static_cast<cudaStream_t>(stream), current_tuning());
+}
+
+int nts_qknorm_rms_qk_mxcast(const void* Q_dev, const float* gamma_q_dev, uint8_t* codes_q_dev,
+                             uint8_t* scales_q_dev, float* rinv_q_dev, const void* K_dev,
+                             const float* gamma_k_dev, uint8_t* codes_k_dev,
+                             uint8_t* scales_k_dev, float* rinv_k_dev, int64_t T, int64_t Hq,
+                             int64_t Hk, float eps, int N, int B, int fmt, void* stream) {
+  int rc = validate_qk_mx(Q_dev, gamma_q_dev, codes_q_dev, scales_q_dev, rinv_q_dev, T, Hq, eps,
+                          N, B, fmt);
+  if (rc != NTS_OK) return rc;
+  rc = validate_qk_mx(K_dev, gamma_k_dev, codes_k_dev, scales_k_dev, rinv_k_dev, T, Hk, eps, N,
+                      B, fmt);
+  if (rc != NTS_OK) return rc;
+  if (T == 0) return NTS_OK;
+  QkRequest rq[2] = {{Q_dev, gamma_q_dev, nullptr, rinv_q_dev, T, Hq},
+                     {K_dev, gamma_k_dev, nullptr, rinv_k_dev, T, Hk}};
+  rq[0].codes = codes_q_dev;
+  rq[0].scales = scales_q_dev;
+  rq[1].codes = codes_k_dev;
+  rq[1].scales = scales_k_dev;
+  QkOptions opt;
+  opt.out_fmt = fmt;
+  opt.B = B;
+  return launch_qknorm(rq, 2, eps, N, opt, static_cast<cudaStream_t>(stream), current_tuning());
 }
 
 int nts_rmsnorm_mxcast(const void* X_dev, const float* gamma_dev, uint8_t* codes_dev,

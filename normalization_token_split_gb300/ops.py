@@ -162,6 +162,35 @@ def qknorm_rms_mxcast(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, N
     return MxOut(codes, scales, rinv, None)
 
 
+def qknorm_rms_qk_mxcast(q: torch.Tensor, gamma_q: torch.Tensor, k: torch.Tensor,
+                         gamma_k: torch.Tensor, eps: float = 1e-6, N: int = 1, B: int = 32,
+                         fmt="e4m3", out_q: Optional["MxOut"] = None,
+                         out_k: Optional["MxOut"] = None, want_rinv: bool = False,
+                         stream=None):
+    """qknorm_rms_mxcast of Q [T, Hq] and K [T, Hk] in one launch.  out_q /
+    out_k may carry preallocated (codes, scales, rinv or None) buffers.
+    Returns (MxOut for Q, MxOut for K)."""
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("gamma_q", gamma_q, torch.float32), ("gamma_k", gamma_k, torch.float32)):
+        _need_cuda(name, t, dt)
+    T, Hq = q.shape
+    Tk, Hk = k.shape
+    if Tk != T:
+        raise ValueError("q and k must have the same number of tokens")
+    f = _fmt(fmt)
+    bufs = []
+    for x, H, o in ((q, Hq, out_q), (k, Hk, out_k)):
+        c, s_, r = (o.codes, o.scales, o.rinv) if o is not None else (None, None, None)
+        c, s_, r, _ = _mx_outputs(x, H, B, f, c, s_, r, None, want_rinv, False)
+        bufs.append((c, s_, r))
+    (cq, sq, rq), (ck, sk, rk) = bufs
+    check(lib().nts_qknorm_rms_qk_mxcast(_ptr(q), _ptr(gamma_q), _ptr(cq), _ptr(sq), _ptr(rq),
+                                         _ptr(k), _ptr(gamma_k), _ptr(ck), _ptr(sk), _ptr(rk),
+                                         T, Hq, Hk, float(eps), int(N), int(B), f,
+                                         _stream(stream)))
+    return MxOut(cq, sq, rq, None), MxOut(ck, sk, rk, None)
+
+
 def qknorm_rms_qk(q: torch.Tensor, gamma_q: torch.Tensor, k: torch.Tensor,
                   gamma_k: torch.Tensor, eps: float = 1e-6, N: int = 1,
                   out_q: Optional[torch.Tensor] = None, out_k: Optional[torch.Tensor] = None,

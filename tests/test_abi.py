@@ -224,6 +224,23 @@ def test_qk_mxcast_argument_checks(lib):
     assert f(T=0, X=None, c=None, s=None) == OK
 
 
+def test_qk_mxcast_fused_argument_checks(lib):
+    def f(**k):
+        return lib.nts_qknorm_rms_qk_mxcast(
+            k.get("Q", A16), A16, k.get("cq", A16), k.get("sq", A16), None,
+            k.get("K", A16), A16, k.get("ck", A16), k.get("sk", A16), None,
+            k.get("T", 4), k.get("Hq", 1024), k.get("Hk", 512), 1e-6, k.get("N", 2),
+            k.get("B", 32), k.get("fmt", 0), None)
+    assert f(sq=None) == INVALID
+    assert f(sk=None) == INVALID
+    assert f(K=None) == INVALID
+    assert f(B=8) == INVALID
+    assert f(fmt=2, B=32) == INVALID
+    assert f(Hk=1040, B=16) == UNSUPPORTED     # K shards of 520 values
+    assert f(ck=MIS) == UNSUPPORTED
+    assert f(T=0, Q=None, K=None, cq=None, sq=None, ck=None, sk=None) == OK
+
+
 def test_noalloc_argument_checks(lib):
     f = lambda **k: lib.nts_mxnorm_cast_host_noalloc(
         k.get("X", A16), None, A16, A16, k.get("T", 4), k.get("D", 256), 1e-6, k.get("B", 32),

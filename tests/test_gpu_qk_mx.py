@@ -93,3 +93,63 @@ def test_forced_launch_shapes(vpt, rows, stages, grid):
             run_and_check(X, g, N, "e4m3", 32, what=f"forced {vpt},{rows},{stages},{grid}")
     finally:
         nts.set_tuning()
+
+
+# ------------------------------------------- Q and K in one launch (f1 + f4)
+
+@pytest.mark.parametrize("fmt,B", [("e4m3", 32), ("e2m1", 64), ("nvfp4", 16), ("e4m3", 16)])
+@pytest.mark.parametrize("N", [1, 2, 4])
+@pytest.mark.parametrize("T,Hq,Hk", [(1, 4096, 1024), (37, 5120, 5120), (300, 2048, 512),
+                                     (2000, 4096, 4096)])
+def test_fused_q_and_k(fmt, B, N, T, Hq, Hk):
+    # Both tensors share the row shape of the wider shard, so with equal
+    # widths each tensor's arithmetic and summation order are those of a
+    # one-tensor call (bit for bit); with unequal widths the narrower one
+    # sums in another order: rinv within fp32 rounding, and the scales and
+    # codes those the oracle's block stage gives for the device's rinv.
+    Q, gq = workloads.qk_inputs(T, Hq, seed=T + Hq + N, outlier_frac=0.01, device=DEV)
+    K, gk = workloads.qk_inputs(T, Hk, seed=T + Hk + N + 1, device=DEV)
+    oq, ok = nts.qknorm_rms_qk_mxcast(Q, gq, K, gk, N=N, B=B, fmt=fmt, want_rinv=True)
+    sq = nts.qknorm_rms_mxcast(Q, gq, N=N, B=B, fmt=fmt, want_rinv=True)
+    sk = nts.qknorm_rms_mxcast(K, gk, N=N, B=B, fmt=fmt, want_rinv=True)
+    nts.check_status()
+    for X, g, a, b, tag in ((Q, gq, oq, sq, "Q"), (K, gk, ok, sk, "K")):
+        if Hq == Hk:
+            assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+            assert torch.equal(a.rinv, b.rinv)
+            continue
+        assert torch.max(torch.abs(a.rinv / b.rinv - 1)).item() < 1e-6
+        Xb = workloads.bf16_bits(X)
+        gn = g.cpu().numpy()
+        ref = oracle.rmsnorm_mxcast(Xb, gn, 1e-6, B, FMTS[fmt])
+        check_mx(Xb, gn, B, FMTS[fmt], (a.codes.cpu().numpy(), a.scales.cpu().numpy(), None),
+                 ref, a.rinv.cpu().numpy(), 1e-6, f"fused {tag} {fmt} N={N} T={T}")
+
+
+@pytest.mark.parametrize("fmt,B", [("e4m3", 32), ("nvfp4", 16)])
+def test_fused_q_and_k_match_oracle(fmt, B):
+    Q, gq = workloads.qk_inputs(333, 4096, seed=61, outlier_frac=0.01)
+    K, gk = workloads.qk_inputs(333, 1024, seed=62)
+    oq, ok = nts.qknorm_rms_qk_mxcast(Q.to(DEV), gq.to(DEV), K.to(DEV), gk.to(DEV), N=4, B=B,
+                                      fmt=fmt, want_rinv=True)
+    nts.check_status()
+    for X, g, out, tag in ((Q, gq, oq, "Q"), (K, gk, ok, "K")):
+        Xb = workloads.bf16_bits(X)
+        gn = g.cpu().numpy()
+        ref = oracle.rmsnorm_mxcast(Xb, gn, 1e-6, B, FMTS[fmt])
+        check_mx(Xb, gn, B, FMTS[fmt], (out.codes.cpu().numpy(), out.scales.cpu().numpy(), None),
+                 ref, out.rinv.cpu().numpy(), 1e-6, f"fused {tag} {fmt}")
+
+
+def test_fused_q_and_k_arguments():
+    Q, gq = workloads.qk_inputs(16, 1024, seed=63, device=DEV)
+    K, gk = workloads.qk_inputs(16, 1000, seed=64, device=DEV)     # 1000/4 = 250: not a multiple of 32
+    with pytest.raises(nts.NtsError, match="UNSUPPORTED"):
+        nts.qknorm_rms_qk_mxcast(Q, gq, K, gk, N=4, B=32)
+    K2, gk2 = workloads.qk_inputs(8, 1024, seed=65, device=DEV)
+    with pytest.raises(ValueError):
+        nts.qknorm_rms_qk_mxcast(Q, gq, K2, gk2, N=4, B=32)
+    E = torch.empty(0, 1024, dtype=torch.bfloat16, device=DEV)
+    oq, ok = nts.qknorm_rms_qk_mxcast(E, gq, E, gk2, N=2, B=32)
+    nts.check_status()
+    assert oq.codes.shape == (0, 1024) and ok.scales.shape == (0, 32)
