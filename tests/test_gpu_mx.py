@@ -125,8 +125,9 @@ def test_degenerate_blocks():
 
 def test_extreme_factors():
     # rows so small that the mean square underflows and rinv = 1/sqrt(eps)
-    # is huge: rinv * 2^-e overflows fp32 for some blocks, so the kernel must
-    # take the two-product path there; other rows sit near its boundary
+    # is huge: rinv * 2^-e would overflow fp32 for some blocks, so a kernel
+    # that folded the two products w*rinv and *2^-e into one would go wrong
+    # there; fp32(w*rinv) itself is subnormal for some elements of others
     X, _ = workloads.mx_inputs(8, 1024, seed=78)
     Xf = X.float()
     for r, sc in enumerate((1e-36, 1e-34, 1e-30, 1e-25, 1e-20, 1e-12, 3e-39, 1.0)):
