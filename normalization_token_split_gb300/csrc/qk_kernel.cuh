@@ -167,11 +167,12 @@ __device__ __forceinline__ void load_vector(const unsigned char* srow, int v, bo
 }
 
 // Registers: 96 per thread (4 CTAs of 160 threads per SM) beat 128 (3 CTAs)
-// by 5-12 % on GB300 for every variant but LayerNorm, whose wider Phase C
-// loses 10 % at 96; the block-cast output with 8 vectors per thread keeps
-// 128 so as not to spill.
+// by 5-12 % on GB300 for every variant but LayerNorm, which runs best at 104
+// (no spills at any width; with a two-stage ring, 7-8 % faster than at 128);
+// the block-cast output with 8 vectors per thread keeps 128 so as not to
+// spill.
 template <int N, int VPT, int IN, int STAT, int OUT>
-__global__ void __maxnreg__((STAT == kQkLn || (OUT != kOutBf16 && VPT == 8)) ? 128 : 96)
+__global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8) ? 128 : 96))
     qknorm_cluster_kernel(const QkParams p) {
   constexpr int ES = (IN == kInBf16) ? 2 : 1;  // bytes per activation
   constexpr int NS = (STAT == kQkLn) ? 2 : 1;  // scalars exchanged per warp
