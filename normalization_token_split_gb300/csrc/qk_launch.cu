@@ -44,11 +44,13 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
 
   // Ring depth: up to 4 stages within the shared-memory budget; the widest
   // shards (whose staged gamma alone is up to 120 KB) fall back to fewer.
-  // LayerNorm, bound by its per-row work rather than by DRAM, takes two
-  // (measured on GB300: 7-8 % faster than four at [8192, 5120], N = 4).
+  // The variants bound by their per-row work rather than by DRAM take
+  // fewer (measured on GB300 at [8192, 5120], N = 4, against four stages):
+  // LayerNorm and the block-cast output two (7-8 % and 4-5 % faster),
+  // E4M3 input three (3 %).
   // gamma is split into the conflict-free layout when both copies fit.
   int gsplit = 1;
-  int S = layernorm ? 2 : 4;
+  int S = (layernorm || mx_out) ? 2 : (opt.in_e4m3 ? 3 : 4);
   const bool nvfp4 = mx_out && opt.out_fmt == NTS_FMT_NVFP4;
   auto layout = [&](int s, int split) {
     return qk_layout(N, s, R, Wmax, psum, rs.G, split, ES, NS, nvfp4);
