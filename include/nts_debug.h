@@ -20,8 +20,8 @@ extern "C" {
 /*
  * Override the automatic launch shape.  Each argument 0 means automatic.
  *   vpt        QK kernel: 16-byte vectors per thread, one of {1,2,3,4,5,6,8};
- *              MX kernels: MX blocks per thread, 1..8 with at most 16
- *              vectors per thread (blocks * B/8)
+ *              MX kernels: MX blocks per thread (halves of 64-value
+ *              blocks for B = 64), 1..8 with at most 16 vectors per thread
  *   rows       token rows per tile (rows * threads-per-row <= 480)
  *   stages     shared-memory ring stages (>= 1)
  *   grid       CTAs (MX kernels) or clusters (QK kernel) of the persistent grid

@@ -126,6 +126,12 @@ __device__ __forceinline__ void weigh_vector(const uint4& v, const float* gp, ui
 template <int VB, int BPT, int FMT, int STAT>
 __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxParams p) {
   constexpr int kB = VB * 8;                                 // block size
+  // A 64-value block is split between two adjacent lanes, 32 values each
+  // (the layout of 32-value blocks), which combine their absmaxes by one
+  // shuffle: a thread's unit is then half a block.
+  constexpr bool kSplit = (VB == 8);
+  constexpr int kUV = kSplit ? 4 : VB;                       // vectors per unit
+  constexpr int kU = kUV * 8;                                // values per unit
   constexpr int kEmax = (FMT == NTS_FMT_E4M3) ? 8 : 2;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x;
@@ -211,7 +217,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
   const int row = tid / p.G;
   const int g = tid - row * p.G;
   const int wir = g >> 5;
-  const int sig = ((lane * VB) >> 3) & (VB - 1);   // bank-conflict-free start vector
+  const int sig = ((lane * kUV) >> 3) & (kUV - 1);   // bank-conflict-free start vector
+  const int units = kSplit ? 2 * p.K : p.K;          // units per row
   const size_t cbytes = (FMT == NTS_FMT_E4M3) ? (size_t)p.D : (size_t)p.D / 2;
   bool aborted = false;
 
@@ -238,15 +245,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
     uint64_t acc[4] = {0, 0, 0, 0};  // RMSNorm: packed sums of x^2
 #pragma unroll
     for (int i = 0; i < BPT; ++i) {
-      const int b = i * p.G + g;
+      const int b = i * p.G + g;   // unit (block, or half block when split)
       am[i] = 0.f;
-      if (valid && b < p.K) {
-        const unsigned char* base = srow + (uint32_t)b * kB * 2;
+      if (valid && b < units) {
+        const unsigned char* base = srow + (uint32_t)b * kU * 2;
         if (p.gamma == nullptr) {
           uint32_t m[4] = {0, 0, 0, 0};
 #pragma unroll
-          for (int k = 0; k < VB; ++k) {
-            const int u = (k + sig) & (VB - 1);
+          for (int k = 0; k < kUV; ++k) {
+            const int u = (k + sig) & (kUV - 1);
             const uint4 v = lds128(base + u * 16);
             m[0] = bf16x2_absmax(m[0], v.x);
             m[1] = bf16x2_absmax(m[1], v.y);
@@ -266,8 +273,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
         } else {
           float mf[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int k = 0; k < VB; ++k) {
-            const int u = (k + sig) & (VB - 1);
+          for (int k = 0; k < kUV; ++k) {
+            const int u = (k + sig) & (kUV - 1);
             const uint4 v = lds128(base + u * 16);
             if (STAT == kStatRms) {
               const uint64_t a = bf16x2_to_f2(v.x), c = bf16x2_to_f2(v.y);
@@ -278,13 +285,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
               acc[3] = f2_fma(e, e, acc[3]);
             }
             uint64_t w[4];
-            weigh_vector(v, p.gamma + (size_t)b * kB + u * 8, w);
+            weigh_vector(v, p.gamma + (size_t)b * kU + u * 8, w);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               mf[q] = fmaxf(mf[q], fmaxf(fabsf(f2_lo(w[q])), fabsf(f2_hi(w[q]))));
           }
           am[i] = fmaxf(fmaxf(mf[0], mf[1]), fmaxf(mf[2], mf[3]));
         }
+      }
+      // the two halves of a split block share one absmax (lanes g, g ^ 1 hold
+      // units b, b ^ 1: same row, both in range or both out, as G and the
+      // unit count are even)
+      if (kSplit) am[i] = fmaxf(am[i], __shfl_xor_sync(0xFFFFFFFFu, am[i], 1));
+      if (valid && b < units && (!kSplit || (g & 1) == 0)) {
         const float a = (STAT != kStatRms && p.post) ? round_pow2(am[i]) : am[i];
         if (STAT == kStatMxP1) stat += a;
         if (STAT == kStatMxP2) stat = fmaf(a, a, stat);
@@ -331,25 +344,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
       uint8_t* crow = p.codes + (size_t)t * cbytes;
 #pragma unroll
       for (int i = 0; i < BPT; ++i) {
-        const int b = i * p.G + g;
-        if (b < p.K) {
+        const int b = i * p.G + g;   // unit
+        if (b < units) {
+          const int blk = kSplit ? (b >> 1) : b;
+          const bool lead = !kSplit || (b & 1) == 0;   // writes the block's scale
           float is;                 // multiplier taking w*rinv to the element grid
           uint32_t keep = ~0u;      // NVFP4: 0 for a block whose scale is zero
           if (FMT == NTS_FMT_NVFP4) {
             const uint32_t sc = nvfp4_scale(am[i] * rinv, rcp, &is);
             keep = sc != 0 ? ~0u : 0u;
-            p.scales[(size_t)t * p.K + b] = (uint8_t)sc;
+            p.scales[(size_t)t * p.K + blk] = (uint8_t)sc;
           } else {
             const int e = e8m0_exponent(am[i] * rinv, kEmax);
             is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
-            p.scales[(size_t)t * p.K + b] = (uint8_t)(e + 127);
+            if (lead) p.scales[(size_t)t * p.K + blk] = (uint8_t)(e + 127);
           }
           const uint64_t ss = f2(is, is);
-          if (p.amax_out != nullptr) p.amax_out[(size_t)t * p.K + b] = am[i];
-          const unsigned char* base = srow + (uint32_t)b * kB * 2;
+          if (p.amax_out != nullptr && lead) p.amax_out[(size_t)t * p.K + blk] = am[i];
+          const unsigned char* base = srow + (uint32_t)b * kU * 2;
 #pragma unroll
-          for (int k = 0; k < VB; ++k) {
-            const int u = (k + sig) & (VB - 1);
+          for (int k = 0; k < kUV; ++k) {
+            const int u = (k + sig) & (kUV - 1);
             const uint4 v = lds128(base + u * 16);
             uint64_t w[4];
             if (p.gamma == nullptr) {
@@ -358,7 +373,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
               w[2] = bf16x2_to_f2(v.z);
               w[3] = bf16x2_to_f2(v.w);
             } else {
-              weigh_vector(v, p.gamma + (size_t)b * kB + u * 8, w);
+              weigh_vector(v, p.gamma + (size_t)b * kU + u * 8, w);
             }
             uint64_t q[4];
 #pragma unroll
@@ -366,11 +381,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
             if (FMT == NTS_FMT_E4M3) {
               const uint32_t lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
               const uint32_t hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
-              st_global_v2(crow + (size_t)b * kB + u * 8, lo, hi);
+              st_global_v2(crow + (size_t)b * kU + u * 8, lo, hi);
             } else {
               const uint32_t c = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]),
                                             f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
-              st_global_u32(crow + (size_t)b * (kB / 2) + u * 4, c & keep);
+              st_global_u32(crow + (size_t)b * (kU / 2) + u * 4, c & keep);
             }
           }
         }
@@ -389,12 +404,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
 
 using MxKernel = void (*)(MxParams);
 
-// The kernel for BPT blocks of VB vectors per thread, or nullptr where a
-// thread would hold more than 16 vectors (256 bytes) of its row (slower on
-// GB300 wherever measured; the launcher never picks them).
+// The kernel for BPT units of a thread (blocks of VB vectors; half blocks of
+// 4 vectors for VB = 8), or nullptr where a thread would hold more than 16
+// vectors (256 bytes) of its row (slower on GB300 wherever measured; the
+// launcher never picks them).
 template <int FMT, int STAT, int VB, int BPT>
 MxKernel mx_kernel_if_small() {
-  if constexpr (BPT * VB <= 16) {
+  if constexpr (BPT * (VB == 8 ? 4 : VB) <= 16) {
     return mx_norm_cast_kernel<VB, BPT, FMT, STAT>;
   } else {
     return nullptr;

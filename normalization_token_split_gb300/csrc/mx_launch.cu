@@ -11,7 +11,7 @@ namespace nts {
 namespace {
 
 struct MxShape {
-  int bpt = 0;  // blocks per consumer thread
+  int bpt = 0;  // units (blocks, or halves of 64-value blocks) per consumer thread
   int G = 0;    // consumer threads per row
 };
 
@@ -22,10 +22,11 @@ int threads_for(int K, int bpt) {
   return n <= 16 ? 16 : (n + 31) / 32 * 32;
 }
 
-// Threads per row: the fewest (16, or whole warps) that cover the row with
-// at most 16 vectors per thread (8 blocks of 16 values, 4 of 32, 2 of 64);
-// then blocks per thread: the fewest that still cover the row with those
-// threads, so the blocks spread over all of them.  Measured on GB300 over
+// Threads per row: the fewest (16, or whole warps) that cover the row's K
+// units of VB vectors with at most 16 vectors per thread (8 blocks of 16
+// values, 4 of 32, 4 halves of 64-value blocks); then units per thread: the
+// fewest that still cover the row with those threads, so the units spread
+// over all of them.  Measured on GB300 over
 // D = 1024..16384 and B = 16..64: more than 16 vectors per thread, or more
 // warps per row than needed, cost up to 40 %; at D = 5120 this picks 3
 // blocks of 32 on 64 threads (6690 GB/s, against 6470 for 4 blocks and
@@ -64,8 +65,12 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   const DeviceInfo& dev = device_info();
   if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
 
-  // tune.force_vpt selects the blocks per thread for this kernel family
-  const MxShape sh = choose_mx_shape(K, rq.B / 8, tune.force_vpt);
+  // tune.force_vpt selects the units per thread for this kernel family; a
+  // unit is a block, or half a block of 64 values (the kernel splits those
+  // between two lanes, each with the 32-value layout)
+  const bool split = rq.B == 64;
+  const MxShape sh = split ? choose_mx_shape(2 * K, 4, tune.force_vpt)
+                           : choose_mx_shape(K, rq.B / 8, tune.force_vpt);
   if (sh.G == 0) return fail(NTS_ERR_UNSUPPORTED, "row too wide: D = %d", D);
 
   // Rows per tile: about four consumer warps and at least 8 KB per stage;

@@ -166,11 +166,12 @@ def test_forced_launch_shapes(vpt, rows, stages, grid):
         nts.set_tuning()
 
 
-@pytest.mark.parametrize("B,bpts", [(16, range(1, 9)), (32, range(1, 5)), (64, range(1, 3))])
+@pytest.mark.parametrize("B,bpts", [(16, range(1, 9)), (32, range(1, 5)), (64, range(1, 5))])
 def test_every_blocks_per_thread_count(B, bpts):
-    # every instantiated blocks-per-thread count, on rows of 165 blocks of
-    # 16, 82 of 32 or 40 of 64 values, which most counts do not divide: the
-    # row's last thread holds fewer blocks and its last warp idles in part
+    # every instantiated blocks-per-thread count (half blocks for B = 64,
+    # split between two lanes), on rows of 165 blocks of 16, 82 of 32 or 40
+    # of 64 values, which most counts do not divide: the row's last thread
+    # holds fewer units and its last warp idles in part
     D = 2640 if B == 16 else 2624 if B == 32 else 2560
     X, g = workloads.mx_inputs(150, D, seed=B + D, t_frac=0.1, with_gamma=True)
     try:
