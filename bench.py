@@ -387,21 +387,27 @@ def run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world):
     for _ in range(2):
         step()
     nts.check_status()
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        step()
-    torch.cuda.synchronize()
-    t1 = time.perf_counter()
-    barrier(world)
+    # three timed runs of `steps` steps; the median one is reported (a host
+    # copy over C2C now and then runs at a fraction of its rate for a while)
+    runs = []
+    for _ in range(3):
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            step()
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        barrier(world)
+        runs.append(t1 - t0)
     nts.check_status()
-    elapsed = max_over_ranks(t1 - t0, world)
+    elapsed = max_over_ranks(statistics.median(runs), world)
     total = sum(step_bytes().values())
     h2d = 2 * QK_T * QK_H * 2 + 3 * MX_T * MX_D * 2
     d2h = 2 * QK_T * QK_H * 2 + 3 * (MX_T * MX_D + MX_T * (MX_D // MX_B))
     return {"value": round(world * total * steps / elapsed / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "runs_ms_per_step": [round(r / steps * 1e3, 3) for r in runs], "reported": "median run",
             "ms_per_step": round(elapsed / steps * 1e3, 4),
             "path": "nts_*_host C ABI entry points, pinned host buffers",
             "copy_only_gbs": copy_ceiling(
@@ -411,7 +417,7 @@ def run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world):
                 + [(scales_h[n], scales_d) for n in KERNELS[1:]], total)}
 
 
-def copy_ceiling(torch, ins, outs, total, reps=4):
+def copy_ceiling(torch, ins, outs, total, reps=5):
     """The step's bytes moved by plain copies alone, between the very host
     and device buffers the e2e step uses (so the same pinned pages): every
     (device, host) pair of `ins` host->device on one stream, every (host,
@@ -437,12 +443,13 @@ def copy_ceiling(torch, ins, outs, total, reps=4):
 
     copies()
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
+    times = []
     for _ in range(reps):
+        t0 = time.perf_counter()
         copies()
-    torch.cuda.synchronize()
-    dt = (time.perf_counter() - t0) / reps
-    return round(total / dt / 1e9, 1)
+        torch.cuda.synchronize()
+        times.append(time.perf_counter() - t0)
+    return round(total / statistics.median(times) / 1e9, 1)
 
 
 def mxnorm_sweep(nts, torch, dev, peak, reps=20):
