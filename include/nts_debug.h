@@ -60,6 +60,16 @@ NTS_API int nts_debug_set_direct(int on);
 NTS_API int nts_debug_set_host_chunks(int max_chunks, int64_t min_chunk_bytes);
 
 /*
+ * Test hook: the next `count` kernel launches (of any entry point, after its
+ * argument checks) return `status` -- NTS_ERR_CUDA, NTS_ERR_UNSUPPORTED or
+ * NTS_ERR_TIMEOUT -- instead of launching, with nts_last_error() saying the
+ * failure was injected; the device is not touched.  count = 0 turns the hook
+ * off.  Lets callers' error handling be tested without a failing GPU.
+ * Errors: INVALID_ARG for count < 0 or another status.
+ */
+NTS_API int nts_debug_inject_failure(int status, int count);
+
+/*
  * Programmatic dependent launch: 1 (default) = every kernel is launched with
  * programmatic stream serialization, so it may be scheduled while the grid
  * before it in the stream finishes (it waits for that grid's completion

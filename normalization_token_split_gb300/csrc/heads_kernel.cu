@@ -260,6 +260,7 @@ bool heads_whole_path(int64_t H, int64_t head_dim, int N) {
 
 int launch_heads(const void* X, const float* gamma, void* Y, float* rinv, int64_t T, int64_t H,
                  int64_t head_dim, float eps, cudaStream_t stream, const LaunchTuning& tune) {
+  if (const int injected = take_injected_failure()) return injected;
   const DeviceInfo& dev = device_info();
   if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
   const int nvec = (int)(H / 8);

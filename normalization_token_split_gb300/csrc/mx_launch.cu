@@ -60,6 +60,7 @@ MxKernel pick_mx(int fmt, int stat, int B, int bpt) {
 }  // namespace
 
 int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune) {
+  if (const int injected = take_injected_failure()) return injected;
   const int D = (int)rq.D;
   const int K = D / rq.B;
   const DeviceInfo& dev = device_info();

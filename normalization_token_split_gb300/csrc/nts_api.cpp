@@ -63,6 +63,18 @@ LaunchTuning current_tuning() {
   return g_tune;
 }
 
+std::atomic<int> g_inject_left{0};
+std::atomic<int> g_inject_status{NTS_OK};
+
+int take_injected_failure() {
+  int left = g_inject_left.load();
+  while (left > 0 && !g_inject_left.compare_exchange_weak(left, left - 1)) {
+  }
+  if (left <= 0) return NTS_OK;
+  return fail(g_inject_status.load(), "injected failure (nts_debug_inject_failure), %d left",
+              left - 1);
+}
+
 // ----------------------------------------------------------- device facts
 
 const DeviceInfo& device_info() {
@@ -734,6 +746,16 @@ int nts_debug_set_host_chunks(int max_chunks, int64_t min_chunk_bytes) {
                 kMaxChunks);
   g_max_chunks = max_chunks == 0 ? kDefaultChunks : max_chunks;
   g_chunk_bytes = min_chunk_bytes == 0 ? kDefaultChunkBytes : (size_t)min_chunk_bytes;
+  return NTS_OK;
+}
+
+int nts_debug_inject_failure(int status, int count) {
+  if (count < 0) return fail(NTS_ERR_INVALID_ARG, "count must be >= 0");
+  if (count > 0 && status != NTS_ERR_CUDA && status != NTS_ERR_UNSUPPORTED &&
+      status != NTS_ERR_TIMEOUT)
+    return fail(NTS_ERR_INVALID_ARG, "status must be NTS_ERR_CUDA, _UNSUPPORTED or _TIMEOUT");
+  g_inject_status = status;
+  g_inject_left = count;
   return NTS_OK;
 }
 

@@ -44,6 +44,11 @@ inline cudaLaunchAttribute pdl_attribute() {
 
 LaunchTuning current_tuning();
 
+// Test hook (nts_debug_inject_failure): while injections remain, the next
+// launch returns the injected status (with last-error text saying so)
+// instead of touching the device; otherwise NTS_OK.
+int take_injected_failure();
+
 // The zeroed counter pair of `stream` for a dynamically scheduled launch
 // (sched.cu), or nullptr: schedule round-robin.
 unsigned int* sched_counters(cudaStream_t stream);

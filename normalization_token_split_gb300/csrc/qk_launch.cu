@@ -10,6 +10,7 @@ namespace nts {
 
 int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkOptions& opt,
                   cudaStream_t stream, const LaunchTuning& tune) {
+  if (const int injected = take_injected_failure()) return injected;
   const int layernorm = opt.layernorm;
   const int ES = opt.in_e4m3 ? 1 : 2;
   const int NS = layernorm ? 2 : 1;

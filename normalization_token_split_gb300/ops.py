@@ -384,6 +384,14 @@ def set_host_chunks(max_chunks: int = 0, min_chunk_bytes: int = 0) -> None:
     check(lib().nts_debug_set_host_chunks(int(max_chunks), int(min_chunk_bytes)))
 
 
+def inject_failure(status: str = "CUDA", count: int = 1) -> None:
+    """The next `count` launches fail with NTS_ERR_<status> (CUDA,
+    UNSUPPORTED or TIMEOUT) without touching the device; count=0 turns the
+    hook off (nts_debug_inject_failure)."""
+    codes = {"CUDA": 3, "UNSUPPORTED": 2, "TIMEOUT": 4}
+    check(lib().nts_debug_inject_failure(codes[status], int(count)))
+
+
 def set_pdl(on: bool) -> None:
     """Launch with programmatic stream serialization (default on); results
     do not depend on it (nts_debug_set_pdl)."""

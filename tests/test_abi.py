@@ -224,6 +224,22 @@ def test_qk_mxcast_argument_checks(lib):
     assert f(T=0, X=None, c=None, s=None) == OK
 
 
+def test_injected_launch_failures_reach_the_caller(lib):
+    CUDA, TIMEOUT = 3, 4
+    try:
+        assert lib.nts_debug_inject_failure(CUDA, 2) == OK
+        assert _qk(lib) == CUDA                       # arguments pass; the launch "fails"
+        assert b"injected" in lib.nts_last_error()
+        assert _mx(lib, "mx") == CUDA
+        assert lib.nts_debug_inject_failure(TIMEOUT, 1) == OK
+        assert _qk(lib) == TIMEOUT
+        assert _qk(lib, H=7) == INVALID               # argument checks still come first
+        assert lib.nts_debug_inject_failure(1, 1) == INVALID
+        assert lib.nts_debug_inject_failure(CUDA, -1) == INVALID
+    finally:
+        assert lib.nts_debug_inject_failure(0, 0) == OK
+
+
 def test_qk_mxcast_fused_argument_checks(lib):
     def f(**k):
         return lib.nts_qknorm_rms_qk_mxcast(
