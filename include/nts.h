@@ -9,11 +9,16 @@
  *    framework such as PyTorch); pointers named *_host are host pointers
  *    (pinned memory gives asynchronous copies).  Entry points without a
  *    suffix take device pointers only.  The caller owns every buffer; the
- *    library allocates no device memory (it keeps one status word per kernel
- *    family as a static device variable).
+ *    library allocates no device memory at run time.  Its static device
+ *    state: one status word per kernel family, a 512 KB pool of tile
+ *    counters (a pair per stream, and one per launch recorded into a CUDA
+ *    graph), and the 16 MiB staging array of nts_mxnorm_cast_host_noalloc.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls only enqueue work and return; results are ready once
- *    the stream has reached that point.
+ *    the stream has reached that point.  Kernels are launched as
+ *    programmatic dependents: one may be scheduled while the previous
+ *    kernel in the stream drains, but it touches no global memory before
+ *    that kernel has completed, so stream order holds as usual.
  *  - Matrices are row-major with one token per row: element (t, j) of a
  *    [T, H] matrix is at index t*H + j.  bf16 means IEEE-style bfloat16
  *    (uint16 storage).  Device pointers must be 16-byte aligned.
