@@ -419,6 +419,29 @@ def test_host_buffer_form_in_chunks(T, D, B, fmt):
         ch.zero_()
 
 
+@pytest.mark.parametrize("chunks,min_bytes", [(64, 1 << 20), (7, 1 << 20), (2, 1 << 20), (1, 0)])
+def test_host_buffer_form_any_chunking(chunks, min_bytes):
+    # the chunk count changes only how the rows flow through the copy
+    # streams: the outputs are those of the device path bit for bit
+    T, D = 7001, 2048
+    X, _ = workloads.mx_inputs(T, D, seed=17 + chunks, t_frac=0.05)
+    Xh = X.pin_memory()
+    ch = torch.empty(T, D // 2, dtype=torch.uint8).pin_memory()
+    sh = torch.empty(T, D // 32, dtype=torch.uint8).pin_memory()
+    Xd = torch.empty_like(X, device=DEV)
+    cd = torch.empty(T, D // 2, dtype=torch.uint8, device=DEV)
+    sd = torch.empty(T, D // 32, dtype=torch.uint8, device=DEV)
+    try:
+        nts.set_host_chunks(chunks, min_bytes)
+        nts.rmsnorm_mxcast_host(Xh, None, ch, sh, Xd, cd, sd, eps=1e-6, B=32, fmt="e2m1")
+        nts.check_status()
+    finally:
+        nts.set_host_chunks()
+    ref = nts.rmsnorm_mxcast(X.to(DEV), None, eps=1e-6, B=32, fmt="e2m1")
+    nts.check_status()
+    assert torch.equal(ch, ref.codes.cpu()) and torch.equal(sh, ref.scales.cpu())
+
+
 def test_graph_replays_alongside_direct_launches():
     # a launch recorded into a CUDA graph owns its tile counters; direct
     # launches on other streams keep theirs, so the two never share one.  The
