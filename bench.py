@@ -203,15 +203,26 @@ def kernel_traffic():
                     found[m.group(1)] = (int(m.group(2)), m.group(3))
     out = {}
     for name, files in KERNEL_SOURCES.items():
-        h = hashlib.sha256()
         try:
-            for f in files:
-                h.update(open(os.path.join(ROOT, f), "rb").read())
+            digest = source_digest(files)
         except OSError:
             continue
-        if name in found and found[name][1] == h.hexdigest()[:16]:
+        if name in found and found[name][1] == digest:
             out[name] = found[name][0]
     return out
+
+
+def source_digest(files):
+    """sha256 (16 hex digits) of the files' code with comments and blank
+    lines removed, so that an edit of comments alone keeps the digest."""
+    h = hashlib.sha256()
+    for f in files:
+        text = open(os.path.join(ROOT, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+        h.update("\n".join(lines).encode())
+    return h.hexdigest()[:16]
 
 
 # ------------------------------------------------------------ GPU arm

@@ -16,21 +16,25 @@
 //    keeps a ring of S shared-memory stages filled with one 1-D bulk TMA copy
 //    per tile (the rows are contiguous); consumer warps hand a stage back
 //    through an "empty" mbarrier;
-//  * every consumer thread owns whole MX blocks, so a block's absmax, its
-//    E8M0 exponent and its scale byte are thread-local: no shuffles, one
-//    exponent per block.  Without a gain the absmax runs on packed bf16
-//    pairs (max.xorsign.abs.bf16x2); the products x*rinv*2^-e run on the
-//    packed f32x2 pipes, and the element cast is the hardware
+//  * every consumer thread owns whole MX blocks of 16 or 32 values, so a
+//    block's absmax, its scale exponent and its scale byte are
+//    thread-local: no shuffles, one exponent per block; a block of 64 values
+//    is split between two adjacent lanes (32 values each) that combine their
+//    absmaxes with one shuffle.  A row takes 16 threads (two rows per warp)
+//    or whole warps.  Without a gain the absmax runs on packed bf16 pairs
+//    (max.xorsign.abs.bf16x2); the products x*rinv*2^-e run on the packed
+//    f32x2 pipes, and the element cast is the hardware
 //    cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32;
-//  * a thread's block is B/8 16-byte vectors 2B bytes apart from its
-//    neighbours'; thread L reads them starting at vector (L*B/64) mod (B/8)
-//    so the eight lanes of each shared-memory phase hit eight distinct bank
-//    groups;
+//  * a thread's unit (a block, or half of a 64-value block) is U 16-byte
+//    vectors 16*U bytes apart from its neighbours'; thread L reads them
+//    starting at vector (L*U/8) mod U so the eight lanes of each
+//    shared-memory phase hit eight distinct bank groups;
 //  * the row is read from shared memory twice (statistic, then cast), so no
 //    thread holds more than its block absmaxes between the passes; the stage
 //    is released after the second pass;
-//  * the row statistic is a warp shuffle reduction; a row wider than one
-//    warp adds one exchange through shared memory guarded by an mbarrier.
+//  * the row statistic is a shuffle reduction over the row's 16 or 32
+//    lanes; a row wider than one warp adds one exchange through shared
+//    memory guarded by an mbarrier.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -55,7 +59,7 @@ struct MxParams {
   int64_t T;
   int64_t ntiles;
   int D;
-  int K;                // D / B blocks per row
+  int K;                // D / B blocks per row (units: K, or 2K for B = 64)
   int G;                // consumer threads per row: 16 (two rows per warp) or a multiple of 32
   int R;                // rows per tile
   int S;                // ring stages
