@@ -5,6 +5,7 @@
 #include <algorithm>
 
 #include "mx_kernel.cuh"
+#include "nts_debug.h"
 
 namespace nts {
 
@@ -59,19 +60,25 @@ MxKernel pick_mx(int fmt, int stat, int B, int bpt) {
 
 }  // namespace
 
-int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune) {
-  if (const int injected = take_injected_failure()) return injected;
-  const int D = (int)rq.D;
-  const int K = D / rq.B;
-  const DeviceInfo& dev = device_info();
-  if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
+// The launch shape of an MX request, without touching the device: units
+// per thread, threads per row, rows per tile, ring stages, shared memory
+// and the kernel, from the request's sizes, the device's SM count and
+// opt-in shared memory per CTA, and the tuning overrides.
+struct MxLaunchShape {
+  int bpt = 0, G = 0, R = 0, S = 0;
+  size_t smem = 0;
+  MxKernel kern = nullptr;
+};
 
+int mx_launch_shape(int64_t T, int D, int B, int fmt, int p, int sm_count, int max_smem_optin,
+                    const LaunchTuning& tune, MxLaunchShape* out) {
+  const int K = D / B;
   // tune.force_vpt selects the units per thread for this kernel family; a
   // unit is a block, or half a block of 64 values (the kernel splits those
   // between two lanes, each with the 32-value layout)
-  const bool split = rq.B == 64;
+  const bool split = B == 64;
   const MxShape sh = split ? choose_mx_shape(2 * K, 4, tune.force_vpt)
-                           : choose_mx_shape(K, rq.B / 8, tune.force_vpt);
+                           : choose_mx_shape(K, B / 8, tune.force_vpt);
   if (sh.G == 0) return fail(NTS_ERR_UNSUPPORTED, "row too wide: D = %d", D);
 
   // Rows per tile: about four consumer warps and at least 8 KB per stage;
@@ -79,7 +86,7 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   int R = std::max(1, 128 / sh.G);
   R = std::max(R, (8192 + 2 * D - 1) / (2 * D));
   R = std::min(R, std::max(1, kMaxConsumers / sh.G));
-  while (R > 1 && (rq.T + R - 1) / R < (int64_t)2 * dev.sm_count) R /= 2;
+  while (R > 1 && (T + R - 1) / R < (int64_t)2 * sm_count) R /= 2;
   if (sh.G < 32) R = (R + 1) / 2 * 2;   // whole warps: an even number of 16-thread rows
   if (tune.force_rows > 0) R = tune.force_rows;
   if (R * sh.G > kMaxConsumers) return fail(NTS_ERR_UNSUPPORTED, "tile of %d rows too large", R);
@@ -92,17 +99,40 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   // with two stages and three CTAs per SM than with three and two).
   const int stage = R * D * 2;
   int S = stage > 24576 ? 2 : (stage >= 12288 ? 3 : 4);
-  const bool nvfp4 = rq.fmt == NTS_FMT_NVFP4;
+  const bool nvfp4 = fmt == NTS_FMT_NVFP4;
   while (S > 2 && mx_layout(S, R, D, sh.G, nvfp4).total > (uint32_t)tune.smem_budget) --S;
-  while (S > 1 && mx_layout(S, R, D, sh.G, nvfp4).total > (uint32_t)dev.max_smem_optin) --S;
+  while (S > 1 && mx_layout(S, R, D, sh.G, nvfp4).total > (uint32_t)max_smem_optin) --S;
   if (tune.force_stages > 0) S = tune.force_stages;
   const size_t smem = mx_layout(S, R, D, sh.G, nvfp4).total;
-  if (smem > (size_t)dev.max_smem_optin)
+  if (smem > (size_t)max_smem_optin)
     return fail(NTS_ERR_UNSUPPORTED, "row too wide for shared memory: D = %d", D);
 
-  const int stat = rq.p == 0 ? kStatRms : (rq.p == 1 ? kStatMxP1 : kStatMxP2);
-  MxKernel kern = pick_mx(rq.fmt, stat, rq.B, sh.bpt);
-  if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for B=%d bpt=%d", rq.B, sh.bpt);
+  const int stat = p == 0 ? kStatRms : (p == 1 ? kStatMxP1 : kStatMxP2);
+  MxKernel kern = pick_mx(fmt, stat, B, sh.bpt);
+  if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for B=%d bpt=%d", B, sh.bpt);
+  out->bpt = sh.bpt;
+  out->G = sh.G;
+  out->R = R;
+  out->S = S;
+  out->smem = smem;
+  out->kern = kern;
+  return NTS_OK;
+}
+
+int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune) {
+  if (const int injected = take_injected_failure()) return injected;
+  const int D = (int)rq.D;
+  const int K = D / rq.B;
+  const DeviceInfo& dev = device_info();
+  if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
+  MxLaunchShape ls;
+  int rc = mx_launch_shape(rq.T, D, rq.B, rq.fmt, rq.p, dev.sm_count, dev.max_smem_optin, tune,
+                           &ls);
+  if (rc != NTS_OK) return rc;
+  const MxShape sh{ls.bpt, ls.G};
+  const int R = ls.R, S = ls.S;
+  const size_t smem = ls.smem;
+  MxKernel kern = ls.kern;
 
   MxParams prm;
   prm.X = static_cast<const __nv_bfloat16*>(rq.X);
@@ -127,7 +157,7 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   prm.missing_tx = tune.missing_tx;
   prm.sched = tune.dynamic ? sched_counters(stream) : nullptr;
 
-  int rc = prepare_kernel((const void*)kern, smem);
+  rc = prepare_kernel((const void*)kern, smem);
   if (rc != NTS_OK) return rc;
 
   const int nthreads = R * sh.G + 32;  // consumers + producer warp
@@ -173,3 +203,23 @@ int read_and_clear_mx_status(unsigned* out) {
 }
 
 }  // namespace nts
+
+extern "C" int nts_debug_mx_launch_shape(int64_t T, int64_t D, int B, int fmt, int p,
+                                         int sm_count, int max_smem_optin, int32_t* shape) {
+  using namespace nts;
+  if (shape == nullptr || T < 0 || D <= 0 || D > (1 << 30) || sm_count <= 0 ||
+      max_smem_optin <= 0 || (B != 16 && B != 32 && B != 64) || D % B != 0 || p < 0 || p > 2 ||
+      (fmt != NTS_FMT_E4M3 && fmt != NTS_FMT_E2M1 && fmt != NTS_FMT_NVFP4) ||
+      (fmt == NTS_FMT_NVFP4 && B != 16))
+    return fail(NTS_ERR_INVALID_ARG, "bad shape query");
+  MxLaunchShape ls;
+  const int rc = mx_launch_shape(T, (int)D, B, fmt, p, sm_count, max_smem_optin,
+                                 current_tuning(), &ls);
+  if (rc != NTS_OK) return rc;
+  shape[0] = ls.bpt;
+  shape[1] = ls.G;
+  shape[2] = ls.R;
+  shape[3] = ls.S;
+  shape[4] = (int32_t)ls.smem;
+  return NTS_OK;
+}
