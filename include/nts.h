@@ -227,8 +227,8 @@ NTS_API int nts_qknorm_rms_qk_mxcast(const void *Q_dev, const float *gamma_q_dev
 
 /*
  * nts_rmsnorm_mxcast -- RMSNorm fused with the MX cast (MXNorm card,
- * Fig. 1 caption, left graph; Fig. 8 "normalization and casting fused into a
- * single kernel"):
+ * Fig. 1 caption, left graph; Fig. 8, where the normalization and the cast
+ * are one fused kernel):
  *
  *     rinv     = 1 / sqrt((1/D) sum_j x_j^2 + eps)      (statistic of x, fp32)
  *     w_j      = fp32(x_j * gamma_j), or x_j when gamma_dev is NULL
@@ -236,7 +236,7 @@ NTS_API int nts_qknorm_rms_qk_mxcast(const void *Q_dev, const float *gamma_q_dev
  *     e_k      = round(log2(fp32(amax_k * rinv))) - emax, clamped to
  *                [-127, 127], where round() is to the nearest integer in the
  *                log2 domain (mantissa >= sqrt 2 rounds up) and emax = 8
- *                (E4M3, "divide by 256") or 2 (E2M1)
+ *                (E4M3: the scale divides the absmax by 256) or 2 (E2M1)
  *     scale_k  = e_k + 127                                   (E8M0 byte)
  *     code_j   = cast_rne_satfinite(fp32(w_j * rinv) * 2^-e_k)
  *
