@@ -369,17 +369,18 @@ NTS_API int nts_mxnorm_cast_host(const void *X_host, const float *gamma_dev,
  *
  * Set-up: the first call on each device looks up the array's device address
  * (and fills the library's host-side launch caches: device facts, kernel
- * attributes, c(B, p), the stream's tile counters).  Its staging is too
- * small for the chunked copies of the other host-buffer forms, so it never
- * creates their copy streams.  Make that first call before any stream
- * capture; later calls on that device and stream allocate nothing, host or
- * device.
+ * attributes, c(B, p), the stream's tile counters).  Its copies and its
+ * kernel all run on `stream` in one piece, never chunked, so it never
+ * creates the copy streams of the other host-buffer forms.  Make that first
+ * call before any stream capture; later calls on that device and stream
+ * allocate nothing, host or device.
  * Sharing: every call on a device uses the same array, so calls that overlap
  * in time (other streams, unordered host threads) race and corrupt each
  * other's staging; serialize them.  Nothing in the array needs to start at
  * zero: each call copies in all the kernel reads.
- * Errors: as nts_mxnorm_cast_host; UNSUPPORTED when the call needs more than
- * 16 MiB of staging (2*T*D bytes of X, 4*D of gamma, T*D or T*D/2 of codes,
+ * Errors: as nts_mxnorm_cast_host, and every argument is checked before
+ * anything is enqueued; UNSUPPORTED when the call needs more than 16 MiB of
+ * staging (2*T*D bytes of X, 4*D of gamma, T*D or T*D/2 of codes,
  * T*D/B of scales, each rounded up to 256 bytes), or for a device ordinal
  * of 64 or more.
  */

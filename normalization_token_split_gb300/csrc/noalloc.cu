@@ -71,20 +71,22 @@ extern "C" {
 int nts_mxnorm_cast_host_noalloc(const void* X_host, const float* gamma_host,
                                  uint8_t* codes_host, uint8_t* scales_host, int64_t T, int64_t D,
                                  float eps, int B, int fmt, int p, void* stream) {
-  if (T < 0) return fail(NTS_ERR_INVALID_ARG, "T must be >= 0, got %lld", (long long)T);
+  // Every argument is checked before anything is enqueued or the array is
+  // touched.  First the scalars (this bounds D by 32768)...
+  int rc = validate_mx_scalars(T, D, eps, B, fmt, p, true);
+  if (rc != NTS_OK) return rc;
   if (T > 0 && (X_host == nullptr || codes_host == nullptr || scales_host == nullptr))
     return fail(NTS_ERR_INVALID_ARG, "X_host, codes_host and scales_host must be non-NULL");
-  if (D <= 0) return fail(NTS_ERR_INVALID_ARG, "D must be > 0, got %lld", (long long)D);
-  if (B != 16 && B != 32 && B != 64)
-    return fail(NTS_ERR_INVALID_ARG, "B must be 16, 32 or 64, got %d", B);
-  if (D % B != 0)
-    return fail(NTS_ERR_INVALID_ARG, "D (%lld) must be a multiple of B (%d)", (long long)D, B);
-  if (fmt != NTS_FMT_E4M3 && fmt != NTS_FMT_E2M1 && fmt != NTS_FMT_NVFP4)
-    return fail(NTS_ERR_INVALID_ARG, "unknown element format %d", fmt);
-  if (p != 1 && p != 2) return fail(NTS_ERR_INVALID_ARG, "p must be 1 or 2, got %d", p);
-
-  // Scratch this call needs; beyond the array's capacity it is refused.
-  const size_t xb = round256((size_t)T * (size_t)D * 2);
+  // ... then the capacity: X alone takes 2*T*D bytes, so a T above
+  // capacity / (2*D) is refused before any product of T is formed (no
+  // product below can then wrap around).
+  const size_t xrow = (size_t)D * 2;
+  if ((uint64_t)T > kNoAllocScratchBytes / xrow)
+    return fail(NTS_ERR_UNSUPPORTED,
+                "T=%lld, D=%lld: X alone exceeds the %zu-byte static scratch "
+                "(use nts_mxnorm_cast_host with caller-owned buffers)",
+                (long long)T, (long long)D, kNoAllocScratchBytes);
+  const size_t xb = round256((size_t)T * xrow);
   const size_t gb = gamma_host != nullptr ? round256((size_t)D * 4) : 0;
   const size_t cb = round256((size_t)T * (size_t)(fmt == NTS_FMT_E4M3 ? D : D / 2));
   const size_t sb = round256((size_t)T * (size_t)(D / B));
@@ -97,7 +99,7 @@ int nts_mxnorm_cast_host_noalloc(const void* X_host, const float* gamma_host,
   if (T == 0) return NTS_OK;
 
   void* base = nullptr;
-  int rc = scratch_address(&base);
+  rc = scratch_address(&base);
   if (rc != NTS_OK) return rc;
   unsigned char* at = static_cast<unsigned char*>(base);
   void* X_dev = at;
@@ -111,9 +113,9 @@ int nts_mxnorm_cast_host_noalloc(const void* X_host, const float* gamma_host,
                                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "copying gamma to the device");
   }
-  // the existing host-buffer path, run on the static staging
-  return nts_mxnorm_cast_host(X_host, gamma_dev, codes_host, scales_host, X_dev, codes_dev,
-                              scales_dev, T, D, eps, B, fmt, p, stream);
+  // copy in, kernel and copy back, all on the caller's stream
+  return mxnorm_cast_host_one_stream(X_host, gamma_dev, codes_host, scales_host, X_dev, codes_dev,
+                                     scales_dev, T, D, eps, B, fmt, p, stream);
 }
 
 }  // extern "C"

@@ -280,12 +280,12 @@ int validate_qk(const void* X, const float* gamma, const void* Y, const float* r
   return NTS_OK;
 }
 
-int validate_mx(const void* X, const float* gamma, const uint8_t* codes, const uint8_t* scales,
-                const float* rinv, const float* amax, int64_t T, int64_t D, float eps, int B,
-                int fmt, int p, bool mxnorm) {
+}  // namespace
+
+// The checks of an MX call that involve no pointer.
+int nts::validate_mx_scalars(int64_t T, int64_t D, float eps, int B, int fmt, int p,
+                             bool mxnorm) {
   if (T < 0) return fail(NTS_ERR_INVALID_ARG, "T must be >= 0, got %lld", (long long)T);
-  if (T > 0 && (X == nullptr || codes == nullptr || scales == nullptr))
-    return fail(NTS_ERR_INVALID_ARG, "X, codes and scales must be non-NULL");
   if (D <= 0) return fail(NTS_ERR_INVALID_ARG, "D must be > 0, got %lld", (long long)D);
   if (B != 16 && B != 32 && B != 64)
     return fail(NTS_ERR_INVALID_ARG, "B must be 16, 32 or 64, got %d", B);
@@ -299,6 +299,18 @@ int validate_mx(const void* X, const float* gamma, const uint8_t* codes, const u
   if (!(eps > 0.f) || !std::isfinite(eps))
     return fail(NTS_ERR_INVALID_ARG, "eps must be positive and finite");
   if (D > 32768) return fail(NTS_ERR_UNSUPPORTED, "D (%lld) exceeds 32768", (long long)D);
+  return NTS_OK;
+}
+
+namespace {
+
+int validate_mx(const void* X, const float* gamma, const uint8_t* codes, const uint8_t* scales,
+                const float* rinv, const float* amax, int64_t T, int64_t D, float eps, int B,
+                int fmt, int p, bool mxnorm) {
+  const int rc = validate_mx_scalars(T, D, eps, B, fmt, p, mxnorm);
+  if (rc != NTS_OK) return rc;
+  if (T > 0 && (X == nullptr || codes == nullptr || scales == nullptr))
+    return fail(NTS_ERR_INVALID_ARG, "X, codes and scales must be non-NULL");
   if (!aligned(X, 16) || !aligned(codes, 16) || (gamma != nullptr && !aligned(gamma, 16)) ||
       (rinv != nullptr && !aligned(rinv, 4)) || (amax != nullptr && !aligned(amax, 4)))
     return fail(NTS_ERR_UNSUPPORTED, "X, gamma and codes must be 16-byte aligned");
@@ -657,10 +669,12 @@ int nts_qknorm_rms_host(const void* X_host, const float* gamma_dev, void* Y_host
   return run_host_pipeline(T, rb, stream, in, kern, out);
 }
 
+// one_stream: every copy and the kernel on the caller's stream, in one piece
+// (no chunking, so the pipeline's own streams and events are never needed).
 static int mx_host(const void* X_host, const float* gamma_dev, uint8_t* codes_host,
                    uint8_t* scales_host, void* X_dev, uint8_t* codes_dev, uint8_t* scales_dev,
                    int64_t T, int64_t D, float eps, int B, int fmt, int p, bool mxnorm,
-                   void* stream) {
+                   void* stream, bool one_stream = false) {
   if (T > 0 && (X_host == nullptr || codes_host == nullptr || scales_host == nullptr))
     return fail(NTS_ERR_INVALID_ARG, "X_host, codes_host and scales_host must be non-NULL");
   int rc = validate_mx(X_dev, gamma_dev, codes_dev, scales_dev, nullptr, nullptr, T, D, eps, B,
@@ -686,6 +700,12 @@ static int mx_host(const void* X_host, const float* gamma_dev, uint8_t* codes_ho
                cudaMemcpyDeviceToHost, st, "copying scales to the host");
     return c;
   };
+  if (one_stream) {
+    rc = in(0, T, stream);
+    if (rc == NTS_OK) rc = kern(0, T, stream);
+    if (rc == NTS_OK) rc = out(0, T, stream);
+    return rc;
+  }
   return run_host_pipeline(T, xr, stream, in, kern, out);
 }
 
@@ -704,6 +724,18 @@ int nts_mxnorm_cast_host(const void* X_host, const float* gamma_dev, uint8_t* co
   return mx_host(X_host, gamma_dev, codes_host, scales_host, X_dev, codes_dev, scales_dev, T, D,
                  eps, B, fmt, p, true, stream);
 }
+
+}  // extern "C"
+
+int nts::mxnorm_cast_host_one_stream(const void* X_host, const float* gamma_dev,
+                                     uint8_t* codes_host, uint8_t* scales_host, void* X_dev,
+                                     uint8_t* codes_dev, uint8_t* scales_dev, int64_t T,
+                                     int64_t D, float eps, int B, int fmt, int p, void* stream) {
+  return mx_host(X_host, gamma_dev, codes_host, scales_host, X_dev, codes_dev, scales_dev, T, D,
+                 eps, B, fmt, p, true, stream, true);
+}
+
+extern "C" {
 
 // ------------------------------------------------------------- debug hooks
 

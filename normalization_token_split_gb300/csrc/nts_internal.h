@@ -133,6 +133,16 @@ int launch_heads(const void* X, const float* gamma, void* Y, float* rinv, int64_
                  int64_t head_dim, float eps, cudaStream_t stream, const LaunchTuning& tune);
 int read_and_clear_heads_status(unsigned* out);
 
+// The checks of an MX call (RMSNorm+MXCast or MXNorm) that involve no
+// pointer: T, D, eps, B, fmt and p.
+int validate_mx_scalars(int64_t T, int64_t D, float eps, int B, int fmt, int p, bool mxnorm);
+// nts_mxnorm_cast_host with its copies and kernel all on `stream`, never
+// chunked (so it creates no copy streams or events).
+int mxnorm_cast_host_one_stream(const void* X_host, const float* gamma_dev, uint8_t* codes_host,
+                                uint8_t* scales_host, void* X_dev, uint8_t* codes_dev,
+                                uint8_t* scales_dev, int64_t T, int64_t D, float eps, int B,
+                                int fmt, int p, void* stream);
+
 int read_and_clear_qk_status(unsigned* out);
 int read_and_clear_mx_status(unsigned* out);
 

@@ -259,8 +259,8 @@ def test_qk_mxcast_fused_argument_checks(lib):
 
 def test_noalloc_argument_checks(lib):
     f = lambda **k: lib.nts_mxnorm_cast_host_noalloc(
-        k.get("X", A16), None, A16, A16, k.get("T", 4), k.get("D", 256), 1e-6, k.get("B", 32),
-        k.get("fmt", 0), k.get("p", 2), None)
+        k.get("X", A16), k.get("g", None), A16, A16, k.get("T", 4), k.get("D", 256),
+        k.get("eps", 1e-6), k.get("B", 32), k.get("fmt", 0), k.get("p", 2), None)
     assert f(X=None) == INVALID
     assert f(B=8) == INVALID
     assert f(p=3) == INVALID
@@ -269,3 +269,13 @@ def test_noalloc_argument_checks(lib):
     assert f(T=4096, D=4096) == UNSUPPORTED      # beyond the 16 MiB static scratch
     assert b"static scratch" in lib.nts_last_error()
     assert f(T=0, X=None) == OK
+    # sizes whose byte counts would wrap around 64 bits are refused before
+    # any product is formed
+    assert f(T=1 << 53, D=32768, B=16) == UNSUPPORTED
+    assert f(T=(1 << 63) - 1, D=32768, B=64, fmt=1) == UNSUPPORTED
+    assert f(T=4, D=65536) == UNSUPPORTED
+    # a refused call enqueues nothing, not even the gamma copy (with no GPU
+    # here, an enqueued copy would surface as a CUDA error, not INVALID)
+    assert f(g=A16, eps=0.0) == INVALID
+    assert f(g=A16, fmt=2, B=32) == INVALID      # NVFP4 blocks are 16 values
+    assert f(g=A16, B=24, D=240) == INVALID
