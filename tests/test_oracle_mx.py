@@ -13,6 +13,14 @@ MXNorm card and mathematics fix.
 * The SwiftQK worked example through the RMSNorm + MXCast statistic.
 * Invariants: scale invariance at eps = 0, gamma = None equals gamma = 1,
   power-mean inequality M_1 <= M_2.
+* Where the gain enters each statistic (Fig. 1 caption: the left graph,
+  RMSNorm + MXCast, takes its statistic from x as Eq. (1) of the SwiftQK
+  notes does and applies the gain afterwards; the right graph, MXNorm, takes
+  it from the block absmaxes of the tensor being cast, w = x*gamma):
+  closed forms on constant rows with a constant gain g != 1, RMSNorm +
+  MXCast's factor unchanged by any gain, and power-of-two gains that make
+  w exactly representable in bf16, so that a call with the gain must equal
+  a call without it on the pre-multiplied tensor.
 
 MXCast semantics beyond these are unpinned by the pages (no worked MX example
 is printed); the pins above are the definition's own consequences and the
@@ -253,3 +261,89 @@ def test_postround_estimate_within_sqrt2_of_preround():
         ratio = r_pre / r_post                      # = rho_post / rho_pre
         assert np.all(ratio >= 2 ** -0.5 * (1 - 1e-12)) and np.all(ratio <= 2 ** 0.5 * (1 + 1e-12))
         assert not np.allclose(ratio, 1.0)          # the rounding does change the estimate
+
+
+# ---- the gain in the two statistics (Fig. 1 caption, left and right graphs)
+
+@pytest.mark.parametrize("B", [16, 32, 64])
+@pytest.mark.parametrize("p", [1, 2])
+@pytest.mark.parametrize("fmt", [oracle.FMT_E4M3, oracle.FMT_E2M1])
+@pytest.mark.parametrize("g", [3.0, 0.375, -2.0])
+def test_constant_rows_with_constant_gain(B, p, fmt, g):
+    # x = c*1 and gamma = g*1 with c*g exact in fp32: every block absmax of
+    # w = x*gamma is |c*g|
+    cs = [1.0, -2.5, 0.0625, 40.0]
+    D, eps = 4 * B, 1e-6
+    Xb = workloads.bf16_bits(workloads.constant_rows(len(cs), D, cs))
+    gam = np.full(D, g, np.float32)
+    cB = oracle.mx_correction(B, p)
+    _, _, rinv_m, amax_m = oracle.mxnorm_cast(Xb, gam, eps, B, fmt, p)
+    _, _, rinv_r, amax_r = oracle.rmsnorm_mxcast(Xb, gam, eps, B, fmt)
+    for t, c in enumerate(cs):
+        assert np.all(amax_m[t] == abs(c * g)) and np.all(amax_r[t] == abs(c * g))
+        # MXNorm: the estimate comes from the absmaxes of w
+        assert rinv_m[t] == pytest.approx(1 / math.sqrt((cB * c * g) ** 2 + eps), rel=1e-14)
+        # RMSNorm + MXCast: the statistic is of x, whatever the gain
+        assert rinv_r[t] == pytest.approx(1 / math.sqrt(c * c + eps), rel=1e-14)
+
+
+@pytest.mark.parametrize("fmt", [oracle.FMT_E4M3, oracle.FMT_E2M1])
+def test_rmsnorm_factor_does_not_depend_on_the_gain(fmt):
+    X, gam = workloads.mx_inputs(32, 1024, seed=41, t_frac=0.1, with_gamma=True)
+    Xb = workloads.bf16_bits(X)
+    _, _, r_g, amax_g = oracle.rmsnorm_mxcast(Xb, gam.numpy(), 1e-6, 32, fmt)
+    _, _, r_0, amax_0 = oracle.rmsnorm_mxcast(Xb, None, 1e-6, 32, fmt)
+    assert np.array_equal(r_g, r_0)                  # bit for bit
+    assert not np.array_equal(amax_g, amax_0)        # while the cast tensor differs
+
+
+def _pow2_gain_and_premultiplied(T, D, seed):
+    """A gain of powers of two (per channel, both signs) and bf16(x*gamma),
+    which equals fp32(x*gamma) exactly: scaling a bf16 value by 2^k stays in
+    bf16 while the exponent stays in range."""
+    X, _ = workloads.mx_inputs(T, D, seed=seed, t_frac=0.1)
+    gen = torch.Generator().manual_seed(seed)
+    k = torch.randint(-3, 4, (D,), generator=gen).float()
+    sign = torch.where(torch.rand(D, generator=gen) < 0.3, -1.0, 1.0)
+    gam = (sign * torch.pow(2.0, k)).float()
+    W = (X.float() * gam).to(torch.bfloat16)
+    assert torch.equal(W.float(), X.float() * gam)
+    return workloads.bf16_bits(X), gam.numpy(), workloads.bf16_bits(W)
+
+
+@pytest.mark.parametrize("B", [16, 32, 64])
+@pytest.mark.parametrize("p", [1, 2])
+@pytest.mark.parametrize("fmt", [oracle.FMT_E4M3, oracle.FMT_E2M1])
+def test_mxnorm_statistic_is_of_the_cast_tensor(B, p, fmt):
+    Xb, gam, Wb = _pow2_gain_and_premultiplied(24, 16 * B, seed=B + 10 * p + fmt)
+    with_gain = oracle.mxnorm_cast(Xb, gam, 1e-6, B, fmt, p)
+    premult = oracle.mxnorm_cast(Wb, None, 1e-6, B, fmt, p)
+    for u, v in zip(with_gain, premult):
+        assert np.array_equal(u, v)
+    # and the gain does change the result (the pin is not vacuous)
+    plain = oracle.mxnorm_cast(Xb, None, 1e-6, B, fmt, p)
+    assert not np.array_equal(with_gain[2], plain[2])
+
+
+@pytest.mark.parametrize("B", [16, 32, 64])
+@pytest.mark.parametrize("fmt", [oracle.FMT_E4M3, oracle.FMT_E2M1])
+@pytest.mark.parametrize("k", [-3, 2, 5])
+def test_power_of_two_gain_shifts_only_the_rmsnorm_scales(B, fmt, k):
+    # gamma = 2^k on every channel: w = 2^k x exactly.  RMSNorm + MXCast keeps
+    # the factor of x, so w*rinv is 2^k times the ungained values: the element
+    # codes stay, every E8M0 scale moves up by exactly k.  MXNorm (eps = 0)
+    # estimates its factor from w, which cancels the gain: nothing changes.
+    X, _ = workloads.mx_inputs(24, 16 * B, seed=B + k, t_frac=0.1)
+    Xb = workloads.bf16_bits(X)
+    gam = np.full(16 * B, 2.0 ** k, np.float32)
+    c_g, s_g, r_g, a_g = oracle.rmsnorm_mxcast(Xb, gam, 1e-6, B, fmt)
+    c_0, s_0, r_0, a_0 = oracle.rmsnorm_mxcast(Xb, None, 1e-6, B, fmt)
+    assert np.array_equal(r_g, r_0)
+    assert np.array_equal(a_g, a_0 * np.float32(2.0 ** k))
+    assert np.array_equal(c_g, c_0)
+    assert np.array_equal(s_g.astype(int), s_0.astype(int) + k)
+    for p in (1, 2):
+        m_g = oracle.mxnorm_cast(Xb, gam, 0.0, B, fmt, p)
+        m_0 = oracle.mxnorm_cast(Xb, None, 0.0, B, fmt, p)
+        assert np.array_equal(m_g[0], m_0[0]) and np.array_equal(m_g[1], m_0[1])
+        assert np.allclose(m_g[2] * 2.0 ** k, m_0[2], rtol=1e-15, atol=0)
