@@ -603,6 +603,147 @@ def decode_latency(nts, torch, dev):
     return out
 
 
+# ------------------------------------------------------- single cases
+
+CASE_DEFAULTS = {
+    "qknorm_rms": dict(T=8192, H=5120, N=4),
+    "qknorm_rms_qk": dict(T=8192, H=5120, N=4),
+    "qknorm_rms_fp8": dict(T=8192, H=5120, N=4),
+    "qknorm_rms_heads": dict(T=8192, H=5120, N=1, hd=128),
+    "layernorm_split": dict(T=8192, H=5120, N=4, beta=1),
+    "qknorm_rms_mxcast": dict(T=8192, H=5120, N=4, B=32, fmt="e4m3"),
+    "qknorm_rms_qk_mxcast": dict(T=8192, H=5120, N=4, B=32, fmt="e4m3"),
+    "rmsnorm_mxcast": dict(T=65536, D=4096, B=32, fmt="e4m3"),
+    "mxnorm_cast": dict(T=65536, D=4096, B=32, fmt="e4m3", p=2),
+    "mxnorm_postround_cast": dict(T=65536, D=4096, B=32, fmt="e4m3", p=2),
+}
+
+
+def parse_case(spec: str):
+    """"name" or "name:key=value,key=value" -> (name, parameters)."""
+    name, _, rest = spec.partition(":")
+    if name not in CASE_DEFAULTS:
+        raise SystemExit(f"unknown case {name!r}; known: {', '.join(CASE_DEFAULTS)}")
+    params = dict(CASE_DEFAULTS[name])
+    for item in filter(None, rest.split(",")):
+        k, _, v = item.partition("=")
+        if k not in params:
+            raise SystemExit(f"case {name} has no parameter {k!r}")
+        params[k] = type(params[k])(v)
+    return name, params
+
+
+def case_bytes(name, q):
+    """Algorithmic HBM bytes of one launch (gamma and beta excluded)."""
+    if name in ("rmsnorm_mxcast", "mxnorm_cast", "mxnorm_postround_cast"):
+        cb = q["D"] if q["fmt"] == "e4m3" else q["D"] // 2
+        return q["T"] * (2 * q["D"] + cb + q["D"] // q["B"])
+    T, H = q["T"], q["H"]
+    if name in ("qknorm_rms_mxcast", "qknorm_rms_qk_mxcast"):
+        cb = H if q["fmt"] == "e4m3" else H // 2
+        n = 2 if name == "qknorm_rms_qk_mxcast" else 1
+        return n * T * (2 * H + cb + H // q["B"])
+    if name == "qknorm_rms_fp8":
+        return 3 * T * H
+    return (2 if name == "qknorm_rms_qk" else 1) * 4 * T * H
+
+
+def make_case(nts, torch, dev, name, q, sets):
+    """`sets` independent input/output sets of the case (rotated between
+    launches, so that small working sets do not stay in L2) and one launch
+    function per set."""
+    import workloads
+    fns = []
+    for k in range(sets):
+        seed = 7000 + 13 * k
+        if name in ("rmsnorm_mxcast", "mxnorm_cast", "mxnorm_postround_cast"):
+            T, D, B, fmt = q["T"], q["D"], q["B"], q["fmt"]
+            X, _ = workloads.mx_inputs(T, D, seed=seed, t_frac=0.05, device=dev)
+            codes = torch.empty(T, D if fmt == "e4m3" else D // 2, dtype=torch.uint8, device=dev)
+            scales = torch.empty(T, D // B, dtype=torch.uint8, device=dev)
+            kw = dict(eps=EPS, B=B, fmt=fmt, codes=codes, scales=scales)
+            if name != "rmsnorm_mxcast":
+                kw["p"] = q["p"]
+            f = getattr(nts, name)
+            fns.append(lambda X=X, f=f, kw=kw: f(X, None, **kw))
+            continue
+        T, H, N = q["T"], q["H"], q["N"]
+        X, g = workloads.qk_inputs(T, H, seed=seed, outlier_frac=0.01, device=dev)
+        Y = torch.empty_like(X)
+        if name == "qknorm_rms":
+            fns.append(lambda X=X, g=g, Y=Y: nts.qknorm_rms(X, g, eps=EPS, N=N, out=Y))
+        elif name == "qknorm_rms_qk":
+            K, gk = workloads.qk_inputs(T, H, seed=seed + 1, outlier_frac=0.01, device=dev)
+            Yk = torch.empty_like(K)
+            fns.append(lambda X=X, g=g, Y=Y, K=K, gk=gk, Yk=Yk: nts.qknorm_rms_qk(
+                X, g, K, gk, eps=EPS, N=N, out_q=Y, out_k=Yk))
+        elif name == "qknorm_rms_fp8":
+            c8, s8, g8 = workloads.qk_inputs_fp8(T, H, seed=seed, outlier_frac=0.01, device=dev)
+            fns.append(lambda c8=c8, s8=s8, g8=g8, Y=Y: nts.qknorm_rms_fp8(
+                c8, s8, g8, eps=EPS, N=N, out=Y))
+        elif name == "qknorm_rms_heads":
+            gh = workloads.gamma_vector(q["hd"], seed=seed, device=dev)
+            fns.append(lambda X=X, gh=gh, Y=Y: nts.qknorm_rms_heads(
+                X, gh, q["hd"], eps=EPS, N=N, out=Y))
+        elif name == "layernorm_split":
+            beta = workloads.beta_vector(H, seed=seed, device=dev) if q["beta"] else None
+            fns.append(lambda X=X, g=g, Y=Y, beta=beta: nts.layernorm_split(
+                X, g, beta, eps=1e-5, N=N, out=Y))
+        else:
+            B, fmt = q["B"], q["fmt"]
+            cb = H if fmt == "e4m3" else H // 2
+            mk = lambda: nts.MxOut(torch.empty(T, cb, dtype=torch.uint8, device=dev),
+                                   torch.empty(T, H // B, dtype=torch.uint8, device=dev),
+                                   None, None)
+            oq = mk()
+            if name == "qknorm_rms_mxcast":
+                fns.append(lambda X=X, g=g, oq=oq: nts.qknorm_rms_mxcast(
+                    X, g, eps=EPS, N=N, B=B, fmt=fmt, codes=oq.codes, scales=oq.scales))
+            else:
+                K, gk = workloads.qk_inputs(T, H, seed=seed + 1, outlier_frac=0.01, device=dev)
+                ok = mk()
+                fns.append(lambda X=X, g=g, oq=oq, K=K, gk=gk, ok=ok: nts.qknorm_rms_qk_mxcast(
+                    X, g, K, gk, eps=EPS, N=N, B=B, fmt=fmt, out_q=oq, out_k=ok))
+    return fns
+
+
+def time_launches(torch, fns, reps, warmup=3):
+    """Mean device time of one launch (ms): `reps` back-to-back launches
+    cycling through `fns`, between two CUDA events on the launching stream,
+    after `warmup` rounds."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for f in fns:
+            f()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for i in range(reps):
+        fns[i % len(fns)]()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / reps
+
+
+def run_case(args):
+    """--case: one kernel alone, for profiling and per-kernel figures."""
+    import torch
+    import normalization_token_split_gb300 as nts
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    name, q = parse_case(args.case)
+    fns = make_case(nts, torch, dev, name, q, args.sets)
+    ms = time_launches(torch, fns, args.steps, warmup=args.warmup)
+    nts.check_status()
+    peak, peak_kind = measured_peaks()
+    nbytes = case_bytes(name, q)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({"case": name, "params": q, "input_sets": args.sets, "launches": args.steps,
+                      "us_per_launch": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+                      "frac_of_measured": round(gbs / peak, 4), "peak_source": peak_kind}),
+          flush=True)
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample_step(rows_qk: int, rows_mx: int, state):
@@ -702,7 +843,15 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", default=None,
+                    help="time one kernel alone, e.g. mxnorm_cast:T=16384,D=1024,B=16,fmt=e2m1")
+    ap.add_argument("--sets", type=int, default=1,
+                    help="--case: input sets rotated between launches")
     args = ap.parse_args(argv)
+    if args.case is not None:
+        args.warmup = max(3, args.warmup)
+        run_case(args)
+        return
     if args.impl == "nts":
         args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
     if args.impl == "reference":
