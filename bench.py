@@ -341,27 +341,31 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": dict(workload_config(), parallelism=
-                                            "replicas" if world > 1 else "single GPU"),
+        "data": "synthetic", "config": workload_config(),
         "tokens_per_s": {n: kernels[n]["tokens_per_s"] for n in KERNELS},
         "frac_of_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
-        "kernels": kernels, "roofline": roofline,
         "gpu_launches": len(launches) * args.steps,
         "clocks": clocks.summary(w0, w2),
         "wall_s_timed": round(w1 - w0, 4),
         "ms_per_step_with_kernel_marks": round(marked_ms, 5),
     }
 
-    if not args.no_e2e:
-        result["e2e"] = run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world)
-    if not args.no_decode:
-        result["decode_qk_us_per_call"] = decode_latency(nts, torch, dev)
-    if not args.no_variants:
-        result["variants"] = variant_rates(nts, torch, dev, Q, gq, X, peak, K, gk)
+    # the long tables first, the per-kernel figures and the roofline last
+    # (a reader of the line's tail sees those)
     if not args.no_sweep:
         result["mxnorm_sweep_gbs"] = mxnorm_sweep(nts, torch, dev, peak)
+        result["mx_vs_rms_by_block"] = mx_vs_rms_by_block(nts, torch, dev, peak)
+        result["mx_config_by_T"] = mx_config_by_T(nts, torch, dev, peak)
+    if not args.no_decode:
+        result["decode_qk"] = decode_latency(nts, torch, dev)
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world)
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if not args.no_variants:
+        result["variants"] = variant_rates(nts, torch, dev, Q, gq, X, peak, K, gk)
+    result["kernels"] = kernels
+    result["roofline"] = roofline
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -385,8 +389,7 @@ def run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world):
     scales_d = torch.empty(MX_T, MX_D // MX_B, dtype=torch.uint8, device=dev)
 
     def step():
-        nts.qknorm_rms_host(Qh, gq, Yqh, Qd, Yqd, eps=EPS, N=QK_N)
-        nts.qknorm_rms_host(Kh, gk, Ykh, Kd, Ykd, eps=EPS, N=QK_N)
+        nts.qknorm_rms_qk_host(Qh, gq, Yqh, Kh, gk, Ykh, Qd, Yqd, Kd, Ykd, eps=EPS, N=QK_N)
         nts.rmsnorm_mxcast_host(Xh, None, codes_h["rmsnorm_mxcast"], scales_h["rmsnorm_mxcast"],
                                 Xd, codes_d, scales_d, eps=EPS, B=MX_B, fmt="e4m3")
         for p in (1, 2):
@@ -420,7 +423,8 @@ def run_e2e(args, nts, torch, dev, Q, K, X, gq, gk, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "runs_ms_per_step": [round(r / steps * 1e3, 3) for r in runs], "reported": "median run",
             "ms_per_step": round(elapsed / steps * 1e3, 4),
-            "path": "nts_*_host C ABI entry points, pinned host buffers",
+            "path": "nts_*_host C ABI entry points (Q and K in one nts_qknorm_rms_qk_host "
+                    "call, as the device step launches them), pinned host buffers",
             "copy_only_gbs": copy_ceiling(
                 torch,
                 [(Qd, Qh), (Kd, Kh)] + [(Xd, Xh)] * 3,
@@ -498,6 +502,61 @@ def mxnorm_sweep(nts, torch, dev, peak, reps=20):
         del X, codes, scales
     nts.check_status()
     return out
+
+
+def mx_vs_rms_by_block(nts, torch, dev, peak, reps=20):
+    """The isolated-kernel comparison of the MXNorm card's Fig. 8 on this
+    GPU: RMSNorm + MX cast against MXNorm (p = 1 and 2) + the same cast at
+    [65536, 4096], for B in {16, 32, 64} and E4M3 / E2M1 elements (rows
+    N(0,1)).  Device time per launch; speedup = RMSNorm time / MXNorm time."""
+    out = {}
+    for fmt in ("e4m3", "e2m1"):
+        for B in (16, 32, 64):
+            t = {}
+            for name, spec in (("rmsnorm_mxcast", f"rmsnorm_mxcast:T=65536,D=4096,B={B},fmt={fmt}"),
+                               ("mxnorm_p1", f"mxnorm_cast:T=65536,D=4096,B={B},fmt={fmt},p=1"),
+                               ("mxnorm_p2", f"mxnorm_cast:T=65536,D=4096,B={B},fmt={fmt},p=2")):
+                cname, q = parse_case(spec)
+                fns = make_case(nts, torch, dev, cname, q, 1)
+                ms = time_launches(torch, fns, reps)
+                gbs = case_bytes(cname, q) / (ms * 1e-3) / 1e9
+                t[name] = {"us": round(ms * 1e3, 1), "gbs": round(gbs, 1),
+                           "frac_of_measured": round(gbs / peak, 4)}
+                del fns
+            for p in ("p1", "p2"):
+                t[f"speedup_mxnorm_{p}"] = round(t["rmsnorm_mxcast"]["us"] / t[f"mxnorm_{p}"]["us"], 3)
+            out[f"B={B},{fmt}"] = t
+    nts.check_status()
+    return out
+
+
+def mx_config_by_T(nts, torch, dev, peak, reps=30):
+    """RMSNorm + MXFP8 and MXNorm p = 1, 2 of X [T, 4096] (B = 32, E4M3) at
+    T in {4096, 16384, 65536}.  Launches rotate through enough independent
+    input/output sets that the data touched between two uses of a set is at
+    least twice the L2 (and at least 3 sets below that size); configurations
+    whose one-launch working set fits in L2 are flagged."""
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    out = {}
+    for T in (4096, 16384, 65536):
+        nbytes = mx_bytes(T, MX_D, MX_B)
+        sets = 1 if nbytes > 2 * l2 else max(3, -(-2 * l2 // nbytes) + 1)
+        row = {"bytes": nbytes, "input_sets": sets, "l2_resident": nbytes <= l2}
+        for name, spec in (("rmsnorm_mxcast", f"rmsnorm_mxcast:T={T},D={MX_D},B={MX_B}"),
+                           ("mxnorm_p1", f"mxnorm_cast:T={T},D={MX_D},B={MX_B},p=1"),
+                           ("mxnorm_p2", f"mxnorm_cast:T={T},D={MX_D},B={MX_B},p=2")):
+            cname, q = parse_case(spec)
+            fns = make_case(nts, torch, dev, cname, q, sets)
+            ms = time_launches(torch, fns, reps)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            row[name] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                         "tokens_per_s": round(T / (ms * 1e-3)),
+                         "frac_of_measured": round(gbs / peak, 4)}
+            del fns
+        out[f"T={T}"] = row
+        torch.cuda.empty_cache()
+    nts.check_status()
+    return {"by_T": out, "l2_bytes": l2}
 
 
 def variant_rates(nts, torch, dev, Q, gq, X, peak, K, gk, reps=20):
@@ -598,9 +657,13 @@ def decode_latency(nts, torch, dev):
                 graph.replay()
             e.record()
             torch.cuda.synchronize()
-            out[f"N={N},T={T}"] = round(s.elapsed_time(e) * 1e3 / 200, 2)
+            us = s.elapsed_time(e) * 1e3 / 200
+            gbs = 2 * qk_bytes(T, 4096) / (us * 1e-6) / 1e9
+            out[f"N={N},T={T}"] = {"us_per_call": round(us, 2), "gbs": round(gbs, 1)}
     nts.check_status()
-    return out
+    return {"per_call": out, "note": "Q and K [T, 4096] each, one fused launch per call; "
+            "CUDA-graph replays of 20 calls (host launch cost excluded); working set in L2 "
+            "(latency-bound sizes: GB/s for information)"}
 
 
 # ------------------------------------------------------- single cases
@@ -746,16 +809,24 @@ def run_case(args):
 
 # ------------------------------------------------------------ CPU oracle
 
-def oracle_sample_step(rows_qk: int, rows_mx: int, state):
+def oracle_sample_step(rows_qk: int, rows_mx: int, state, pool=None, nthreads: int = 1):
     """One bounded sample of the step through the CPU oracle; returns the
-    algorithmic bytes it covered."""
+    algorithmic bytes it covered.  With a thread pool, the rows of every
+    call are split into `nthreads` contiguous chunks that run at once (the
+    oracle's C entry points release the GIL, and rows are independent)."""
     import oracle
     Qb, gq, Kb, gk, Xb = state
-    oracle.qknorm_rms(Qb[:rows_qk], gq, EPS, QK_N)
-    oracle.qknorm_rms(Kb[:rows_qk], gk, EPS, QK_N)
-    oracle.rmsnorm_mxcast(Xb[:rows_mx], None, EPS, MX_B, 0)
-    oracle.mxnorm_cast(Xb[:rows_mx], None, EPS, MX_B, 0, 1)
-    oracle.mxnorm_cast(Xb[:rows_mx], None, EPS, MX_B, 0, 2)
+    calls = [(lambda a, b: oracle.qknorm_rms(Qb[a:b], gq, EPS, QK_N), rows_qk),
+             (lambda a, b: oracle.qknorm_rms(Kb[a:b], gk, EPS, QK_N), rows_qk),
+             (lambda a, b: oracle.rmsnorm_mxcast(Xb[a:b], None, EPS, MX_B, 0), rows_mx),
+             (lambda a, b: oracle.mxnorm_cast(Xb[a:b], None, EPS, MX_B, 0, 1), rows_mx),
+             (lambda a, b: oracle.mxnorm_cast(Xb[a:b], None, EPS, MX_B, 0, 2), rows_mx)]
+    for fn, rows in calls:
+        if pool is None:
+            fn(0, rows)
+        else:
+            cuts = [rows * k // nthreads for k in range(nthreads + 1)]
+            list(pool.map(lambda k: fn(cuts[k], cuts[k + 1]), range(nthreads)))
     return 2 * qk_bytes(rows_qk, QK_H) + 3 * mx_bytes(rows_mx, MX_D, MX_B)
 
 
@@ -768,30 +839,63 @@ def oracle_inputs(rows_qk, rows_mx):
             workloads.bf16_bits(X))
 
 
-def cpu_baseline(seconds: float):
-    """The oracle, single-threaded, on repeated row samples of the step
-    (128 rows of Q and of K, 1024 rows of X per MX function) for about
-    `seconds` of CPU time."""
+def host_threads() -> int:
+    """The cores this process may run on (its affinity mask)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def time_oracle(seconds: float, nthreads: int):
+    """The oracle on repeated row samples of the step for about `seconds`:
+    16 rows of Q and of K and 128 rows of X per thread and pass."""
+    from concurrent.futures import ThreadPoolExecutor
     import oracle
     oracle.build()
-    rows_qk, rows_mx = 128, 1024
+    rows_qk, rows_mx = 16 * nthreads, 128 * nthreads
     state = oracle_inputs(rows_qk, rows_mx)
-    done, t0 = 0, time.perf_counter()
-    passes = 0
-    while True:
-        done += oracle_sample_step(rows_qk, rows_mx, state)
-        passes += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": round(done / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"{passes} passes of 128 rows of Q and of K (H=5120, N=4) and 1024 rows "
-                       f"of X (D=4096) through rmsnorm_mxcast, mxnorm p=1, p=2; "
-                       f"{dt:.1f} s; single thread"),
+    pool = ThreadPoolExecutor(nthreads) if nthreads > 1 else None
+    try:
+        oracle_sample_step(rows_qk, rows_mx, state, pool, nthreads)   # warm-up
+        done, passes, t0 = 0, 0, time.perf_counter()
+        while True:
+            done += oracle_sample_step(rows_qk, rows_mx, state, pool, nthreads)
+            passes += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
+    finally:
+        if pool is not None:
+            pool.shutdown()
+    return done / dt / 1e9, passes, dt, rows_qk, rows_mx
+
+
+def cpu_baseline(seconds: float):
+    """The oracle as it stands, on the host cores: over tokens on every core
+    of the affinity mask (the reported value), and single-threaded beside
+    it, each for about half of `seconds`."""
+    n = host_threads()
+    v1, p1, d1, q1, m1 = time_oracle(seconds / 2, 1)
+    vn, pn, dn, qn, mn = time_oracle(seconds / 2, n)
+    return {"value": round(vn, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": (f"{pn} passes of {qn} rows of Q and of K (H=5120, N=4) and {mn} rows of "
+                       f"X (D=4096) through qknorm_rms, rmsnorm_mxcast, mxnorm p=1, p=2, each "
+                       f"call's rows split over {n} threads (over tokens); {dn:.1f} s"),
+            "single_thread": {"value": round(v1, 4), "cores": 1,
+                              "sample": f"{p1} passes of {q1} / {m1} rows; {d1:.1f} s"},
             "cpu": cpu_model()}
 
 
 def cpu_model():
+    """The host CPU's model name (lscpu), else what /proc/cpuinfo names."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
@@ -803,18 +907,23 @@ def cpu_model():
 
 
 def run_reference(args):
+    from concurrent.futures import ThreadPoolExecutor
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    rows_qk, rows_mx = 16, 64
+    import oracle
+    oracle.build()
+    n = host_threads()
+    rows_qk, rows_mx = 4 * n, 32 * n
     state = oracle_inputs(rows_qk, rows_mx)
-    for _ in range(args.warmup):
-        oracle_sample_step(rows_qk, rows_mx, state)
-    t0 = time.perf_counter()
-    done = 0
-    for _ in range(args.steps):
-        done += oracle_sample_step(rows_qk, rows_mx, state)
-    dt = time.perf_counter() - t0
+    with ThreadPoolExecutor(n) as pool:
+        for _ in range(args.warmup):
+            oracle_sample_step(rows_qk, rows_mx, state, pool, n)
+        t0 = time.perf_counter()
+        done = 0
+        for _ in range(args.steps):
+            done += oracle_sample_step(rows_qk, rows_mx, state, pool, n)
+        dt = time.perf_counter() - t0
     value = round(done / dt / 1e9, 4)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
@@ -822,9 +931,10 @@ def run_reference(args):
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "per step: 16 rows of Q and of K (H=5120, N=4), 64 rows of "
-                                   "X (D=4096) through the three MX functions; single thread",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": n, "kind": "oracle",
+                         "sample": (f"per step: {rows_qk} rows of Q and of K (H=5120, N=4), "
+                                    f"{rows_mx} rows of X (D=4096) through qknorm_rms and the "
+                                    f"three MX functions, rows split over {n} threads"),
                          "cpu": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)

@@ -340,6 +340,24 @@ NTS_API int nts_qknorm_rms_host(const void *X_host, const float *gamma_dev,
                         void *Y_dev, float *rinv_dev, int64_t T, int64_t H,
                         float eps, int N, void *stream);
 
+/*
+ * nts_qknorm_rms_qk_host -- nts_qknorm_rms_qk on host buffers: the copies of
+ * Q and K to the device, the one launch that normalizes both, and the copies
+ * of Yq and Yk back, enqueued as nts_qknorm_rms_host enqueues its work (in
+ * row chunks through the library's copy streams for large calls; the
+ * caller's stream is ordered after the last copy back).
+ *   Q_host bf16 [T, Hq], K_host bf16 [T, Hk]: read.
+ *   Yq_host, Yk_host: written once the stream reaches the end of the call.
+ *   Q_dev, Yq_dev, K_dev, Yk_dev: caller-owned device staging of the same
+ *   sizes (16-byte aligned); gamma_q_dev, gamma_k_dev: device gains.
+ * Errors: as nts_qknorm_rms_qk; CUDA also covers a failed copy.
+ */
+NTS_API int nts_qknorm_rms_qk_host(const void *Q_host, const float *gamma_q_dev,
+                                   void *Yq_host, const void *K_host,
+                                   const float *gamma_k_dev, void *Yk_host, void *Q_dev,
+                                   void *Yq_dev, void *K_dev, void *Yk_dev, int64_t T,
+                                   int64_t Hq, int64_t Hk, float eps, int N, void *stream);
+
 NTS_API int nts_rmsnorm_mxcast_host(const void *X_host, const float *gamma_dev,
                             uint8_t *codes_host, uint8_t *scales_host,
                             void *X_dev, uint8_t *codes_dev,

@@ -14,7 +14,7 @@ Build the library with ``python -m normalization_token_split_gb300.build``.
 """
 from ._lib import NtsError
 from .ops import (FMT_E2M1, FMT_E4M3, FMT_NVFP4, MxOut, check_status, codes_row_bytes, mxnorm_cast,
-                  mxnorm_cast_host, mxnorm_cast_host_noalloc, mxnorm_correction, mxnorm_postround_cast, qknorm_rms, qknorm_rms_host,
+                  mxnorm_cast_host, mxnorm_cast_host_noalloc, mxnorm_correction, mxnorm_postround_cast, qknorm_rms, qknorm_rms_host, qknorm_rms_qk_host,
                   qknorm_rms_fp8, qknorm_rms_heads, qknorm_rms_qk, layernorm_split, qknorm_rms_mxcast,
                   qknorm_rms_qk_mxcast,
                   rmsnorm_mxcast, rmsnorm_mxcast_host, set_missing_tx, set_schedule, set_direct, set_tuning,
@@ -23,7 +23,7 @@ from .ops import (FMT_E2M1, FMT_E4M3, FMT_NVFP4, MxOut, check_status, codes_row_
 
 __all__ = [
     "NtsError", "FMT_E4M3", "FMT_E2M1", "FMT_NVFP4", "MxOut", "qknorm_rms", "qknorm_rms_fp8", "qknorm_rms_heads", "qknorm_rms_qk", "layernorm_split", "qknorm_rms_mxcast", "qknorm_rms_qk_mxcast", "rmsnorm_mxcast", "mxnorm_cast", "mxnorm_postround_cast",
-    "mxnorm_correction", "check_status", "codes_row_bytes", "qknorm_rms_host",
+    "mxnorm_correction", "check_status", "codes_row_bytes", "qknorm_rms_host", "qknorm_rms_qk_host",
     "rmsnorm_mxcast_host", "mxnorm_cast_host", "mxnorm_cast_host_noalloc", "set_tuning", "set_wait_limit_ns",
     "set_missing_tx", "set_schedule", "set_direct", "check_nvfp4_scale", "set_pdl", "set_host_chunks", "check_e8m0", "inject_failure",
 ]

@@ -46,6 +46,8 @@ def _declare(lib):
         "nts_qknorm_rms_host": ([P, P, P, P, P, P, P, i64, i64, f32, i32, P], i32),
         "nts_rmsnorm_mxcast_host": ([P, P, P, P, P, P, P, i64, i64, f32, i32, i32, P], i32),
         "nts_mxnorm_cast_host": ([P, P, P, P, P, P, P, i64, i64, f32, i32, i32, i32, P], i32),
+        "nts_qknorm_rms_qk_host": ([P, P, P, P, P, P, P, P, P, P, i64, i64, i64, f32, i32, P],
+                                   i32),
         "nts_mxnorm_cast_host_noalloc": ([P, P, P, P, i64, i64, f32, i32, i32, i32, P], i32),
         "nts_debug_set_tuning": ([i32, i32, i32, i64, i32], i32),
         "nts_debug_set_wait_limit_ns": ([ctypes.c_uint64], i32),

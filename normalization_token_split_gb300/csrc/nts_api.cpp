@@ -671,6 +671,46 @@ int nts_qknorm_rms_host(const void* X_host, const float* gamma_dev, void* Y_host
 
 // one_stream: every copy and the kernel on the caller's stream, in one piece
 // (no chunking, so the pipeline's own streams and events are never needed).
+int nts_qknorm_rms_qk_host(const void* Q_host, const float* gamma_q_dev, void* Yq_host,
+                           const void* K_host, const float* gamma_k_dev, void* Yk_host,
+                           void* Q_dev, void* Yq_dev, void* K_dev, void* Yk_dev, int64_t T,
+                           int64_t Hq, int64_t Hk, float eps, int N, void* stream) {
+  if (T > 0 && (Q_host == nullptr || Yq_host == nullptr || K_host == nullptr ||
+                Yk_host == nullptr))
+    return fail(NTS_ERR_INVALID_ARG, "Q_host, Yq_host, K_host and Yk_host must be non-NULL");
+  int rc = validate_qk(Q_dev, gamma_q_dev, Yq_dev, nullptr, T, Hq, eps, N);
+  if (rc != NTS_OK) return rc;
+  rc = validate_qk(K_dev, gamma_k_dev, Yk_dev, nullptr, T, Hk, eps, N);
+  if (rc != NTS_OK) return rc;
+  if (T == 0) return NTS_OK;
+  const size_t qb = (size_t)Hq * 2, kb = (size_t)Hk * 2;  // bytes per row
+  auto at = [](const void* base, size_t rb, int64_t r) {
+    return const_cast<char*>(static_cast<const char*>(base) + (size_t)r * rb);
+  };
+  auto in = [&](int64_t r0, int64_t r1, void* st) {
+    int c = copy(at(Q_dev, qb, r0), at(Q_host, qb, r0), (size_t)(r1 - r0) * qb,
+                 cudaMemcpyHostToDevice, st, "copying Q to the device");
+    if (c == NTS_OK)
+      c = copy(at(K_dev, kb, r0), at(K_host, kb, r0), (size_t)(r1 - r0) * kb,
+               cudaMemcpyHostToDevice, st, "copying K to the device");
+    return c;
+  };
+  auto kern = [&](int64_t r0, int64_t r1, void* st) {
+    return nts_qknorm_rms_qk(at(Q_dev, qb, r0), gamma_q_dev, at(Yq_dev, qb, r0), nullptr,
+                             at(K_dev, kb, r0), gamma_k_dev, at(Yk_dev, kb, r0), nullptr, r1 - r0,
+                             Hq, Hk, eps, N, st);
+  };
+  auto out = [&](int64_t r0, int64_t r1, void* st) {
+    int c = copy(at(Yq_host, qb, r0), at(Yq_dev, qb, r0), (size_t)(r1 - r0) * qb,
+                 cudaMemcpyDeviceToHost, st, "copying Yq to the host");
+    if (c == NTS_OK)
+      c = copy(at(Yk_host, kb, r0), at(Yk_dev, kb, r0), (size_t)(r1 - r0) * kb,
+               cudaMemcpyDeviceToHost, st, "copying Yk to the host");
+    return c;
+  };
+  return run_host_pipeline(T, qb + kb, stream, in, kern, out);
+}
+
 static int mx_host(const void* X_host, const float* gamma_dev, uint8_t* codes_host,
                    uint8_t* scales_host, void* X_dev, uint8_t* codes_dev, uint8_t* scales_dev,
                    int64_t T, int64_t D, float eps, int B, int fmt, int p, bool mxnorm,

@@ -317,6 +317,23 @@ def qknorm_rms_host(x_host, gamma_dev, y_host, x_dev, y_dev, eps=1e-6, N=1, rinv
                                     int(N), _stream(stream)))
 
 
+def qknorm_rms_qk_host(q_host, gamma_q_dev, yq_host, k_host, gamma_k_dev, yk_host, q_dev,
+                       yq_dev, k_dev, yk_dev, eps=1e-6, N=1, stream=None) -> None:
+    """Enqueue the H2D copies of q and k, the one launch normalizing both,
+    and the D2H copies of yq and yk."""
+    for name, t in (("q_host", q_host), ("yq_host", yq_host), ("k_host", k_host),
+                    ("yk_host", yk_host)):
+        _need_host(name, t)
+    T, Hq = q_host.shape
+    Tk, Hk = k_host.shape
+    if Tk != T:
+        raise ValueError("q and k must have the same number of tokens")
+    check(lib().nts_qknorm_rms_qk_host(
+        _ptr(q_host), _ptr(gamma_q_dev), _ptr(yq_host), _ptr(k_host), _ptr(gamma_k_dev),
+        _ptr(yk_host), _ptr(q_dev), _ptr(yq_dev), _ptr(k_dev), _ptr(yk_dev), T, Hq, Hk,
+        float(eps), int(N), _stream(stream)))
+
+
 def rmsnorm_mxcast_host(x_host, gamma_dev, codes_host, scales_host, x_dev, codes_dev,
                         scales_dev, eps=1e-6, B=32, fmt="e4m3", stream=None) -> None:
     _need_host("x_host", x_host)

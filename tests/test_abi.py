@@ -117,6 +117,20 @@ def test_host_forms_argument_checks(lib):
                                        None) == OK
 
 
+def test_fused_qk_host_form_argument_checks(lib):
+    def f(**k):
+        return lib.nts_qknorm_rms_qk_host(
+            k.get("Q", A16), A16, k.get("Yq", A16), k.get("K", A16), A16, A16, A16, A16,
+            k.get("Kd", A16), A16, k.get("T", 4), 64, k.get("Hk", 64), 1e-6, k.get("N", 2), None)
+    assert f(Q=None) == INVALID
+    assert f(Yq=None) == INVALID
+    assert f(K=None) == INVALID
+    assert f(Hk=65) == INVALID
+    assert f(N=3) == INVALID
+    assert f(Kd=MIS) == UNSUPPORTED
+    assert f(T=0, Q=None, K=None, Yq=None) == OK
+
+
 def test_debug_hooks_validate(lib):
     assert lib.nts_debug_set_tuning(9, 0, 0, 0, 0) == INVALID
     assert lib.nts_debug_set_tuning(-1, 0, 0, 0, 0) == INVALID

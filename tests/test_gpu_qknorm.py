@@ -356,6 +356,31 @@ def test_host_buffer_form_in_chunks(T, H, N):
         Yh.zero_()
 
 
+@pytest.mark.parametrize("T,Hq,Hk,N", [(8192, 5120, 5120, 4), (5000, 4096, 1024, 2), (7, 2048, 2048, 8)])
+def test_fused_qk_host_buffer_form(T, Hq, Hk, N):
+    # the host-buffer form of the fused Q+K launch (in chunks for the large
+    # cases) equals the device form bit for bit, and the device form is
+    # checked against the oracle elsewhere; two calls in a row
+    Q, gq = workloads.qk_inputs(T, Hq, seed=T + Hq, outlier_frac=0.01)
+    K, gk = workloads.qk_inputs(T, Hk, seed=T + Hk + 1, outlier_frac=0.01)
+    Qh, Kh = Q.pin_memory(), K.pin_memory()
+    Yqh, Ykh = torch.empty_like(Qh).pin_memory(), torch.empty_like(Kh).pin_memory()
+    stage = [torch.empty_like(t, device=DEV) for t in (Q, Q, K, K)]
+    gqd, gkd = gq.to(DEV), gk.to(DEV)
+    yq, yk, _, rk = nts.qknorm_rms_qk(Q.to(DEV), gqd, K.to(DEV), gkd, eps=1e-6, N=N,
+                                      want_rinv=True)
+    nts.check_status()
+    for rep in range(2):
+        nts.qknorm_rms_qk_host(Qh, gqd, Yqh, Kh, gkd, Ykh, *stage, eps=1e-6, N=N)
+        nts.check_status()
+        assert torch.equal(Yqh, yq.cpu()) and torch.equal(Ykh, yk.cpu())
+        Yqh.zero_()
+        Ykh.zero_()
+    Yo, ro, _ = oracle.qknorm_rms(workloads.bf16_bits(K[:64]), gk.numpy(), 1e-6, N)
+    check_qk(workloads.bf16_bits(Ykh[:64].copy_(yk[:64].cpu())), rk[:64].cpu().numpy(), Yo, ro,
+             "fused host form")
+
+
 @pytest.mark.parametrize("N", [1, 2, 4, 8])
 @pytest.mark.parametrize("T", [1, 3, 64, 200])
 def test_decode_direct_kernel_equals_persistent(T, N):
