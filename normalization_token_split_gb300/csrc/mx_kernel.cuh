@@ -121,15 +121,53 @@ __device__ __forceinline__ float round_pow2(float a) {
 __device__ __forceinline__ void weigh_vector(const uint4& v, const float* gp, uint64_t (&w)[4]) {
   const float4 g0 = __ldg(reinterpret_cast<const float4*>(gp));
   const float4 g1 = __ldg(reinterpret_cast<const float4*>(gp) + 1);
-  w[0] = f2_mul(bf16x2_to_f2(v.x), f2(g0.x, g0.y));
-  w[1] = f2_mul(bf16x2_to_f2(v.y), f2(g0.z, g0.w));
-  w[2] = f2_mul(bf16x2_to_f2(v.z), f2(g1.x, g1.y));
-  w[3] = f2_mul(bf16x2_to_f2(v.w), f2(g1.z, g1.w));
+  w[0] = f2_mul(bf16x2_to_f2c(v.x), f2c(g0.x, g0.y));
+  w[1] = f2_mul(bf16x2_to_f2c(v.y), f2c(g0.z, g0.w));
+  w[2] = f2_mul(bf16x2_to_f2c(v.z), f2c(g1.x, g1.y));
+  w[3] = f2_mul(bf16x2_to_f2c(v.w), f2c(g1.z, g1.w));
+}
+
+// Element codes of one unit (UV 16-byte vectors of a row staged in shared
+// memory at `base`, read from vector `sig` on): q = w * a (ONE) or
+// (w * a) * c, w = x or fp32(x * gamma), then the packed conversions and
+// the stores into the codes row `crow` (`keep` masks NVFP4 blocks with a
+// zero scale).
+template <int FMT, int UV, bool ONE>
+__device__ __forceinline__ void cast_unit(const unsigned char* base, int sig, const float* gamma,
+                                          int b, int kU, uint64_t a, uint64_t c, uint8_t* crow,
+                                          uint32_t keep) {
+  // the two-product form only runs for extreme rows: kept rolled up, so that
+  // it adds no registers to the unrolled one-product loop
+#pragma unroll(ONE ? UV : 1)
+  for (int k = 0; k < UV; ++k) {
+    const int u = (k + sig) & (UV - 1);
+    const uint4 v = lds128(base + u * 16);
+    uint64_t w[4];
+    if (gamma == nullptr) {
+      w[0] = bf16x2_to_f2c(v.x);
+      w[1] = bf16x2_to_f2c(v.y);
+      w[2] = bf16x2_to_f2c(v.z);
+      w[3] = bf16x2_to_f2c(v.w);
+    } else {
+      weigh_vector(v, gamma + (size_t)b * kU + u * 8, w);
+    }
+    uint64_t q[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) q[h] = ONE ? f2_mul(w[h], a) : f2_mul(f2_mul(w[h], a), c);
+    if (FMT == NTS_FMT_E4M3) {
+      const uint32_t lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
+      const uint32_t hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
+      st_global_v2(crow + (size_t)b * kU + u * 8, lo, hi);
+    } else {
+      const uint32_t cc = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]),
+                                     f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
+      st_global_u32(crow + (size_t)b * (kU / 2) + u * 4, cc & keep);
+    }
+  }
 }
 
 template <int VB, int BPT, int FMT, int STAT>
 __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxParams p) {
-  constexpr int kB = VB * 8;                                 // block size
   // A 64-value block is split between two adjacent lanes, 32 values each
   // (the layout of 32-value blocks), which combine their absmaxes by one
   // shuffle: a thread's unit is then half a block.
@@ -137,6 +175,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
   constexpr int kUV = kSplit ? 4 : VB;                       // vectors per unit
   constexpr int kU = kUV * 8;                                // values per unit
   constexpr int kEmax = (FMT == NTS_FMT_E4M3) ? 8 : 2;
+  // smallest exponent with one product per element (e8m0_single_multiplier)
+  constexpr int kEminOne = (FMT == NTS_FMT_E4M3) ? -116 : -124;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -264,8 +304,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
             m[2] = bf16x2_absmax(m[2], v.z);
             m[3] = bf16x2_absmax(m[3], v.w);
             if (STAT == kStatRms) {
-              const uint64_t a = bf16x2_to_f2(v.x), c = bf16x2_to_f2(v.y);
-              const uint64_t d = bf16x2_to_f2(v.z), e = bf16x2_to_f2(v.w);
+              const uint64_t a = bf16x2_to_f2c(v.x), c = bf16x2_to_f2c(v.y);
+              const uint64_t d = bf16x2_to_f2c(v.z), e = bf16x2_to_f2c(v.w);
               acc[0] = f2_fma(a, a, acc[0]);
               acc[1] = f2_fma(c, c, acc[1]);
               acc[2] = f2_fma(d, d, acc[2]);
@@ -281,8 +321,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
             const int u = (k + sig) & (kUV - 1);
             const uint4 v = lds128(base + u * 16);
             if (STAT == kStatRms) {
-              const uint64_t a = bf16x2_to_f2(v.x), c = bf16x2_to_f2(v.y);
-              const uint64_t d = bf16x2_to_f2(v.z), e = bf16x2_to_f2(v.w);
+              const uint64_t a = bf16x2_to_f2c(v.x), c = bf16x2_to_f2c(v.y);
+              const uint64_t d = bf16x2_to_f2c(v.z), e = bf16x2_to_f2c(v.w);
               acc[0] = f2_fma(a, a, acc[0]);
               acc[1] = f2_fma(c, c, acc[1]);
               acc[2] = f2_fma(d, d, acc[2]);
@@ -290,9 +330,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
             }
             uint64_t w[4];
             weigh_vector(v, p.gamma + (size_t)b * kU + u * 8, w);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              mf[q] = fmaxf(mf[q], fmaxf(fabsf(f2_lo(w[q])), fabsf(f2_hi(w[q]))));
+            mf[k & 3] = absmax8(mf[k & 3], w);
           }
           am[i] = fmaxf(fmaxf(mf[0], mf[1]), fmaxf(mf[2], mf[3]));
         }
@@ -344,7 +382,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
 
     // ---- pass 2: scales and element codes
     if (valid) {
-      const uint64_t rr = f2(rinv, rinv);
+      const uint64_t rr = f2c(rinv, rinv);
       uint8_t* crow = p.codes + (size_t)t * cbytes;
 #pragma unroll
       for (int i = 0; i < BPT; ++i) {
@@ -354,43 +392,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
           const bool lead = !kSplit || (b & 1) == 0;   // writes the block's scale
           float is;                 // multiplier taking w*rinv to the element grid
           uint32_t keep = ~0u;      // NVFP4: 0 for a block whose scale is zero
+          int e = 0;                // E8M0 exponent
           if (FMT == NTS_FMT_NVFP4) {
             const uint32_t sc = nvfp4_scale(am[i] * rinv, rcp, &is);
             keep = sc != 0 ? ~0u : 0u;
             p.scales[(size_t)t * p.K + blk] = (uint8_t)sc;
           } else {
-            const int e = e8m0_exponent(am[i] * rinv, kEmax);
+            e = e8m0_exponent(am[i] * rinv, kEmax);
             is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
             if (lead) p.scales[(size_t)t * p.K + blk] = (uint8_t)(e + 127);
           }
-          const uint64_t ss = f2(is, is);
           if (p.amax_out != nullptr && lead) p.amax_out[(size_t)t * p.K + blk] = am[i];
           const unsigned char* base = srow + (uint32_t)b * kU * 2;
-#pragma unroll
-          for (int k = 0; k < kUV; ++k) {
-            const int u = (k + sig) & (kUV - 1);
-            const uint4 v = lds128(base + u * 16);
-            uint64_t w[4];
-            if (p.gamma == nullptr) {
-              w[0] = bf16x2_to_f2(v.x);
-              w[1] = bf16x2_to_f2(v.y);
-              w[2] = bf16x2_to_f2(v.z);
-              w[3] = bf16x2_to_f2(v.w);
-            } else {
-              weigh_vector(v, p.gamma + (size_t)b * kU + u * 8, w);
-            }
-            uint64_t q[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) q[h] = f2_mul(f2_mul(w[h], rr), ss);
-            if (FMT == NTS_FMT_E4M3) {
-              const uint32_t lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
-              const uint32_t hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
-              st_global_v2(crow + (size_t)b * kU + u * 8, lo, hi);
-            } else {
-              const uint32_t c = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]),
-                                            f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
-              st_global_u32(crow + (size_t)b * (kU / 2) + u * 4, c & keep);
-            }
+          // E8M0: one product per element by m = rinv * 2^-e where that gives
+          // the bits of the two products (every block of ordinary rows)
+          float m = 0.f;
+          const bool one = FMT != NTS_FMT_NVFP4 &&
+                           e8m0_single_multiplier(rinv, is, e, kEminOne, &m);
+          if (one) {
+            cast_unit<FMT, kUV, true>(base, sig, p.gamma, b, kU, f2c(m, m), 0, crow, keep);
+          } else {
+            cast_unit<FMT, kUV, false>(base, sig, p.gamma, b, kU, rr, f2c(is, is), crow, keep);
           }
         }
       }

@@ -284,6 +284,25 @@ __device__ __forceinline__ int e8m0_exponent(float ay, int emax) {
   return max(-127, min(127, e));
 }
 
+// The element cast needs q = fl(fl(w * rinv) * 2^-e) for every w of a block
+// (the two fp32 products in which the codes are decided).  One product
+// w * m with m = fl(rinv * 2^-e) gives the same bits whenever
+//  * m is a normal number: then it is exact (rinv is normal and 2^-e a power
+//    of two), and scaling by a power of two commutes with the rounding of a
+//    normal product;
+//  * e >= emin_one: an element whose fl(w * rinv) is subnormal (where the
+//    two forms may round differently) then has |q| <= 2^-126 * 2^-e, at
+//    most half the smallest nonzero magnitude of the element format (E4M3
+//    2^-9: e >= -116; E2M1 2^-1: e >= -124), so both forms cast it to the
+//    signed zero; a subnormal q is likewise a signed zero either way.
+// Returns whether the one-product form applies and, in *m, the multiplier.
+__device__ __forceinline__ bool e8m0_single_multiplier(float rinv, float is, int e, int emin_one,
+                                                       float* m) {
+  *m = rinv * is;
+  const uint32_t field = (__float_as_uint(*m) >> 23) & 0xFFu;
+  return e >= emin_one && field - 1u < 254u;
+}
+
 // The same exponent by the plain definition (exponent field, mantissa
 // compare, zero/subnormal special case): the reference of the self-check.
 __device__ __forceinline__ int e8m0_exponent_by_fields(float ay, int emax) {
@@ -324,6 +343,17 @@ __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t v) {
   return f2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
+// The same two constructors in plain integer arithmetic instead of an asm
+// register move: the compiler then sees which 32-bit halves form a pair and
+// places them without copies.  Measured on GB300: 3-8 % faster in the MX
+// kernels, slower in the split-H kernel, which keeps the asm forms.
+__device__ __forceinline__ uint64_t f2c(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t bf16x2_to_f2c(uint32_t v) {
+  return ((uint64_t)(v & 0xFFFF0000u) << 32) | (uint32_t)(v << 16);
+}
+
 // Two E4M3 codes (low byte = element 0) -> their exact fp32 values, via the
 // hardware's exact E4M3 -> f16 conversion.
 __device__ __forceinline__ uint64_t e4m3x2_to_f2(uint16_t v) {
@@ -349,6 +379,22 @@ __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
 __device__ __forceinline__ float bf16x2_hmax_abs(uint32_t m) {
   m &= 0x7FFF7FFFu;
   return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Largest magnitude of the eight fp32 values of four pairs, folded into `m`
+// (>= 0): four three-input maxima.
+__device__ __forceinline__ float absmax8(float m, const uint64_t (&w)[4]) {
+  m = fmax3(m, fabsf(f2_lo(w[0])), fabsf(f2_hi(w[0])));
+  m = fmax3(m, fabsf(f2_lo(w[1])), fabsf(f2_hi(w[1])));
+  m = fmax3(m, fabsf(f2_lo(w[2])), fabsf(f2_hi(w[2])));
+  return fmax3(m, fabsf(f2_lo(w[3])), fabsf(f2_hi(w[3])));
 }
 
 __device__ __forceinline__ void st_global_v2(void* p, uint32_t a, uint32_t b) {

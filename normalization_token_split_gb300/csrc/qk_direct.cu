@@ -93,7 +93,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qk_direct_kernel(const QkParam
   // Phase A, in the persistent kernel's order
   uint64_t w[VPT][4];
   uint64_t acc[4] = {0, 0, 0, 0};
-  uint64_t sum2[2] = {0, 0};
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     if (IN == kInBf16) {
@@ -108,19 +107,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qk_direct_kernel(const QkParam
       w[i][2] = f2_mul(e4m3x2_to_f2((uint16_t)(xv[i].y & 0xFFFFu)), sc);
       w[i][3] = f2_mul(e4m3x2_to_f2((uint16_t)(xv[i].y >> 16)), sc);
     }
+    if (STAT != kQkLn) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = f2_fma(w[i][q], w[i][q], acc[q]);
-    if (STAT == kQkLn) {
-      sum2[0] = f2_add(sum2[0], f2_add(w[i][0], w[i][1]));
-      sum2[1] = f2_add(sum2[1], f2_add(w[i][2], w[i][3]));
+      for (int q = 0; q < 4; ++q) acc[q] = f2_fma(w[i][q], w[i][q], acc[q]);
     }
   }
-  const uint64_t a = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
-  const float ss = warp_sum(f2_lo(a) + f2_hi(a));
-  float s1 = 0.f;
+  // RMSNorm: ss = this warp's sum of squares.  LayerNorm: ss = its sum, s1 =
+  // its M2 about its own mean
+  float ss, s1 = 0.f;
+  // LayerNorm counts: computed here as the persistent kernel tabulates them
+  auto cnt = [&](int wi) { return ln_count_pair(ln_warp_count<VPT>(nvec, p.G, wi)); };
   if (STAT == kQkLn) {
-    const uint64_t c = f2_add(sum2[0], sum2[1]);
-    s1 = warp_sum(f2_lo(c) + f2_hi(c));
+    ln_warp_stats<VPT>(w, p.G, g, nvec, cnt(wir), &ss, &s1);
+  } else {
+    const uint64_t a = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+    ss = warp_sum(f2_lo(a) + f2_hi(a));
   }
 
   // Phase B: w = x * gamma (RMSNorm; LayerNorm multiplies after centring)
@@ -133,18 +134,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qk_direct_kernel(const QkParam
   }
 
   // exchange: slot [row][rank][warp] of every CTA of the cluster
-  float S = ss, S1 = s1;
+  float S = ss, mu = 0.f, var = 0.f;
   if (N > 1 || wpr > 1) {
     float* slots = part + (size_t)row * N * wpr * NS;
     if (N > 1) {
       cluster_wait_acquire();
-      if (lane == 0) {
+      if (lane < N) {   // lane k stores into rank k
         const uint32_t slot = smem_addr(slots + NS * (rank * wpr + wir));
-#pragma unroll
-        for (int k = 0; k < N; ++k) {
-          st_cluster_f32(map_to_rank(slot, k), ss);
-          if (STAT == kQkLn) st_cluster_f32(map_to_rank(slot + 4, k), s1);
-        }
+        st_cluster_f32(map_to_rank(slot, lane), ss);
+        if (STAT == kQkLn) st_cluster_f32(map_to_rank(slot + 4, lane), s1);
       }
       __syncwarp();
       cluster_arrive_release();
@@ -156,20 +154,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qk_direct_kernel(const QkParam
       }
       __syncthreads();
     }
-    S = 0.f;
-    S1 = 0.f;
-    for (int k = 0; k < N * wpr; ++k) {
-      S += slots[NS * k];
-      if (STAT == kQkLn) S1 += slots[NS * k + 1];
+    if (STAT == kQkLn) {
+      ln_combine(slots, N, wpr, cnt, tn.inv_H, &mu, &var);
+    } else {
+      S = 0.f;
+      for (int k = 0; k < N * wpr; ++k) S += slots[k];
     }
+  } else if (STAT == kQkLn) {
+    const float own[2] = {ss, s1};
+    ln_combine(own, 1, 1, cnt, tn.inv_H, &mu, &var);
   }
 
   // Phase C
   if (valid) {
-    float rinv, mu = 0.f;
+    float rinv;
     if (STAT == kQkLn) {
-      mu = S1 * tn.inv_H;
-      const float var = fmaxf(fmaf(S, tn.inv_H, -mu * mu), 0.f);
       rinv = rsqrtf(var + p.eps);
     } else {
       rinv = rsqrtf(fmaf(S, tn.inv_H, p.eps));

@@ -116,7 +116,9 @@ struct QkLayout {
   uint32_t ring, gstg, gam, full, empty, gbar, xbar, tbar, tile, tloc, part, rcp, total;
 };
 
-// rcp: the NVFP4 scale reciprocals (128 floats; empty for other outputs).
+// rcp: the NVFP4 scale reciprocals (128 floats), or for LayerNorm the
+// {n, 1/n} pairs of every warp of a shard row of each tensor ([2][16]
+// float2); empty otherwise.
 __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int Wsum, int G,
                                               int gsplit, int esize, int ns, bool nvfp4) {
   QkLayout L;
@@ -132,7 +134,7 @@ __host__ __device__ inline QkLayout qk_layout(int N, int S, int R, int Wmax, int
   L.tloc = L.tile + (uint32_t)(S + 1) * 8;
   L.part = L.tloc + (uint32_t)S * 8;
   L.rcp = L.part + (uint32_t)2 * R * N * (G / 32) * 4 * ns;
-  L.total = L.rcp + (nvfp4 ? 128u * 4u : 0u);
+  L.total = L.rcp + (nvfp4 ? 128u * 4u : (ns == 2 ? 2u * 16u * 8u : 0u));
   return L;
 }
 
@@ -164,6 +166,87 @@ __device__ __forceinline__ void load_vector(const unsigned char* srow, int v, bo
     w[2] = f2_mul(e4m3x2_to_f2((uint16_t)(x.y & 0xFFFFu)), sc);
     w[3] = f2_mul(e4m3x2_to_f2((uint16_t)(x.y >> 16)), sc);
   }
+}
+
+// ---- LayerNorm statistics that combine exactly across shards and warps
+//
+// The SwiftQK notes (Sec. 5e) reduce LayerNorm to two scalars per shard that
+// add up across shards.  Sending (sum x, sum x^2) and forming
+// var = sum x^2 / H - mu^2 loses var to cancellation when |mu| >> sigma, so
+// each warp sends instead its sum s1 and M2 = sum (x - m)^2 about its own
+// mean m = s1 * fp32(1/n) (n: its number of values).  With mu the row mean,
+//   sum (x - mu)^2 = sum_k [ M2_k + n_k (m_k - mu)^2 ]
+// (the parallel-axis identity, exact for means used consistently; Chan,
+// Golub and LeVeque's pairwise update), still two scalars per warp.
+
+// Values of the row shard held by warp `wir`: vectors i*G + 32*wir + lane
+// below nvec, 8 values each.
+template <int VPT>
+__device__ __forceinline__ int ln_warp_count(int nvec, int G, int wir) {
+  int n = 0;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) n += min(max(nvec - i * G - 32 * wir, 0), 32);
+  return 8 * n;
+}
+
+// {n, fp32(1/n)} of a warp's count n (1/n = 0 for an empty warp): the mean a
+// warp's M2 is taken about is s1 * fp32(1/n), the same expression on the
+// sending and on the receiving side.
+__device__ __forceinline__ float2 ln_count_pair(int n) {
+  return make_float2((float)n, n > 0 ? 1.0f / (float)n : 0.f);
+}
+
+// s1 and M2 of this warp's values w (vectors beyond nvec hold zeros and are
+// left out of M2); `c` = ln_count_pair of the warp's count; whole warp.
+template <int VPT>
+__device__ __forceinline__ void ln_warp_stats(const uint64_t (&w)[VPT][4], int G, int g, int nvec,
+                                              float2 c, float* s1_out, float* m2_out) {
+  uint64_t c0 = 0, c1 = 0;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    c0 = f2_add(c0, f2_add(w[i][0], w[i][1]));
+    c1 = f2_add(c1, f2_add(w[i][2], w[i][3]));
+  }
+  const uint64_t cs = f2_add(c0, c1);
+  const float s1 = warp_sum(f2_lo(cs) + f2_hi(cs));
+  const float m = s1 * c.y;
+  const uint64_t nm = f2(-m, -m);
+  uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    if (i * G + g < nvec) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint64_t d = f2_add(w[i][q], nm);
+        acc[q] = f2_fma(d, d, acc[q]);
+      }
+    }
+  }
+  const uint64_t a = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+  *s1_out = s1;
+  *m2_out = warp_sum(f2_lo(a) + f2_hi(a));
+}
+
+// Row mean and variance from the (s1, M2) pairs of the row's N shards x
+// wpr warps (`parts`, rank order then warp order, pairs 8 bytes apart),
+// every shard's warps laid out alike; cnt(w) = ln_count_pair of warp w.
+template <typename Cnt>
+__device__ __forceinline__ void ln_combine(const float* parts, int N, int wpr, Cnt cnt,
+                                           float inv_H, float* mu_out, float* var_out) {
+  float s1 = 0.f;
+  for (int k = 0; k < N * wpr; ++k) s1 += parts[2 * k];
+  const float mu = s1 * inv_H;
+  float m2 = 0.f;
+  for (int w = 0; w < wpr; ++w) {
+    const float2 c = cnt(w);
+    for (int r = 0; r < N; ++r) {
+      const float* pk = parts + 2 * (r * wpr + w);
+      const float d = pk[0] * c.y - mu;
+      m2 = fmaf(c.x * d, d, m2 + pk[1]);
+    }
+  }
+  *mu_out = mu;
+  *var_out = m2 * inv_H;
 }
 
 // Registers: 96 per thread (4 CTAs of 160 threads per SM) beat 128 (3 CTAs)
@@ -217,6 +300,13 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
   }
   float* rcp = reinterpret_cast<float*>(smem + L.rcp);
   if (OUT == kOutNvfp4) fill_e4m3_reciprocals(rcp, tid, (int)blockDim.x);
+  float2* lnc = reinterpret_cast<float2*>(smem + L.rcp);
+  if (STAT == kQkLn) {
+    for (int q = tid; q < 32; q += (int)blockDim.x) {
+      const int k = q >> 4;
+      lnc[q] = ln_count_pair(k < p.ntensors ? ln_warp_count<VPT>(p.ten[k].nvec, p.G, q & 15) : 0);
+    }
+  }
   __syncthreads();
   // everything above touched shared memory only
   grid_dependency_wait();
@@ -355,7 +445,8 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       const int64_t tile = *reinterpret_cast<volatile int64_t*>(tloc + s);
       if (tile < 0 || tile >= p.ntiles) break;   // no more tiles
       int64_t t0;
-      const QkTensor& tn = p.ten[qk_tile(p, tile, &t0)];
+      const int tk = qk_tile(p, tile, &t0);   // tensor of the tile
+      const QkTensor& tn = p.ten[tk];
       const int64_t t = t0 + row;
       const bool valid = t < tn.T;
       const int nvec = tn.nvec;
@@ -365,18 +456,15 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       // as fp32 pairs in w; independent accumulators keep chains short.
       uint64_t w[VPT][4];
       uint64_t acc[4] = {0, 0, 0, 0};  // {0.f, 0.f} each
-      uint64_t sum2[2] = {0, 0};
       const unsigned char* srow =
           smem + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * tn.W * ES;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = i * p.G + g;
         load_vector<IN>(srow, v, valid && v < nvec, p.x_scale, w[i]);
+        if (STAT != kQkLn) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = f2_fma(w[i][q], w[i][q], acc[q]);
-        if (STAT == kQkLn) {
-          sum2[0] = f2_add(sum2[0], f2_add(w[i][0], w[i][1]));
-          sum2[1] = f2_add(sum2[1], f2_add(w[i][2], w[i][3]));
+          for (int q = 0; q < 4; ++q) acc[q] = f2_fma(w[i][q], w[i][q], acc[q]);
         }
       }
       // The cluster start-up wait comes before the stage goes back: rank 0's
@@ -389,13 +477,15 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       // the stage's data is in registers: hand it back to the producer
       __syncwarp();
       if (lane == 0) mbar_arrive(sbase + L.empty + 8 * s);
-      const uint64_t a01 = f2_add(acc[0], acc[1]), a23 = f2_add(acc[2], acc[3]);
-      const uint64_t a = f2_add(a01, a23);
-      const float ss = warp_sum(f2_lo(a) + f2_hi(a));
-      float s1 = 0.f;
+      // RMSNorm: ss = this warp's sum of squares.  LayerNorm: ss = its sum,
+      // s1 = its M2 about its own mean (ln_warp_stats)
+      float ss, s1 = 0.f;
       if (STAT == kQkLn) {
-        const uint64_t c = f2_add(sum2[0], sum2[1]);
-        s1 = warp_sum(f2_lo(c) + f2_hi(c));
+        ln_warp_stats<VPT>(w, p.G, g, nvec, lnc[16 * tk + wir], &ss, &s1);
+      } else {
+        const uint64_t a01 = f2_add(acc[0], acc[1]), a23 = f2_add(acc[2], acc[3]);
+        const uint64_t a = f2_add(a01, a23);
+        ss = warp_sum(f2_lo(a) + f2_hi(a));
       }
 
       // ---- exchange: send this warp's partial to every shard of the row
@@ -404,15 +494,13 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       const uint32_t slot0 = sbase + L.part + 4 * NS * (uint32_t)((b * p.R + row) * N * wpr);
       if (exchange) {
         if (g == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(N * wpr * 4 * NS));
-        if (lane == 0) {
+        // lane k sends to rank k: the N stores leave in one instruction
+        if (lane < N) {
           const uint32_t slot = slot0 + 4 * NS * (rank * wpr + wir);
-#pragma unroll
-          for (int k = 0; k < N; ++k) {
-            if (STAT == kQkLn)
-              st_async_f32x2(map_to_rank(slot, k), ss, s1, map_to_rank(xbar, k));
-            else
-              st_async_f32(map_to_rank(slot, k), ss, map_to_rank(xbar, k));
-          }
+          if (STAT == kQkLn)
+            st_async_f32x2(map_to_rank(slot, lane), ss, s1, map_to_rank(xbar, lane));
+          else
+            st_async_f32(map_to_rank(slot, lane), ss, map_to_rank(xbar, lane));
         }
       }
 
@@ -468,10 +556,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       if (OUT != kOutBf16) {
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
-          float m = 0.f;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            m = fmaxf(m, fmaxf(fabsf(f2_lo(w[i][q])), fabsf(f2_hi(w[i][q]))));
+          float m = absmax8(0.f, w[i]);
           // bv = B/8 is 2, 4 or 8: at most three steps, unrolled and guarded
           // by the (warp-uniform) block size; NVFP4 blocks are always 16
 #pragma unroll
@@ -482,27 +567,28 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       }
 
       // ---- combine in rank order (then warp order within a shard)
-      float S = ss, S1 = s1;
+      float S = ss, mu = 0.f, var = 0.f;
       if (exchange) {
         if (!mbar_wait_bounded(xbar, (uint32_t)((j >> 1) & 1), aborted ? 0 : p.wait_limit_ns)) {
           if (!aborted) atomicOr(&g_qk_status, kStatusTimeout);
           aborted = true;
         }
         const float* sl = reinterpret_cast<const float*>(smem + (slot0 - sbase));
-        S = 0.f;
-        S1 = 0.f;
-        for (int k = 0; k < N * wpr; ++k) {
-          S += sl[NS * k];
-          if (STAT == kQkLn) S1 += sl[NS * k + 1];
+        if (STAT == kQkLn) {
+          ln_combine(sl, N, wpr, [&](int w) { return lnc[16 * tk + w]; }, tn.inv_H, &mu, &var);
+        } else {
+          S = 0.f;
+          for (int k = 0; k < N * wpr; ++k) S += sl[k];
         }
+      } else if (STAT == kQkLn) {
+        const float own[2] = {ss, s1};
+        ln_combine(own, 1, 1, [&](int w) { return lnc[16 * tk + w]; }, tn.inv_H, &mu, &var);
       }
 
       // ---- Phase C: scale (and for LayerNorm centre and shift), store
       if (valid) {
-        float rinv, mu = 0.f;
+        float rinv;
         if (STAT == kQkLn) {
-          mu = S1 * tn.inv_H;
-          const float var = fmaxf(fmaf(S, tn.inv_H, -mu * mu), 0.f);
           rinv = rsqrtf(var + p.eps);
         } else {
           // the hardware reciprocal square root (a few 1e-8 relative error)
@@ -527,8 +613,9 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
           if (OUT != kOutBf16) {
             if (v < nvec) {
               // scale of this vector's block, then its eight codes
-              float is;
+              float is, m = 0.f;
               uint32_t keep = ~0u, sbyte;
+              bool one = false;   // one product per element (e8m0_single_multiplier)
               if (OUT == kOutNvfp4) {
                 sbyte = nvfp4_scale(am[i] * rinv, rcp, &is);
                 keep = sbyte != 0 ? ~0u : 0u;
@@ -536,12 +623,19 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
                 const int e = e8m0_exponent(am[i] * rinv, OUT == kOutE4M3 ? 8 : 2);
                 is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
                 sbyte = (uint32_t)(e + 127);
+                one = e8m0_single_multiplier(rinv, is, e, OUT == kOutE4M3 ? -116 : -124, &m);
               }
               if ((g & (kBv - 1)) == 0) srow_sc[v >> vshift] = (uint8_t)sbyte;
-              const uint64_t ss = f2(is, is);
               uint64_t q[4];
+              if (one) {
+                const uint64_t mm = f2(m, m);
 #pragma unroll
-              for (int h = 0; h < 4; ++h) q[h] = f2_mul(f2_mul(w[i][h], rr), ss);
+                for (int h = 0; h < 4; ++h) q[h] = f2_mul(w[i][h], mm);
+              } else {
+                const uint64_t ss = f2(is, is);
+#pragma unroll
+                for (int h = 0; h < 4; ++h) q[h] = f2_mul(f2_mul(w[i][h], rr), ss);
+              }
               if (OUT == kOutE4M3) {
                 const uint32_t lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
                 const uint32_t hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
