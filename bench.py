@@ -47,9 +47,11 @@ EPS = 1e-6
 KERNELS = ["qknorm_rms_qk[Q+K]", "rmsnorm_mxcast", "mxnorm_cast[p=1]", "mxnorm_cast[p=2]"]
 KERNEL_SOURCES = {   # files whose content the committed ncu traffic figures belong to
     "qknorm_rms_qk[Q+K]": ["normalization_token_split_gb300/csrc/qk_kernel.cuh",
-                           "normalization_token_split_gb300/csrc/qk_launch.cu"],
+                           "normalization_token_split_gb300/csrc/qk_launch.cu",
+                           "normalization_token_split_gb300/csrc/nts_device.cuh"],
     "rmsnorm_mxcast": ["normalization_token_split_gb300/csrc/mx_kernel.cuh",
-                       "normalization_token_split_gb300/csrc/mx_launch.cu"],
+                       "normalization_token_split_gb300/csrc/mx_launch.cu",
+                       "normalization_token_split_gb300/csrc/nts_device.cuh"],
 }
 KERNEL_SOURCES["mxnorm_cast[p=1]"] = KERNEL_SOURCES["rmsnorm_mxcast"]
 KERNEL_SOURCES["mxnorm_cast[p=2]"] = KERNEL_SOURCES["rmsnorm_mxcast"]
@@ -704,6 +706,21 @@ def parse_case(spec: str):
     return name, params
 
 
+TUNE_KEYS = ("vpt", "rows", "stages", "grid", "smem_budget")
+
+
+def parse_tune(spec):
+    """"key=value,..." over TUNE_KEYS (launch-shape overrides, 0 = automatic)
+    -> keyword arguments of nts.set_tuning."""
+    out = {}
+    for item in filter(None, (spec or "").split(",")):
+        k, _, v = item.partition("=")
+        if k not in TUNE_KEYS:
+            raise SystemExit(f"unknown tuning key {k!r}; known: {', '.join(TUNE_KEYS)}")
+        out[k] = int(v)
+    return out
+
+
 def case_bytes(name, q):
     """Algorithmic HBM bytes of one launch (gamma and beta excluded)."""
     if name in ("rmsnorm_mxcast", "mxnorm_cast", "mxnorm_postround_cast"):
@@ -804,13 +821,20 @@ def run_case(args):
     dev = "cuda:0"
     torch.cuda.set_device(0)
     name, q = parse_case(args.case)
+    tune = parse_tune(args.tune)
     fns = make_case(nts, torch, dev, name, q, args.sets)
-    ms = time_launches(torch, fns, args.steps, warmup=args.warmup)
-    nts.check_status()
+    if tune:
+        nts.set_tuning(**tune)
+    try:
+        ms = time_launches(torch, fns, args.steps, warmup=args.warmup)
+        nts.check_status()
+    finally:
+        nts.set_tuning()
     peak, peak_kind = measured_peaks()
     nbytes = case_bytes(name, q)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    print(json.dumps({"case": name, "params": q, "input_sets": args.sets, "launches": args.steps,
+    print(json.dumps({"case": name, "params": q, "tune": tune, "input_sets": args.sets,
+                      "launches": args.steps,
                       "us_per_launch": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
                       "frac_of_measured": round(gbs / peak, 4), "peak_source": peak_kind}),
           flush=True)
@@ -964,6 +988,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--case", default=None,
                     help="time one kernel alone, e.g. mxnorm_cast:T=16384,D=1024,B=16,fmt=e2m1")
+    ap.add_argument("--tune", default="",
+                    help="--case: launch-shape overrides, e.g. vpt=4,rows=2,stages=3")
     ap.add_argument("--sets", type=int, default=1,
                     help="--case: input sets rotated between launches")
     args = ap.parse_args(argv)

@@ -26,9 +26,10 @@
 //    f32x2 pipes, and the element cast is the hardware
 //    cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32;
 //  * a thread's unit (a block, or half of a 64-value block) is U 16-byte
-//    vectors 16*U bytes apart from its neighbours'; thread L reads them
-//    starting at vector (L*U/8) mod U so the eight lanes of each
-//    shared-memory phase hit eight distinct bank groups;
+//    vectors 16*U bytes apart from its neighbours'; thread L reads them in
+//    the order k ^ ((L*U/8) mod U) so the eight lanes of each shared-memory
+//    phase hit eight distinct bank groups, and writes the unit's codes back
+//    in element order with one store;
 //  * the row is read from shared memory twice (statistic, then cast), so no
 //    thread holds more than its block absmaxes between the passes; the stage
 //    is released after the second pass;
@@ -66,6 +67,7 @@ struct MxParams {
   float eps;
   float corr;           // MXNorm: c(B,1) for p = 1, c(B,2)^2 for p = 2
   int post;             // MXNorm: 1 = statistic from E8M0-rounded absmaxes (post-round)
+  int wide;             // 1: every codes row starts on a 32-byte boundary (32-byte stores)
   uint64_t wait_limit_ns;
   uint32_t missing_tx;  // test hook: bytes expected on the first stage but never sent
   unsigned int* sched;  // zeroed counter pair (next tile, CTAs done), or nullptr:
@@ -128,22 +130,28 @@ __device__ __forceinline__ void weigh_vector(const uint4& v, const float* gp, ui
 }
 
 // Element codes of one unit (UV 16-byte vectors of a row staged in shared
-// memory at `base`, read from vector `sig` on): q = w * a (ONE) or
-// (w * a) * c, w = x or fp32(x * gamma), then the packed conversions and
-// the stores into the codes row `crow` (`keep` masks NVFP4 blocks with a
-// zero scale).
-template <int FMT, int UV, bool ONE>
+// memory at `base`, read in the order k ^ sig, k = 0..UV-1): q = w * a (ONE)
+// or (w * a) * c, w = x or fp32(x * gamma) (GAMMA), then the packed
+// conversions.  ONE: the codes are put back in element order in registers
+// (a butterfly of selects on the bits of sig) and leave in one store of the
+// whole unit (32 bytes when `wide`: the codes row is 32-byte aligned), so
+// that every store instruction writes whole 32-byte sectors; otherwise one
+// store per vector (`keep` masks NVFP4 blocks with a zero scale).
+template <int FMT, int UV, bool ONE, bool GAMMA>
 __device__ __forceinline__ void cast_unit(const unsigned char* base, int sig, const float* gamma,
-                                          int b, int kU, uint64_t a, uint64_t c, uint8_t* crow,
-                                          uint32_t keep) {
+                                          int b, uint64_t a, uint64_t c, uint8_t* crow,
+                                          uint32_t keep, bool wide) {
+  constexpr int kU = UV * 8;
+  constexpr int kW = FMT == NTS_FMT_E4M3 ? 2 : 1;   // code words per vector
+  uint32_t cw[UV][kW];
   // the two-product form only runs for extreme rows: kept rolled up, so that
   // it adds no registers to the unrolled one-product loop
 #pragma unroll(ONE ? UV : 1)
   for (int k = 0; k < UV; ++k) {
-    const int u = (k + sig) & (UV - 1);
+    const int u = k ^ sig;
     const uint4 v = lds128(base + u * 16);
     uint64_t w[4];
-    if (gamma == nullptr) {
+    if (!GAMMA) {
       w[0] = bf16x2_to_f2c(v.x);
       w[1] = bf16x2_to_f2c(v.y);
       w[2] = bf16x2_to_f2c(v.z);
@@ -154,19 +162,140 @@ __device__ __forceinline__ void cast_unit(const unsigned char* base, int sig, co
     uint64_t q[4];
 #pragma unroll
     for (int h = 0; h < 4; ++h) q[h] = ONE ? f2_mul(w[h], a) : f2_mul(f2_mul(w[h], a), c);
+    uint32_t lo, hi = 0;
     if (FMT == NTS_FMT_E4M3) {
-      const uint32_t lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
-      const uint32_t hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
+      lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
+      hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
+    } else {
+      lo = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]), f2_lo(q[2]),
+                      f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3])) & keep;
+    }
+    if (ONE) {
+      cw[k][0] = lo;
+      if (kW == 2) cw[k][kW - 1] = hi;
+    } else if (FMT == NTS_FMT_E4M3) {
       st_global_v2(crow + (size_t)b * kU + u * 8, lo, hi);
     } else {
-      const uint32_t cc = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]),
-                                     f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
-      st_global_u32(crow + (size_t)b * (kU / 2) + u * 4, cc & keep);
+      st_global_u32(crow + (size_t)b * (kU / 2) + u * 4, lo);
+    }
+  }
+  if (ONE) {
+    // cw[k] holds vector k ^ sig: swap the pairs that differ in each set bit
+#pragma unroll
+    for (int bit = 1; bit < UV; bit <<= 1) {
+      const bool sw = (sig & bit) != 0;
+#pragma unroll
+      for (int k = 0; k < UV; ++k) {
+        if (k & bit) continue;
+#pragma unroll
+        for (int h = 0; h < kW; ++h) {
+          const uint32_t x = cw[k][h], y = cw[k | bit][h];
+          cw[k][h] = sw ? y : x;
+          cw[k | bit][h] = sw ? x : y;
+        }
+      }
+    }
+    uint8_t* dst = crow + (size_t)b * (UV * 4 * kW);
+    if (UV * kW == 8) {          // 32 bytes: E4M3 with 4 vectors
+      if (wide) {
+        st_global_v8(dst, cw[0][0], cw[0][kW - 1], cw[1][0], cw[1][kW - 1], cw[2 % UV][0],
+                     cw[2 % UV][kW - 1], cw[3 % UV][0], cw[3 % UV][kW - 1]);
+      } else {
+        st_global_v4(dst, cw[0][0], cw[0][kW - 1], cw[1][0], cw[1][kW - 1]);
+        st_global_v4(dst + 16, cw[2 % UV][0], cw[2 % UV][kW - 1], cw[3 % UV][0],
+                     cw[3 % UV][kW - 1]);
+      }
+    } else if (UV * kW == 4) {   // 16 bytes: E4M3 with 2 vectors, E2M1 with 4
+      if (kW == 2)
+        st_global_v4(dst, cw[0][0], cw[0][kW - 1], cw[1 % UV][0], cw[1 % UV][kW - 1]);
+      else
+        st_global_v4(dst, cw[0][0], cw[1 % UV][0], cw[2 % UV][0], cw[3 % UV][0]);
+    } else {                     // 8 bytes: E2M1 with 2 vectors
+      st_global_v2(dst, cw[0][0], cw[1 % UV][0]);
     }
   }
 }
 
-template <int VB, int BPT, int FMT, int STAT>
+// Pass 1 over a thread's units of a staged row: the absmax of w = x (or
+// fp32(x * gamma)) of every unit into am[], and for RMSNorm the packed sums
+// of x^2 into acc.  Four independent chains per reduction (one per 32-bit
+// lane of a vector), so that a unit is not one long dependency chain.
+template <int UV, int BPT, bool GAMMA, bool SUMSQ>
+__device__ __forceinline__ void mx_absmax_pass(const unsigned char* srow, const float* gamma,
+                                               int G, int g, int units, bool valid, int sig,
+                                               float (&am)[BPT], uint64_t (&acc)[4]) {
+  constexpr int kU = UV * 8;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    const int b = i * G + g;
+    am[i] = 0.f;
+    if (valid && b < units) {
+      const unsigned char* base = srow + (uint32_t)b * kU * 2;
+      if (!GAMMA) {
+        uint32_t m[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < UV; ++k) {
+          const int u = k ^ sig;
+          const uint4 v = lds128(base + u * 16);
+          m[0] = bf16x2_absmax(m[0], v.x);
+          m[1] = bf16x2_absmax(m[1], v.y);
+          m[2] = bf16x2_absmax(m[2], v.z);
+          m[3] = bf16x2_absmax(m[3], v.w);
+          if (SUMSQ) {
+            const uint64_t a = bf16x2_to_f2c(v.x), c = bf16x2_to_f2c(v.y);
+            const uint64_t d = bf16x2_to_f2c(v.z), e = bf16x2_to_f2c(v.w);
+            acc[0] = f2_fma(a, a, acc[0]);
+            acc[1] = f2_fma(c, c, acc[1]);
+            acc[2] = f2_fma(d, d, acc[2]);
+            acc[3] = f2_fma(e, e, acc[3]);
+          }
+        }
+        am[i] = bf16x2_hmax_abs(bf16x2_absmax(bf16x2_absmax(m[0], m[1]),
+                                              bf16x2_absmax(m[2], m[3])));
+      } else {
+        float mf[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < UV; ++k) {
+          const int u = k ^ sig;
+          const uint4 v = lds128(base + u * 16);
+          if (SUMSQ) {
+            const uint64_t a = bf16x2_to_f2c(v.x), c = bf16x2_to_f2c(v.y);
+            const uint64_t d = bf16x2_to_f2c(v.z), e = bf16x2_to_f2c(v.w);
+            acc[0] = f2_fma(a, a, acc[0]);
+            acc[1] = f2_fma(c, c, acc[1]);
+            acc[2] = f2_fma(d, d, acc[2]);
+            acc[3] = f2_fma(e, e, acc[3]);
+          }
+          uint64_t w[4];
+          weigh_vector(v, gamma + (size_t)b * kU + u * 8, w);
+          mf[k & 3] = absmax8(mf[k & 3], w);
+        }
+        am[i] = fmaxf(fmaxf(mf[0], mf[1]), fmaxf(mf[2], mf[3]));
+      }
+    }
+  }
+}
+
+// MXNorm statistic of a thread's block absmaxes: sum a (p = 1) or sum a^2
+// (p = 2), a = the absmax, or its E8M0-rounded power of two (POST); the
+// units that lead a block (every unit, or the even half of a split block).
+template <int BPT, int STAT, bool POST, bool SPLIT>
+__device__ __forceinline__ float mx_block_stat(const float (&am)[BPT], int G, int g, int units,
+                                               bool valid) {
+  float stat = 0.f;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    const int b = i * G + g;
+    if (valid && b < units && (!SPLIT || (g & 1) == 0)) {
+      const float a = POST ? round_pow2(am[i]) : am[i];
+      if (STAT == kStatMxP1) stat += a;
+      if (STAT == kStatMxP2) stat = fmaf(a, a, stat);
+    }
+  }
+  return stat;
+}
+
+template <int VB, int BPT, int FMT, int STAT, bool GAMMA>
 __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxParams p) {
   // A 64-value block is split between two adjacent lanes, 32 values each
   // (the layout of 32-value blocks), which combine their absmaxes by one
@@ -282,72 +411,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
     const unsigned char* srow = smem + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * p.D * 2;
 
     // ---- pass 1: block absmaxes (of w = x or x*gamma) and the statistic
-    // Four independent chains for every reduction (one per 32-bit lane of a
-    // vector), so that a block of 64 values is not one long dependency chain.
     float am[BPT];
-    float stat = 0.f;
     uint64_t acc[4] = {0, 0, 0, 0};  // RMSNorm: packed sums of x^2
+    mx_absmax_pass<kUV, BPT, GAMMA, STAT == kStatRms>(srow, p.gamma, p.G, g, units, valid, sig,
+                                                      am, acc);
+    // the two halves of a split block share one absmax (lanes g, g ^ 1 hold
+    // units b, b ^ 1: same row, both in range or both out, as G and the
+    // unit count are even)
+    if (kSplit) {
 #pragma unroll
-    for (int i = 0; i < BPT; ++i) {
-      const int b = i * p.G + g;   // unit (block, or half block when split)
-      am[i] = 0.f;
-      if (valid && b < units) {
-        const unsigned char* base = srow + (uint32_t)b * kU * 2;
-        if (p.gamma == nullptr) {
-          uint32_t m[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int k = 0; k < kUV; ++k) {
-            const int u = (k + sig) & (kUV - 1);
-            const uint4 v = lds128(base + u * 16);
-            m[0] = bf16x2_absmax(m[0], v.x);
-            m[1] = bf16x2_absmax(m[1], v.y);
-            m[2] = bf16x2_absmax(m[2], v.z);
-            m[3] = bf16x2_absmax(m[3], v.w);
-            if (STAT == kStatRms) {
-              const uint64_t a = bf16x2_to_f2c(v.x), c = bf16x2_to_f2c(v.y);
-              const uint64_t d = bf16x2_to_f2c(v.z), e = bf16x2_to_f2c(v.w);
-              acc[0] = f2_fma(a, a, acc[0]);
-              acc[1] = f2_fma(c, c, acc[1]);
-              acc[2] = f2_fma(d, d, acc[2]);
-              acc[3] = f2_fma(e, e, acc[3]);
-            }
-          }
-          am[i] = bf16x2_hmax_abs(bf16x2_absmax(bf16x2_absmax(m[0], m[1]),
-                                                bf16x2_absmax(m[2], m[3])));
-        } else {
-          float mf[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int k = 0; k < kUV; ++k) {
-            const int u = (k + sig) & (kUV - 1);
-            const uint4 v = lds128(base + u * 16);
-            if (STAT == kStatRms) {
-              const uint64_t a = bf16x2_to_f2c(v.x), c = bf16x2_to_f2c(v.y);
-              const uint64_t d = bf16x2_to_f2c(v.z), e = bf16x2_to_f2c(v.w);
-              acc[0] = f2_fma(a, a, acc[0]);
-              acc[1] = f2_fma(c, c, acc[1]);
-              acc[2] = f2_fma(d, d, acc[2]);
-              acc[3] = f2_fma(e, e, acc[3]);
-            }
-            uint64_t w[4];
-            weigh_vector(v, p.gamma + (size_t)b * kU + u * 8, w);
-            mf[k & 3] = absmax8(mf[k & 3], w);
-          }
-          am[i] = fmaxf(fmaxf(mf[0], mf[1]), fmaxf(mf[2], mf[3]));
-        }
-      }
-      // the two halves of a split block share one absmax (lanes g, g ^ 1 hold
-      // units b, b ^ 1: same row, both in range or both out, as G and the
-      // unit count are even)
-      if (kSplit) am[i] = fmaxf(am[i], __shfl_xor_sync(0xFFFFFFFFu, am[i], 1));
-      if (valid && b < units && (!kSplit || (g & 1) == 0)) {
-        const float a = (STAT != kStatRms && p.post) ? round_pow2(am[i]) : am[i];
-        if (STAT == kStatMxP1) stat += a;
-        if (STAT == kStatMxP2) stat = fmaf(a, a, stat);
-      }
+      for (int i = 0; i < BPT; ++i) am[i] = fmaxf(am[i], __shfl_xor_sync(0xFFFFFFFFu, am[i], 1));
     }
+    float stat;
     if (STAT == kStatRms) {
       const uint64_t a = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
       stat = f2_lo(a) + f2_hi(a);
+    } else if (p.post) {
+      stat = mx_block_stat<BPT, STAT, true, kSplit>(am, p.G, g, units, valid);
+    } else {
+      stat = mx_block_stat<BPT, STAT, false, kSplit>(am, p.G, g, units, valid);
     }
     stat = group_sum(stat, min(p.G, 32));
     if (wpr > 1) {
@@ -381,38 +463,77 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
     if (valid && p.rinv_out != nullptr && g == 0) p.rinv_out[t] = rinv;
 
     // ---- pass 2: scales and element codes
-    if (valid) {
-      const uint64_t rr = f2c(rinv, rinv);
-      uint8_t* crow = p.codes + (size_t)t * cbytes;
+    uint8_t* crow = p.codes + (size_t)t * cbytes;
+    uint8_t* srow_sc = p.scales + (size_t)t * p.K;
+    if (FMT == NTS_FMT_NVFP4) {
+      if (valid) {
+        const uint64_t rr = f2c(rinv, rinv);
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) {
+          const int b = i * p.G + g;   // unit = block (B = 16)
+          if (b < units) {
+            float is;
+            const uint32_t sc = nvfp4_scale(am[i] * rinv, rcp, &is);
+            srow_sc[b] = (uint8_t)sc;
+            if (p.amax_out != nullptr) p.amax_out[(size_t)t * p.K + b] = am[i];
+            cast_unit<FMT, kUV, false, GAMMA>(srow + (uint32_t)b * kU * 2, sig, p.gamma, b, rr,
+                                              f2c(is, is), crow, sc != 0 ? ~0u : 0u, false);
+          }
+        }
+      }
+    } else {
+      // E8M0: every block's scale byte first, then the codes.  When every
+      // block of the warp's rows takes one product per element by
+      // m = rinv * 2^-e (ordinary rows: e8m0_single_multiplier; a block of
+      // zeros with m = 0), one unrolled loop runs over all units; otherwise
+      // the form is picked per unit.
+      const OneProductRange opr = one_product_range(rinv, kEminOne);
+      float mul[BPT];
+      bool all_one = true;
 #pragma unroll
       for (int i = 0; i < BPT; ++i) {
         const int b = i * p.G + g;   // unit
-        if (b < units) {
+        mul[i] = 0.f;
+        if (valid && b < units) {
           const int blk = kSplit ? (b >> 1) : b;
           const bool lead = !kSplit || (b & 1) == 0;   // writes the block's scale
-          float is;                 // multiplier taking w*rinv to the element grid
-          uint32_t keep = ~0u;      // NVFP4: 0 for a block whose scale is zero
-          int e = 0;                // E8M0 exponent
-          if (FMT == NTS_FMT_NVFP4) {
-            const uint32_t sc = nvfp4_scale(am[i] * rinv, rcp, &is);
-            keep = sc != 0 ? ~0u : 0u;
-            p.scales[(size_t)t * p.K + blk] = (uint8_t)sc;
-          } else {
-            e = e8m0_exponent(am[i] * rinv, kEmax);
-            is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
-            if (lead) p.scales[(size_t)t * p.K + blk] = (uint8_t)(e + 127);
-          }
+          const uint32_t sbyte = (uint32_t)(e8m0_exponent(am[i] * rinv, kEmax) + 127);
+          if (lead) srow_sc[blk] = (uint8_t)sbyte;
           if (p.amax_out != nullptr && lead) p.amax_out[(size_t)t * p.K + blk] = am[i];
-          const unsigned char* base = srow + (uint32_t)b * kU * 2;
-          // E8M0: one product per element by m = rinv * 2^-e where that gives
-          // the bits of the two products (every block of ordinary rows)
-          float m = 0.f;
-          const bool one = FMT != NTS_FMT_NVFP4 &&
-                           e8m0_single_multiplier(rinv, is, e, kEminOne, &m);
-          if (one) {
-            cast_unit<FMT, kUV, true>(base, sig, p.gamma, b, kU, f2c(m, m), 0, crow, keep);
-          } else {
-            cast_unit<FMT, kUV, false>(base, sig, p.gamma, b, kU, rr, f2c(is, is), crow, keep);
+          // a block of zeros casts to signed zeros by any finite multiplier
+          const bool zero = am[i] == 0.f;
+          all_one = all_one && (zero || (sbyte - opr.lo) <= opr.span);
+          mul[i] = zero ? 0.f : __uint_as_float(opr.cm - (sbyte << 23));
+        }
+      }
+      if (__all_sync(0xFFFFFFFFu, all_one)) {
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < BPT; ++i) {
+            const int b = i * p.G + g;
+            if (b < units)
+              cast_unit<FMT, kUV, true, GAMMA>(srow + (uint32_t)b * kU * 2, sig, p.gamma, b,
+                                               f2c(mul[i], mul[i]), 0, crow, ~0u, p.wide);
+          }
+        }
+      } else if (valid) {
+        const uint64_t rr = f2c(rinv, rinv);
+        // (unrolled over the units so that am[] stays in registers; each
+        // unit's vectors run rolled up)
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) {
+          const int b = i * p.G + g;
+          if (b < units) {
+            const int e = e8m0_exponent(am[i] * rinv, kEmax);
+            const float is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+            const unsigned char* base = srow + (uint32_t)b * kU * 2;
+            float m = 0.f;
+            if (e8m0_single_multiplier(rinv, is, e, kEminOne, &m))
+              cast_unit<FMT, kUV, false, GAMMA>(base, sig, p.gamma, b, f2c(m, m), f2c(1.f, 1.f),
+                                                crow, ~0u, false);
+            else
+              cast_unit<FMT, kUV, false, GAMMA>(base, sig, p.gamma, b, rr, f2c(is, is), crow,
+                                                ~0u, false);
           }
         }
       }
@@ -431,39 +552,40 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
 using MxKernel = void (*)(MxParams);
 
 // The kernel for BPT units of a thread (blocks of VB vectors; half blocks of
-// 4 vectors for VB = 8), or nullptr where a thread would hold more than 16
-// vectors (256 bytes) of its row (slower on GB300 wherever measured; the
-// launcher never picks them).
+// 4 vectors for VB = 8), with or without a gain, or nullptr where a thread
+// would hold more than 16 vectors (256 bytes) of its row (slower on GB300
+// wherever measured; the launcher never picks them).
 template <int FMT, int STAT, int VB, int BPT>
-MxKernel mx_kernel_if_small() {
+MxKernel mx_kernel_if_small(bool gamma) {
   if constexpr (BPT * (VB == 8 ? 4 : VB) <= 16) {
-    return mx_norm_cast_kernel<VB, BPT, FMT, STAT>;
+    return gamma ? mx_norm_cast_kernel<VB, BPT, FMT, STAT, true>
+                 : mx_norm_cast_kernel<VB, BPT, FMT, STAT, false>;
   } else {
     return nullptr;
   }
 }
 
 template <int FMT, int STAT, int VB>
-MxKernel pick_mx_bpt(int bpt) {
+MxKernel pick_mx_bpt(int bpt, bool gamma) {
   switch (bpt) {
-    case 1: return mx_kernel_if_small<FMT, STAT, VB, 1>();
-    case 2: return mx_kernel_if_small<FMT, STAT, VB, 2>();
-    case 3: return mx_kernel_if_small<FMT, STAT, VB, 3>();
-    case 4: return mx_kernel_if_small<FMT, STAT, VB, 4>();
-    case 5: return mx_kernel_if_small<FMT, STAT, VB, 5>();
-    case 6: return mx_kernel_if_small<FMT, STAT, VB, 6>();
-    case 7: return mx_kernel_if_small<FMT, STAT, VB, 7>();
-    case 8: return mx_kernel_if_small<FMT, STAT, VB, 8>();
+    case 1: return mx_kernel_if_small<FMT, STAT, VB, 1>(gamma);
+    case 2: return mx_kernel_if_small<FMT, STAT, VB, 2>(gamma);
+    case 3: return mx_kernel_if_small<FMT, STAT, VB, 3>(gamma);
+    case 4: return mx_kernel_if_small<FMT, STAT, VB, 4>(gamma);
+    case 5: return mx_kernel_if_small<FMT, STAT, VB, 5>(gamma);
+    case 6: return mx_kernel_if_small<FMT, STAT, VB, 6>(gamma);
+    case 7: return mx_kernel_if_small<FMT, STAT, VB, 7>(gamma);
+    case 8: return mx_kernel_if_small<FMT, STAT, VB, 8>(gamma);
     default: return nullptr;
   }
 }
 
 template <int FMT, int STAT>
-MxKernel pick_mx_block(int B, int bpt) {
+MxKernel pick_mx_block(int B, int bpt, bool gamma) {
   switch (B) {
-    case 16: return pick_mx_bpt<FMT, STAT, 2>(bpt);
-    case 32: return pick_mx_bpt<FMT, STAT, 4>(bpt);
-    case 64: return pick_mx_bpt<FMT, STAT, 8>(bpt);
+    case 16: return pick_mx_bpt<FMT, STAT, 2>(bpt, gamma);
+    case 32: return pick_mx_bpt<FMT, STAT, 4>(bpt, gamma);
+    case 64: return pick_mx_bpt<FMT, STAT, 8>(bpt, gamma);
     default: return nullptr;
   }
 }
@@ -481,17 +603,19 @@ static inline int read_and_clear_local_mx_status(unsigned* out) {
 // One translation unit per element format and statistic (mx_e4m3_rms.cu,
 // ..., mx_e2m1_p2.cu; NVFP4 in mx_nvfp4.cu), so that they compile in
 // parallel; each has its own status word.
-#define NTS_MX_UNIT(NAME, FMT, STAT)                                              \
-  MxKernel pick_##NAME(int B, int bpt) { return pick_mx_block<FMT, STAT>(B, bpt); } \
+#define NTS_MX_UNIT(NAME, FMT, STAT)                                            \
+  MxKernel pick_##NAME(int B, int bpt, bool gamma) {                             \
+    return pick_mx_block<FMT, STAT>(B, bpt, gamma);                              \
+  }                                                                              \
   int read_and_clear_##NAME##_status(unsigned* out) { return read_and_clear_local_mx_status(out); }
 
-MxKernel pick_mx_e4m3_rms(int B, int bpt);
-MxKernel pick_mx_e4m3_p1(int B, int bpt);
-MxKernel pick_mx_e4m3_p2(int B, int bpt);
-MxKernel pick_mx_e2m1_rms(int B, int bpt);
-MxKernel pick_mx_e2m1_p1(int B, int bpt);
-MxKernel pick_mx_e2m1_p2(int B, int bpt);
-MxKernel pick_mx_nvfp4(int stat, int B, int bpt);
+MxKernel pick_mx_e4m3_rms(int B, int bpt, bool gamma);
+MxKernel pick_mx_e4m3_p1(int B, int bpt, bool gamma);
+MxKernel pick_mx_e4m3_p2(int B, int bpt, bool gamma);
+MxKernel pick_mx_e2m1_rms(int B, int bpt, bool gamma);
+MxKernel pick_mx_e2m1_p1(int B, int bpt, bool gamma);
+MxKernel pick_mx_e2m1_p2(int B, int bpt, bool gamma);
+MxKernel pick_mx_nvfp4(int stat, int B, int bpt, bool gamma);
 int read_and_clear_mx_e4m3_rms_status(unsigned* out);
 int read_and_clear_mx_e4m3_p1_status(unsigned* out);
 int read_and_clear_mx_e4m3_p2_status(unsigned* out);

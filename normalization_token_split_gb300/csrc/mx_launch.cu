@@ -46,16 +46,16 @@ MxShape choose_mx_shape(int K, int VB, int force_bpt) {
   return sh;
 }
 
-// The kernel for element format fmt, statistic stat, block size B and bpt
-// blocks per thread (nullptr if none is built).
-MxKernel pick_mx(int fmt, int stat, int B, int bpt) {
-  if (fmt == NTS_FMT_NVFP4) return pick_mx_nvfp4(stat, B, bpt);
+// The kernel for element format fmt, statistic stat, block size B, bpt
+// blocks per thread and a gain or none (nullptr if none is built).
+MxKernel pick_mx(int fmt, int stat, int B, int bpt, bool gamma) {
+  if (fmt == NTS_FMT_NVFP4) return pick_mx_nvfp4(stat, B, bpt, gamma);
   if (stat < kStatRms || stat > kStatMxP2 || (fmt != NTS_FMT_E4M3 && fmt != NTS_FMT_E2M1))
     return nullptr;
-  MxKernel (*const table[2][3])(int, int) = {
+  MxKernel (*const table[2][3])(int, int, bool) = {
       {pick_mx_e4m3_rms, pick_mx_e4m3_p1, pick_mx_e4m3_p2},
       {pick_mx_e2m1_rms, pick_mx_e2m1_p1, pick_mx_e2m1_p2}};
-  return table[fmt == NTS_FMT_E2M1 ? 1 : 0][stat](B, bpt);
+  return table[fmt == NTS_FMT_E2M1 ? 1 : 0][stat](B, bpt, gamma);
 }
 
 }  // namespace
@@ -70,8 +70,8 @@ struct MxLaunchShape {
   MxKernel kern = nullptr;
 };
 
-int mx_launch_shape(int64_t T, int D, int B, int fmt, int p, int sm_count, int max_smem_optin,
-                    const LaunchTuning& tune, MxLaunchShape* out) {
+int mx_launch_shape(int64_t T, int D, int B, int fmt, int p, bool gamma, int sm_count,
+                    int max_smem_optin, const LaunchTuning& tune, MxLaunchShape* out) {
   const int K = D / B;
   // tune.force_vpt selects the units per thread for this kernel family; a
   // unit is a block, or half a block of 64 values (the kernel splits those
@@ -108,7 +108,7 @@ int mx_launch_shape(int64_t T, int D, int B, int fmt, int p, int sm_count, int m
     return fail(NTS_ERR_UNSUPPORTED, "row too wide for shared memory: D = %d", D);
 
   const int stat = p == 0 ? kStatRms : (p == 1 ? kStatMxP1 : kStatMxP2);
-  MxKernel kern = pick_mx(fmt, stat, B, sh.bpt);
+  MxKernel kern = pick_mx(fmt, stat, B, sh.bpt, gamma);
   if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for B=%d bpt=%d", B, sh.bpt);
   out->bpt = sh.bpt;
   out->G = sh.G;
@@ -126,8 +126,8 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   const DeviceInfo& dev = device_info();
   if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
   MxLaunchShape ls;
-  int rc = mx_launch_shape(rq.T, D, rq.B, rq.fmt, rq.p, dev.sm_count, dev.max_smem_optin, tune,
-                           &ls);
+  int rc = mx_launch_shape(rq.T, D, rq.B, rq.fmt, rq.p, rq.gamma != nullptr, dev.sm_count,
+                           dev.max_smem_optin, tune, &ls);
   if (rc != NTS_OK) return rc;
   const MxShape sh{ls.bpt, ls.G};
   const int R = ls.R, S = ls.S;
@@ -153,6 +153,10 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   if (rq.p == 1) prm.corr = (float)rq.corr;
   if (rq.p == 2) prm.corr = (float)(rq.corr * rq.corr);
   prm.post = rq.post;
+  // every codes row starts 32-byte aligned when the base does and a row is
+  // a whole number of 32-byte pieces
+  const size_t crow_bytes = rq.fmt == NTS_FMT_E4M3 ? (size_t)D : (size_t)D / 2;
+  prm.wide = (reinterpret_cast<uintptr_t>(rq.codes) % 32 == 0 && crow_bytes % 32 == 0) ? 1 : 0;
   prm.wait_limit_ns = tune.wait_limit_ns;
   prm.missing_tx = tune.missing_tx;
   prm.sched = tune.dynamic ? sched_counters(stream) : nullptr;
@@ -213,7 +217,7 @@ extern "C" int nts_debug_mx_launch_shape(int64_t T, int64_t D, int B, int fmt, i
       (fmt == NTS_FMT_NVFP4 && B != 16))
     return fail(NTS_ERR_INVALID_ARG, "bad shape query");
   MxLaunchShape ls;
-  const int rc = mx_launch_shape(T, (int)D, B, fmt, p, sm_count, max_smem_optin,
+  const int rc = mx_launch_shape(T, (int)D, B, fmt, p, false, sm_count, max_smem_optin,
                                  current_tuning(), &ls);
   if (rc != NTS_OK) return rc;
   shape[0] = ls.bpt;

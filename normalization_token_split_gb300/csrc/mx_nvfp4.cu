@@ -5,12 +5,12 @@
 
 namespace nts {
 
-MxKernel pick_mx_nvfp4(int stat, int B, int bpt) {
+MxKernel pick_mx_nvfp4(int stat, int B, int bpt, bool gamma) {
   if (B != 16) return nullptr;
   switch (stat) {
-    case kStatRms: return pick_mx_bpt<NTS_FMT_NVFP4, kStatRms, 2>(bpt);
-    case kStatMxP1: return pick_mx_bpt<NTS_FMT_NVFP4, kStatMxP1, 2>(bpt);
-    case kStatMxP2: return pick_mx_bpt<NTS_FMT_NVFP4, kStatMxP2, 2>(bpt);
+    case kStatRms: return pick_mx_bpt<NTS_FMT_NVFP4, kStatRms, 2>(bpt, gamma);
+    case kStatMxP1: return pick_mx_bpt<NTS_FMT_NVFP4, kStatMxP1, 2>(bpt, gamma);
+    case kStatMxP2: return pick_mx_bpt<NTS_FMT_NVFP4, kStatMxP2, 2>(bpt, gamma);
     default: return nullptr;
   }
 }

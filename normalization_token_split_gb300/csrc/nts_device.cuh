@@ -303,6 +303,29 @@ __device__ __forceinline__ bool e8m0_single_multiplier(float rinv, float is, int
   return e >= emin_one && field - 1u < 254u;
 }
 
+// Per-row bounds of the E8M0 scale bytes (e + 127) whose blocks take one
+// product per element (e8m0_single_multiplier): m = rinv * 2^-e is normal,
+// i.e. its exponent field f_r + 127 - byte lies in [1, 254] (f_r: the field
+// of rinv), and e >= emin_one.  A byte qualifies iff (byte - lo) <= span as
+// unsigned; no byte does when rinv is zero or subnormal.
+struct OneProductRange {
+  uint32_t lo, span;
+  uint32_t cm;   // bits of rinv * 2^127: the multiplier's bits are cm - (byte << 23)
+};
+
+__device__ __forceinline__ OneProductRange one_product_range(float rinv, int emin_one) {
+  const uint32_t rb = __float_as_uint(rinv);
+  const int fr = (int)(rb >> 23);   // rinv > 0: no sign bit
+  const int lo = max(fr - 127, emin_one + 127);
+  const int hi = fr + 126;
+  OneProductRange r;
+  const bool any = fr >= 1 && fr <= 254 && hi >= lo;
+  r.lo = any ? (uint32_t)lo : 0x7FFFFFFFu;
+  r.span = any ? (uint32_t)(hi - lo) : 0u;
+  r.cm = rb + 0x3F800000u;
+  return r;
+}
+
 // The same exponent by the plain definition (exponent field, mantissa
 // compare, zero/subnormal special case): the reference of the self-check.
 __device__ __forceinline__ int e8m0_exponent_by_fields(float ay, int emax) {
@@ -399,6 +422,21 @@ __device__ __forceinline__ float absmax8(float m, const uint64_t (&w)[4]) {
 
 __device__ __forceinline__ void st_global_v2(void* p, uint32_t a, uint32_t b) {
   *reinterpret_cast<uint2*>(p) = make_uint2(a, b);
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+
+// 32-byte store (one whole sector; sm_100 and later), p 32-byte aligned.
+// No memory clobber: the kernels never read what they store, so shared-
+// memory loads may move across it.
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d, uint32_t e, uint32_t f, uint32_t g,
+                                             uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a),
+               "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h));
 }
 
 __device__ __forceinline__ void st_global_u32(void* p, uint32_t a) {

@@ -111,31 +111,38 @@ def test_row_widths_and_ragged_tails(D, T):
             compare(kind, X, g, 1e-6, B, fmt, p, what=f"{kind}{p} T={T} D={D} {fmt}")
 
 
-def test_degenerate_blocks():
+@pytest.mark.parametrize("B", [16, 32, 64])
+def test_degenerate_blocks(B):
     X, _ = workloads.mx_inputs(64, 512, seed=77)
     X[0] = 0                          # all-zero row
-    X[1, :32] = 0                     # one zero block
-    X[2, 32:64] = 1e-38               # tiny block (scale clamps at 2^-127)
-    X[3, 64:96] = -1.0e17             # large values (sum of squares stays finite in fp32)
+    X[1, :B] = 0                      # one zero block
+    X[5, B:3 * B] = 0                 # two zero blocks among ordinary ones
+    X[2, 64:128] = 1e-38              # tiny blocks (scale clamps at 2^-127)
+    X[3, 128:192] = -1.0e17           # large values (sum of squares stays finite in fp32)
     X[4, ::2] = -0.0
+    X[6, 1::3] = 0                    # scattered zeros
     for kind, p in KINDS:
         for fmt in ("e4m3", "e2m1"):
-            compare(kind, X, None, 1e-6, 32, fmt, p, what=f"degenerate {kind}{p} {fmt}")
+            compare(kind, X, None, 1e-6, B, fmt, p, what=f"degenerate {kind}{p} B={B} {fmt}")
 
 
-def test_extreme_factors():
+@pytest.mark.parametrize("B", [16, 32, 64])
+@pytest.mark.parametrize("with_gamma", [False, True])
+def test_extreme_factors(B, with_gamma):
     # rows so small that the mean square underflows and rinv = 1/sqrt(eps)
     # is huge: rinv * 2^-e would overflow fp32 for some blocks, so a kernel
     # that folded the two products w*rinv and *2^-e into one would go wrong
-    # there; fp32(w*rinv) itself is subnormal for some elements of others
-    X, _ = workloads.mx_inputs(8, 1024, seed=78)
+    # there; fp32(w*rinv) itself is subnormal for some elements of others.
+    # Ordinary rows share warps and tiles with them (both forms in one launch).
+    X, g = workloads.mx_inputs(40, 1024, seed=78 + B, with_gamma=with_gamma)
     Xf = X.float()
     for r, sc in enumerate((1e-36, 1e-34, 1e-30, 1e-25, 1e-20, 1e-12, 3e-39, 1.0)):
-        Xf[r] *= sc
+        Xf[3 * r] *= sc
     X = Xf.to(torch.bfloat16)
     for kind, p in KINDS:
         for fmt in ("e4m3", "e2m1"):
-            compare(kind, X, None, 1e-38, 32, fmt, p, what=f"extreme {kind}{p} {fmt}")
+            compare(kind, X, g, 1e-38, B, fmt, p,
+                    what=f"extreme {kind}{p} B={B} {fmt} gamma={with_gamma}")
 
 
 def test_zero_tokens_launches_nothing():
