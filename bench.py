@@ -328,6 +328,16 @@ def run_gpu(args):
                          "gbs": round(gbs, 1), "tokens_per_s": round(tokens[name] / (per_kernel_ms[name] * 1e-3)),
                          "frac_of_measured": round(gbs / peak, 4),
                          "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
+    # each launch's marginal cost inside the step, with no marks: the time of
+    # the unmarked step minus that of the step without it (the same
+    # programmatic dependent launches between the others)
+    for i, (name, _) in enumerate(launches):
+        rest = [fn for j, (_, fn) in enumerate(launches) if j != i]
+        ms_rest = time_launches(torch, rest, args.steps * len(rest), warmup=3)
+        marginal = ms_per_step - ms_rest * len(rest)
+        gbs = per_bytes[name] / (marginal * 1e-3) / 1e9
+        kernels[name]["marginal_in_step"] = {"ms": round(marginal, 5), "gbs": round(gbs, 1),
+                                             "frac_of_measured": round(gbs / peak, 4)}
     # each launch of the step alone, back to back (so every launch follows
     # one of its own kind): the kernel's steady-state rate, without the
     # write-back of the previous kernel's dirty L2 lines or the marks' gaps
@@ -374,6 +384,13 @@ def run_gpu(args):
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if not args.no_variants:
         result["variants"] = variant_rates(nts, torch, dev, Q, gq, X, peak, K, gk)
+        # the split-H paths again at T = 32768 rows (inputs and outputs of
+        # every launch well above L2; launch ramp and tail a smaller share)
+        Q4, gq4 = workloads.qk_inputs(4 * QK_T, QK_H, seed=3002, outlier_frac=0.01, device=dev)
+        K4, gk4 = workloads.qk_inputs(4 * QK_T, QK_H, seed=3003, outlier_frac=0.01, device=dev)
+        result["variants_T32768"] = variant_rates(nts, torch, dev, Q4, gq4, X, peak, K4, gk4,
+                                                  with_mx=False)
+        del Q4, K4
     result["kernels"] = kernels
     result["roofline"] = roofline
     if rank == 0:
@@ -569,10 +586,11 @@ def mx_config_by_T(nts, torch, dev, peak, reps=30):
     return {"by_T": out, "l2_bytes": l2}
 
 
-def variant_rates(nts, torch, dev, Q, gq, X, peak, K, gk, reps=20):
+def variant_rates(nts, torch, dev, Q, gq, X, peak, K, gk, reps=20, with_mx=True):
     """The widened paths outside the step, each at the step's sizes: device
     time per launch (CUDA events around `reps` back-to-back launches on the
-    launching stream, after 3 warm-up launches) and algorithmic GB/s."""
+    launching stream, after 3 warm-up launches) and algorithmic GB/s.
+    with_mx=False: only the split-H (QK) paths, at the size of Q."""
     import workloads
     T, H = Q.shape
     Tm, D = X.shape
@@ -621,6 +639,8 @@ def variant_rates(nts, torch, dev, Q, gq, X, peak, K, gk, reps=20):
             Tm * (2 * D + D // 2 + D // MX_B), lambda: nts.rmsnorm_mxcast(
                 X, None, eps=EPS, B=MX_B, fmt="e2m1", codes=codes4, scales=scales)),
     }
+    if not with_mx:
+        cases = {k: v for k, v in cases.items() if not k.startswith(("mxnorm", "rmsnorm"))}
     stream = torch.cuda.current_stream()
     out = {}
     for name, (nbytes, fn) in cases.items():

@@ -129,24 +129,33 @@ __device__ __forceinline__ void weigh_vector(const uint4& v, const float* gp, ui
   w[3] = f2_mul(bf16x2_to_f2c(v.w), f2c(g1.z, g1.w));
 }
 
+// How cast_unit forms and stores a unit's codes.
+enum {
+  kCastOne = 0,     // q = w * a, unrolled, codes stored in element order at once
+  kCastTwo = 1,     // q = (w * a) * c, unrolled, stored at once (NVFP4)
+  kCastRolled = 2,  // q = (w * a) * c, rolled up, one store per vector (extreme rows)
+};
+
 // Element codes of one unit (UV 16-byte vectors of a row staged in shared
-// memory at `base`, read in the order k ^ sig, k = 0..UV-1): q = w * a (ONE)
-// or (w * a) * c, w = x or fp32(x * gamma) (GAMMA), then the packed
-// conversions.  ONE: the codes are put back in element order in registers
-// (a butterfly of selects on the bits of sig) and leave in one store of the
-// whole unit (32 bytes when `wide`: the codes row is 32-byte aligned), so
-// that every store instruction writes whole 32-byte sectors; otherwise one
-// store per vector (`keep` masks NVFP4 blocks with a zero scale).
-template <int FMT, int UV, bool ONE, bool GAMMA>
+// memory at `base`, read in the order k ^ sig, k = 0..UV-1): q = w * a
+// (kCastOne) or (w * a) * c, w = x or fp32(x * gamma) (GAMMA), then the
+// packed conversions (`keep` masks NVFP4 blocks with a zero scale).  The
+// unrolled modes put the codes back in element order in registers (a
+// butterfly of selects on the bits of sig) and store the whole unit at once
+// (32 bytes when `wide`: the codes row is 32-byte aligned), so that every
+// store instruction writes whole 32-byte sectors; kCastRolled, which only
+// extreme rows take, stores each vector's codes on their own and adds no
+// registers to the unrolled loops.
+template <int FMT, int UV, int MODE, bool GAMMA>
 __device__ __forceinline__ void cast_unit(const unsigned char* base, int sig, const float* gamma,
                                           int b, uint64_t a, uint64_t c, uint8_t* crow,
                                           uint32_t keep, bool wide) {
   constexpr int kU = UV * 8;
   constexpr int kW = FMT == NTS_FMT_E4M3 ? 2 : 1;   // code words per vector
+  constexpr bool kOne = MODE == kCastOne;
+  constexpr bool kAtOnce = MODE != kCastRolled;
   uint32_t cw[UV][kW];
-  // the two-product form only runs for extreme rows: kept rolled up, so that
-  // it adds no registers to the unrolled one-product loop
-#pragma unroll(ONE ? UV : 1)
+#pragma unroll(kAtOnce ? UV : 1)
   for (int k = 0; k < UV; ++k) {
     const int u = k ^ sig;
     const uint4 v = lds128(base + u * 16);
@@ -161,7 +170,7 @@ __device__ __forceinline__ void cast_unit(const unsigned char* base, int sig, co
     }
     uint64_t q[4];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) q[h] = ONE ? f2_mul(w[h], a) : f2_mul(f2_mul(w[h], a), c);
+    for (int h = 0; h < 4; ++h) q[h] = kOne ? f2_mul(w[h], a) : f2_mul(f2_mul(w[h], a), c);
     uint32_t lo, hi = 0;
     if (FMT == NTS_FMT_E4M3) {
       lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
@@ -170,7 +179,7 @@ __device__ __forceinline__ void cast_unit(const unsigned char* base, int sig, co
       lo = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]), f2_lo(q[2]),
                       f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3])) & keep;
     }
-    if (ONE) {
+    if (kAtOnce) {
       cw[k][0] = lo;
       if (kW == 2) cw[k][kW - 1] = hi;
     } else if (FMT == NTS_FMT_E4M3) {
@@ -179,7 +188,7 @@ __device__ __forceinline__ void cast_unit(const unsigned char* base, int sig, co
       st_global_u32(crow + (size_t)b * (kU / 2) + u * 4, lo);
     }
   }
-  if (ONE) {
+  if (kAtOnce) {
     // cw[k] holds vector k ^ sig: swap the pairs that differ in each set bit
 #pragma unroll
     for (int bit = 1; bit < UV; bit <<= 1) {
@@ -476,8 +485,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
             const uint32_t sc = nvfp4_scale(am[i] * rinv, rcp, &is);
             srow_sc[b] = (uint8_t)sc;
             if (p.amax_out != nullptr) p.amax_out[(size_t)t * p.K + b] = am[i];
-            cast_unit<FMT, kUV, false, GAMMA>(srow + (uint32_t)b * kU * 2, sig, p.gamma, b, rr,
-                                              f2c(is, is), crow, sc != 0 ? ~0u : 0u, false);
+            cast_unit<FMT, kUV, kCastTwo, GAMMA>(srow + (uint32_t)b * kU * 2, sig, p.gamma, b, rr,
+                                                 f2c(is, is), crow, sc != 0 ? ~0u : 0u, false);
           }
         }
       }
@@ -512,8 +521,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
           for (int i = 0; i < BPT; ++i) {
             const int b = i * p.G + g;
             if (b < units)
-              cast_unit<FMT, kUV, true, GAMMA>(srow + (uint32_t)b * kU * 2, sig, p.gamma, b,
-                                               f2c(mul[i], mul[i]), 0, crow, ~0u, p.wide);
+              cast_unit<FMT, kUV, kCastOne, GAMMA>(srow + (uint32_t)b * kU * 2, sig, p.gamma, b,
+                                                   f2c(mul[i], mul[i]), 0, crow, ~0u, p.wide);
           }
         }
       } else if (valid) {
@@ -529,11 +538,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
             const unsigned char* base = srow + (uint32_t)b * kU * 2;
             float m = 0.f;
             if (e8m0_single_multiplier(rinv, is, e, kEminOne, &m))
-              cast_unit<FMT, kUV, false, GAMMA>(base, sig, p.gamma, b, f2c(m, m), f2c(1.f, 1.f),
-                                                crow, ~0u, false);
+              cast_unit<FMT, kUV, kCastRolled, GAMMA>(base, sig, p.gamma, b, f2c(m, m),
+                                                      f2c(1.f, 1.f), crow, ~0u, false);
             else
-              cast_unit<FMT, kUV, false, GAMMA>(base, sig, p.gamma, b, rr, f2c(is, is), crow,
-                                                ~0u, false);
+              cast_unit<FMT, kUV, kCastRolled, GAMMA>(base, sig, p.gamma, b, rr, f2c(is, is),
+                                                      crow, ~0u, false);
           }
         }
       }
