@@ -254,24 +254,28 @@ __device__ __forceinline__ void ln_combine(const float* parts, int N, int wpr, C
 // (no spills at any width; with a two-stage ring, 7-8 % faster than at 128);
 // the block-cast output with 8 vectors per thread keeps 128 so as not to
 // spill.
-template <int N, int VPT, int IN, int STAT, int OUT>
+// GC: the consumer threads per row when known at compile time (32, the
+// common shape: slot offsets then fold into the instructions' immediates,
+// measured 4-7 % faster for the variants not bound by DRAM), or 0: p.G.
+template <int N, int VPT, int IN, int STAT, int OUT, int GC>
 __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8) ? 128 : 96))
     qknorm_cluster_kernel(const QkParams p) {
   constexpr int ES = (IN == kInBf16) ? 2 : 1;  // bytes per activation
+  const int G = GC > 0 ? GC : p.G;
   constexpr int NS = (STAT == kQkLn) ? 2 : 1;  // scalars exchanged per warp
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t rank = (N > 1) ? cluster_ctarank() : 0u;
   const int64_t cid = cluster_id_x();
   const int64_t ncl = num_clusters_x();
   const int tid = threadIdx.x;
-  const int nconsumer = p.R * p.G;
+  const int nconsumer = p.R * G;
   const int lane = tid & 31;
-  const int wpr = p.G >> 5;
+  const int wpr = G >> 5;
   // block-cast output: vectors per block and log2 of the block size (NVFP4
   // blocks are 16 values: fixed at compile time)
   const int kBv = OUT == kOutNvfp4 ? 2 : p.bv;
   const int kBshift = OUT == kOutNvfp4 ? 4 : p.bshift;
-  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, p.psum, p.G, p.gsplit, ES, NS,
+  const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, p.psum, G, p.gsplit, ES, NS,
                                OUT == kOutNvfp4);
   const uint32_t sbase = smem_addr(smem);
   const uint32_t stage_bytes = (uint32_t)p.R * p.Wmax * ES;
@@ -304,7 +308,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
   if (STAT == kQkLn) {
     for (int q = tid; q < 32; q += (int)blockDim.x) {
       const int k = q >> 4;
-      lnc[q] = ln_count_pair(k < p.ntensors ? ln_warp_count<VPT>(p.ten[k].nvec, p.G, q & 15) : 0);
+      lnc[q] = ln_count_pair(k < p.ntensors ? ln_warp_count<VPT>(p.ten[k].nvec, G, q & 15) : 0);
     }
   }
   __syncthreads();
@@ -428,8 +432,8 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
     bool started = (N == 1);
     bool have_gamma = false;
 
-    const int row = tid / p.G;
-    const int g = tid - row * p.G;
+    const int row = tid / G;
+    const int g = tid - row * G;
     const int wir = g >> 5;
     const bool exchange = (N > 1) || (wpr > 1);
     bool aborted = false;
@@ -460,7 +464,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
           smem + L.ring + (uint32_t)s * stage_bytes + (uint32_t)row * tn.W * ES;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
-        const int v = i * p.G + g;
+        const int v = i * G + g;
         load_vector<IN>(srow, v, valid && v < nvec, p.x_scale, w[i]);
         if (STAT != kQkLn) {
 #pragma unroll
@@ -481,7 +485,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       // s1 = its M2 about its own mean (ln_warp_stats)
       float ss, s1 = 0.f;
       if (STAT == kQkLn) {
-        ln_warp_stats<VPT>(w, p.G, g, nvec, lnc[16 * tk + wir], &ss, &s1);
+        ln_warp_stats<VPT>(w, G, g, nvec, lnc[16 * tk + wir], &ss, &s1);
       } else {
         const uint64_t a01 = f2_add(acc[0], acc[1]), a23 = f2_add(acc[2], acc[3]);
         const uint64_t a = f2_add(a01, a23);
@@ -542,7 +546,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       const uint32_t gstride = p.gsplit ? 16u : 32u;
 #pragma unroll
       for (int i = 0; i < VPT && STAT != kQkLn; ++i) {
-        const int v = min(i * p.G + g, nvec - 1);
+        const int v = min(i * G + g, nvec - 1);
         const uint4 glo = lds128(gam_lo + v * gstride);
         const uint4 ghi = lds128(gam_hi + v * gstride);
         w[i][0] = f2_mul(w[i][0], f2(__uint_as_float(glo.x), __uint_as_float(glo.y)));
@@ -609,7 +613,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
         }
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
-          const int v = i * p.G + g;
+          const int v = i * G + g;
           if (OUT != kOutBf16) {
             if (v < nvec) {
               // scale of this vector's block, then its eight codes
@@ -705,29 +709,34 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
 
 using QkKernel = void (*)(QkParams);
 
-template <int N, int IN, int STAT, int OUT>
+template <int N, int IN, int STAT, int OUT, int GC>
 QkKernel pick_qk_vpt(int vpt) {
   switch (vpt) {
-    case 1: return qknorm_cluster_kernel<N, 1, IN, STAT, OUT>;
-    case 2: return qknorm_cluster_kernel<N, 2, IN, STAT, OUT>;
-    case 3: return qknorm_cluster_kernel<N, 3, IN, STAT, OUT>;
-    case 4: return qknorm_cluster_kernel<N, 4, IN, STAT, OUT>;
-    case 5: return qknorm_cluster_kernel<N, 5, IN, STAT, OUT>;
-    case 6: return qknorm_cluster_kernel<N, 6, IN, STAT, OUT>;
-    case 8: return qknorm_cluster_kernel<N, 8, IN, STAT, OUT>;
+    case 1: return qknorm_cluster_kernel<N, 1, IN, STAT, OUT, GC>;
+    case 2: return qknorm_cluster_kernel<N, 2, IN, STAT, OUT, GC>;
+    case 3: return qknorm_cluster_kernel<N, 3, IN, STAT, OUT, GC>;
+    case 4: return qknorm_cluster_kernel<N, 4, IN, STAT, OUT, GC>;
+    case 5: return qknorm_cluster_kernel<N, 5, IN, STAT, OUT, GC>;
+    case 6: return qknorm_cluster_kernel<N, 6, IN, STAT, OUT, GC>;
+    case 8: return qknorm_cluster_kernel<N, 8, IN, STAT, OUT, GC>;
     default: return nullptr;
   }
 }
 
+template <int N, int IN, int STAT, int OUT>
+QkKernel pick_qk_rows(int vpt, int G) {
+  return G == 32 ? pick_qk_vpt<N, IN, STAT, OUT, 32>(vpt) : pick_qk_vpt<N, IN, STAT, OUT, 0>(vpt);
+}
+
 // Instantiates every QK kernel for input type IN, statistic STAT and output
-// OUT in the calling unit.
+// OUT in the calling unit; G = consumer threads per row.
 template <int IN, int STAT, int OUT = kOutBf16>
-QkKernel pick_qk_input(int N, int vpt) {
+QkKernel pick_qk_input(int N, int vpt, int G) {
   switch (N) {
-    case 1: return pick_qk_vpt<1, IN, STAT, OUT>(vpt);
-    case 2: return pick_qk_vpt<2, IN, STAT, OUT>(vpt);
-    case 4: return pick_qk_vpt<4, IN, STAT, OUT>(vpt);
-    case 8: return pick_qk_vpt<8, IN, STAT, OUT>(vpt);
+    case 1: return pick_qk_rows<1, IN, STAT, OUT>(vpt, G);
+    case 2: return pick_qk_rows<2, IN, STAT, OUT>(vpt, G);
+    case 4: return pick_qk_rows<4, IN, STAT, OUT>(vpt, G);
+    case 8: return pick_qk_rows<8, IN, STAT, OUT>(vpt, G);
     default: return nullptr;
   }
 }
@@ -746,12 +755,12 @@ static inline int read_and_clear_local_qk_status(unsigned* out) {
 QkKernel pick_qk_direct(int N, int vpt, int in_e4m3, int layernorm);
 
 // Defined by qk_bf16.cu, qk_e4m3.cu, qk_ln.cu and qk_mx_*.cu.
-QkKernel pick_qk_bf16(int N, int vpt);
-QkKernel pick_qk_e4m3(int N, int vpt);
-QkKernel pick_qk_ln(int N, int vpt);
-QkKernel pick_qk_mx_e4m3(int N, int vpt);
-QkKernel pick_qk_mx_e2m1(int N, int vpt);
-QkKernel pick_qk_mx_nvfp4(int N, int vpt);
+QkKernel pick_qk_bf16(int N, int vpt, int G);
+QkKernel pick_qk_e4m3(int N, int vpt, int G);
+QkKernel pick_qk_ln(int N, int vpt, int G);
+QkKernel pick_qk_mx_e4m3(int N, int vpt, int G);
+QkKernel pick_qk_mx_e2m1(int N, int vpt, int G);
+QkKernel pick_qk_mx_nvfp4(int N, int vpt, int G);
 int read_and_clear_qk_bf16_status(unsigned* out);
 int read_and_clear_qk_e4m3_status(unsigned* out);
 int read_and_clear_qk_ln_status(unsigned* out);

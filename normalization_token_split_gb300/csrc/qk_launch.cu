@@ -67,13 +67,13 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
 
   QkKernel kern;
   if (mx_out)
-    kern = opt.out_fmt == NTS_FMT_E4M3   ? pick_qk_mx_e4m3(N, rs.vpt)
-           : opt.out_fmt == NTS_FMT_E2M1 ? pick_qk_mx_e2m1(N, rs.vpt)
-                                         : pick_qk_mx_nvfp4(N, rs.vpt);
+    kern = opt.out_fmt == NTS_FMT_E4M3   ? pick_qk_mx_e4m3(N, rs.vpt, rs.G)
+           : opt.out_fmt == NTS_FMT_E2M1 ? pick_qk_mx_e2m1(N, rs.vpt, rs.G)
+                                         : pick_qk_mx_nvfp4(N, rs.vpt, rs.G);
   else
-    kern = layernorm    ? pick_qk_ln(N, rs.vpt)
-           : opt.in_e4m3 ? pick_qk_e4m3(N, rs.vpt)
-                         : pick_qk_bf16(N, rs.vpt);
+    kern = layernorm    ? pick_qk_ln(N, rs.vpt, rs.G)
+           : opt.in_e4m3 ? pick_qk_e4m3(N, rs.vpt, rs.G)
+                         : pick_qk_bf16(N, rs.vpt, rs.G);
   if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for N=%d vpt=%d", N, rs.vpt);
 
   QkParams prm = {};
