@@ -255,9 +255,10 @@ __device__ __forceinline__ void ln_combine(const float* parts, int N, int wpr, C
 // the block-cast output with 8 vectors per thread keeps 128 so as not to
 // spill.
 // GC: the consumer threads per row when known at compile time (32, the
-// common shape: slot offsets then fold into the instructions' immediates,
-// measured 4-7 % faster for the variants not bound by DRAM), or 0: p.G.
-template <int N, int VPT, int IN, int STAT, int OUT, int GC>
+// common shape: slot offsets then fold into the instructions' immediates),
+// or 0: p.G.  BV: the E8M0 block-cast output's vectors per block when known
+// at compile time (2, 4 or 8), or 0: p.bv.
+template <int N, int VPT, int IN, int STAT, int OUT, int GC, int BV>
 __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8) ? 128 : 96))
     qknorm_cluster_kernel(const QkParams p) {
   constexpr int ES = (IN == kInBf16) ? 2 : 1;  // bytes per activation
@@ -273,8 +274,8 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
   const int wpr = G >> 5;
   // block-cast output: vectors per block and log2 of the block size (NVFP4
   // blocks are 16 values: fixed at compile time)
-  const int kBv = OUT == kOutNvfp4 ? 2 : p.bv;
-  const int kBshift = OUT == kOutNvfp4 ? 4 : p.bshift;
+  const int kBv = OUT == kOutNvfp4 ? 2 : (BV > 0 ? BV : p.bv);
+  const int kBshift = OUT == kOutNvfp4 ? 4 : (BV == 2 ? 4 : BV == 4 ? 5 : BV == 8 ? 6 : p.bshift);
   const QkLayout L = qk_layout(N, p.S, p.R, p.Wmax, p.psum, G, p.gsplit, ES, NS,
                                OUT == kOutNvfp4);
   const uint32_t sbase = smem_addr(smem);
@@ -611,6 +612,9 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
           srow_sc = tn.scales + (first >> kBshift);
           vshift = kBshift - 3;
         }
+        // E8M0 output: the bounds of the scale bytes whose blocks take one
+        // product per element (a block of zeros takes m = 0)
+        const OneProductRange opr = one_product_range(rinv, OUT == kOutE4M3 ? -116 : -124);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
           const int v = i * G + g;
@@ -624,10 +628,10 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
                 sbyte = nvfp4_scale(am[i] * rinv, rcp, &is);
                 keep = sbyte != 0 ? ~0u : 0u;
               } else {
-                const int e = e8m0_exponent(am[i] * rinv, OUT == kOutE4M3 ? 8 : 2);
-                is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
-                sbyte = (uint32_t)(e + 127);
-                one = e8m0_single_multiplier(rinv, is, e, OUT == kOutE4M3 ? -116 : -124, &m);
+                sbyte = (uint32_t)(e8m0_exponent(am[i] * rinv, OUT == kOutE4M3 ? 8 : 2) + 127);
+                is = __uint_as_float((254u - sbyte) << 23);  // 2^-e, e = sbyte - 127
+                one = am[i] == 0.f || (sbyte - opr.lo) <= opr.span;
+                m = am[i] == 0.f ? 0.f : __uint_as_float(opr.cm - (sbyte << 23));
               }
               if ((g & (kBv - 1)) == 0) srow_sc[v >> vshift] = (uint8_t)sbyte;
               uint64_t q[4];
@@ -709,34 +713,50 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
 
 using QkKernel = void (*)(QkParams);
 
-template <int N, int IN, int STAT, int OUT, int GC>
+template <int N, int IN, int STAT, int OUT, int GC, int BV>
 QkKernel pick_qk_vpt(int vpt) {
   switch (vpt) {
-    case 1: return qknorm_cluster_kernel<N, 1, IN, STAT, OUT, GC>;
-    case 2: return qknorm_cluster_kernel<N, 2, IN, STAT, OUT, GC>;
-    case 3: return qknorm_cluster_kernel<N, 3, IN, STAT, OUT, GC>;
-    case 4: return qknorm_cluster_kernel<N, 4, IN, STAT, OUT, GC>;
-    case 5: return qknorm_cluster_kernel<N, 5, IN, STAT, OUT, GC>;
-    case 6: return qknorm_cluster_kernel<N, 6, IN, STAT, OUT, GC>;
-    case 8: return qknorm_cluster_kernel<N, 8, IN, STAT, OUT, GC>;
+    case 1: return qknorm_cluster_kernel<N, 1, IN, STAT, OUT, GC, BV>;
+    case 2: return qknorm_cluster_kernel<N, 2, IN, STAT, OUT, GC, BV>;
+    case 3: return qknorm_cluster_kernel<N, 3, IN, STAT, OUT, GC, BV>;
+    case 4: return qknorm_cluster_kernel<N, 4, IN, STAT, OUT, GC, BV>;
+    case 5: return qknorm_cluster_kernel<N, 5, IN, STAT, OUT, GC, BV>;
+    case 6: return qknorm_cluster_kernel<N, 6, IN, STAT, OUT, GC, BV>;
+    case 8: return qknorm_cluster_kernel<N, 8, IN, STAT, OUT, GC, BV>;
     default: return nullptr;
   }
 }
 
+// One-warp shard rows (G = 32) take the kernels with G, and for the E8M0
+// block-cast outputs the block size, fixed at compile time; other shapes
+// read both from the parameters.
 template <int N, int IN, int STAT, int OUT>
-QkKernel pick_qk_rows(int vpt, int G) {
-  return G == 32 ? pick_qk_vpt<N, IN, STAT, OUT, 32>(vpt) : pick_qk_vpt<N, IN, STAT, OUT, 0>(vpt);
+QkKernel pick_qk_rows(int vpt, int G, int bv) {
+  if (G == 32) {
+    if constexpr (OUT == kOutE4M3 || OUT == kOutE2M1) {
+      switch (bv) {
+        case 2: return pick_qk_vpt<N, IN, STAT, OUT, 32, 2>(vpt);
+        case 4: return pick_qk_vpt<N, IN, STAT, OUT, 32, 4>(vpt);
+        case 8: return pick_qk_vpt<N, IN, STAT, OUT, 32, 8>(vpt);
+        default: return nullptr;
+      }
+    } else {
+      return pick_qk_vpt<N, IN, STAT, OUT, 32, 0>(vpt);
+    }
+  }
+  return pick_qk_vpt<N, IN, STAT, OUT, 0, 0>(vpt);
 }
 
 // Instantiates every QK kernel for input type IN, statistic STAT and output
-// OUT in the calling unit; G = consumer threads per row.
+// OUT in the calling unit; G = consumer threads per row, bv = 16-byte
+// vectors per block of the block-cast output.
 template <int IN, int STAT, int OUT = kOutBf16>
-QkKernel pick_qk_input(int N, int vpt, int G) {
+QkKernel pick_qk_input(int N, int vpt, int G, int bv) {
   switch (N) {
-    case 1: return pick_qk_rows<1, IN, STAT, OUT>(vpt, G);
-    case 2: return pick_qk_rows<2, IN, STAT, OUT>(vpt, G);
-    case 4: return pick_qk_rows<4, IN, STAT, OUT>(vpt, G);
-    case 8: return pick_qk_rows<8, IN, STAT, OUT>(vpt, G);
+    case 1: return pick_qk_rows<1, IN, STAT, OUT>(vpt, G, bv);
+    case 2: return pick_qk_rows<2, IN, STAT, OUT>(vpt, G, bv);
+    case 4: return pick_qk_rows<4, IN, STAT, OUT>(vpt, G, bv);
+    case 8: return pick_qk_rows<8, IN, STAT, OUT>(vpt, G, bv);
     default: return nullptr;
   }
 }
@@ -755,12 +775,12 @@ static inline int read_and_clear_local_qk_status(unsigned* out) {
 QkKernel pick_qk_direct(int N, int vpt, int in_e4m3, int layernorm);
 
 // Defined by qk_bf16.cu, qk_e4m3.cu, qk_ln.cu and qk_mx_*.cu.
-QkKernel pick_qk_bf16(int N, int vpt, int G);
-QkKernel pick_qk_e4m3(int N, int vpt, int G);
-QkKernel pick_qk_ln(int N, int vpt, int G);
-QkKernel pick_qk_mx_e4m3(int N, int vpt, int G);
-QkKernel pick_qk_mx_e2m1(int N, int vpt, int G);
-QkKernel pick_qk_mx_nvfp4(int N, int vpt, int G);
+QkKernel pick_qk_bf16(int N, int vpt, int G, int bv);
+QkKernel pick_qk_e4m3(int N, int vpt, int G, int bv);
+QkKernel pick_qk_ln(int N, int vpt, int G, int bv);
+QkKernel pick_qk_mx_e4m3(int N, int vpt, int G, int bv);
+QkKernel pick_qk_mx_e2m1(int N, int vpt, int G, int bv);
+QkKernel pick_qk_mx_nvfp4(int N, int vpt, int G, int bv);
 int read_and_clear_qk_bf16_status(unsigned* out);
 int read_and_clear_qk_e4m3_status(unsigned* out);
 int read_and_clear_qk_ln_status(unsigned* out);

@@ -65,15 +65,16 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
   if (smem > (size_t)dev.max_smem_optin)
     return fail(NTS_ERR_UNSUPPORTED, "shard row too wide for shared memory: H/N = %d", Wmax);
 
+  const int bv = mx_out ? opt.B / 8 : 1;   // block-cast output: vectors per block
   QkKernel kern;
   if (mx_out)
-    kern = opt.out_fmt == NTS_FMT_E4M3   ? pick_qk_mx_e4m3(N, rs.vpt, rs.G)
-           : opt.out_fmt == NTS_FMT_E2M1 ? pick_qk_mx_e2m1(N, rs.vpt, rs.G)
-                                         : pick_qk_mx_nvfp4(N, rs.vpt, rs.G);
+    kern = opt.out_fmt == NTS_FMT_E4M3   ? pick_qk_mx_e4m3(N, rs.vpt, rs.G, bv)
+           : opt.out_fmt == NTS_FMT_E2M1 ? pick_qk_mx_e2m1(N, rs.vpt, rs.G, bv)
+                                         : pick_qk_mx_nvfp4(N, rs.vpt, rs.G, bv);
   else
-    kern = layernorm    ? pick_qk_ln(N, rs.vpt, rs.G)
-           : opt.in_e4m3 ? pick_qk_e4m3(N, rs.vpt, rs.G)
-                         : pick_qk_bf16(N, rs.vpt, rs.G);
+    kern = layernorm    ? pick_qk_ln(N, rs.vpt, rs.G, bv)
+           : opt.in_e4m3 ? pick_qk_e4m3(N, rs.vpt, rs.G, bv)
+                         : pick_qk_bf16(N, rs.vpt, rs.G, bv);
   if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for N=%d vpt=%d", N, rs.vpt);
 
   QkParams prm = {};
