@@ -49,18 +49,30 @@ FMT_E2M1 = 1
 FMT_NVFP4 = 2
 
 
+# The mutation tests load a copy of the oracle with a planted mistake from
+# the path in this variable (never set outside those tests).
+_LIB_OVERRIDE = os.environ.get("NTS_ORACLE_LIB")
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc src -> shared library `out`, with the flags of the oracle build."""
+    tmp = out + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-fvisibility=hidden", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c with gcc into oracle/_build/liboracle.so."""
+    if _LIB_OVERRIDE:
+        return _LIB_OVERRIDE
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
-    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
-           "-fno-fast-math", "-fvisibility=hidden", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
 
 
 def _load():
