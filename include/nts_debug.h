@@ -73,15 +73,18 @@ NTS_API int nts_debug_inject_failure(int status, int count);
  * The launch shape an MX request (T rows of D values, block size B, format
  * fmt, statistic p: 0 = RMSNorm, 1 or 2 = MXNorm) would get on a device
  * with `sm_count` SMs and `max_smem_optin` bytes of opt-in shared memory per
- * CTA, under the current tuning, computed on the host without touching any
- * device: shape[0] units per thread (blocks, or halves of 64-value blocks),
+ * CTA, for a kernel of `regs` registers per thread (0: not limited by
+ * registers; a launch uses the chosen kernel's own count), under the
+ * current tuning, computed on the host without touching any device:
+ * shape[0] units per thread (blocks, or halves of 64-value blocks),
  * shape[1] threads per row, shape[2] rows per tile, shape[3] ring stages,
  * shape[4] dynamic shared memory bytes.  Lets the launch rules be checked
  * exhaustively without a GPU.
- * Errors: INVALID_ARG for a bad query; UNSUPPORTED when no kernel serves it.
+ * Errors: INVALID_ARG for a bad query (regs outside 0..255 included);
+ * UNSUPPORTED when no kernel serves it.
  */
 NTS_API int nts_debug_mx_launch_shape(int64_t T, int64_t D, int B, int fmt, int p, int sm_count,
-                                      int max_smem_optin, int32_t *shape);
+                                      int max_smem_optin, int regs, int32_t *shape);
 
 /*
  * Programmatic dependent launch: 1 (default) = every kernel is launched with

@@ -55,7 +55,7 @@ def _declare(lib):
         "nts_debug_set_schedule": ([i32], i32),
         "nts_debug_set_direct": ([i32], i32),
         "nts_debug_set_pdl": ([i32], i32),
-        "nts_debug_mx_launch_shape": ([i64, i64, i32, i32, i32, i32, i32,
+        "nts_debug_mx_launch_shape": ([i64, i64, i32, i32, i32, i32, i32, i32,
                                        ctypes.POINTER(ctypes.c_int32)], i32),
         "nts_debug_inject_failure": ([i32, i32], i32),
         "nts_debug_check_e8m0": ([ctypes.POINTER(ctypes.c_uint64)], i32),

@@ -70,8 +70,24 @@ struct MxLaunchShape {
   MxKernel kern = nullptr;
 };
 
+// CTAs of `threads` threads with `smem` bytes of dynamic shared memory and
+// `regs` registers per thread that fit on one SM (0 registers: not limited
+// by them): the shared memory of an SM is the opt-in maximum per CTA plus
+// the 1 KB each CTA reserves, registers are allocated per warp in units of
+// 8 per thread from 64 K, and an SM holds at most 2048 threads.
+int mx_ctas_per_sm(int threads, size_t smem, int regs, int max_smem_optin) {
+  const size_t kReserved = 1024;
+  const size_t smem_sm = (size_t)max_smem_optin + kReserved;
+  const int warps = (threads + 31) / 32;
+  int n = (int)(smem_sm / (smem + kReserved));
+  if (regs > 0) n = std::min(n, 65536 / (((regs + 7) / 8 * 8) * 32 * warps));
+  n = std::min(n, 2048 / (warps * 32));
+  return std::min(n, 32);
+}
+
 int mx_launch_shape(int64_t T, int D, int B, int fmt, int p, bool gamma, int sm_count,
-                    int max_smem_optin, const LaunchTuning& tune, MxLaunchShape* out) {
+                    int max_smem_optin, int regs, const LaunchTuning& tune,
+                    MxLaunchShape* out) {
   const int K = D / B;
   // tune.force_vpt selects the units per thread for this kernel family; a
   // unit is a block, or half a block of 64 values (the kernel splits those
@@ -93,14 +109,23 @@ int mx_launch_shape(int64_t T, int D, int B, int fmt, int p, bool gamma, int sm_
   if ((R * sh.G) % 32 != 0)
     return fail(NTS_ERR_UNSUPPORTED, "%d rows of %d threads are not whole warps", R, sh.G);
 
-  // Ring depth: up to four small stages, three while three CTAs still fit
-  // on an SM (a ring of at most 72 KB), else two (measured on GB300: more
-  // CTAs per SM beat a deeper ring; D = 7168 with R = 2 runs 1.24x faster
-  // with two stages and three CTAs per SM than with three and two).
-  const int stage = R * D * 2;
-  int S = stage > 24576 ? 2 : (stage >= 12288 ? 3 : 4);
+  // Ring depth: the deepest ring of at most four stages that keeps as many
+  // CTAs per SM as two stages allow (registers `regs` per thread, when
+  // known).  Measured on GB300 over the MXNorm grid: resident CTAs first,
+  // ring depth second -- D = 5120, 16-value E2M1 blocks, two rows of
+  // 10 KB per tile: two stages (four CTAs per SM) 126.0 us, three (three
+  // CTAs) 140.6 us; D = 1024 with 16 KB stages: three stages 31.1 us, two
+  // 32.1 us at the same four CTAs.
   const bool nvfp4 = fmt == NTS_FMT_NVFP4;
-  while (S > 2 && mx_layout(S, R, D, sh.G, nvfp4).total > (uint32_t)tune.smem_budget) --S;
+  const int nthreads = R * sh.G + 32;
+  auto ctas = [&](int s) {
+    return mx_ctas_per_sm(nthreads, mx_layout(s, R, D, sh.G, nvfp4).total, regs, max_smem_optin);
+  };
+  const int most = ctas(2);
+  int S = 4;
+  while (S > 2 && (ctas(S) < most ||
+                   mx_layout(S, R, D, sh.G, nvfp4).total > (uint32_t)tune.smem_budget))
+    --S;
   while (S > 1 && mx_layout(S, R, D, sh.G, nvfp4).total > (uint32_t)max_smem_optin) --S;
   if (tune.force_stages > 0) S = tune.force_stages;
   const size_t smem = mx_layout(S, R, D, sh.G, nvfp4).total;
@@ -125,9 +150,17 @@ int launch_mx(const MxRequest& rq, cudaStream_t stream, const LaunchTuning& tune
   const int K = D / rq.B;
   const DeviceInfo& dev = device_info();
   if (!dev.ok) return fail(NTS_ERR_CUDA, "could not query the current device");
+  // the kernel does not depend on the ring depth or the rows per tile: its
+  // register count enters the choice of both
   MxLaunchShape ls;
   int rc = mx_launch_shape(rq.T, D, rq.B, rq.fmt, rq.p, rq.gamma != nullptr, dev.sm_count,
-                           dev.max_smem_optin, tune, &ls);
+                           dev.max_smem_optin, 0, tune, &ls);
+  if (rc != NTS_OK) return rc;
+  int regs = 0;
+  rc = kernel_registers((const void*)ls.kern, &regs);
+  if (rc != NTS_OK) return rc;
+  rc = mx_launch_shape(rq.T, D, rq.B, rq.fmt, rq.p, rq.gamma != nullptr, dev.sm_count,
+                       dev.max_smem_optin, regs, tune, &ls);
   if (rc != NTS_OK) return rc;
   const MxShape sh{ls.bpt, ls.G};
   const int R = ls.R, S = ls.S;
@@ -209,15 +242,17 @@ int read_and_clear_mx_status(unsigned* out) {
 }  // namespace nts
 
 extern "C" int nts_debug_mx_launch_shape(int64_t T, int64_t D, int B, int fmt, int p,
-                                         int sm_count, int max_smem_optin, int32_t* shape) {
+                                         int sm_count, int max_smem_optin, int regs,
+                                         int32_t* shape) {
   using namespace nts;
   if (shape == nullptr || T < 0 || D <= 0 || D > (1 << 30) || sm_count <= 0 ||
-      max_smem_optin <= 0 || (B != 16 && B != 32 && B != 64) || D % B != 0 || p < 0 || p > 2 ||
+      max_smem_optin <= 0 || regs < 0 || regs > 255 || (B != 16 && B != 32 && B != 64) ||
+      D % B != 0 || p < 0 || p > 2 ||
       (fmt != NTS_FMT_E4M3 && fmt != NTS_FMT_E2M1 && fmt != NTS_FMT_NVFP4) ||
       (fmt == NTS_FMT_NVFP4 && B != 16))
     return fail(NTS_ERR_INVALID_ARG, "bad shape query");
   MxLaunchShape ls;
-  const int rc = mx_launch_shape(T, (int)D, B, fmt, p, false, sm_count, max_smem_optin,
+  const int rc = mx_launch_shape(T, (int)D, B, fmt, p, false, sm_count, max_smem_optin, regs,
                                  current_tuning(), &ls);
   if (rc != NTS_OK) return rc;
   shape[0] = ls.bpt;

@@ -131,6 +131,23 @@ int prepare_kernel(const void* kernel, size_t smem) {
   return NTS_OK;
 }
 
+int kernel_registers(const void* kernel, int* regs) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int>, int> cache;
+  const int dev = device_info().device;
+  std::lock_guard<std::mutex> lk(mu);
+  auto key = std::make_tuple(kernel, dev);
+  auto it = cache.find(key);
+  if (it == cache.end()) {
+    cudaFuncAttributes a;
+    const cudaError_t e = cudaFuncGetAttributes(&a, kernel);
+    if (e != cudaSuccess) return fail_cuda(e, "reading a kernel's attributes");
+    it = cache.emplace(key, a.numRegs).first;
+  }
+  *regs = it->second;
+  return NTS_OK;
+}
+
 int max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cfg, int cluster,
                         int64_t* out) {
   static std::mutex mu;

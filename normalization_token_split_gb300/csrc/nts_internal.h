@@ -72,6 +72,8 @@ RowShape choose_row_shape(int nvec, int force_vpt);
 
 // Raise the kernel's dynamic shared memory limit (once per kernel/device).
 int prepare_kernel(const void* kernel, size_t smem);
+// Registers per thread of a kernel (cached per device).
+int kernel_registers(const void* kernel, int* regs);
 // Co-resident clusters of `cluster` CTAs for this launch configuration.
 int max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cfg, int cluster,
                         int64_t* out);

@@ -26,10 +26,21 @@ SM, SMEM = 152, 232448          # GB300: SMs and opt-in shared memory per CTA
 INVALID, UNSUPPORTED, OK = 1, 2, 0
 
 
-def shape(T, D, B, fmt, p=2, sm=SM, smem=SMEM):
+def shape(T, D, B, fmt, p=2, sm=SM, smem=SMEM, regs=96):
     out = (ctypes.c_int32 * 5)()
-    rc = _lib.lib().nts_debug_mx_launch_shape(T, D, B, fmt, p, sm, smem, out)
+    rc = _lib.lib().nts_debug_mx_launch_shape(T, D, B, fmt, p, sm, smem, regs, out)
     return rc, list(out)
+
+
+def ctas_per_sm(threads, smem_cta, regs, smem_optin=SMEM):
+    """CTAs per SM on GB300: 228 KB of shared memory with 1 KB reserved per
+    CTA, 64 K registers allocated per warp in units of 8 per thread, 2048
+    threads."""
+    warps = -(-threads // 32)
+    n = (smem_optin + 1024) // (smem_cta + 1024)
+    if regs:
+        n = min(n, 65536 // (-(-regs // 8) * 8 * 32 * warps))
+    return min(n, 2048 // (warps * 32), 32)
 
 
 def widths():
@@ -86,13 +97,43 @@ def test_measured_shapes():
     assert shape(65536, 3072, 32, E4M3)[1][:2] == [3, 32]
     # two stages for rows above 24 KB a stage (three CTAs per SM)
     assert shape(65536, 7168, 32, E4M3)[1][3] == 2
+    # the ring depth keeps the most CTAs per SM: two stages of two 10 KB rows
+    # at D = 5120 (four CTAs of 96 registers per thread, where three stages
+    # leave three), three stages of 16 KB at D = 1024 (four CTAs either way)
+    assert shape(65536, 5120, 16, E2M1)[1][2:4] == [2, 2]
+    assert shape(65536, 3072, 32, E4M3)[1][3] == 2
+    assert shape(65536, 1024, 16, E2M1)[1][2:4] == [8, 3]
+    # with 104 registers only three CTAs fit anyway: the deeper ring
+    assert shape(65536, 3072, 32, E4M3, regs=104)[1][3] == 3
+
+
+@pytest.mark.parametrize("regs", [0, 64, 96, 104, 128])
+def test_ring_depth_keeps_the_most_ctas_per_sm(regs):
+    # over the grid of widths: the chosen ring holds as many CTAs per SM as
+    # two stages would, and no deeper ring of at most four stages does
+    for D, B in itertools.product(widths(), [16, 32, 64]):
+        if D % B:
+            continue
+        rc, (bpt, G, R, S, smem) = shape(65536, D, B, E4M3, regs=regs)
+        if rc != OK or S < 2:
+            continue
+        threads = R * G + 32
+        stage = R * D * 2
+        fixed = smem - S * stage                     # barriers and slots
+        best = ctas_per_sm(threads, fixed + 2 * stage, regs)
+        assert ctas_per_sm(threads, smem, regs) == best, (D, B, regs, R, S)
+        for deeper in range(S + 1, 5):
+            size = fixed + deeper * stage
+            assert size > 102400 or ctas_per_sm(threads, size, regs) < best, (D, B, regs, S)
 
 
 def test_query_arguments():
     out = (ctypes.c_int32 * 5)()
     lib = _lib.lib()
-    assert lib.nts_debug_mx_launch_shape(10, 100, 32, E4M3, 2, SM, SMEM, out) == INVALID  # D % B
-    assert lib.nts_debug_mx_launch_shape(10, 256, 32, NVFP4, 2, SM, SMEM, out) == INVALID
-    assert lib.nts_debug_mx_launch_shape(10, 256, 32, E4M3, 3, SM, SMEM, out) == INVALID
-    assert lib.nts_debug_mx_launch_shape(10, 256, 32, E4M3, 2, SM, SMEM, None) == INVALID
-    assert lib.nts_debug_mx_launch_shape(10, 256, 32, E4M3, 2, SM, SMEM, out) == OK
+    assert lib.nts_debug_mx_launch_shape(10, 100, 32, E4M3, 2, SM, SMEM, 96, out) == INVALID  # D % B
+    assert lib.nts_debug_mx_launch_shape(10, 256, 32, NVFP4, 2, SM, SMEM, 96, out) == INVALID
+    assert lib.nts_debug_mx_launch_shape(10, 256, 32, E4M3, 3, SM, SMEM, 96, out) == INVALID
+    assert lib.nts_debug_mx_launch_shape(10, 256, 32, E4M3, 2, SM, SMEM, 96, None) == INVALID
+    assert lib.nts_debug_mx_launch_shape(10, 256, 32, E4M3, 2, SM, SMEM, -1, out) == INVALID
+    assert lib.nts_debug_mx_launch_shape(10, 256, 32, E4M3, 2, SM, SMEM, 256, out) == INVALID
+    assert lib.nts_debug_mx_launch_shape(10, 256, 32, E4M3, 2, SM, SMEM, 96, out) == OK
