@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qk_direct_kernel(const QkParam
   // LayerNorm counts: computed here as the persistent kernel tabulates them
   auto cnt = [&](int wi) { return ln_count_pair(ln_warp_count<VPT>(nvec, p.G, wi)); };
   if (STAT == kQkLn) {
-    ln_warp_stats<VPT>(w, p.G, g, nvec, cnt(wir), &ss, &s1);
+    ln_warp_stats<VPT, false>(w, p.G, g, nvec, cnt(wir), &ss, &s1);
   } else {
     const uint64_t a = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
     ss = warp_sum(f2_lo(a) + f2_hi(a));

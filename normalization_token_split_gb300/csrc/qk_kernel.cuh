@@ -197,8 +197,9 @@ __device__ __forceinline__ float2 ln_count_pair(int n) {
 }
 
 // s1 and M2 of this warp's values w (vectors beyond nvec hold zeros and are
-// left out of M2); `c` = ln_count_pair of the warp's count; whole warp.
-template <int VPT>
+// left out of M2; FULL: there are none); `c` = ln_count_pair of the warp's
+// count; whole warp.
+template <int VPT, bool FULL>
 __device__ __forceinline__ void ln_warp_stats(const uint64_t (&w)[VPT][4], int G, int g, int nvec,
                                               float2 c, float* s1_out, float* m2_out) {
   uint64_t c0 = 0, c1 = 0;
@@ -214,7 +215,7 @@ __device__ __forceinline__ void ln_warp_stats(const uint64_t (&w)[VPT][4], int G
   uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    if (i * G + g < nvec) {
+    if (FULL || i * G + g < nvec) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint64_t d = f2_add(w[i][q], nm);
@@ -256,13 +257,16 @@ __device__ __forceinline__ void ln_combine(const float* parts, int N, int wpr, C
 // spill.
 // GC: the consumer threads per row when known at compile time (32, the
 // common shape: slot offsets then fold into the instructions' immediates),
-// or 0: p.G.  BV: the E8M0 block-cast output's vectors per block when known
-// at compile time (2, 4 or 8), or 0: p.bv.
+// or 0: p.G.  GC > 0 also promises that every shard row of every tensor
+// fills all VPT x GC vector slots, so the slots need no range checks.  BV:
+// the E8M0 block-cast output's vectors per block when known at compile time
+// (2, 4 or 8), or 0: p.bv.
 template <int N, int VPT, int IN, int STAT, int OUT, int GC, int BV>
 __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8) ? 128 : 96))
     qknorm_cluster_kernel(const QkParams p) {
   constexpr int ES = (IN == kInBf16) ? 2 : 1;  // bytes per activation
   const int G = GC > 0 ? GC : p.G;
+  constexpr bool kFull = GC > 0;   // nvec == VPT * G for every tensor
   constexpr int NS = (STAT == kQkLn) ? 2 : 1;  // scalars exchanged per warp
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t rank = (N > 1) ? cluster_ctarank() : 0u;
@@ -466,7 +470,9 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = i * G + g;
-        load_vector<IN>(srow, v, valid && v < nvec, p.x_scale, w[i]);
+        // a row beyond T (last tile) reads stale shared memory when full: its
+        // partial sums only reach its own, unstored, combine
+        load_vector<IN>(srow, v, kFull || (valid && v < nvec), p.x_scale, w[i]);
         if (STAT != kQkLn) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) acc[q] = f2_fma(w[i][q], w[i][q], acc[q]);
@@ -486,7 +492,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       // s1 = its M2 about its own mean (ln_warp_stats)
       float ss, s1 = 0.f;
       if (STAT == kQkLn) {
-        ln_warp_stats<VPT>(w, G, g, nvec, lnc[16 * tk + wir], &ss, &s1);
+        ln_warp_stats<VPT, kFull>(w, G, g, nvec, lnc[16 * tk + wir], &ss, &s1);
       } else {
         const uint64_t a01 = f2_add(acc[0], acc[1]), a23 = f2_add(acc[2], acc[3]);
         const uint64_t a = f2_add(a01, a23);
@@ -547,7 +553,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       const uint32_t gstride = p.gsplit ? 16u : 32u;
 #pragma unroll
       for (int i = 0; i < VPT && STAT != kQkLn; ++i) {
-        const int v = min(i * G + g, nvec - 1);
+        const int v = kFull ? i * G + g : min(i * G + g, nvec - 1);
         const uint4 glo = lds128(gam_lo + v * gstride);
         const uint4 ghi = lds128(gam_hi + v * gstride);
         w[i][0] = f2_mul(w[i][0], f2(__uint_as_float(glo.x), __uint_as_float(glo.y)));
@@ -619,7 +625,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
         for (int i = 0; i < VPT; ++i) {
           const int v = i * G + g;
           if (OUT != kOutBf16) {
-            if (v < nvec) {
+            if (kFull || v < nvec) {
               // scale of this vector's block, then its eight codes
               float is, m = 0.f;
               uint32_t keep = ~0u, sbyte;
@@ -656,7 +662,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
             }
             continue;
           }
-          if (v < nvec) {
+          if (kFull || v < nvec) {
             uint4 o;
             uint64_t y0, y1, y2, y3;
             if (STAT == kQkLn) {
@@ -727,9 +733,10 @@ QkKernel pick_qk_vpt(int vpt) {
   }
 }
 
-// One-warp shard rows (G = 32) take the kernels with G, and for the E8M0
-// block-cast outputs the block size, fixed at compile time; other shapes
-// read both from the parameters.
+// One-warp shard rows that fill their slots (G = 32: the launcher passes 32
+// only then) take the kernels with G, and for the E8M0 block-cast outputs
+// the block size, fixed at compile time; other shapes read both from the
+// parameters.
 template <int N, int IN, int STAT, int OUT>
 QkKernel pick_qk_rows(int vpt, int G, int bv) {
   if (G == 32) {

@@ -66,15 +66,20 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
     return fail(NTS_ERR_UNSUPPORTED, "shard row too wide for shared memory: H/N = %d", Wmax);
 
   const int bv = mx_out ? opt.B / 8 : 1;   // block-cast output: vectors per block
+  // the kernels with G fixed at compile time serve one-warp shard rows that
+  // fill all their vector slots, in every tensor of the launch
+  bool full = rs.G == 32;
+  for (int k = 0; k < ntensors; ++k) full = full && rq[k].H / N / 8 == (int64_t)rs.vpt * rs.G;
+  const int gsel = full ? 32 : 0;
   QkKernel kern;
   if (mx_out)
-    kern = opt.out_fmt == NTS_FMT_E4M3   ? pick_qk_mx_e4m3(N, rs.vpt, rs.G, bv)
-           : opt.out_fmt == NTS_FMT_E2M1 ? pick_qk_mx_e2m1(N, rs.vpt, rs.G, bv)
-                                         : pick_qk_mx_nvfp4(N, rs.vpt, rs.G, bv);
+    kern = opt.out_fmt == NTS_FMT_E4M3   ? pick_qk_mx_e4m3(N, rs.vpt, gsel, bv)
+           : opt.out_fmt == NTS_FMT_E2M1 ? pick_qk_mx_e2m1(N, rs.vpt, gsel, bv)
+                                         : pick_qk_mx_nvfp4(N, rs.vpt, gsel, bv);
   else
-    kern = layernorm    ? pick_qk_ln(N, rs.vpt, rs.G, bv)
-           : opt.in_e4m3 ? pick_qk_e4m3(N, rs.vpt, rs.G, bv)
-                         : pick_qk_bf16(N, rs.vpt, rs.G, bv);
+    kern = layernorm    ? pick_qk_ln(N, rs.vpt, gsel, bv)
+           : opt.in_e4m3 ? pick_qk_e4m3(N, rs.vpt, gsel, bv)
+                         : pick_qk_bf16(N, rs.vpt, gsel, bv);
   if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for N=%d vpt=%d", N, rs.vpt);
 
   QkParams prm = {};
