@@ -129,33 +129,22 @@ __device__ __forceinline__ void weigh_vector(const uint4& v, const float* gp, ui
   w[3] = f2_mul(bf16x2_to_f2c(v.w), f2c(g1.z, g1.w));
 }
 
-// How cast_unit forms and stores a unit's codes.
-enum {
-  kCastOne = 0,     // q = w * a, unrolled, codes stored in element order at once
-  kCastTwo = 1,     // q = (w * a) * c, unrolled, stored at once (NVFP4)
-  kCastRolled = 2,  // q = (w * a) * c, rolled up, one store per vector (extreme rows)
-};
-
 // Element codes of one unit (UV 16-byte vectors of a row staged in shared
-// memory at `base`, read in the order k ^ sig, k = 0..UV-1): q = w * a
-// (kCastOne) or (w * a) * c, w = x or fp32(x * gamma) (GAMMA), then the
-// packed conversions (`keep` masks NVFP4 blocks with a zero scale).  The
-// unrolled modes put the codes back in element order in registers (a
-// butterfly of selects on the bits of sig) and store the whole unit at once
-// (32 bytes when `wide`: the codes row is 32-byte aligned), so that every
-// store instruction writes whole 32-byte sectors; kCastRolled, which only
-// extreme rows take, stores each vector's codes on their own and adds no
-// registers to the unrolled loops.
-template <int FMT, int UV, int MODE, bool GAMMA>
+// memory at `base`, read in the order k ^ sig, k = 0..UV-1): q = (w * a) * c
+// with w = x or fp32(x * gamma) (GAMMA), then the packed conversions (`keep`
+// masks NVFP4 blocks with a zero scale).  The codes are put back in element
+// order in registers (a butterfly of selects on the bits of sig) and the
+// whole unit leaves in one store (32 bytes when `wide`: the codes row is
+// 32-byte aligned), so that every store instruction writes whole 32-byte
+// sectors.
+template <int FMT, int UV, bool GAMMA>
 __device__ __forceinline__ void cast_unit(const unsigned char* base, int sig, const float* gamma,
                                           int b, uint64_t a, uint64_t c, uint8_t* crow,
                                           uint32_t keep, bool wide) {
   constexpr int kU = UV * 8;
   constexpr int kW = FMT == NTS_FMT_E4M3 ? 2 : 1;   // code words per vector
-  constexpr bool kOne = MODE == kCastOne;
-  constexpr bool kAtOnce = MODE != kCastRolled;
   uint32_t cw[UV][kW];
-#pragma unroll(kAtOnce ? UV : 1)
+#pragma unroll
   for (int k = 0; k < UV; ++k) {
     const int u = k ^ sig;
     const uint4 v = lds128(base + u * 16);
@@ -170,58 +159,47 @@ __device__ __forceinline__ void cast_unit(const unsigned char* base, int sig, co
     }
     uint64_t q[4];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) q[h] = kOne ? f2_mul(w[h], a) : f2_mul(f2_mul(w[h], a), c);
-    uint32_t lo, hi = 0;
+    for (int h = 0; h < 4; ++h) q[h] = f2_mul(f2_mul(w[h], a), c);
     if (FMT == NTS_FMT_E4M3) {
-      lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
-      hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
+      cw[k][0] = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
+      cw[k][kW - 1] = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
     } else {
-      lo = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]), f2_lo(q[2]),
-                      f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3])) & keep;
-    }
-    if (kAtOnce) {
-      cw[k][0] = lo;
-      if (kW == 2) cw[k][kW - 1] = hi;
-    } else if (FMT == NTS_FMT_E4M3) {
-      st_global_v2(crow + (size_t)b * kU + u * 8, lo, hi);
-    } else {
-      st_global_u32(crow + (size_t)b * (kU / 2) + u * 4, lo);
+      cw[k][0] = cvt_e2m1x8(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]), f2_lo(q[2]),
+                            f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3])) & keep;
     }
   }
-  if (kAtOnce) {
-    // cw[k] holds vector k ^ sig: swap the pairs that differ in each set bit
+  // cw[k] holds vector k ^ sig: swap the pairs that differ in each set bit
 #pragma unroll
-    for (int bit = 1; bit < UV; bit <<= 1) {
-      const bool sw = (sig & bit) != 0;
+  for (int bit = 1; bit < UV; bit <<= 1) {
+    const bool sw = (sig & bit) != 0;
 #pragma unroll
-      for (int k = 0; k < UV; ++k) {
-        if (k & bit) continue;
+    for (int k = 0; k < UV; ++k) {
+      if (k & bit) continue;
 #pragma unroll
-        for (int h = 0; h < kW; ++h) {
-          const uint32_t x = cw[k][h], y = cw[k | bit][h];
-          cw[k][h] = sw ? y : x;
-          cw[k | bit][h] = sw ? x : y;
-        }
+      for (int h = 0; h < kW; ++h) {
+        const uint32_t x = cw[k][h], y = cw[k | bit][h];
+        cw[k][h] = sw ? y : x;
+        cw[k | bit][h] = sw ? x : y;
       }
     }
-    uint8_t* dst = crow + (size_t)b * (UV * 4 * kW);
-    if (UV * kW == 8) {          // 32 bytes: E4M3 with 4 vectors
-      if (wide) {
-        st_global_v8(dst, cw[0][0], cw[0][kW - 1], cw[1][0], cw[1][kW - 1], cw[2 % UV][0],
-                     cw[2 % UV][kW - 1], cw[3 % UV][0], cw[3 % UV][kW - 1]);
-      } else {
-        st_global_v4(dst, cw[0][0], cw[0][kW - 1], cw[1][0], cw[1][kW - 1]);
-        st_global_v4(dst + 16, cw[2 % UV][0], cw[2 % UV][kW - 1], cw[3 % UV][0],
-                     cw[3 % UV][kW - 1]);
-      }
-    } else if (UV * kW == 4) {   // 16 bytes: E4M3 with 2 vectors, E2M1 with 4
-      if (kW == 2)
-        st_global_v4(dst, cw[0][0], cw[0][kW - 1], cw[1 % UV][0], cw[1 % UV][kW - 1]);
-      else
-        st_global_v4(dst, cw[0][0], cw[1 % UV][0], cw[2 % UV][0], cw[3 % UV][0]);
-    } else {                     // 8 bytes: E2M1 with 2 vectors
-      st_global_v2(dst, cw[0][0], cw[1 % UV][0]);
+  }
+  uint8_t* dst = crow + (size_t)b * (UV * 4 * kW);
+  if (UV * kW == 8) {          // 32 bytes: E4M3 with 4 vectors
+    if (wide) {
+      st_global_v8(dst, cw[0][0], cw[0][kW - 1], cw[1][0], cw[1][kW - 1], cw[2 % UV][0],
+                   cw[2 % UV][kW - 1], cw[3 % UV][0], cw[3 % UV][kW - 1]);
+    } else {
+      st_global_v4(dst, cw[0][0], cw[0][kW - 1], cw[1][0], cw[1][kW - 1]);
+      st_global_v4(dst + 16, cw[2 % UV][0], cw[2 % UV][kW - 1], cw[3 % UV][0],
+                   cw[3 % UV][kW - 1]);
     }
+  } else if (UV * kW == 4) {   // 16 bytes: E4M3 with 2 vectors, E2M1 with 4
+    if (kW == 2)
+      st_global_v4(dst, cw[0][0], cw[0][kW - 1], cw[1 % UV][0], cw[1 % UV][kW - 1]);
+    else
+      st_global_v4(dst, cw[0][0], cw[1 % UV][0], cw[2 % UV][0], cw[3 % UV][0]);
+  } else {                     // 8 bytes: E2M1 with 2 vectors
+    st_global_v2(dst, cw[0][0], cw[1 % UV][0]);
   }
 }
 
@@ -313,8 +291,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
   constexpr int kUV = kSplit ? 4 : VB;                       // vectors per unit
   constexpr int kU = kUV * 8;                                // values per unit
   constexpr int kEmax = (FMT == NTS_FMT_E4M3) ? 8 : 2;
-  // smallest exponent with one product per element (e8m0_single_multiplier)
-  constexpr int kEminOne = (FMT == NTS_FMT_E4M3) ? -116 : -124;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -485,65 +461,39 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mx_norm_cast_kernel(const MxPa
             const uint32_t sc = nvfp4_scale(am[i] * rinv, rcp, &is);
             srow_sc[b] = (uint8_t)sc;
             if (p.amax_out != nullptr) p.amax_out[(size_t)t * p.K + b] = am[i];
-            cast_unit<FMT, kUV, kCastTwo, GAMMA>(srow + (uint32_t)b * kU * 2, sig, p.gamma, b, rr,
-                                                 f2c(is, is), crow, sc != 0 ? ~0u : 0u, false);
+            cast_unit<FMT, kUV, GAMMA>(srow + (uint32_t)b * kU * 2, sig, p.gamma, b, rr,
+                                       f2c(is, is), crow, sc != 0 ? ~0u : 0u, false);
           }
         }
       }
     } else {
-      // E8M0: every block's scale byte first, then the codes.  When every
-      // block of the warp's rows takes one product per element by
-      // m = rinv * 2^-e (ordinary rows: e8m0_single_multiplier; a block of
-      // zeros with m = 0), one unrolled loop runs over all units; otherwise
-      // the form is picked per unit.
-      const OneProductRange opr = one_product_range(rinv, kEminOne);
-      float mul[BPT];
-      bool all_one = true;
+      // E8M0: every block's scale byte first, then the codes, each by the
+      // two products of the definition, q = fp32(fp32(w * rinv) * 2^-e)
+      // (measured on GB300: folding them into one product by a per-block
+      // multiplier, with the bound checks that keep it bit-identical and a
+      // warp vote, was no faster)
+      float isc[BPT];   // 2^-e of every unit
 #pragma unroll
       for (int i = 0; i < BPT; ++i) {
         const int b = i * p.G + g;   // unit
-        mul[i] = 0.f;
+        isc[i] = 0.f;
         if (valid && b < units) {
           const int blk = kSplit ? (b >> 1) : b;
           const bool lead = !kSplit || (b & 1) == 0;   // writes the block's scale
           const uint32_t sbyte = (uint32_t)(e8m0_exponent(am[i] * rinv, kEmax) + 127);
           if (lead) srow_sc[blk] = (uint8_t)sbyte;
           if (p.amax_out != nullptr && lead) p.amax_out[(size_t)t * p.K + blk] = am[i];
-          // a block of zeros casts to signed zeros by any finite multiplier
-          const bool zero = am[i] == 0.f;
-          all_one = all_one && (zero || (sbyte - opr.lo) <= opr.span);
-          mul[i] = zero ? 0.f : __uint_as_float(opr.cm - (sbyte << 23));
+          isc[i] = __uint_as_float((254u - sbyte) << 23);   // 2^-e, e = sbyte - 127
         }
       }
-      if (__all_sync(0xFFFFFFFFu, all_one)) {
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < BPT; ++i) {
-            const int b = i * p.G + g;
-            if (b < units)
-              cast_unit<FMT, kUV, kCastOne, GAMMA>(srow + (uint32_t)b * kU * 2, sig, p.gamma, b,
-                                                   f2c(mul[i], mul[i]), 0, crow, ~0u, p.wide);
-          }
-        }
-      } else if (valid) {
+      if (valid) {
         const uint64_t rr = f2c(rinv, rinv);
-        // (unrolled over the units so that am[] stays in registers; each
-        // unit's vectors run rolled up)
 #pragma unroll
         for (int i = 0; i < BPT; ++i) {
           const int b = i * p.G + g;
-          if (b < units) {
-            const int e = e8m0_exponent(am[i] * rinv, kEmax);
-            const float is = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
-            const unsigned char* base = srow + (uint32_t)b * kU * 2;
-            float m = 0.f;
-            if (e8m0_single_multiplier(rinv, is, e, kEminOne, &m))
-              cast_unit<FMT, kUV, kCastRolled, GAMMA>(base, sig, p.gamma, b, f2c(m, m),
-                                                      f2c(1.f, 1.f), crow, ~0u, false);
-            else
-              cast_unit<FMT, kUV, kCastRolled, GAMMA>(base, sig, p.gamma, b, rr, f2c(is, is),
-                                                      crow, ~0u, false);
-          }
+          if (b < units)
+            cast_unit<FMT, kUV, GAMMA>(srow + (uint32_t)b * kU * 2, sig, p.gamma, b, rr,
+                                       f2c(isc[i], isc[i]), crow, ~0u, p.wide);
         }
       }
     }

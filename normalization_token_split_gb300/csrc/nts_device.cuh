@@ -284,48 +284,6 @@ __device__ __forceinline__ int e8m0_exponent(float ay, int emax) {
   return max(-127, min(127, e));
 }
 
-// The element cast needs q = fl(fl(w * rinv) * 2^-e) for every w of a block
-// (the two fp32 products in which the codes are decided).  One product
-// w * m with m = fl(rinv * 2^-e) gives the same bits whenever
-//  * m is a normal number: then it is exact (rinv is normal and 2^-e a power
-//    of two), and scaling by a power of two commutes with the rounding of a
-//    normal product;
-//  * e >= emin_one: an element whose fl(w * rinv) is subnormal (where the
-//    two forms may round differently) then has |q| <= 2^-126 * 2^-e, at
-//    most half the smallest nonzero magnitude of the element format (E4M3
-//    2^-9: e >= -116; E2M1 2^-1: e >= -124), so both forms cast it to the
-//    signed zero; a subnormal q is likewise a signed zero either way.
-// Returns whether the one-product form applies and, in *m, the multiplier.
-__device__ __forceinline__ bool e8m0_single_multiplier(float rinv, float is, int e, int emin_one,
-                                                       float* m) {
-  *m = rinv * is;
-  const uint32_t field = (__float_as_uint(*m) >> 23) & 0xFFu;
-  return e >= emin_one && field - 1u < 254u;
-}
-
-// Per-row bounds of the E8M0 scale bytes (e + 127) whose blocks take one
-// product per element (e8m0_single_multiplier): m = rinv * 2^-e is normal,
-// i.e. its exponent field f_r + 127 - byte lies in [1, 254] (f_r: the field
-// of rinv), and e >= emin_one.  A byte qualifies iff (byte - lo) <= span as
-// unsigned; no byte does when rinv is zero or subnormal.
-struct OneProductRange {
-  uint32_t lo, span;
-  uint32_t cm;   // bits of rinv * 2^127: the multiplier's bits are cm - (byte << 23)
-};
-
-__device__ __forceinline__ OneProductRange one_product_range(float rinv, int emin_one) {
-  const uint32_t rb = __float_as_uint(rinv);
-  const int fr = (int)(rb >> 23);   // rinv > 0: no sign bit
-  const int lo = max(fr - 127, emin_one + 127);
-  const int hi = fr + 126;
-  OneProductRange r;
-  const bool any = fr >= 1 && fr <= 254 && hi >= lo;
-  r.lo = any ? (uint32_t)lo : 0x7FFFFFFFu;
-  r.span = any ? (uint32_t)(hi - lo) : 0u;
-  r.cm = rb + 0x3F800000u;
-  return r;
-}
-
 // The same exponent by the plain definition (exponent field, mantissa
 // compare, zero/subnormal special case): the reference of the self-check.
 __device__ __forceinline__ int e8m0_exponent_by_fields(float ay, int emax) {

@@ -618,38 +618,30 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
           srow_sc = tn.scales + (first >> kBshift);
           vshift = kBshift - 3;
         }
-        // E8M0 output: the bounds of the scale bytes whose blocks take one
-        // product per element (a block of zeros takes m = 0)
-        const OneProductRange opr = one_product_range(rinv, OUT == kOutE4M3 ? -116 : -124);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
           const int v = i * G + g;
           if (OUT != kOutBf16) {
             if (kFull || v < nvec) {
               // scale of this vector's block, then its eight codes
-              float is, m = 0.f;
+              float is;
               uint32_t keep = ~0u, sbyte;
-              bool one = false;   // one product per element (e8m0_single_multiplier)
               if (OUT == kOutNvfp4) {
                 sbyte = nvfp4_scale(am[i] * rinv, rcp, &is);
                 keep = sbyte != 0 ? ~0u : 0u;
               } else {
                 sbyte = (uint32_t)(e8m0_exponent(am[i] * rinv, OUT == kOutE4M3 ? 8 : 2) + 127);
                 is = __uint_as_float((254u - sbyte) << 23);  // 2^-e, e = sbyte - 127
-                one = am[i] == 0.f || (sbyte - opr.lo) <= opr.span;
-                m = am[i] == 0.f ? 0.f : __uint_as_float(opr.cm - (sbyte << 23));
               }
               if ((g & (kBv - 1)) == 0) srow_sc[v >> vshift] = (uint8_t)sbyte;
+              // q = fp32(fp32(w * rinv) * s), s = 2^-e or fp32(1/scale): the
+              // two products of the definition, with no per-vector choice
+              // (measured on GB300: the one-product form's per-vector
+              // bound check and branch cost more than the product it saves)
               uint64_t q[4];
-              if (one) {
-                const uint64_t mm = f2(m, m);
+              const uint64_t ss = f2(is, is);
 #pragma unroll
-                for (int h = 0; h < 4; ++h) q[h] = f2_mul(w[i][h], mm);
-              } else {
-                const uint64_t ss = f2(is, is);
-#pragma unroll
-                for (int h = 0; h < 4; ++h) q[h] = f2_mul(f2_mul(w[i][h], rr), ss);
-              }
+              for (int h = 0; h < 4; ++h) q[h] = f2_mul(f2_mul(w[i][h], rr), ss);
               if (OUT == kOutE4M3) {
                 const uint32_t lo = cvt_e4m3x4(f2_lo(q[0]), f2_hi(q[0]), f2_lo(q[1]), f2_hi(q[1]));
                 const uint32_t hi = cvt_e4m3x4(f2_lo(q[2]), f2_hi(q[2]), f2_lo(q[3]), f2_hi(q[3]));
