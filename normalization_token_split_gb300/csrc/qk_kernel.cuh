@@ -258,7 +258,8 @@ __device__ __forceinline__ void ln_combine(const float* parts, int N, int wpr, C
 // GC: the consumer threads per row when known at compile time (32, the
 // common shape: slot offsets then fold into the instructions' immediates),
 // or 0: p.G.  GC > 0 also promises that every shard row of every tensor
-// fills all VPT x GC vector slots, so the slots need no range checks.  BV:
+// fills all VPT x GC vector slots, so the slots need no range checks, and
+// that gamma (and beta) are staged in the split layout.  BV:
 // the E8M0 block-cast output's vectors per block when known at compile time
 // (2, 4 or 8), or 0: p.bv.
 template <int N, int VPT, int IN, int STAT, int OUT, int GC, int BV>
@@ -458,7 +459,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       const QkTensor& tn = p.ten[tk];
       const int64_t t = t0 + row;
       const bool valid = t < tn.T;
-      const int nvec = tn.nvec;
+      const int nvec = kFull ? VPT * GC : tn.nvec;
 
       // ---- Phase A: this shard's sum of squares (and, for LayerNorm, its
       // sum) in fp32 packed pairs.  The values are converted once and kept
@@ -548,9 +549,11 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
       }
       // split layout: halves nvec*16 bytes apart, vectors 16 apart; as
       // copied: halves 16 apart, vectors 32 apart
+      // (the GC = 32 kernels always have the split layout)
+      const bool gsplit = kFull || p.gsplit;
       const unsigned char* gam_lo = smem + tn.gam;
-      const unsigned char* gam_hi = gam_lo + (p.gsplit ? (uint32_t)nvec * 16 : 16u);
-      const uint32_t gstride = p.gsplit ? 16u : 32u;
+      const unsigned char* gam_hi = gam_lo + (gsplit ? (uint32_t)nvec * 16 : 16u);
+      const uint32_t gstride = gsplit ? 16u : 32u;
 #pragma unroll
       for (int i = 0; i < VPT && STAT != kQkLn; ++i) {
         const int v = kFull ? i * G + g : min(i * G + g, nvec - 1);
@@ -664,7 +667,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8)
               uint4 blo = make_uint4(0, 0, 0, 0), bhi = make_uint4(0, 0, 0, 0);
               if (tn.beta != nullptr) {
                 const unsigned char* bet_lo = smem + tn.bet;
-                const unsigned char* bet_hi = bet_lo + (p.gsplit ? (uint32_t)nvec * 16 : 16u);
+                const unsigned char* bet_hi = bet_lo + (gsplit ? (uint32_t)nvec * 16 : 16u);
                 blo = lds128(bet_lo + v * gstride);
                 bhi = lds128(bet_hi + v * gstride);
               }

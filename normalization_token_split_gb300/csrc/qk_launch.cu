@@ -67,8 +67,9 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
 
   const int bv = mx_out ? opt.B / 8 : 1;   // block-cast output: vectors per block
   // the kernels with G fixed at compile time serve one-warp shard rows that
-  // fill all their vector slots, in every tensor of the launch
-  bool full = rs.G == 32;
+  // fill all their vector slots, in every tensor of the launch, with gamma
+  // in the split layout
+  bool full = rs.G == 32 && gsplit == 1;
   for (int k = 0; k < ntensors; ++k) full = full && rq[k].H / N / 8 == (int64_t)rs.vpt * rs.G;
   const int gsel = full ? 32 : 0;
   QkKernel kern;
