@@ -251,10 +251,10 @@ __device__ __forceinline__ void ln_combine(const float* parts, int N, int wpr, C
 }
 
 // Registers: 96 per thread (4 CTAs of 160 threads per SM) beat 128 (3 CTAs)
-// by 5-12 % on GB300 for every variant but LayerNorm, which runs best at 104
-// (no spills at any width; with a two-stage ring, 7-8 % faster than at 128);
-// the block-cast output with 8 vectors per thread keeps 128 so as not to
-// spill.
+// by 5-12 % on GB300, and 112 or 72-80 by 5-15 %, for every variant;
+// LayerNorm (92 at 96, no spills; 2-6 % faster than at 104, where it took
+// 102 and 3 CTAs) and the block-cast output with 8 vectors per thread keep
+// 104 and 128 there so as not to spill.
 // GC: the consumer threads per row when known at compile time (32, the
 // common shape: slot offsets then fold into the instructions' immediates),
 // or 0: p.G.  GC > 0 also promises that every shard row of every tensor
@@ -263,7 +263,7 @@ __device__ __forceinline__ void ln_combine(const float* parts, int N, int wpr, C
 // the E8M0 block-cast output's vectors per block when known at compile time
 // (2, 4 or 8), or 0: p.bv.
 template <int N, int VPT, int IN, int STAT, int OUT, int GC, int BV>
-__global__ void __maxnreg__(STAT == kQkLn ? 104 : ((OUT != kOutBf16 && VPT == 8) ? 128 : 96))
+__global__ void __maxnreg__(STAT == kQkLn ? (VPT == 8 ? 104 : 96) : ((OUT != kOutBf16 && VPT == 8) ? 128 : 96))
     qknorm_cluster_kernel(const QkParams p) {
   constexpr int ES = (IN == kInBf16) ? 2 : 1;  // bytes per activation
   const int G = GC > 0 ? GC : p.G;
