@@ -251,10 +251,10 @@ __device__ __forceinline__ void ln_combine(const float* parts, int N, int wpr, C
 }
 
 // Registers: 96 per thread (4 CTAs of 160 threads per SM) beat 128 (3 CTAs)
-// by 5-12 % on GB300, and 112 or 72-80 by 5-15 %, for every variant;
-// LayerNorm (92 at 96, no spills; 2-6 % faster than at 104, where it took
-// 102 and 3 CTAs) and the block-cast output with 8 vectors per thread keep
-// 104 and 128 there so as not to spill.
+// by 5-12 % on GB300, and 112 or 72-80 by 5-15 %, for every variant (the
+// LayerNorm kernel takes 92 at 96 with no spills, 2-6 % faster than at 104,
+// where it took 102 and 3 CTAs).  At 8 vectors per thread LayerNorm keeps
+// 104 and the block-cast output 128, so as not to spill.
 // GC: the consumer threads per row when known at compile time (32, the
 // common shape: slot offsets then fold into the instructions' immediates),
 // or 0: p.G.  GC > 0 also promises that every shard row of every tensor
