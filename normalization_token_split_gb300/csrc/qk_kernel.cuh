@@ -621,6 +621,38 @@ __global__ void __maxnreg__(STAT == kQkLn ? (VPT == 8 ? 104 : 96) : ((OUT != kOu
           srow_sc = tn.scales + (first >> kBshift);
           vshift = kBshift - 3;
         }
+        // Block scales spread over the lanes of a block (B/8 adjacent lanes
+        // hold a block's vectors and, after the shuffles above, its absmax):
+        // lane r of the group forms the scales of the slots r, r + B/8, ...,
+        // stores their scale bytes (one store per round serves 32 blocks)
+        // and hands each slot's multiplier to the others by one shuffle.
+        constexpr int kBvC = OUT == kOutNvfp4 ? 2 : (BV > 0 ? BV : 1);
+        constexpr bool kDist = kFull && OUT != kOutBf16 && (OUT == kOutNvfp4 || BV > 0);
+        constexpr int kRounds = kDist ? (VPT + kBvC - 1) / kBvC : 1;
+        float isd[kRounds];
+        if (kDist) {
+          constexpr int kGroupShift = kBvC == 2 ? 1 : kBvC == 4 ? 2 : 3;
+          const int r = g & (kBvC - 1);
+          const int grp = g >> kGroupShift;
+#pragma unroll
+          for (int j = 0; j < kRounds; ++j) {
+            float a = am[j * kBvC];
+#pragma unroll
+            for (int q = 1; q < kBvC; ++q)
+              if (j * kBvC + q < VPT) a = r == q ? am[j * kBvC + q] : a;
+            const int sl = j * kBvC + r;   // this lane's slot
+            float is;
+            uint32_t sbyte;
+            if (OUT == kOutNvfp4) {
+              sbyte = nvfp4_scale(a * rinv, rcp, &is);
+            } else {
+              sbyte = (uint32_t)(e8m0_exponent(a * rinv, OUT == kOutE4M3 ? 8 : 2) + 127);
+              is = __uint_as_float((254u - sbyte) << 23);
+            }
+            if (sl < VPT) srow_sc[sl * (32 / kBvC) + grp] = (uint8_t)sbyte;
+            isd[j] = is;
+          }
+        }
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
           const int v = i * G + g;
@@ -629,6 +661,10 @@ __global__ void __maxnreg__(STAT == kQkLn ? (VPT == 8 ? 104 : 96) : ((OUT != kOu
               // scale of this vector's block, then its eight codes
               float is;
               uint32_t keep = ~0u, sbyte;
+              if (kDist) {
+                is = __shfl_sync(0xFFFFFFFFu, isd[i / kBvC], (lane & ~(kBvC - 1)) | (i % kBvC));
+                if (OUT == kOutNvfp4) keep = is != 0.f ? ~0u : 0u;
+              } else {
               if (OUT == kOutNvfp4) {
                 sbyte = nvfp4_scale(am[i] * rinv, rcp, &is);
                 keep = sbyte != 0 ? ~0u : 0u;
@@ -637,6 +673,7 @@ __global__ void __maxnreg__(STAT == kQkLn ? (VPT == 8 ? 104 : 96) : ((OUT != kOu
                 is = __uint_as_float((254u - sbyte) << 23);  // 2^-e, e = sbyte - 127
               }
               if ((g & (kBv - 1)) == 0) srow_sc[v >> vshift] = (uint8_t)sbyte;
+              }
               // q = fp32(fp32(w * rinv) * s), s = 2^-e or fp32(1/scale): the
               // two products of the definition, with no per-vector choice
               // (measured on GB300: the one-product form's per-vector
