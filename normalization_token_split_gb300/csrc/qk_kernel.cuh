@@ -662,17 +662,19 @@ __global__ void __maxnreg__(STAT == kQkLn ? (VPT == 8 ? 104 : 96) : ((OUT != kOu
               float is;
               uint32_t keep = ~0u, sbyte;
               if (kDist) {
+                // the multiplier from the lane that formed it (NVFP4: a zero
+                // scale has the multiplier 0)
                 is = __shfl_sync(0xFFFFFFFFu, isd[i / kBvC], (lane & ~(kBvC - 1)) | (i % kBvC));
                 if (OUT == kOutNvfp4) keep = is != 0.f ? ~0u : 0u;
               } else {
-              if (OUT == kOutNvfp4) {
-                sbyte = nvfp4_scale(am[i] * rinv, rcp, &is);
-                keep = sbyte != 0 ? ~0u : 0u;
-              } else {
-                sbyte = (uint32_t)(e8m0_exponent(am[i] * rinv, OUT == kOutE4M3 ? 8 : 2) + 127);
-                is = __uint_as_float((254u - sbyte) << 23);  // 2^-e, e = sbyte - 127
-              }
-              if ((g & (kBv - 1)) == 0) srow_sc[v >> vshift] = (uint8_t)sbyte;
+                if (OUT == kOutNvfp4) {
+                  sbyte = nvfp4_scale(am[i] * rinv, rcp, &is);
+                  keep = sbyte != 0 ? ~0u : 0u;
+                } else {
+                  sbyte = (uint32_t)(e8m0_exponent(am[i] * rinv, OUT == kOutE4M3 ? 8 : 2) + 127);
+                  is = __uint_as_float((254u - sbyte) << 23);  // 2^-e, e = sbyte - 127
+                }
+                if ((g & (kBv - 1)) == 0) srow_sc[v >> vshift] = (uint8_t)sbyte;
               }
               // q = fp32(fp32(w * rinv) * s), s = 2^-e or fp32(1/scale): the
               // two products of the definition, with no per-vector choice
