@@ -261,8 +261,9 @@ __device__ __forceinline__ void ln_combine(const float* parts, int N, int wpr, C
 // fills all VPT x GC vector slots, so the slots need no range checks, and
 // that gamma (and beta) are staged in the split layout.  BV:
 // the E8M0 block-cast output's vectors per block when known at compile time
-// (2, 4 or 8), or 0: p.bv.
-template <int N, int VPT, int IN, int STAT, int OUT, int GC, int BV>
+// (2, 4 or 8), or 0: p.bv.  NT: 1 when the launch has exactly one tensor
+// (its parameters then need no indexing by the tile), or 0: p.ntensors.
+template <int N, int VPT, int IN, int STAT, int OUT, int GC, int BV, int NT>
 __global__ void __maxnreg__(STAT == kQkLn ? (VPT == 8 ? 104 : 96) : ((OUT != kOutBf16 && VPT == 8) ? 128 : 96))
     qknorm_cluster_kernel(const QkParams p) {
   constexpr int ES = (IN == kInBf16) ? 2 : 1;  // bytes per activation
@@ -392,7 +393,8 @@ __global__ void __maxnreg__(STAT == kQkLn ? (VPT == 8 ? 104 : 96) : ((OUT != kOu
         }
         tloc[s] = tile;
         int64_t t0;
-        const QkTensor& tn = p.ten[qk_tile(p, tile, &t0)];
+        const QkTensor& tn = p.ten[NT == 1 ? 0 : qk_tile(p, tile, &t0)];
+        if (NT == 1) t0 = tile * p.R;
         const int nrows = (int)min64(p.R, tn.T - t0);
         const uint32_t row_bytes = (uint32_t)tn.W * ES;
         const uint32_t dst = sbase + L.ring + (uint32_t)s * stage_bytes;
@@ -455,8 +457,9 @@ __global__ void __maxnreg__(STAT == kQkLn ? (VPT == 8 ? 104 : 96) : ((OUT != kOu
       const int64_t tile = *reinterpret_cast<volatile int64_t*>(tloc + s);
       if (tile < 0 || tile >= p.ntiles) break;   // no more tiles
       int64_t t0;
-      const int tk = qk_tile(p, tile, &t0);   // tensor of the tile
-      const QkTensor& tn = p.ten[tk];
+      const int tk = NT == 1 ? 0 : qk_tile(p, tile, &t0);   // tensor of the tile
+      if (NT == 1) t0 = tile * p.R;
+      const QkTensor& tn = p.ten[NT == 1 ? 0 : tk];
       const int64_t t = t0 + row;
       const bool valid = t < tn.T;
       const int nvec = kFull ? VPT * GC : tn.nvec;
@@ -753,16 +756,16 @@ __global__ void __maxnreg__(STAT == kQkLn ? (VPT == 8 ? 104 : 96) : ((OUT != kOu
 
 using QkKernel = void (*)(QkParams);
 
-template <int N, int IN, int STAT, int OUT, int GC, int BV>
+template <int N, int IN, int STAT, int OUT, int GC, int BV, int NT>
 QkKernel pick_qk_vpt(int vpt) {
   switch (vpt) {
-    case 1: return qknorm_cluster_kernel<N, 1, IN, STAT, OUT, GC, BV>;
-    case 2: return qknorm_cluster_kernel<N, 2, IN, STAT, OUT, GC, BV>;
-    case 3: return qknorm_cluster_kernel<N, 3, IN, STAT, OUT, GC, BV>;
-    case 4: return qknorm_cluster_kernel<N, 4, IN, STAT, OUT, GC, BV>;
-    case 5: return qknorm_cluster_kernel<N, 5, IN, STAT, OUT, GC, BV>;
-    case 6: return qknorm_cluster_kernel<N, 6, IN, STAT, OUT, GC, BV>;
-    case 8: return qknorm_cluster_kernel<N, 8, IN, STAT, OUT, GC, BV>;
+    case 1: return qknorm_cluster_kernel<N, 1, IN, STAT, OUT, GC, BV, NT>;
+    case 2: return qknorm_cluster_kernel<N, 2, IN, STAT, OUT, GC, BV, NT>;
+    case 3: return qknorm_cluster_kernel<N, 3, IN, STAT, OUT, GC, BV, NT>;
+    case 4: return qknorm_cluster_kernel<N, 4, IN, STAT, OUT, GC, BV, NT>;
+    case 5: return qknorm_cluster_kernel<N, 5, IN, STAT, OUT, GC, BV, NT>;
+    case 6: return qknorm_cluster_kernel<N, 6, IN, STAT, OUT, GC, BV, NT>;
+    case 8: return qknorm_cluster_kernel<N, 8, IN, STAT, OUT, GC, BV, NT>;
     default: return nullptr;
   }
 }
@@ -770,34 +773,44 @@ QkKernel pick_qk_vpt(int vpt) {
 // One-warp shard rows that fill their slots (G = 32: the launcher passes 32
 // only then) take the kernels with G, and for the E8M0 block-cast outputs
 // the block size, fixed at compile time; other shapes read both from the
-// parameters.
+// parameters.  Launches of one tensor (nt = 1) take the kernels without
+// per-tile tensor indexing where that was measured to pay (block-cast
+// outputs: 4 %; LayerNorm, E4M3 input: 2 %; bf16 output: none) -- the
+// E8M0 outputs for 32-value blocks only, to bound the instantiations.
 template <int N, int IN, int STAT, int OUT>
-QkKernel pick_qk_rows(int vpt, int G, int bv) {
+QkKernel pick_qk_rows(int vpt, int G, int bv, int nt) {
   if (G == 32) {
     if constexpr (OUT == kOutE4M3 || OUT == kOutE2M1) {
       switch (bv) {
-        case 2: return pick_qk_vpt<N, IN, STAT, OUT, 32, 2>(vpt);
-        case 4: return pick_qk_vpt<N, IN, STAT, OUT, 32, 4>(vpt);
-        case 8: return pick_qk_vpt<N, IN, STAT, OUT, 32, 8>(vpt);
+        case 2: return pick_qk_vpt<N, IN, STAT, OUT, 32, 2, 0>(vpt);
+        case 4: return nt == 1 ? pick_qk_vpt<N, IN, STAT, OUT, 32, 4, 1>(vpt)
+                               : pick_qk_vpt<N, IN, STAT, OUT, 32, 4, 0>(vpt);
+        case 8: return pick_qk_vpt<N, IN, STAT, OUT, 32, 8, 0>(vpt);
         default: return nullptr;
       }
+    } else if constexpr (OUT == kOutNvfp4) {
+      return nt == 1 ? pick_qk_vpt<N, IN, STAT, OUT, 32, 0, 1>(vpt)
+                     : pick_qk_vpt<N, IN, STAT, OUT, 32, 0, 0>(vpt);
+    } else if constexpr (STAT == kQkLn || IN != kInBf16) {
+      // no entry point launches two such tensors at once
+      if (nt == 1) return pick_qk_vpt<N, IN, STAT, OUT, 32, 0, 1>(vpt);
     } else {
-      return pick_qk_vpt<N, IN, STAT, OUT, 32, 0>(vpt);
+      return pick_qk_vpt<N, IN, STAT, OUT, 32, 0, 0>(vpt);
     }
   }
-  return pick_qk_vpt<N, IN, STAT, OUT, 0, 0>(vpt);
+  return pick_qk_vpt<N, IN, STAT, OUT, 0, 0, 0>(vpt);
 }
 
 // Instantiates every QK kernel for input type IN, statistic STAT and output
 // OUT in the calling unit; G = consumer threads per row, bv = 16-byte
-// vectors per block of the block-cast output.
+// vectors per block of the block-cast output, nt = tensors of the launch.
 template <int IN, int STAT, int OUT = kOutBf16>
-QkKernel pick_qk_input(int N, int vpt, int G, int bv) {
+QkKernel pick_qk_input(int N, int vpt, int G, int bv, int nt) {
   switch (N) {
-    case 1: return pick_qk_rows<1, IN, STAT, OUT>(vpt, G, bv);
-    case 2: return pick_qk_rows<2, IN, STAT, OUT>(vpt, G, bv);
-    case 4: return pick_qk_rows<4, IN, STAT, OUT>(vpt, G, bv);
-    case 8: return pick_qk_rows<8, IN, STAT, OUT>(vpt, G, bv);
+    case 1: return pick_qk_rows<1, IN, STAT, OUT>(vpt, G, bv, nt);
+    case 2: return pick_qk_rows<2, IN, STAT, OUT>(vpt, G, bv, nt);
+    case 4: return pick_qk_rows<4, IN, STAT, OUT>(vpt, G, bv, nt);
+    case 8: return pick_qk_rows<8, IN, STAT, OUT>(vpt, G, bv, nt);
     default: return nullptr;
   }
 }
@@ -816,12 +829,12 @@ static inline int read_and_clear_local_qk_status(unsigned* out) {
 QkKernel pick_qk_direct(int N, int vpt, int in_e4m3, int layernorm);
 
 // Defined by qk_bf16.cu, qk_e4m3.cu, qk_ln.cu and qk_mx_*.cu.
-QkKernel pick_qk_bf16(int N, int vpt, int G, int bv);
-QkKernel pick_qk_e4m3(int N, int vpt, int G, int bv);
-QkKernel pick_qk_ln(int N, int vpt, int G, int bv);
-QkKernel pick_qk_mx_e4m3(int N, int vpt, int G, int bv);
-QkKernel pick_qk_mx_e2m1(int N, int vpt, int G, int bv);
-QkKernel pick_qk_mx_nvfp4(int N, int vpt, int G, int bv);
+QkKernel pick_qk_bf16(int N, int vpt, int G, int bv, int nt);
+QkKernel pick_qk_e4m3(int N, int vpt, int G, int bv, int nt);
+QkKernel pick_qk_ln(int N, int vpt, int G, int bv, int nt);
+QkKernel pick_qk_mx_e4m3(int N, int vpt, int G, int bv, int nt);
+QkKernel pick_qk_mx_e2m1(int N, int vpt, int G, int bv, int nt);
+QkKernel pick_qk_mx_nvfp4(int N, int vpt, int G, int bv, int nt);
 int read_and_clear_qk_bf16_status(unsigned* out);
 int read_and_clear_qk_e4m3_status(unsigned* out);
 int read_and_clear_qk_ln_status(unsigned* out);

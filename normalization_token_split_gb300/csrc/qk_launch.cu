@@ -74,13 +74,13 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
   const int gsel = full ? 32 : 0;
   QkKernel kern;
   if (mx_out)
-    kern = opt.out_fmt == NTS_FMT_E4M3   ? pick_qk_mx_e4m3(N, rs.vpt, gsel, bv)
-           : opt.out_fmt == NTS_FMT_E2M1 ? pick_qk_mx_e2m1(N, rs.vpt, gsel, bv)
-                                         : pick_qk_mx_nvfp4(N, rs.vpt, gsel, bv);
+    kern = opt.out_fmt == NTS_FMT_E4M3   ? pick_qk_mx_e4m3(N, rs.vpt, gsel, bv, ntensors)
+           : opt.out_fmt == NTS_FMT_E2M1 ? pick_qk_mx_e2m1(N, rs.vpt, gsel, bv, ntensors)
+                                         : pick_qk_mx_nvfp4(N, rs.vpt, gsel, bv, ntensors);
   else
-    kern = layernorm    ? pick_qk_ln(N, rs.vpt, gsel, bv)
-           : opt.in_e4m3 ? pick_qk_e4m3(N, rs.vpt, gsel, bv)
-                         : pick_qk_bf16(N, rs.vpt, gsel, bv);
+    kern = layernorm    ? pick_qk_ln(N, rs.vpt, gsel, bv, ntensors)
+           : opt.in_e4m3 ? pick_qk_e4m3(N, rs.vpt, gsel, bv, ntensors)
+                         : pick_qk_bf16(N, rs.vpt, gsel, bv, ntensors);
   if (kern == nullptr) return fail(NTS_ERR_UNSUPPORTED, "no kernel for N=%d vpt=%d", N, rs.vpt);
 
   QkParams prm = {};

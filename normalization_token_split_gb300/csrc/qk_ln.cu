@@ -5,8 +5,8 @@
 
 namespace nts {
 
-QkKernel pick_qk_ln(int N, int vpt, int G, int bv) {
-  return pick_qk_input<kInBf16, kQkLn>(N, vpt, G, bv);
+QkKernel pick_qk_ln(int N, int vpt, int G, int bv, int nt) {
+  return pick_qk_input<kInBf16, kQkLn>(N, vpt, G, bv, nt);
 }
 
 int read_and_clear_qk_ln_status(unsigned* out) { return read_and_clear_local_qk_status(out); }
