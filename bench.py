@@ -48,7 +48,8 @@ KERNELS = ["qknorm_rms_qk[Q+K]", "rmsnorm_mxcast", "mxnorm_cast[p=1]", "mxnorm_c
 KERNEL_SOURCES = {   # files whose content the committed ncu traffic figures belong to
     "qknorm_rms_qk[Q+K]": ["normalization_token_split_gb300/csrc/qk_kernel.cuh",
                            "normalization_token_split_gb300/csrc/qk_launch.cu",
-                           "normalization_token_split_gb300/csrc/nts_device.cuh"],
+                           "normalization_token_split_gb300/csrc/nts_device.cuh",
+                           "normalization_token_split_gb300/csrc/nts_internal.h"],
     "rmsnorm_mxcast": ["normalization_token_split_gb300/csrc/mx_kernel.cuh",
                        "normalization_token_split_gb300/csrc/mx_launch.cu",
                        "normalization_token_split_gb300/csrc/nts_device.cuh"],

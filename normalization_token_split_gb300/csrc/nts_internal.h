@@ -42,6 +42,21 @@ inline cudaLaunchAttribute pdl_attribute() {
   return a;
 }
 
+// The launch attribute that lets the hardware balance the CTAs of a cluster
+// over the SMs of its GPC as it sees fit.  With the default placement, a
+// grid of the occupancy query's maximum cluster count, placed while the
+// previous grid drains, sometimes left a cluster without room until other
+// clusters had finished (per-CTA timelines on GB300: a split-H launch after
+// an MX launch started one cluster ~48 us late, in half of the launches);
+// with this policy every cluster started at once, and the occupancy query,
+// which sees the attribute, admits one or two more clusters.
+inline cudaLaunchAttribute cluster_policy_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+  a.val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
+  return a;
+}
+
 LaunchTuning current_tuning();
 
 // Test hook (nts_debug_inject_failure): while injections remain, the next

@@ -136,23 +136,24 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
     QkKernel dk = pick_qk_direct(N, rs.vpt, opt.in_e4m3, layernorm);
     const size_t dsmem = (size_t)R * N * (rs.G / 32) * 4 * NS;
     cudaLaunchConfig_t dc = {};
-    cudaLaunchAttribute da[2];
+    cudaLaunchAttribute da[3];
     da[0].id = cudaLaunchAttributeClusterDimension;
     da[0].val.clusterDim.x = N;
     da[0].val.clusterDim.y = 1;
     da[0].val.clusterDim.z = 1;
+    da[1] = cluster_policy_attribute();
     dc.blockDim = dim3(R * rs.G);
     dc.dynamicSmemBytes = dsmem;
     dc.stream = stream;
     dc.attrs = da;
-    dc.numAttrs = 1;
+    dc.numAttrs = 2;
     int64_t dmax = 0;
     int rc = dk != nullptr ? max_active_clusters((const void*)dk, dc, N, &dmax) : NTS_OK;
     if (rc != NTS_OK) return rc;
     if (dk != nullptr && ntiles <= dmax) {
       dc.gridDim = dim3((unsigned)(ntiles * N));
-      da[1] = pdl_attribute();
-      dc.numAttrs = tune.pdl ? 2 : 1;
+      da[2] = pdl_attribute();
+      dc.numAttrs = tune.pdl ? 3 : 2;
       log_launch(layernorm ? "layernorm_split" : "qknorm_rms", "direct: tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d clusters=%lld",
                  ntensors, (long long)rq[0].T, (int)rq[0].H, N, rs.vpt, rs.G, R,
                  (long long)ntiles);
@@ -167,16 +168,17 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
   if (rc != NTS_OK) return rc;
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = N;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = cluster_policy_attribute();
   cfg.blockDim = dim3(nthreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
 
   int64_t max_clusters = 0;
   rc = max_active_clusters((const void*)kern, cfg, N, &max_clusters);
@@ -184,8 +186,8 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
   int64_t ncl = std::min<int64_t>(ntiles, max_clusters);
   if (tune.force_grid > 0) ncl = std::min<int64_t>(ntiles, tune.force_grid);
   cfg.gridDim = dim3((unsigned)(ncl * N));
-  attr[1] = pdl_attribute();
-  cfg.numAttrs = tune.pdl ? 2 : 1;
+  attr[2] = pdl_attribute();
+  cfg.numAttrs = tune.pdl ? 3 : 2;
 
   log_launch(layernorm ? "layernorm_split" : (mx_out ? "qknorm_rms_mxcast" : "qknorm_rms"),
              "tensors=%d T=%lld H=%d N=%d vpt=%d G=%d R=%d S=%d gsplit=%d "
