@@ -46,12 +46,14 @@ int launch_qknorm(const QkRequest* rq, int ntensors, float eps, int N, const QkO
   // Ring depth: up to 4 stages within the shared-memory budget; the widest
   // shards (whose staged gamma alone is up to 120 KB) fall back to fewer.
   // The variants bound by their per-row work rather than by DRAM take
-  // fewer (measured on GB300 at [8192, 5120], N = 4, against four stages):
-  // LayerNorm and the block-cast output two (7-8 % and 4-5 % faster),
-  // E4M3 input three (3 %).
+  // fewer (measured on GB300 at [8192, 5120], N = 4, back-to-back launches):
+  // the block-cast output of one tensor two (4-5 % faster than four),
+  // of Q and K in one launch three (3 % faster than two), LayerNorm three
+  // (1.5 % faster than two, which was 7-8 % faster than four), E4M3 input
+  // three (3 % faster than four, 8 % faster than two).
   // gamma is split into the conflict-free layout when both copies fit.
   int gsplit = 1;
-  int S = (layernorm || mx_out) ? 2 : (opt.in_e4m3 ? 3 : 4);
+  int S = layernorm ? 3 : mx_out ? (ntensors > 1 ? 3 : 2) : (opt.in_e4m3 ? 3 : 4);
   const bool nvfp4 = mx_out && opt.out_fmt == NTS_FMT_NVFP4;
   auto layout = [&](int s, int split) {
     return qk_layout(N, s, R, Wmax, psum, rs.G, split, ES, NS, nvfp4);
